@@ -1,0 +1,216 @@
+"""CPU oracle for the DeepSeekMoE layer forward, load count and bias update.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
+module.  The CUDA library never calls it and shares no code with it; the two
+meet only in the seeded inputs of ``moe_inputs``.
+
+Plain, slow and written to be checked by eye against the pages:
+everything is float64 numpy, one step per equation, no blocking or fusion.
+Library primitives used as steps: matrix product (``@``), ``np.exp``,
+``np.lexsort``, ``np.bincount``, ``np.cumsum``.
+
+Sources (DeepSeekMoE pages):
+- "DeepSeekMoE架构解析" (V3 walk-through), section 2.1, eqs. (13)-(15): Sigmoid
+  affinity, hard top-K_r, renormalisation over the chosen experts;
+  section 2.2, eq. (16): the balancing bias enters the top-K decision only;
+  section 2.2, update rule: overloaded experts b_i -= gamma, underloaded
+  b_i += gamma, gamma = 0.001; section 3.1: output = u_t + shared + routed.
+- course chapter "MoE" (blog.zero43.top), section 4: the 2024 DeepSeekMoE
+  gates are not renormalised (their sum is generally below 1); section 5: the
+  bias is updated after every batch and takes effect for the next one;
+  section 6: no token is dropped.
+
+Readings where the pages are silent (all also listed in the design doc):
+- The top-K decision is taken on float32 keys fp32(fp32(s_i) + b_i): the pages
+  fix no precision, so the decision uses the CUDA kernel's.  Equal keys go to
+  the lower expert index; chosen experts are listed by descending key.
+- Expert FFN is SwiGLU without linear biases: W2 (SiLU(Wg u) * (Wu u)).
+- Shared experts enter the sum with weight 1, the residual u_t is optional.
+- "Overloaded" means count_i * E > T * K (exactly above the mean load); equal
+  to the mean leaves b_i unchanged.  The update is float32 arithmetic.
+- Softmax mode (2024 layer) normalises over all E experts before selection.
+- If the chosen scores sum to 0 the renormalised gates are 0.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SIGMOID = 0
+SOFTMAX = 1
+
+
+def _f64(a) -> np.ndarray:
+    """Exact upcast of a numpy array or a torch tensor (any device/dtype) to fp64."""
+    if hasattr(a, "detach"):
+        import torch
+        return a.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def _f32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        import torch
+        return a.detach().to("cpu", torch.float32).numpy()
+    return np.asarray(a, dtype=np.float32)
+
+
+# ----------------------------------------------------------------------------
+# Router: eqs. (15), (16), (14), (13)
+# ----------------------------------------------------------------------------
+
+def affinity_logits(u, centroids) -> np.ndarray:
+    """u_t^T e_i for every token t and expert i (inner product of eq. 15).
+    u [T, d], centroids [E, d] -> [T, E] fp64."""
+    return _f64(u) @ _f64(centroids).T
+
+
+def expert_scores(logits: np.ndarray, score_func: int = SIGMOID) -> np.ndarray:
+    """s_{i,t}.  SIGMOID: eq. (15), applied to each expert on its own.
+    SOFTMAX: the 2024 gating, normalised over all E experts."""
+    if score_func == SIGMOID:
+        return 1.0 / (1.0 + np.exp(-logits))
+    if score_func == SOFTMAX:
+        z = logits - logits.max(axis=1, keepdims=True)
+        ez = np.exp(z)
+        return ez / ez.sum(axis=1, keepdims=True)
+    raise ValueError("score_func")
+
+
+def selection_keys(s: np.ndarray, bias) -> np.ndarray:
+    """Biased keys s_{i,t} + b_i of eq. (16), formed in float32 (see header)."""
+    return (s.astype(np.float32) + _f32(bias)[None, :]).astype(np.float32)
+
+
+def select_topk(keys: np.ndarray, K: int):
+    """Top-K_r of eq. (14)/(16): the K largest keys per token, by descending key,
+    equal keys to the lower expert index.  Returns idx [T, K] int32 and the
+    margin key_(K) - key_(K+1) per token (inf when K == E)."""
+    T, E = keys.shape
+    idx = np.empty((T, K), dtype=np.int32)
+    margin = np.full(T, np.inf)
+    experts = np.arange(E)
+    for t in range(T):
+        # lexsort sorts by the last key first: descending key, then ascending index
+        order = np.lexsort((experts, -keys[t].astype(np.float64)))
+        idx[t] = order[:K]
+        if K < E:
+            margin[t] = float(keys[t, order[K - 1]]) - float(keys[t, order[K]])
+    return idx, margin
+
+
+def gate_values(s: np.ndarray, idx: np.ndarray, normalize: int) -> np.ndarray:
+    """g'_{i,t} = s_{i,t} for the chosen experts (eq. 14; the bias is not used),
+    then g = g' / sum_j g'_j over the chosen experts (eq. 13) when ``normalize``."""
+    g = np.take_along_axis(s, idx.astype(np.int64), axis=1)
+    if normalize:
+        tot = g.sum(axis=1, keepdims=True)
+        g = np.where(tot > 0, g / np.where(tot > 0, tot, 1.0), 0.0)
+    return g
+
+
+def route(u, centroids, bias, K: int, score_func: int = SIGMOID, normalize: int = 1):
+    """Whole router for the given tokens: idx, gates (fp64), margins, scores."""
+    s = expert_scores(affinity_logits(u, centroids), score_func)
+    idx, margin = select_topk(selection_keys(s, bias), K)
+    return idx, gate_values(s, idx, normalize), margin, s
+
+
+# ----------------------------------------------------------------------------
+# Dispatch: no-drop assignment of every (token, slot) to its expert
+# ----------------------------------------------------------------------------
+
+def dispatch(idx: np.ndarray, E: int):
+    """counts[i] = #(t,k) with idx[t,k] = i; offsets = exclusive prefix sum
+    (length E+1); rows of expert i are its tokens in ascending token order:
+    perm_tok[offsets[i] + r] = r-th such token; pos[t,k] = row of (t,k).
+    Nothing is dropped: every (t,k) gets a row (course chapter, section 6)."""
+    T, K = idx.shape
+    counts = np.bincount(idx.reshape(-1), minlength=E).astype(np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    fill = offsets[:-1].copy()
+    perm_tok = np.empty(T * K, dtype=np.int64)
+    pos = np.empty((T, K), dtype=np.int64)
+    for t in range(T):
+        for k in range(K):
+            i = idx[t, k]
+            pos[t, k] = fill[i]
+            perm_tok[fill[i]] = t
+            fill[i] += 1
+    return counts, offsets, perm_tok, pos
+
+
+# ----------------------------------------------------------------------------
+# Experts and combine
+# ----------------------------------------------------------------------------
+
+def silu(z: np.ndarray) -> np.ndarray:
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
+    """One expert: W2 (SiLU(Wg u) * (Wu u)); w13 [2I, d] = [Wg; Wu], w2 [d, I].
+    u [n, d] fp64 -> [n, d] fp64."""
+    w13 = _f64(w13)
+    I = w13.shape[0] // 2
+    h = u @ w13.T
+    a = silu(h[:, :I]) * h[:, I:]
+    return a @ _f64(w2).T
+
+
+def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
+              add_residual: int = 1, tokens=None) -> dict:
+    """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
+    ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
+
+    ``inp`` holds x, centroids, bias, w13, w2, ws13, ws2 (see moe_inputs).
+    Expert weights are read one expert at a time, so large layers can be
+    evaluated on a token sample.  Returns out (fp64), delta = out - residual,
+    idx, gates, margin."""
+    x = inp["x"]
+    if tokens is not None:
+        tokens = np.asarray(tokens, dtype=np.int64)
+        x = x[tokens] if not hasattr(x, "detach") else x[_torch_index(tokens, x)]
+    u = _f64(x)
+    n = u.shape[0]
+    idx, gates, margin, _ = route(u, inp["centroids"], inp["bias"], K, score_func,
+                                  normalize)
+    d = u.shape[1]
+    delta = np.zeros((n, d))
+    S = inp["ws13"].shape[0]
+    for s in range(S):
+        delta += swiglu_ffn(u, inp["ws13"][s], inp["ws2"][s])
+    routed = np.zeros((n, K, d))
+    for e in np.unique(idx):
+        rows, slots = np.nonzero(idx == e)
+        routed[rows, slots] = swiglu_ffn(u[rows], inp["w13"][int(e)], inp["w2"][int(e)])
+    for k in range(K):
+        delta += gates[:, k:k + 1] * routed[:, k]
+    out = delta + u if add_residual else delta.copy()
+    return {"out": out, "delta": delta, "idx": idx, "gates": gates, "margin": margin}
+
+
+def _torch_index(tokens, ref):
+    import torch
+    return torch.as_tensor(tokens, device=ref.device)
+
+
+# ----------------------------------------------------------------------------
+# Load count and bias update (section 2.2 of the V3 walk-through)
+# ----------------------------------------------------------------------------
+
+def update_bias(counts, bias, T: int, K: int, gamma: float = 1e-3):
+    """b_i -= gamma if expert i took more than the mean load T*K/E, += gamma if
+    less, unchanged if equal.  Comparison in integers (count_i*E vs T*K), the
+    add in float32.  Returns (new bias fp32 [E], (max/mean, min/mean))."""
+    c = np.asarray(counts, dtype=np.int64)
+    E = c.shape[0]
+    b = _f32(bias).copy()
+    g = np.float32(gamma)
+    over = c * E > T * K
+    under = c * E < T * K
+    b[over] = (b[over] - g).astype(np.float32)
+    b[under] = (b[under] + g).astype(np.float32)
+    mean = T * K / E
+    return b, (float(c.max()) / mean, float(c.min()) / mean)

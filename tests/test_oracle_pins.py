@@ -1,0 +1,293 @@
+"""Pins for the CPU oracle: hand-worked golden values, closed forms, brute force
+and invariants that the DeepSeekMoE pages fix.  CPU only."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+from oracle import moe_oracle as O
+from moe_inputs import small_cases, make_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+_NS = {"LN3": math.log(3.0), "LN9": math.log(9.0),
+       "S2": 1.0 / (1.0 + math.exp(-2.0)), "__builtins__": {}}
+
+
+def _num(tok):
+    return float(eval(tok, _NS))  # fixture tokens are small arithmetic expressions
+
+
+def _rows(text, conv=_num):
+    return [[conv(t) for t in r.split()] for r in text.split("|")]
+
+
+def _read(name):
+    lines = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for ln in f:
+            ln = ln.strip()
+            if ln and not ln.startswith("#"):
+                k, v = ln.split(":", 1)
+                lines.append((k.strip(), v.strip()))
+    return lines
+
+
+# ---------------------------------------------------------------- golden cases
+
+def test_golden_routing():
+    lines = _read("routing_hand.txt")
+    kv = dict(lines[:2])
+    C = np.array(_rows(kv["centroids"]))
+    X = np.array(_rows(kv["x"]))
+    cases = [v for k, v in lines if k == "case"]
+    idxs = [v for k, v in lines if k == "idx"]
+    gates = [v for k, v in lines if k == "gates"]
+    assert len(cases) == 3
+    for case, ii, gg in zip(cases, idxs, gates):
+        bias_txt, norm_txt = case[len("bias="):].split(" normalize=")
+        bias = np.array([float(t) for t in bias_txt.split()], dtype=np.float32)
+        norm = int(norm_txt)
+        idx, g, margin, _ = O.route(X, C, bias, 2, O.SIGMOID, norm)
+        np.testing.assert_array_equal(idx, np.array(_rows(ii, int)))
+        np.testing.assert_allclose(g, np.array(_rows(gg)), rtol=0, atol=1e-12)
+
+
+def test_golden_dispatch():
+    kv = dict(_read("dispatch_hand.txt"))
+    E = int(kv["E"])
+    idx = np.array(_rows(kv["idx"], int), dtype=np.int32)
+    counts, offsets, perm, pos = O.dispatch(idx, E)
+    np.testing.assert_array_equal(counts, [int(t) for t in kv["counts"].split()])
+    np.testing.assert_array_equal(offsets, [int(t) for t in kv["offsets"].split()])
+    np.testing.assert_array_equal(perm, [int(t) for t in kv["perm_tok"].split()])
+    np.testing.assert_array_equal(pos, np.array(_rows(kv["pos"], int)))
+
+
+def test_golden_bias_update():
+    kv = dict(_read("bias_update_hand.txt"))
+    counts = [int(t) for t in kv["counts"].split()]
+    bias = np.array([float(t) for t in kv["bias_in"].split()], dtype=np.float32)
+    b, stats = O.update_bias(counts, bias, int(kv["T"]), int(kv["K"]), float(kv["gamma"]))
+    want = np.array([int(h, 16) for h in kv["bias_out_f32hex"].split()], dtype=np.uint32)
+    np.testing.assert_array_equal(b.view(np.uint32), want)
+    np.testing.assert_allclose(stats, [float(t) for t in kv["load_stats"].split()])
+
+
+def test_golden_swiglu():
+    kv = dict(_read("swiglu_hand.txt"))
+    u = np.array([_rows(kv["u"])[0]])
+    w13 = np.array(_rows(kv["w13"]))
+    w2 = np.array(_rows(kv["w2"]))
+    y = O.swiglu_ffn(u, w13, w2)
+    np.testing.assert_allclose(y[0], _rows(kv["y"])[0], rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute_topk(keys_row, K):
+    """The unique K-subset S with: every chosen i beats every unchosen j
+    (key_i > key_j, or equal keys and i < j).  Enumerates all C(E, K) subsets."""
+    E = len(keys_row)
+    good = []
+    for S in itertools.combinations(range(E), K):
+        Sset = set(S)
+        ok = all(keys_row[i] > keys_row[j] or (keys_row[i] == keys_row[j] and i < j)
+                 for i in Sset for j in range(E) if j not in Sset)
+        if ok:
+            good.append(S)
+    assert len(good) == 1
+    return set(good[0])
+
+
+@pytest.mark.parametrize("E,K", [(6, 1), (6, 3), (8, 4), (7, 7), (10, 2)])
+def test_topk_brute_force(E, K):
+    rng = np.random.default_rng(E * 10 + K)
+    for trial in range(40):
+        # quantised keys force many exact ties
+        keys = (rng.integers(0, 5, size=(1, E)) / 4.0).astype(np.float32)
+        idx, margin = O.select_topk(keys, K)
+        assert set(idx[0].tolist()) == _brute_topk(keys[0].tolist(), K)
+        # listed by descending key, ties by ascending index
+        ks = keys[0][idx[0]]
+        for a in range(K - 1):
+            assert ks[a] > ks[a + 1] or (ks[a] == ks[a + 1] and idx[0][a] < idx[0][a + 1])
+        if K == E:
+            assert margin[0] == np.inf
+        else:
+            rest = [keys[0][j] for j in range(E) if j not in set(idx[0].tolist())]
+            assert margin[0] == pytest.approx(float(ks[-1]) - float(max(rest)))
+
+
+def test_topk_k1_is_argmax():
+    rng = np.random.default_rng(3)
+    keys = rng.standard_normal((50, 13)).astype(np.float32)
+    idx, _ = O.select_topk(keys, 1)
+    np.testing.assert_array_equal(idx[:, 0], np.argmax(keys, axis=1))
+
+
+# ---------------------------------------------------------------- closed forms / invariants
+
+def test_sigmoid_scores_closed_form():
+    rng = np.random.default_rng(5)
+    L = rng.standard_normal((4, 6)) * 3
+    s = O.expert_scores(L, O.SIGMOID)
+    for t in range(4):
+        for i in range(6):
+            assert s[t, i] == pytest.approx(1.0 / (1.0 + math.exp(-L[t, i])), rel=1e-14)
+
+
+def test_softmax_scores_match_scipy_and_norenorm_sum_below_one():
+    rng = np.random.default_rng(6)
+    L = rng.standard_normal((30, 64))
+    s = O.expert_scores(L, O.SOFTMAX)
+    np.testing.assert_allclose(s, scipy.special.softmax(L, axis=1), rtol=1e-12)
+    keys = O.selection_keys(s, np.zeros(64, np.float32))
+    idx, _ = O.select_topk(keys, 6)
+    g = O.gate_values(s, idx, normalize=0)
+    assert np.all(g.sum(axis=1) < 1.0)          # 2024 variant: sum generally < 1
+    np.testing.assert_allclose(g, np.take_along_axis(scipy.special.softmax(L, axis=1), idx,
+                                                     axis=1), rtol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "ragged_bf16", "softmax_norenorm",
+                                  "sigmoid_norenorm", "wide_e"])
+def test_routing_invariants(name):
+    cfg = small_cases()[name]
+    inp = make_inputs(cfg, "cpu")
+    idx, g, margin, s = O.route(inp["x"], inp["centroids"], inp["bias"], cfg.K,
+                                cfg.score_func, cfg.normalize)
+    T, K, E = cfg.T, cfg.K, cfg.E
+    assert idx.shape == (T, K)
+    assert np.all((idx >= 0) & (idx < E))
+    assert all(len(set(r.tolist())) == K for r in idx)     # K distinct experts, no drop
+    if cfg.normalize:
+        np.testing.assert_allclose(g.sum(axis=1), 1.0, atol=1e-12)
+    else:
+        np.testing.assert_array_equal(g, np.take_along_axis(s, idx.astype(np.int64), 1))
+    counts, offsets, perm, pos = O.dispatch(idx, E)
+    assert counts.sum() == T * K
+    assert offsets[0] == 0 and offsets[-1] == T * K
+    np.testing.assert_array_equal(np.diff(offsets), counts)
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(seg) > 0)                      # ascending token order
+        assert np.all((idx[seg] == e).sum(axis=1) == 1)      # each row's token chose e
+    for t in range(T):
+        for k in range(K):
+            assert perm[pos[t, k]] == t
+            assert offsets[idx[t, k]] <= pos[t, k] < offsets[idx[t, k] + 1]
+
+
+def test_bias_changes_selection_not_gates():
+    cfg = small_cases()["small_bf16"]
+    inp = make_inputs(cfg, "cpu")
+    x, C = inp["x"], inp["centroids"]
+    idx0, g0, margin, s = O.route(x, C, np.zeros(cfg.E, np.float32), cfg.K)
+    # a bias far smaller than every margin leaves the selection and the gates alone
+    tiny = (np.arange(cfg.E, dtype=np.float32) - cfg.E / 2) * np.float32(1e-9)
+    keep = margin > 1e-6
+    idx1, g1, _, _ = O.route(x, C, tiny, cfg.K)
+    np.testing.assert_array_equal(idx1[keep], idx0[keep])
+    np.testing.assert_array_equal(g1[keep], g0[keep])
+    # a large bias on expert 5 forces it into every token's set, at its own score
+    big = np.zeros(cfg.E, np.float32)
+    big[5] = 10.0
+    idx2, g2, _, s2 = O.route(x, C, big, cfg.K)
+    assert np.all(idx2[:, 0] == 5)
+    chosen = np.take_along_axis(s2, idx2.astype(np.int64), 1)
+    np.testing.assert_allclose(g2[:, 0], s2[:, 5] / chosen.sum(axis=1), rtol=1e-13)
+
+
+def test_update_bias_direction():
+    rng = np.random.default_rng(9)
+    E, T, K = 32, 100, 8
+    for trial in range(20):
+        idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)])
+        counts = np.bincount(idx.reshape(-1), minlength=E)
+        b0 = rng.uniform(-0.01, 0.01, E).astype(np.float32)
+        b1, (mx, mn) = O.update_bias(counts, b0, T, K, 1e-3)
+        mean = T * K / E
+        for e in range(E):
+            if counts[e] > mean:
+                assert b1[e] < b0[e]
+            elif counts[e] < mean:
+                assert b1[e] > b0[e]
+            else:
+                assert b1[e] == b0[e]
+        assert mx == pytest.approx(counts.max() / mean) and mn == pytest.approx(counts.min()
+                                                                                / mean)
+
+
+# ---------------------------------------------------------------- expert / combine special cases
+
+def _dense_swiglu_torch(u, w13, w2):
+    """Independent dense SwiGLU via torch.nn.functional, fp64."""
+    u = torch.as_tensor(u, dtype=torch.float64)
+    w13 = torch.as_tensor(w13, dtype=torch.float64)
+    w2 = torch.as_tensor(w2, dtype=torch.float64)
+    I = w13.shape[0] // 2
+    gate = F.linear(u, w13[:I])
+    up = F.linear(u, w13[I:])
+    return F.linear(F.silu(gate) * up, w2).numpy()
+
+
+def test_identical_experts_reduce_to_dense_ffn():
+    """With every routed expert identical and renormalised gates, the routed sum
+    is the dense FFN itself (sum of gates is 1), plus shared, plus u."""
+    cfg = small_cases()["ragged_bf16"]
+    inp = make_inputs(cfg, "cpu")
+    inp = dict(inp)
+    inp["w13"] = inp["w13"][:1].expand(cfg.E, -1, -1)
+    inp["w2"] = inp["w2"][:1].expand(cfg.E, -1, -1)
+    res = O.moe_layer(inp, cfg.K, normalize=1)
+    u = inp["x"].double().numpy()
+    want = u + _dense_swiglu_torch(u, inp["w13"][0], inp["w2"][0])
+    for s in range(cfg.S):
+        want += _dense_swiglu_torch(u, inp["ws13"][s], inp["ws2"][s])
+    np.testing.assert_allclose(res["out"], want, rtol=1e-10, atol=1e-12)
+
+
+def test_zero_routed_down_gives_shared_plus_residual():
+    cfg = small_cases()["softmax_norenorm"]
+    inp = dict(make_inputs(cfg, "cpu"))
+    inp["w2"] = torch.zeros_like(inp["w2"])
+    for resid in (0, 1):
+        res = O.moe_layer(inp, cfg.K, cfg.normalize, cfg.score_func, add_residual=resid)
+        u = inp["x"].double().numpy()
+        want = sum(_dense_swiglu_torch(u, inp["ws13"][s], inp["ws2"][s]) for s in range(cfg.S))
+        if resid:
+            want = want + u
+        np.testing.assert_allclose(res["out"], want, rtol=1e-10, atol=1e-12)
+
+
+def test_routed_combine_weights_by_gate():
+    """A single routed expert (E=K=1) with renorm has gate exactly 1; with
+    no renorm the gate is its Sigmoid score."""
+    rng = np.random.default_rng(11)
+    d, I = 8, 4
+    inp = {"x": rng.standard_normal((5, d)), "centroids": rng.standard_normal((1, d)),
+           "bias": np.zeros(1, np.float32), "w13": rng.standard_normal((1, 2 * I, d)),
+           "w2": rng.standard_normal((1, d, I)), "ws13": np.zeros((0, 2 * I, d)),
+           "ws2": np.zeros((0, d, I))}
+    dense = _dense_swiglu_torch(inp["x"], inp["w13"][0], inp["w2"][0])
+    r1 = O.moe_layer(inp, 1, normalize=1, add_residual=0)
+    np.testing.assert_allclose(r1["out"], dense, rtol=1e-12)
+    r0 = O.moe_layer(inp, 1, normalize=0, add_residual=0)
+    sig = 1.0 / (1.0 + np.exp(-(inp["x"] @ inp["centroids"][0])))
+    np.testing.assert_allclose(r0["out"], dense * sig[:, None], rtol=1e-12)
+
+
+def test_token_subset_equals_full_batch():
+    cfg = small_cases()["small_bf16"]
+    inp = make_inputs(cfg, "cpu")
+    full = O.moe_layer(inp, cfg.K)
+    tok = [0, 7, 100, 511, 250]
+    sub = O.moe_layer(inp, cfg.K, tokens=tok)
+    np.testing.assert_array_equal(sub["idx"], full["idx"][tok])
+    np.testing.assert_allclose(sub["out"], full["out"][tok], rtol=1e-12, atol=1e-14)
