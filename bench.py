@@ -1,0 +1,367 @@
+"""Benchmark of the DeepSeekMoE layer forward (+ balancing-bias update) on B300.
+
+One step = moe_forward (route -> dispatch -> gate/up grouped GEMM + SwiGLU ->
+down grouped GEMM -> combine) + moe_update_bias over one batch of synthetic
+tokens, on the V3-shaped prefill layer by default (T=8192, d=7168, 256 routed
+experts top-8 + 1 shared, intermediate 2048, bf16).
+
+    python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
+of the layer on its own batch (replicas, weak scaling); times are the max over
+ranks.  --impl reference times the CPU oracle on a bounded token sample of
+the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_inputs import get_config, make_inputs  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (256e top-8, T=8192, bf16) + grouped-GEMM % of tensor peak"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, ws, local
+    return None, 0, 1, 0
+
+
+def _max_over_ranks(dist, v: float, device) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist, device):
+    if dist is not None:
+        if device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def kernel_roofline(cfg, traces, peaks):
+    """Per-kernel algorithmic work / measured average launch time."""
+    T, d, E, K, S, I = cfg.T, cfg.d, cfg.E, cfg.K, cfg.S, cfg.I
+    R = T * K + S * T
+    es = 2
+    work = {
+        # flops
+        "gemm_gateup_swiglu": ("TFLOP/s", 2.0 * R * d * 2 * I),
+        "gemm_down": ("TFLOP/s", 2.0 * R * I * d),
+        # bytes: algorithmic traffic (inputs read once, outputs written once)
+        "gemm_router": ("GB/s", es * (T * d + E * d) + 4.0 * T * E),
+        "router_topk": ("GB/s", 4.0 * T * E + 8.0 * T * K),
+        "dispatch_scatter": ("GB/s", es * (T * d + T * K * d) + 4.0 * T * K),
+        "combine": ("GB/s", es * (R * d + 2 * T * d) + 8.0 * T * K),
+    }
+    out = {}
+    for name, launches, ms in traces:
+        if name in work and launches > 0:
+            unit, amount = work[name]
+            avg_s = ms / launches / 1e3
+            if unit == "TFLOP/s":
+                ach = amount / avg_s / 1e12
+                peak = peaks["bf16_tflops_sustained"]
+            else:
+                ach = amount / avg_s / 1e9
+                peak = peaks["hbm_gbs"]
+            out[name] = {"unit": unit, "achieved": round(ach, 2), "peak": peak,
+                         "frac": round(ach / peak, 4), "avg_ms": round(avg_s * 1e3, 4),
+                         "launches": launches}
+    return out
+
+
+def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7):
+    """Times the CPU oracle on n_tokens tokens of the workload (weights of the
+    experts those tokens use are copied to host first, untimed)."""
+    from oracle import moe_oracle as O
+    rng = np.random.default_rng(seed)
+    tok = np.sort(rng.choice(cfg.T, n_tokens, replace=False))
+    x_host = inp["x"][torch.as_tensor(tok, device=inp["x"].device)].cpu()
+    idx, _, _, _ = O.route(x_host, inp["centroids"].cpu(), inp["bias"].cpu(), cfg.K,
+                           cfg.score_func, cfg.normalize)
+    used = sorted(set(int(e) for e in idx.reshape(-1)))
+
+    class _Experts:
+        def __init__(self, src, ids):
+            self.shape = src.shape
+            self.d = {e: src[e].cpu() for e in ids}
+
+        def __getitem__(self, e):
+            return self.d[int(e)]
+
+    host = {"x": x_host, "centroids": inp["centroids"].cpu(), "bias": inp["bias"].cpu(),
+            "w13": _Experts(inp["w13"], used), "w2": _Experts(inp["w2"], used),
+            "ws13": inp["ws13"].cpu(), "ws2": inp["ws2"].cpu()}
+    t0 = time.perf_counter()
+    O.moe_layer(host, cfg.K, cfg.normalize, cfg.score_func, cfg.add_residual)
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count()
+    return n_tokens / dt, dt, cores
+
+
+def run_reference(args, cfg, dist, rank, ws, device):
+    """Reference arm: the CPU oracle timed on bounded token samples."""
+    if rank != 0:
+        return
+    inp = make_inputs(cfg, device if device.type == "cuda" else "cpu")
+    per_step = max(1, args.ref_tokens)
+    rates = []
+    cores = None
+    for i in range(args.warmup + args.steps):
+        r, dt, cores = cpu_oracle_tokens_per_s(cfg, inp, per_step, seed=100 + i)
+        if i >= args.warmup:
+            rates.append((per_step, dt))
+    tok = sum(t for t, _ in rates)
+    secs = sum(s for _, s in rates)
+    value = tok / secs
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / len(rates) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
+                       "S": cfg.S, "I": cfg.I, "sample_tokens_per_step": per_step},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"{per_step} random tokens of the {cfg.name} batch per "
+                                       f"step through the fp64 oracle"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="v3_prefill")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=8,
+                    help="tokens of the oracle CPU-baseline sample")
+    ap.add_argument("--ref-tokens", type=int, default=1,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    dist, rank, ws, local = _dist()
+    device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    if device.type == "cuda":
+        torch.cuda.set_device(device)
+    cfg = get_config(args.config)
+
+    if args.impl == "reference":
+        run_reference(args, cfg, dist, rank, ws, device)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import mixture_experts_layer_88_b300 as m
+    peaks = _peaks()
+    inp = make_inputs(cfg, device, seed=rank)
+    mc = m.cfg_from_layer(cfg)
+    layer = m.MoeLayer(mc, inp, device=device)
+    x = inp["x"]
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    # ---- device-resident timed region
+    for _ in range(args.warmup):
+        layer.step(x, out)
+    torch.cuda.synchronize()
+    assert m.get_status() == 0, "device error during warm-up"
+    m.trace_enable(True)
+    m.trace_read_all()
+    _barrier(dist, device)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            layer.step(x, out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    _barrier(dist, device)
+    traces = m.trace_read_all()
+    m.trace_enable(False)
+    st = m.get_status()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = _max_over_ranks(dist, ms, device)
+    ms_step = ms_max / args.steps
+    value = ws * cfg.T / (ms_step / 1e3)
+
+    # ---- end to end: pinned host tokens in, pinned host output back, every step
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(args.warmup):
+        layer.step_host(x_host, out_host, x_dev, out)
+    _barrier(dist, device)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.step_host(x_host, out_host, x_dev, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1), device) / args.steps
+    e2e_value = ws * cfg.T / (e2e_ms / 1e3)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    roof = kernel_roofline(cfg, traces, peaks)
+    top = roof.get("gemm_gateup_swiglu")
+    gemm_flops = cfg.gemm_flops()
+    gemm_ms = sum(t[2] for t in traces if t[0] in ("gemm_gateup_swiglu", "gemm_down"))
+    gemm_ms_step = gemm_ms / args.steps if gemm_ms else None
+    gemm_tflops = gemm_flops / (gemm_ms_step / 1e3) / 1e12 if gemm_ms_step else None
+    launches = sum(t[1] for t in traces)
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get(cfg.name, {}).get("gemm_gateup_swiglu")
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random tokens and random-init weights of the layer's shape)",
+        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
+                   "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
+                   "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
+                         if cfg.name.startswith("v3") else "inputs larger than L2"},
+        "grouped_gemm": {"tflops": round(gemm_tflops, 1) if gemm_tflops else None,
+                         "frac_of_peak": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4)
+                         if gemm_tflops else None,
+                         "peak_tflops": peaks["bf16_tflops_sustained"],
+                         "peak_kind": f"bf16 sustained, {peaks['source']}",
+                         "ms_per_step": round(gemm_ms_step, 4) if gemm_ms_step else None},
+        "roofline": ({"kernel": "gemm_gateup_swiglu", "bound": "tensor",
+                      "achieved": top["achieved"], "peak": top["peak"], "unit": "TFLOP/s",
+                      "frac": top["frac"], "traffic": traffic,
+                      "peak_kind": f"bf16 sustained, {peaks['source']}"} if top else None),
+        "kernels": roof,
+        "gpu_launches": launches,
+        "device_status": st,
+        "clocks": clk.summary(),
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "ms_per_step": round(e2e_ms, 4)},
+    }
+    if not args.no_cpu_baseline:
+        rate, secs, cores = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{args.cpu_tokens} random tokens of the {cfg.name} "
+                                          f"batch through the fp64 oracle ({secs:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

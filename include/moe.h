@@ -1,0 +1,219 @@
+/*
+ * moe.h - C ABI of the DeepSeekMoE layer forward for NVIDIA B300 (sm_103a).
+ *
+ * One DeepSeekMoE layer: a Sigmoid router with an auxiliary-loss-free
+ * balancing bias, hard top-K_r selection, renormalised gates, no-drop dispatch
+ * to fine-grained SwiGLU routed experts, always-on shared experts, a
+ * gate-weighted combine, and the per-batch load count / sign bias update.
+ *
+ * Sources ("DeepSeekMoE架构解析", the DeepSeek-V3 walk-through, is "V3";
+ * the course chapter "MoE" on blog.zero43.top is "course"):
+ *   V3 section 2.1, eqs. (13)-(15)   score, top-K, renormalisation
+ *   V3 section 2.2, eq. (16)         bias changes selection only
+ *   V3 section 2.2, update rule      b_i -/+ gamma for over/under-loaded experts
+ *   V3 section 3.1                   output = u + shared + gate-weighted routed
+ *   course section 4                 2024 variant: gates not renormalised
+ *   course sections 5, 6             bias applies to the next batch; no drops
+ *
+ * Conventions for every entry point
+ *   - All tensors are row-major, densely packed, in device memory, unless a
+ *     parameter says "host".  The caller allocates and owns every buffer; the
+ *     library allocates nothing on any call below.
+ *   - Floating tensors use cfg->act_dtype (tokens, activations, outputs) or
+ *     cfg->wgt_dtype (centroids, expert weights).  Supported pairs:
+ *     (MOE_F32, MOE_F32) and (MOE_BF16, MOE_BF16).  Bias, gates and load
+ *     statistics are always fp32; indices, counts, offsets are int32.
+ *   - For MOE_BF16, d and I must be multiples of 128 and every pointer must be
+ *     16-byte aligned.  Limits: 1 <= K <= min(E, 32), E <= 1024, S <= 64,
+ *     T*K + S*T < 2^31.  T == 0 is a valid empty batch (nothing is launched).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: argument errors are returned synchronously, launch errors
+ *     map to MOE_ERR_CUDA, and faults the kernels detect on the device
+ *     (a bounded wait that ran out) are read back with moe_get_status().
+ *   - `ws` is caller-owned scratch of at least moe_workspace_size(cfg, which)
+ *     bytes, 256-byte aligned; its contents on entry do not matter.
+ *   - Calls sharing a workspace must be ordered on one stream.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* bad shape, null or misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2,     /* valid but not built (dtype pair, device) */
+  MOE_ERR_WORKSPACE = 3,       /* ws too small */
+  MOE_ERR_CUDA = 4,            /* a CUDA runtime/launch error */
+  MOE_ERR_DEVICE_TIMEOUT = 5,  /* a device-side bounded wait ran out */
+  MOE_ERR_DEVICE_BOUNDS = 6    /* a device-side index check failed */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype_t;
+
+/* Expert score s_{i,t}.  SIGMOID: V3 eq. (15).  SOFTMAX: the earlier gating
+ * that V3 replaced (V3 section 2.1), used by the 2024 16B layer. */
+typedef enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_score_t;
+
+typedef struct {
+  int32_t T;            /* tokens in the batch */
+  int32_t d;            /* hidden size */
+  int32_t E;            /* routed experts */
+  int32_t K;            /* routed experts per token, K_r */
+  int32_t S;            /* shared experts (always active) */
+  int32_t I;            /* intermediate size of every expert (routed and shared) */
+  int32_t act_dtype;    /* moe_dtype_t of x, activations, outputs */
+  int32_t wgt_dtype;    /* moe_dtype_t of centroids and expert weights */
+  int32_t score_func;   /* moe_score_t */
+  int32_t normalize;    /* 1: g = g'/sum g' (V3 eq. 13); 0: g = s (course section 4) */
+  int32_t add_residual; /* 1: out = u + ... (V3 section 3.1); 0: MoE term only */
+  float gamma;          /* bias update speed, 0.001 in V3 section 2.2 */
+} moe_cfg_t;
+
+/* Which call a workspace is sized for. */
+typedef enum {
+  MOE_WS_ROUTE = 0,
+  MOE_WS_DISPATCH = 1,
+  MOE_WS_EXPERTS = 2,
+  MOE_WS_FORWARD = 3
+} moe_ws_kind_t;
+
+/* Bytes of scratch that `which` needs for this cfg (0 on an invalid cfg). */
+size_t moe_workspace_size(const moe_cfg_t* cfg, int32_t which);
+
+/* Check cfg alone (shape limits, dtype pair).  No CUDA calls. */
+moe_status_t moe_check_cfg(const moe_cfg_t* cfg);
+
+/*
+ * moe_route - router of V3 eqs. (15), (16), (14), (13).
+ *   x         [T, d]   act_dtype   tokens u_t
+ *   centroids [E, d]   wgt_dtype   expert centroids e_i
+ *   bias      [E]      fp32        balancing bias b_i (read only)
+ *   idx       [T, K]   int32  out  chosen experts, by descending s+b,
+ *                                  equal keys to the lower index
+ *   gates     [T, K]   fp32   out  g_{i,t}: s_i / sum of chosen s (normalize=1)
+ *                                  or s_i (normalize=0); never uses b
+ * Scores and keys are fp32; logits are accumulated in fp32.
+ */
+moe_status_t moe_route(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                       const float* bias, int32_t* idx, float* gates,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_dispatch - no-drop dispatch (course section 6): every (t, k) gets a row.
+ *   x         [T, d]       act_dtype   tokens
+ *   idx       [T, K]       int32       from moe_route
+ *   counts    [E]          int32  out  load count c_i = #{(t,k): idx = i}
+ *   offsets   [E+1]        int32  out  exclusive prefix sum of counts
+ *   xp        [T*K, d]     act_dtype out  rows of expert i at offsets[i] ..,
+ *                                  its tokens in ascending token order
+ *   perm_tok  [T*K]        int32  out  source token of each xp row
+ *   pos       [T, K]       int32  out  xp row of (t, k)
+ * Integer results are deterministic.  idx entries must lie in [0, E) and be
+ * distinct per token (as moe_route writes them).
+ */
+moe_status_t moe_dispatch(const moe_cfg_t* cfg, const void* x, const int32_t* idx,
+                          int32_t* counts, int32_t* offsets, void* xp,
+                          int32_t* perm_tok, int32_t* pos,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_experts - fine-grained SwiGLU experts (V3 section 1 and the section 3.1
+ * sketch): y = W2 (SiLU(Wg u) * (Wu u)) for each routed row of xp with its
+ * expert's weights, and for every token with each shared expert.
+ *   xp       [T*K, d]        act_dtype   dispatched rows (moe_dispatch)
+ *   x        [T, d]          act_dtype   tokens (input of the shared experts)
+ *   offsets  [E+1]           int32       from moe_dispatch
+ *   w13      [E, 2I, d]      wgt_dtype   rows 0..I-1 gate Wg, rows I..2I-1 up Wu
+ *   w2       [E, d, I]       wgt_dtype   down projection
+ *   ws13     [S, 2I, d], ws2 [S, d, I]   shared experts, same layout (may be
+ *                                        NULL when S == 0)
+ *   act      [T*K + S*T, I]  act_dtype out  SiLU(gate) * up, rounded to act_dtype
+ *   y        [T*K + S*T, d]  act_dtype out  rows 0..T*K-1: routed expert outputs in
+ *                                  xp order; row T*K + s*T + t: shared expert s on
+ *                                  token t
+ * Accumulation is fp32.
+ */
+moe_status_t moe_experts(const moe_cfg_t* cfg, const void* xp, const void* x,
+                         const int32_t* offsets, const void* w13, const void* w2,
+                         const void* ws13, const void* ws2, void* act, void* y,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_combine - V3 section 3.1: out_t = [u_t] + sum_s y_shared(s,t)
+ *               + sum_k g_{t,k} y[pos[t,k]], summed in fp32 in the order
+ *               k = 0..K-1, then shared s = 0..S-1, then the residual.
+ *   y      [T*K + S*T, d]  act_dtype   from moe_experts
+ *   gates  [T, K] fp32, pos [T, K] int32 (moe_route, moe_dispatch)
+ *   x      [T, d]          act_dtype   residual u (read only if add_residual)
+ *   out    [T, d]          act_dtype out
+ */
+moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y, const float* gates,
+                         const int32_t* pos, const void* x, void* out, void* stream);
+
+/*
+ * moe_update_bias - V3 section 2.2 update rule, applied after the batch and
+ * used by the next one (course section 5):
+ *   counts[i] * E > T*K  ->  bias[i] -= gamma   (overloaded)
+ *   counts[i] * E < T*K  ->  bias[i] += gamma   (underloaded)
+ *   equal                ->  unchanged
+ * Integer comparison, fp32 add (round to nearest even).
+ *   counts     [E] int32        load counts of this batch
+ *   bias       [E] fp32 in/out  updated in place
+ *   load_stats [2] fp32 out     {max c_i / mean, min c_i / mean}, or NULL
+ */
+moe_status_t moe_update_bias(const moe_cfg_t* cfg, const int32_t* counts, float* bias,
+                             float* load_stats, void* stream);
+
+/*
+ * moe_forward - the whole layer: moe_route -> moe_dispatch -> moe_experts ->
+ * moe_combine on one stream with no host synchronisation.  Dispatched rows,
+ * activations and expert outputs live in ws (MOE_WS_FORWARD).  The bias is
+ * read, not updated: call moe_update_bias(counts) afterwards to apply the
+ * balancing step for the next batch.
+ *   x [T,d], centroids [E,d], bias [E], w13, w2, ws13, ws2 as above;
+ *   idx [T,K] int32 out, gates [T,K] fp32 out, counts [E] int32 out,
+ *   out [T,d] act_dtype out.
+ */
+moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                         const float* bias, const void* w13, const void* w2,
+                         const void* ws13, const void* ws2, int32_t* idx,
+                         float* gates, int32_t* counts, void* out,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then returns and clears this device's error word
+ * (MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS) or MOE_ERR_CUDA. */
+moe_status_t moe_get_status(void* stream);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status_t st);
+
+/*
+ * Kernel timing (tracing).  While enabled, every kernel the calls above
+ * launch is bracketed by CUDA events on its own stream, and its name, launch
+ * count and summed device time are kept per calling thread.  Events come from
+ * a pool created on first use; no device memory is allocated.
+ */
+typedef struct {
+  char name[48];
+  int32_t launches;
+  float total_ms;
+} moe_kernel_time_t;
+
+moe_status_t moe_trace_enable(int32_t on);
+/* Synchronises the traced events, writes up to `max` entries, sets *n to the
+ * number of distinct kernels, and clears the record. */
+moe_status_t moe_trace_read(moe_kernel_time_t* out, int32_t max, int32_t* n);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,188 @@
+"""ctypes binding of libmoe.so: argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module turns
+torch tensors into device pointers and the current torch stream into a
+cudaStream_t.  If the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
+MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
+MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_EXPERTS, MOE_WS_FORWARD = 0, 1, 2, 3
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
+          6: "MOE_ERR_DEVICE_BOUNDS"}
+
+# every symbol include/moe.h declares
+SYMBOLS = ["moe_workspace_size", "moe_check_cfg", "moe_route", "moe_dispatch", "moe_experts",
+           "moe_combine", "moe_update_bias", "moe_forward", "moe_get_status",
+           "moe_status_string", "moe_trace_enable", "moe_trace_read", "moe_version"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+class MoeCfg(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("S", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32), ("wgt_dtype", ctypes.c_int32),
+                ("score_func", ctypes.c_int32), ("normalize", ctypes.c_int32),
+                ("add_residual", ctypes.c_int32), ("gamma", ctypes.c_float)]
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32),
+                ("total_ms", ctypes.c_float)]
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libmoe.so not built at {path}; run "
+                          "`python -m mixture_experts_layer_88_b300.build`")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    cfgp = ctypes.POINTER(MoeCfg)
+    sig = {
+        "moe_workspace_size": (SZ, [cfgp, I32]),
+        "moe_check_cfg": (I32, [cfgp]),
+        "moe_route": (I32, [cfgp, P, P, P, P, P, P, SZ, P]),
+        "moe_dispatch": (I32, [cfgp, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_experts": (I32, [cfgp, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_combine": (I32, [cfgp, P, P, P, P, P, P]),
+        "moe_update_bias": (I32, [cfgp, P, P, P, P]),
+        "moe_forward": (I32, [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_get_status": (I32, [P]),
+        "moe_status_string": (ctypes.c_char_p, [I32]),
+        "moe_trace_enable": (I32, [I32]),
+        "moe_trace_read": (I32, [ctypes.POINTER(KernelTime), I32, ctypes.POINTER(I32)]),
+        "moe_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_LIB = load_library()   # fails loudly at import when the library is missing
+
+
+def lib() -> ctypes.CDLL:
+    return _LIB
+
+
+# ----------------------------------------------------------------------------
+
+_DT = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16}
+
+
+def make_cfg(T, d, E, K, S, I, dtype=MOE_BF16, score_func=MOE_SCORE_SIGMOID, normalize=1,
+             add_residual=1, gamma=1e-3) -> MoeCfg:
+    return MoeCfg(T, d, E, K, S, I, dtype, dtype, score_func, normalize, add_residual, gamma)
+
+
+def cfg_from_layer(layer_cfg, T=None) -> MoeCfg:
+    """MoeCfg from a moe_inputs.LayerCfg-like object (shape fields only)."""
+    dt = {"f32": MOE_F32, "bf16": MOE_BF16, "e4m3": MOE_E4M3}
+    c = layer_cfg
+    return MoeCfg(c.T if T is None else T, c.d, c.E, c.K, c.S, c.I, dt[c.act], dt[c.wgt],
+                  c.score_func, c.normalize, c.add_residual, c.gamma)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(code, where):
+    if code != 0:
+        raise MoeError(code, where)
+
+
+def workspace_size(cfg: MoeCfg, which: int) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(cfg), which))
+
+
+def check_cfg(cfg: MoeCfg) -> int:
+    return int(lib().moe_check_cfg(ctypes.byref(cfg)))
+
+
+def alloc_workspace(cfg: MoeCfg, which: int, device="cuda") -> torch.Tensor:
+    n = max(256, workspace_size(cfg, which))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def route(cfg, x, centroids, bias, idx, gates, ws, stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(centroids), _p(bias), _p(idx),
+                           _p(gates), _p(ws), ws.numel(), _stream(stream)), "moe_route")
+
+
+def dispatch(cfg, x, idx, counts, offsets, xp, perm_tok, pos, ws, stream=None):
+    _check(lib().moe_dispatch(ctypes.byref(cfg), _p(x), _p(idx), _p(counts), _p(offsets),
+                              _p(xp), _p(perm_tok), _p(pos), _p(ws), ws.numel(),
+                              _stream(stream)), "moe_dispatch")
+
+
+def experts(cfg, xp, x, offsets, w13, w2, ws13, ws2, act, y, ws, stream=None):
+    _check(lib().moe_experts(ctypes.byref(cfg), _p(xp), _p(x), _p(offsets), _p(w13), _p(w2),
+                             _p(ws13), _p(ws2), _p(act), _p(y), _p(ws), ws.numel(),
+                             _stream(stream)), "moe_experts")
+
+
+def combine(cfg, y, gates, pos, x, out, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _p(y), _p(gates), _p(pos), _p(x), _p(out),
+                             _stream(stream)), "moe_combine")
+
+
+def update_bias(cfg, counts, bias, load_stats=None, stream=None):
+    _check(lib().moe_update_bias(ctypes.byref(cfg), _p(counts), _p(bias), _p(load_stats),
+                                 _stream(stream)), "moe_update_bias")
+
+
+def forward(cfg, x, centroids, bias, w13, w2, ws13, ws2, idx, gates, counts, out, ws,
+            stream=None):
+    _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(centroids), _p(bias), _p(w13),
+                             _p(w2), _p(ws13), _p(ws2), _p(idx), _p(gates), _p(counts),
+                             _p(out), _p(ws), ws.numel(), _stream(stream)), "moe_forward")
+
+
+def get_status(stream=None) -> int:
+    return int(lib().moe_get_status(_stream(stream)))
+
+
+def trace_enable(on: bool):
+    lib().moe_trace_enable(1 if on else 0)
+
+
+def trace_read_all(max_kernels: int = 64) -> list:
+    """[(name, launches, total_ms)] of every traced kernel since the last read."""
+    arr = (KernelTime * max_kernels)()
+    n = ctypes.c_int32(0)
+    _check(lib().moe_trace_read(arr, max_kernels, ctypes.byref(n)), "moe_trace_read")
+    return [(arr[i].name.decode(), int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(min(n.value, max_kernels))]
+
+
+def version() -> str:
+    return lib().moe_version().decode()

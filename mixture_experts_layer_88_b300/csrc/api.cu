@@ -1,0 +1,492 @@
+// C ABI of the DeepSeekMoE layer library: argument checks, workspace layout,
+// tensor maps, launch sequencing, device error word and kernel tracing.
+#include <cuda.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "kernels.cuh"
+
+// Device error word, one per device (module-scope variable).
+__device__ unsigned g_moe_status_word;
+
+namespace moe {
+
+unsigned* device_status_word() {
+  static unsigned* cached[64] = {nullptr};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cached[dev]) return cached[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_moe_status_word) != cudaSuccess) return nullptr;
+  if (dev < 64) cached[dev] = static_cast<unsigned*>(p);
+  return static_cast<unsigned*>(p);
+}
+
+// ---------------------------------------------------------------- tracing
+namespace {
+struct TraceRec {
+  const char* name;
+  cudaEvent_t ev0, ev1;
+};
+struct TraceState {
+  bool on = false;
+  std::vector<TraceRec> recs;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+thread_local TraceState g_trace;
+}  // namespace
+
+void trace_begin(cudaStream_t s, const char* name) {
+  if (!g_trace.on) return;
+  TraceRec r{name, g_trace.get(), g_trace.get()};
+  cudaEventRecord(r.ev0, s);
+  g_trace.recs.push_back(r);
+}
+void trace_end(cudaStream_t s) {
+  if (!g_trace.on || g_trace.recs.empty()) return;
+  cudaEventRecord(g_trace.recs.back().ev1, s);
+}
+
+// ---------------------------------------------------------------- plans
+namespace {
+
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per barrier wait
+constexpr int kRouterTargetCtas = 148;
+
+size_t esize(int dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+struct RouterPlan {
+  int bs, nb, eb, k_blocks, splits, kps;
+};
+
+RouterPlan router_plan(const moe_cfg_t& c) {
+  RouterPlan p{};
+  token_blocks(c.T, &p.bs, &p.nb);
+  p.eb = ceil_div(c.E, 256);
+  p.k_blocks = c.d / 64;
+  const int base = p.nb * p.eb > 0 ? p.nb * p.eb : 1;
+  int s = ceil_div(kRouterTargetCtas, base);
+  s = s < 1 ? 1 : s;
+  s = s > 16 ? 16 : s;
+  s = s > p.k_blocks ? p.k_blocks : s;
+  p.kps = ceil_div(p.k_blocks, s);
+  p.splits = ceil_div(p.k_blocks, p.kps);
+  return p;
+}
+
+size_t route_ws(const moe_cfg_t& c) {
+  if (c.act_dtype == MOE_BF16) {
+    const RouterPlan p = router_plan(c);
+    return align_up(static_cast<size_t>(p.splits) * c.T * c.E * sizeof(float), 256);
+  }
+  return align_up(static_cast<size_t>(c.T) * c.E * sizeof(float), 256);
+}
+size_t dispatch_ws(const moe_cfg_t& c) {
+  return align_up(static_cast<size_t>(ceil_div(c.T, kDispatchChunk)) * c.E * sizeof(int32_t) + 4,
+                  256);
+}
+size_t experts_ws(const moe_cfg_t& c) {
+  const size_t G = static_cast<size_t>(c.E) + c.S;
+  return align_up(5 * (G + 1) * sizeof(int32_t), 256);
+}
+
+struct ForwardLayout {
+  size_t route, dispatch, experts, offsets, perm, pos, xp, act, y, total;
+};
+
+ForwardLayout forward_layout(const moe_cfg_t& c) {
+  ForwardLayout L{};
+  const size_t es = esize(c.act_dtype);
+  const size_t TK = static_cast<size_t>(c.T) * c.K;
+  const size_t R = TK + static_cast<size_t>(c.S) * c.T;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes, 256);
+    return o;
+  };
+  L.route = take(route_ws(c));
+  L.dispatch = take(dispatch_ws(c));
+  L.experts = take(experts_ws(c));
+  L.offsets = take((c.E + 1) * sizeof(int32_t));
+  L.perm = take(TK * sizeof(int32_t));
+  L.pos = take(TK * sizeof(int32_t));
+  L.xp = take(TK * c.d * es);
+  L.act = take(R * c.I * es);
+  L.y = take(R * c.d * es);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_ptrs(const moe_cfg_t& c, std::initializer_list<const void*> dtype_ptrs,
+                        std::initializer_list<const void*> other_ptrs) {
+  for (const void* p : dtype_ptrs) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if (c.act_dtype == MOE_BF16 && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  for (const void* p : other_ptrs)
+    if (!p) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return MOE_OK;
+  if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename P>
+P* at(void* base, size_t off) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(base) + off);
+}
+
+// ---------------------------------------------------------------- step bodies (no checks)
+
+moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
+                      const float* bias, int32_t* idx, float* gates, void* ws,
+                      cudaStream_t st) {
+  if (c.act_dtype == MOE_BF16) {
+    const RouterPlan p = router_plan(c);
+    float* partial = static_cast<float*>(ws);
+    CUtensorMap maps[4];
+    if (!make_tmap_bf16(&maps[0], centroids, c.E, c.d, 128) ||
+        !make_tmap_bf16(&maps[2], x, c.T, c.d, 16))
+      return MOE_ERR_CUDA;
+    maps[1] = maps[0];
+    maps[3] = maps[2];
+    GemmArgs a{};
+    a.G = 1;
+    a.E = 1;
+    a.m_blocks = p.eb;
+    a.a_rows_per_group = 0;
+    a.a1_off = 128;
+    a.k_blocks = p.k_blocks;
+    a.k_splits = p.splits;
+    a.k_per_split = p.kps;
+    a.router_T = c.T;
+    a.router_bs = p.bs;
+    a.router_nb = p.nb;
+    a.out_ld = c.E;
+    a.out_cols = c.E;
+    a.out_split_stride = static_cast<long long>(c.T) * c.E;
+    a.out = partial;
+    a.status = device_status_word();
+    a.timeout_ns = kWaitTimeoutNs;
+    const int tiles = p.nb * p.eb * p.splits;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    moe_status_t s = launch_gemm_tc(GM_ROUTER, maps, a, grid, st);
+    if (s != MOE_OK) return s;
+    return launch_topk(partial, p.splits, a.out_split_stride, bias, c.T, c.E, c.K, c.score_func,
+                       c.normalize, idx, gates, st);
+  }
+  float* logits = static_cast<float*>(ws);
+  moe_status_t s = launch_logits_f32(static_cast<const float*>(x),
+                                     static_cast<const float*>(centroids), c.T, c.d, c.E, logits,
+                                     st);
+  if (s != MOE_OK) return s;
+  return launch_topk(logits, 1, 0, bias, c.T, c.E, c.K, c.score_func, c.normalize, idx, gates,
+                     st);
+}
+
+moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
+                        const int32_t* offsets, const void* w13, const void* w2,
+                        const void* ws13, const void* ws2, void* act, void* y, void* ws,
+                        cudaStream_t st) {
+  if (c.act_dtype != MOE_BF16) {
+    return launch_experts_f32(static_cast<const float*>(xp), static_cast<const float*>(x),
+                              offsets, static_cast<const float*>(w13),
+                              static_cast<const float*>(w2), static_cast<const float*>(ws13),
+                              static_cast<const float*>(ws2), static_cast<float*>(act),
+                              static_cast<float*>(y), c.T, c.K, c.E, c.S, c.d, c.I, st);
+  }
+  const int G = c.E + c.S;
+  int32_t* tab = static_cast<int32_t*>(ws);
+  int32_t* rows = tab;
+  int32_t* brow = rows + (G + 1);
+  int32_t* orow = brow + (G + 1);
+  int32_t* bs = orow + (G + 1);
+  int32_t* bstart = bs + (G + 1);
+  moe_status_t s = launch_build_groups(offsets, c.T, c.K, c.E, c.S, rows, brow, orow, bs, bstart,
+                                       st);
+  if (s != MOE_OK) return s;
+  const long long TK = static_cast<long long>(c.T) * c.K;
+  const long long R = TK + static_cast<long long>(c.S) * c.T;
+  const int grid = num_sms();
+
+  // gate/up + SwiGLU: A = W13 rows, B = dispatched rows (routed) or tokens (shared)
+  CUtensorMap m1[4];
+  if (!make_tmap_bf16(&m1[0], w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.d, 128) ||
+      !make_tmap_bf16(&m1[2], xp, TK, c.d, 16) || !make_tmap_bf16(&m1[3], x, c.T, c.d, 16))
+    return MOE_ERR_CUDA;
+  if (c.S > 0) {
+    if (!make_tmap_bf16(&m1[1], ws13, static_cast<uint64_t>(c.S) * 2 * c.I, c.d, 128))
+      return MOE_ERR_CUDA;
+  } else {
+    m1[1] = m1[0];
+  }
+  GemmArgs a{};
+  a.gt = GroupTable{rows, brow, orow, bs, bstart};
+  a.G = G;
+  a.E = c.E;
+  a.m_blocks = c.I / 128;
+  a.a_rows_per_group = 2 * c.I;
+  a.a1_off = c.I;
+  a.k_blocks = c.d / 64;
+  a.k_splits = 1;
+  a.k_per_split = a.k_blocks;
+  a.out_ld = c.I;
+  a.out_cols = c.I;
+  a.out = act;
+  a.status = device_status_word();
+  a.timeout_ns = kWaitTimeoutNs;
+  s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st);
+  if (s != MOE_OK) return s;
+
+  // down: A = W2 rows (two 128-row boxes), B = activations
+  CUtensorMap m2[4];
+  if (!make_tmap_bf16(&m2[0], w2, static_cast<uint64_t>(c.E) * c.d, c.I, 128) ||
+      !make_tmap_bf16(&m2[2], act, R, c.I, 16))
+    return MOE_ERR_CUDA;
+  if (c.S > 0) {
+    if (!make_tmap_bf16(&m2[1], ws2, static_cast<uint64_t>(c.S) * c.d, c.I, 128))
+      return MOE_ERR_CUDA;
+  } else {
+    m2[1] = m2[0];
+  }
+  m2[3] = m2[2];
+  GemmArgs b = a;
+  b.gt = GroupTable{rows, orow, orow, bs, bstart};
+  b.m_blocks = ceil_div(c.d, 256);
+  b.a_rows_per_group = c.d;
+  b.a1_off = 128;
+  b.k_blocks = c.I / 64;
+  b.k_per_split = b.k_blocks;
+  b.out_ld = c.d;
+  b.out_cols = c.d;
+  b.out = y;
+  return launch_gemm_tc(GM_DOWN, m2, b, grid, st);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_check_cfg(const moe_cfg_t* cfg) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  const moe_cfg_t& c = *cfg;
+  if (c.T < 0 || c.d < 1 || c.E < 1 || c.E > kMaxE || c.K < 1 || c.K > kMaxK || c.K > c.E ||
+      c.S < 0 || c.S > kMaxS || c.I < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c.score_func != MOE_SCORE_SIGMOID && c.score_func != MOE_SCORE_SOFTMAX)
+    return MOE_ERR_INVALID_ARG;
+  if ((c.normalize != 0 && c.normalize != 1) || (c.add_residual != 0 && c.add_residual != 1))
+    return MOE_ERR_INVALID_ARG;
+  if (c.act_dtype < MOE_F32 || c.act_dtype > MOE_E4M3 || c.wgt_dtype < MOE_F32 ||
+      c.wgt_dtype > MOE_E4M3)
+    return MOE_ERR_INVALID_ARG;
+  if (c.act_dtype != c.wgt_dtype || c.act_dtype == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(c.T) * c.K + static_cast<long long>(c.S) * c.T;
+  if (rows >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  if (c.act_dtype == MOE_BF16 && (c.d % 128 != 0 || c.I % 128 != 0)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+size_t moe_workspace_size(const moe_cfg_t* cfg, int32_t which) {
+  if (moe_check_cfg(cfg) != MOE_OK) return 0;
+  const moe_cfg_t& c = *cfg;
+  switch (which) {
+    case MOE_WS_ROUTE: return route_ws(c);
+    case MOE_WS_DISPATCH: return dispatch_ws(c);
+    case MOE_WS_EXPERTS: return experts_ws(c);
+    case MOE_WS_FORWARD: return forward_layout(c).total;
+    default: return 0;
+  }
+}
+
+moe_status_t moe_route(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                       const float* bias, int32_t* idx, float* gates, void* ws, size_t ws_bytes,
+                       void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (c.T == 0) return MOE_OK;
+  if ((s = check_ptrs(c, {x, centroids}, {bias, idx, gates})) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, route_ws(c))) != MOE_OK) return s;
+  return do_route(c, x, centroids, bias, idx, gates, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_dispatch(const moe_cfg_t* cfg, const void* x, const int32_t* idx,
+                          int32_t* counts, int32_t* offsets, void* xp, int32_t* perm_tok,
+                          int32_t* pos, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0) {
+    if ((s = check_ptrs(c, {x, xp}, {idx, perm_tok, pos})) != MOE_OK) return s;
+  }
+  if ((s = check_ws(ws, ws_bytes, dispatch_ws(c))) != MOE_OK) return s;
+  return launch_dispatch(x, static_cast<size_t>(c.d) * esize(c.act_dtype), idx, c.T, c.K, c.E,
+                         counts, offsets, xp, perm_tok, pos, static_cast<int32_t*>(ws),
+                         static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_experts(const moe_cfg_t* cfg, const void* xp, const void* x,
+                         const int32_t* offsets, const void* w13, const void* w2,
+                         const void* ws13, const void* ws2, void* act, void* y, void* ws,
+                         size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (c.T == 0) return MOE_OK;
+  if ((s = check_ptrs(c, {xp, x, w13, w2, act, y}, {offsets})) != MOE_OK) return s;
+  if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, experts_ws(c))) != MOE_OK) return s;
+  return do_experts(c, xp, x, offsets, w13, w2, ws13, ws2, act, y, ws,
+                    static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y, const float* gates,
+                         const int32_t* pos, const void* x, void* out, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (c.T == 0) return MOE_OK;
+  if ((s = check_ptrs(c, {y, out}, {gates, pos})) != MOE_OK) return s;
+  if (c.add_residual && (s = check_ptrs(c, {x}, {})) != MOE_OK) return s;
+  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d, c.add_residual,
+                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_update_bias(const moe_cfg_t* cfg, const int32_t* counts, float* bias,
+                             float* load_stats, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!counts || !bias) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;  // no load observed: nothing to balance
+  return launch_update_bias(counts, bias, load_stats, c.E, c.T, c.K, c.gamma,
+                            static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                         const float* bias, const void* w13, const void* w2, const void* ws13,
+                         const void* ws2, int32_t* idx, float* gates, int32_t* counts, void* out,
+                         void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!counts) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) {
+    TraceScope tr(st, "forward_empty");
+    cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
+    return launch_status();
+  }
+  if ((s = check_ptrs(c, {x, centroids, w13, w2, out}, {bias, idx, gates})) != MOE_OK) return s;
+  if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
+  const ForwardLayout L = forward_layout(c);
+  if ((s = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return s;
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  void* xp = at<void>(ws, L.xp);
+  void* act = at<void>(ws, L.act);
+  void* y = at<void>(ws, L.y);
+  if ((s = do_route(c, x, centroids, bias, idx, gates, at<void>(ws, L.route), st)) != MOE_OK)
+    return s;
+  if ((s = launch_dispatch(x, static_cast<size_t>(c.d) * esize(c.act_dtype), idx, c.T, c.K, c.E,
+                           counts, offsets, xp, perm, pos, at<int32_t>(ws, L.dispatch), st)) !=
+      MOE_OK)
+    return s;
+  if ((s = do_experts(c, xp, x, offsets, w13, w2, ws13, ws2, act, y, at<void>(ws, L.experts),
+                      st)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d, c.add_residual,
+                        st);
+}
+
+moe_status_t moe_get_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_moe_status_word, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_moe_status_word, &zero, sizeof(zero)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (v & ERRBIT_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+  if (v & ERRBIT_BOUNDS) return MOE_ERR_DEVICE_BOUNDS;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "device index out of bounds";
+    default: return "unknown status";
+  }
+}
+
+moe_status_t moe_trace_enable(int32_t on) {
+  g_trace.on = on != 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_trace_read(moe_kernel_time_t* out, int32_t max, int32_t* n) {
+  std::vector<moe_kernel_time_t> agg;
+  moe_status_t st = MOE_OK;
+  for (TraceRec& r : g_trace.recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.ev1) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, r.ev0, r.ev1) != cudaSuccess)
+      st = MOE_ERR_CUDA;
+    size_t i = 0;
+    for (; i < agg.size(); ++i)
+      if (strncmp(agg[i].name, r.name, sizeof(agg[i].name)) == 0) break;
+    if (i == agg.size()) {
+      moe_kernel_time_t k{};
+      strncpy(k.name, r.name, sizeof(k.name) - 1);
+      agg.push_back(k);
+    }
+    agg[i].launches += 1;
+    agg[i].total_ms += ms;
+    g_trace.pool.push_back(r.ev0);
+    g_trace.pool.push_back(r.ev1);
+  }
+  g_trace.recs.clear();
+  if (n) *n = static_cast<int32_t>(agg.size());
+  if (out)
+    for (int32_t i = 0; i < max && i < static_cast<int32_t>(agg.size()); ++i) out[i] = agg[i];
+  return st;
+}
+
+const char* moe_version(void) { return "moe-b300 0.1 (sm_103a)"; }
+
+}  // extern "C"

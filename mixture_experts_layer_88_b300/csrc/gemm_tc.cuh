@@ -1,0 +1,69 @@
+// Host-side interface of the tcgen05 grouped GEMM (internal).
+#pragma once
+
+#include <cuda.h>
+#include "common.cuh"
+
+namespace moe {
+
+enum GemmMode : int { GM_GATEUP = 0, GM_DOWN = 1, GM_ROUTER = 2 };
+
+// Per-group table on the device (G groups; bstart has G+1 entries).
+struct GroupTable {
+  const int* rows;    // tokens of the group
+  const int* brow;    // first row of the group in the B (token) source
+  const int* orow;    // first output row of the group
+  const int* bs;      // token-block size of the group (multiple of 16, <= 256)
+  const int* bstart;  // exclusive prefix of token blocks per group
+};
+
+struct GemmArgs {
+  GroupTable gt;
+  int G;                     // groups (grouped modes)
+  int E;                     // groups g < E read A/B map 0, others map 1
+  int m_blocks;              // weight-row blocks per group
+  int a_rows_per_group;      // rows of A per group (2I or d; 0 in router mode)
+  int a1_off;                // row offset of the second A box
+  int k_blocks;              // K / 64
+  int k_splits;              // router mode: K splits (1 otherwise)
+  int k_per_split;           // k-blocks per split
+  int router_T;              // router mode: tokens
+  int router_bs;             // router mode: token-block size
+  int router_nb;             // router mode: token blocks
+  int out_ld;                // output leading dimension (elements)
+  int out_cols;              // valid output columns
+  long long out_split_stride;  // router mode: elements between split partials
+  void* out;
+  unsigned* status;
+  unsigned long long timeout_ns;  // bound of every barrier wait
+};
+
+// Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of
+// {64 columns, box_rows rows} with 128-byte swizzle.  False on failure.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
+// Launches the persistent grouped GEMM.  maps = {A0, A1, B0, B1}.
+moe_status_t launch_gemm_tc(int mode, const CUtensorMap* maps, const GemmArgs& args,
+                            int grid, cudaStream_t stream);
+
+// Builds the group table of the expert GEMMs from the dispatch offsets:
+// groups 0..E-1 are routed experts (rows = counts), E..E+S-1 the shared
+// experts (rows = T).  Writes rows, brow (gate/up source row), orow, bs, bstart.
+moe_status_t launch_build_groups(const int* offsets, int T, int K, int E, int S, int* rows,
+                                 int* brow_gu, int* orow, int* bs, int* bstart,
+                                 cudaStream_t stream);
+
+int num_sms();
+
+// Token-block size and count for `rows` tokens: blocks of at most 256 tokens,
+// balanced, each a multiple of 16.
+__host__ __device__ inline void token_blocks(int rows, int* bs, int* nb) {
+  if (rows <= 0) { *bs = 16; *nb = 0; return; }
+  int n0 = (rows + 255) / 256;
+  int b = ((rows + n0 - 1) / n0 + 15) / 16 * 16;
+  *bs = b;
+  *nb = (rows + b - 1) / b;
+}
+
+}  // namespace moe

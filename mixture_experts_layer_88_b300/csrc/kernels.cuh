@@ -1,0 +1,37 @@
+// Launchers of the SIMT kernels (router top-K, dispatch, combine, bias update,
+// fp32 expert GEMMs).  Internal.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kDispatchChunk = 256;   // tokens per count/rank CTA (8 warps x 32)
+
+moe_status_t launch_topk(const float* logits, int splits, long long split_stride,
+                         const float* bias, int T, int E, int K, int score_func, int normalize,
+                         int32_t* idx, float* gates, cudaStream_t stream);
+moe_status_t launch_logits_f32(const float* x, const float* c, int T, int d, int E, float* out,
+                               cudaStream_t stream);
+
+// hist: [ceil(T/256), E] int32 scratch
+moe_status_t launch_dispatch(const void* x, size_t row_bytes, const int32_t* idx, int T, int K,
+                             int E, int32_t* counts, int32_t* offsets, void* xp,
+                             int32_t* perm_tok, int32_t* pos, int32_t* hist,
+                             cudaStream_t stream);
+
+moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, const int32_t* pos,
+                            const void* x, void* out, int T, int K, int S, int d,
+                            int add_residual, cudaStream_t stream);
+
+moe_status_t launch_update_bias(const int32_t* counts, float* bias, float* stats, int E, int T,
+                                int K, float gamma, cudaStream_t stream);
+
+// fp32 expert FFNs over the group table (rows of the routed groups in xp,
+// shared groups read x).  act [R, I], y [R, d], R = T*K + S*T.
+moe_status_t launch_experts_f32(const float* xp, const float* x, const int32_t* offsets,
+                                const float* w13, const float* w2, const float* ws13,
+                                const float* ws2, float* act, float* y, int T, int K, int E,
+                                int S, int d, int I, cudaStream_t stream);
+
+}  // namespace moe

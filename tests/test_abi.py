@@ -1,0 +1,95 @@
+"""The C-ABI library loads, exports every symbol include/moe.h declares, and its
+host-side argument checks behave.  CPU only: no call here launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+m = pytest.importorskip("mixture_experts_layer_88_b300")
+L = m._lib
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", txt)))
+
+
+def test_header_symbols_exported():
+    syms = declared_symbols()
+    assert len(syms) >= 13
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), s
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r" T (moe_\w+)", out))
+    assert set(syms) <= exported
+    assert set(L.SYMBOLS) == set(syms)
+
+
+def test_version_and_status_strings():
+    assert "sm_103a" in m.version()
+    for code in range(7):
+        assert L.lib().moe_status_string(code)
+
+
+def _cfg(**kw):
+    base = dict(T=64, d=256, E=16, K=4, S=1, I=128)
+    base.update({k: v for k, v in kw.items() if k in base})
+    c = m.make_cfg(**base)
+    for k, v in kw.items():
+        if k not in base:
+            setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), 0),
+    (dict(K=0), 1), (dict(K=17, E=16), 1), (dict(K=33, E=64), 1), (dict(E=1025), 1),
+    (dict(S=65), 1), (dict(T=-1), 1), (dict(d=0), 1), (dict(I=0), 1),
+    (dict(d=192), 1),                       # bf16 needs d % 128 == 0
+    (dict(I=96), 1),                        # bf16 needs I % 128 == 0
+    (dict(score_func=2), 1), (dict(normalize=2), 1),
+    (dict(act_dtype=0, wgt_dtype=1), 2),    # mixed pair not built
+    (dict(act_dtype=2, wgt_dtype=2), 2),    # fp8 not built yet
+    (dict(act_dtype=0, wgt_dtype=0, d=96, I=40), 0),   # fp32 takes any d, I
+    (dict(T=0), 0),
+])
+def test_check_cfg(kw, code):
+    assert m.check_cfg(_cfg(**kw)) == code
+
+
+def test_workspace_sizes():
+    c = m.make_cfg(8192, 7168, 256, 8, 1, 2048)
+    f = m.workspace_size(c, m.MOE_WS_FORWARD)
+    # forward scratch holds xp [T*K, d], act [R, I], y [R, d] in bf16
+    R = 8192 * 8 + 8192
+    assert f >= 2 * (8192 * 8 * 7168 + R * 2048 + R * 7168)
+    for w in (m.MOE_WS_ROUTE, m.MOE_WS_DISPATCH, m.MOE_WS_EXPERTS):
+        assert 0 < m.workspace_size(c, w) < f
+    assert m.workspace_size(_cfg(K=0), m.MOE_WS_FORWARD) == 0
+
+
+def test_argument_errors_return_before_any_launch():
+    c = _cfg()
+    lib = L.lib()
+    P = None
+    # null pointers -> MOE_ERR_INVALID_ARG, synchronously, without touching CUDA
+    assert lib.moe_route(ctypes.byref(c), P, P, P, P, P, P, 0, P) == 1
+    assert lib.moe_combine(ctypes.byref(c), P, P, P, P, P, P) == 1
+    assert lib.moe_update_bias(ctypes.byref(c), P, P, P, P) == 1
+    # misaligned bf16 pointer
+    assert lib.moe_route(ctypes.byref(c), 8, 16, 16, 16, 16, P, 0, P) == 1
+    # workspace too small
+    assert lib.moe_route(ctypes.byref(c), 16, 16, 16, 16, 16, 256, 4, P) == 3
+    # empty batch is valid and launches nothing
+    c0 = _cfg(T=0)
+    assert lib.moe_route(ctypes.byref(c0), P, P, P, P, P, P, 0, P) == 0
+    assert lib.moe_combine(ctypes.byref(c0), P, P, P, P, P, P) == 0
+    assert lib.moe_experts(ctypes.byref(c0), P, P, P, P, P, P, P, P, P, P, 0, P) == 0

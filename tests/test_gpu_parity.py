@@ -1,0 +1,331 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing: expert indices bit-exact and gates within 1e-5, except tokens whose
+K-th vs (K+1)-th biased-key margin is below 1e-5 (excluded and counted).
+Dispatch: counts, offsets, perm_tok, pos bit-exact on the same indices;
+dispatched rows byte-equal to their token rows.  Layer outputs: relative
+Frobenius and max-abs error of the MoE term within the dtype's bar."""
+import numpy as np
+import pytest
+import torch
+
+from moe_inputs import small_cases, get_config, make_inputs
+from oracle import moe_oracle as O
+from tests._util import (GpuRun, gpu_inputs, assert_close, to_np, GATE_ATOL, MARGIN_EXCLUDE,
+                         rel_frob)
+
+pytestmark = pytest.mark.gpu
+
+m = pytest.importorskip("mixture_experts_layer_88_b300")
+
+SMALL = list(small_cases().keys())
+FULL = ["v3_decode", "v3_prefill", "dsmoe16b"]
+
+
+def _cfg(name):
+    return small_cases()[name] if name in small_cases() else get_config(name)
+
+
+def _route_oracle(cfg, c, tokens=None):
+    x = c["x"] if tokens is None else c["x"][torch.as_tensor(tokens, device=c["x"].device)]
+    return O.route(x, c["centroids"], c["bias"], cfg.K, cfg.score_func, cfg.normalize)
+
+
+def _check_routing(cfg, idx_g, gates_g, idx_o, gates_o, margin):
+    T, K, E = idx_g.shape[0], cfg.K, cfg.E
+    assert np.all((idx_g >= 0) & (idx_g < E))
+    assert all(len(set(r.tolist())) == K for r in idx_g)          # K distinct, no drop
+    keep = margin >= MARGIN_EXCLUDE
+    n_excl = int((~keep).sum())
+    assert n_excl <= max(2, T // 50), f"{n_excl} near-tie tokens excluded of {T}"
+    np.testing.assert_array_equal(idx_g[keep], idx_o[keep])
+    np.testing.assert_allclose(gates_g[keep], gates_o[keep], rtol=0, atol=GATE_ATOL)
+    return keep, n_excl
+
+
+# ---------------------------------------------------------------- router
+
+@pytest.mark.parametrize("name", SMALL + FULL)
+def test_route_parity(name):
+    cfg = _cfg(name)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g)
+    run.route()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    idx_o, gates_o, margin, _ = _route_oracle(cfg, c)
+    _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), idx_o, gates_o, margin)
+
+
+def test_route_bias_forces_expert_and_keeps_gate():
+    cfg = small_cases()["small_bf16"]
+    g, c = gpu_inputs(cfg)
+    g["bias"] = torch.zeros(cfg.E, device="cuda")
+    g["bias"][7] = 5.0
+    run = GpuRun(m, cfg, g)
+    run.route()
+    idx = run.idx.cpu().numpy()
+    assert np.all(idx[:, 0] == 7)
+    cb = dict(c)
+    cb["bias"] = g["bias"].cpu()
+    idx_o, gates_o, margin, s = _route_oracle(cfg, cb)
+    _check_routing(cfg, idx, run.gates.cpu().numpy(), idx_o, gates_o, margin)
+
+
+# ---------------------------------------------------------------- dispatch
+
+@pytest.mark.parametrize("name", SMALL + FULL)
+def test_dispatch_bit_exact(name):
+    cfg = _cfg(name)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g)
+    idx_o, _, _, _ = _route_oracle(cfg, c)
+    idx_t = torch.as_tensor(idx_o, dtype=torch.int32, device="cuda")
+    run.dispatch(idx_t)
+    torch.cuda.synchronize()
+    counts, offsets, perm, pos = O.dispatch(idx_o, cfg.E)
+    np.testing.assert_array_equal(run.counts.cpu().numpy(), counts)
+    np.testing.assert_array_equal(run.offsets.cpu().numpy(), offsets)
+    np.testing.assert_array_equal(run.perm.cpu().numpy(), perm)
+    np.testing.assert_array_equal(run.pos.cpu().numpy(), pos)
+    # every dispatched row is a byte copy of its source token row
+    src = g["x"][torch.as_tensor(perm, device="cuda")]
+    assert torch.equal(run.xp, src)
+
+
+# ---------------------------------------------------------------- experts + combine on oracle routing
+
+@pytest.mark.parametrize("name", SMALL)
+def test_experts_combine_on_oracle_routing(name):
+    """Experts and combine fed the oracle's own indices and gates: every token
+    is compared, so no near-tie exclusion is involved."""
+    cfg = _cfg(name)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=0)
+    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    run.dispatch(torch.as_tensor(ref["idx"], dtype=torch.int32, device="cuda"))
+    run.experts()
+    gates = torch.as_tensor(ref["gates"], dtype=torch.float32, device="cuda")
+    run.combine(gates=gates)
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    assert_close(to_np(run.out), ref["delta"], cfg.act, f"{name} delta")
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_expert_outputs_rowwise(name):
+    """Each expert output row y[r] against the oracle's FFN of its token."""
+    cfg = _cfg(name)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=0)
+    idx_o, _, _, _ = _route_oracle(cfg, c)
+    run.dispatch(torch.as_tensor(idx_o, dtype=torch.int32, device="cuda"))
+    run.experts()
+    torch.cuda.synchronize()
+    counts, offsets, perm, pos = O.dispatch(idx_o, cfg.E)
+    u = O._f64(c["x"])
+    y = to_np(run.y)
+    want = np.zeros_like(y)
+    for e in range(cfg.E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            want[r0:r1] = O.swiglu_ffn(u[perm[r0:r1]], c["w13"][e], c["w2"][e])
+    TK = cfg.T * cfg.K
+    for s in range(cfg.S):
+        want[TK + s * cfg.T: TK + (s + 1) * cfg.T] = O.swiglu_ffn(u, c["ws13"][s], c["ws2"][s])
+    assert_close(y, want, cfg.act, f"{name} expert rows")
+
+
+# ---------------------------------------------------------------- whole layer
+
+@pytest.mark.parametrize("name", SMALL)
+def test_forward_parity_all_tokens(name):
+    cfg = _cfg(name)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=0)
+    run.forward()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    keep, _ = _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), ref["idx"],
+                             ref["gates"], ref["margin"])
+    assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, f"{name} forward")
+    # counts of the forward are the histogram of its own indices
+    np.testing.assert_array_equal(run.counts.cpu().numpy(),
+                                  np.bincount(run.idx.cpu().numpy().reshape(-1),
+                                              minlength=cfg.E))
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "tiny"])
+def test_forward_with_residual(name):
+    cfg = _cfg(name)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=1)
+    run.forward()
+    torch.cuda.synchronize()
+    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=1)
+    keep = ref["margin"] >= MARGIN_EXCLUDE
+    assert_close(to_np(run.out)[keep], ref["out"][keep], cfg.act, f"{name} out")
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_forward_equals_step_by_step(name):
+    cfg = _cfg(name)
+    g, _ = gpu_inputs(cfg)
+    a = GpuRun(m, cfg, g)
+    a.forward()
+    b = GpuRun(m, cfg, g)
+    b.route()
+    b.dispatch()
+    b.experts()
+    b.combine()
+    torch.cuda.synchronize()
+    assert torch.equal(a.idx, b.idx) and torch.equal(a.gates, b.gates)
+    assert torch.equal(a.counts, b.counts)
+    assert torch.equal(a.out, b.out)
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "ragged_bf16", "v3_decode"])
+def test_forward_deterministic(name):
+    cfg = _cfg(name)
+    g, _ = gpu_inputs(cfg)
+    a = GpuRun(m, cfg, g)
+    a.forward()
+    first = (a.idx.clone(), a.gates.clone(), a.counts.clone(), a.out.clone())
+    a.forward()
+    torch.cuda.synchronize()
+    assert torch.equal(first[0], a.idx) and torch.equal(first[1], a.gates)
+    assert torch.equal(first[2], a.counts) and torch.equal(first[3], a.out)
+
+
+# ---------------------------------------------------------------- full-size configs, sampled
+
+SAMPLES = {"v3_decode": 12, "v3_prefill": 8, "dsmoe16b": 48}
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_forward_full_size_sampled(name):
+    """The layer at full size, in the launch configuration the benchmark
+    times (moe_forward): routing on all tokens, outputs on a token sample that
+    the oracle evaluates one expert at a time, invariants on every token."""
+    cfg = _cfg(name)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=0)
+    run.forward()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    idx_g = run.idx.cpu().numpy()
+    counts = run.counts.cpu().numpy()
+    assert counts.sum() == cfg.T * cfg.K
+    np.testing.assert_array_equal(counts, np.bincount(idx_g.reshape(-1), minlength=cfg.E))
+    assert torch.isfinite(run.out.float()).all()
+    rng = np.random.default_rng(1234)
+    tok = np.sort(rng.choice(cfg.T, SAMPLES[name], replace=False))
+    tok[0] = 0
+    tok[-1] = cfg.T - 1                       # first and last token (ragged tail)
+    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0, tokens=tok)
+    keep = ref["margin"] >= MARGIN_EXCLUDE
+    np.testing.assert_array_equal(idx_g[tok][keep], ref["idx"][keep])
+    out = to_np(run.out)[tok]
+    assert_close(out[keep], ref["delta"][keep], cfg.act, f"{name} sampled tokens")
+
+
+# ---------------------------------------------------------------- edge cases
+
+EDGE = {
+    "one_token": small_cases()["small_bf16"].with_(name="one_token", T=1),
+    "k_equals_e": small_cases()["small_bf16"].with_(name="k_equals_e", E=8, K=8, T=100),
+    "no_shared": small_cases()["ragged_bf16"].with_(name="no_shared", S=0),
+    "k1_many_empty": small_cases()["small_bf16"].with_(name="k1_many_empty", T=20, E=64, K=1),
+    "f32_one_token": small_cases()["tiny"].with_(name="f32_one_token", T=1),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_cases(name):
+    cfg = EDGE[name]
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=0)
+    run.forward()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    keep, _ = _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), ref["idx"],
+                             ref["gates"], ref["margin"])
+    assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, name)
+
+
+def test_hot_expert_spans_several_token_blocks():
+    """A bias that sends every token to expert 3 gives it T = 600 rows: three
+    token blocks of one group, the last one ragged."""
+    cfg = small_cases()["small_bf16"].with_(name="hot", T=600)
+    g, c = gpu_inputs(cfg)
+    g["bias"] = torch.zeros(cfg.E, device="cuda")
+    g["bias"][3] = 4.0
+    c = dict(c)
+    c["bias"] = g["bias"].cpu()
+    run = GpuRun(m, cfg, g, add_residual=0)
+    run.forward()
+    torch.cuda.synchronize()
+    assert run.counts[3].item() == 600
+    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    keep = ref["margin"] >= MARGIN_EXCLUDE
+    assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, "hot expert")
+
+
+def test_empty_batch():
+    cfg = small_cases()["small_bf16"]
+    c = m.cfg_from_layer(cfg, T=0)
+    counts = torch.full((cfg.E,), 7, dtype=torch.int32, device="cuda")
+    ws = m.alloc_workspace(c, m.MOE_WS_FORWARD)
+    m.forward(c, None, None, None, None, None, None, None, None, None, counts, None, ws)
+    torch.cuda.synchronize()
+    assert counts.sum().item() == 0
+
+
+# ---------------------------------------------------------------- bias update
+
+def test_update_bias_bit_exact():
+    rng = np.random.default_rng(5)
+    for E, T, K in [(256, 8192, 8), (64, 32768, 6), (16, 64, 4), (1000, 333, 32)]:
+        cfg = m.make_cfg(T, 128, E, K, 1, 128)
+        counts = rng.multinomial(T * K, np.ones(E) / E).astype(np.int32)
+        counts[0] = T * K // E if (T * K) % E == 0 else counts[0]   # one exactly at the mean
+        bias = rng.uniform(-0.01, 0.01, E).astype(np.float32)
+        cb = torch.as_tensor(counts, device="cuda")
+        bb = torch.as_tensor(bias, device="cuda")
+        st = torch.zeros(2, device="cuda")
+        m.update_bias(cfg, cb, bb, st)
+        torch.cuda.synchronize()
+        want, stats = O.update_bias(counts, bias, T, K, 1e-3)
+        np.testing.assert_array_equal(bb.cpu().numpy().view(np.uint32), want.view(np.uint32))
+        np.testing.assert_allclose(st.cpu().numpy(), stats, rtol=1e-6)
+
+
+def test_balancing_loop_follows_oracle_rule():
+    """Twenty batches of forward + bias update: at every step the GPU bias
+    equals the oracle's rule applied to the GPU's own counts."""
+    cfg = small_cases()["small_bf16"].with_(name="loop", T=512, E=32, K=4, bias_range=0.0)
+    g, _ = gpu_inputs(cfg)
+    # skewed popularity: centroid norms grow with the expert index
+    g["centroids"] = (g["centroids"].float() *
+                      torch.linspace(0.5, 2.0, cfg.E, device="cuda")[:, None]).to(g["x"].dtype)
+    run = GpuRun(m, cfg, g)
+    bias = np.zeros(cfg.E, np.float32)
+    stats = torch.zeros(2, device="cuda")
+    hot = None
+    for step in range(20):
+        g["x"] = make_inputs(cfg.with_(seed=step + 1), "cuda")["x"]
+        run.inp = g
+        run.forward()
+        counts = run.counts.cpu().numpy()
+        m.update_bias(run.cfg, run.counts, g["bias"], stats)
+        torch.cuda.synchronize()
+        bias, (mx, _) = O.update_bias(counts, bias, cfg.T, cfg.K, cfg.gamma)
+        np.testing.assert_array_equal(g["bias"].cpu().numpy().view(np.uint32),
+                                      bias.view(np.uint32))
+        assert abs(stats[0].item() - mx) < 1e-5
+        if hot is None:
+            hot = int(np.argmax(counts))
+    # the most loaded expert of the first batch was pushed down
+    assert g["bias"][hot].item() < 0
