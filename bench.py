@@ -239,6 +239,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=1,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="comma-separated shape overrides, e.g. T=1024,E=32 (profiling cases)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -247,6 +249,9 @@ def main():
     if device.type == "cuda":
         torch.cuda.set_device(device)
     cfg = get_config(args.config)
+    if args.override:
+        kv = dict(item.split("=") for item in args.override.split(","))
+        cfg = cfg.with_(name=f"{cfg.name}[{args.override}]", **{k: int(v) for k, v in kv.items()})
 
     if args.impl == "reference":
         run_reference(args, cfg, dist, rank, ws, device)

@@ -1,6 +1,9 @@
 """Builds libmoe.so (the C-ABI library) in-tree for sm_103a with nvcc.
 
-    python -m mixture_experts_layer_88_b300.build [--verbose] [--ptxas-info]
+    python mixture_experts_layer_88_b300/build.py [--verbose] [--ptxas-info] [--force]
+
+Run it by path (or through __graft_entry__.build()): importing the package
+loads libmoe.so, so the builder must not depend on the package.
 """
 from __future__ import annotations
 
