@@ -145,6 +145,29 @@ moe_status_t moe_experts(const moe_cfg_t* cfg, const void* xp, const void* x,
                          void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_experts_static - moe_experts without a caller workspace, for callers
+ * that cannot allocate device memory: an inference runtime that reserves all
+ * of its device memory at start-up and forbids allocation on the request
+ * path, or a plugin whose host framework owns the allocator and passes no
+ * scratch buffer.  The pages have no counterpart; this is a packaging of the
+ * same computation.
+ *   Arguments, layouts and results as moe_experts (minus ws, ws_bytes).
+ *   Its scratch (the per-expert group table, about 22 KB) is a fixed array
+ *   inside the library, sized for E + S <= 1088 groups; larger E + S returns
+ *   MOE_ERR_INVALID_ARG.  Every GPU that loads the library holds that array
+ *   until the process exits.
+ *   The first call on a device looks up the array's device address (no
+ *   allocation); make that first call before any stream capture.
+ *   Calls share the array: calls that may overlap on the GPU (different
+ *   streams without ordering between them) race and give wrong results.
+ *   Calls no allocating routine (no cudaMalloc/cudaFree).
+ */
+moe_status_t moe_experts_static(const moe_cfg_t* cfg, const void* xp, const void* x,
+                                const int32_t* offsets, const void* w13, const void* w2,
+                                const void* ws13, const void* ws2, void* act, void* y,
+                                void* stream);
+
+/*
  * moe_combine - V3 section 3.1: out_t = [u_t] + sum_s y_shared(s,t)
  *               + sum_k g_{t,k} y[pos[t,k]], summed in fp32 in the order
  *               k = 0..K-1, then shared s = 0..S-1, then the residual.

@@ -24,6 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # every symbol include/moe.h declares
 SYMBOLS = ["moe_workspace_size", "moe_check_cfg", "moe_route", "moe_dispatch", "moe_experts",
+           "moe_experts_static",
            "moe_combine", "moe_update_bias", "moe_forward", "moe_get_status",
            "moe_status_string", "moe_trace_enable", "moe_trace_read", "moe_version"]
 
@@ -60,6 +61,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_route": (I32, [cfgp, P, P, P, P, P, P, SZ, P]),
         "moe_dispatch": (I32, [cfgp, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_experts": (I32, [cfgp, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_experts_static": (I32, [cfgp, P, P, P, P, P, P, P, P, P, P]),
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P]),
         "moe_update_bias": (I32, [cfgp, P, P, P, P]),
         "moe_forward": (I32, [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
@@ -148,6 +150,13 @@ def experts(cfg, xp, x, offsets, w13, w2, ws13, ws2, act, y, ws, stream=None):
     _check(lib().moe_experts(ctypes.byref(cfg), _p(xp), _p(x), _p(offsets), _p(w13), _p(w2),
                              _p(ws13), _p(ws2), _p(act), _p(y), _p(ws), ws.numel(),
                              _stream(stream)), "moe_experts")
+
+
+def experts_static(cfg, xp, x, offsets, w13, w2, ws13, ws2, act, y, stream=None):
+    """moe_experts with the library's fixed internal scratch (no workspace)."""
+    _check(lib().moe_experts_static(ctypes.byref(cfg), _p(xp), _p(x), _p(offsets), _p(w13),
+                                    _p(w2), _p(ws13), _p(ws2), _p(act), _p(y),
+                                    _stream(stream)), "moe_experts_static")
 
 
 def combine(cfg, y, gates, pos, x, out, stream=None):

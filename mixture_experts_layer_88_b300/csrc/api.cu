@@ -366,6 +366,57 @@ moe_status_t moe_experts(const moe_cfg_t* cfg, const void* xp, const void* x,
                     static_cast<cudaStream_t>(stream));
 }
 
+// ---------------------------------------------------------------- moe_experts_static
+// The expert FFNs for callers that cannot allocate device memory: the group
+// table that moe_experts keeps in the caller's workspace lives here in a
+// module-scope device array instead.  Capacity: E + S <= kStaticMaxGroups
+// groups (5 int32 arrays of kStaticMaxGroups + 1 entries, about 22 KB), which
+// every device that loads this library keeps until the process exits.  The
+// array's address is looked up once per device (cudaGetSymbolAddress) on that
+// device's first call.  All calls share the one array and keep the last
+// call's table; every entry a call reads is first written by that call, so
+// nothing needs clearing, but two calls that overlap on the GPU (different
+// streams, no ordering) race on the table.
+} // extern "C"
+
+namespace {
+constexpr int kStaticMaxGroups = kMaxE + kMaxS;
+}  // namespace
+
+static __device__ __align__(256) int32_t g_static_group_table[5 * (kStaticMaxGroups + 1)];
+
+namespace {
+int32_t* static_group_table() {
+  static int32_t* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_group_table) != cudaSuccess) return nullptr;
+  if (dev < 64) cached[dev] = static_cast<int32_t*>(p);
+  return static_cast<int32_t*>(p);
+}
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_experts_static(const moe_cfg_t* cfg, const void* xp, const void* x,
+                                const int32_t* offsets, const void* w13, const void* w2,
+                                const void* ws13, const void* ws2, void* act, void* y,
+                                void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (c.E + c.S > kStaticMaxGroups) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if ((s = check_ptrs(c, {xp, x, w13, w2, act, y}, {offsets})) != MOE_OK) return s;
+  if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
+  int32_t* table = static_group_table();
+  if (!table) return MOE_ERR_CUDA;
+  return do_experts(c, xp, x, offsets, w13, w2, ws13, ws2, act, y, table,
+                    static_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y, const float* gates,
                          const int32_t* pos, const void* x, void* out, void* stream) {
   moe_status_t s = moe_check_cfg(cfg);
