@@ -165,12 +165,9 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
   if (c.act_dtype == MOE_BF16) {
     const RouterPlan p = router_plan(c);
     float* partial = static_cast<float*>(ws);
-    CUtensorMap maps[4];
-    if (!make_tmap_bf16(&maps[0], centroids, c.E, c.d, 128) ||
-        !make_tmap_bf16(&maps[2], x, c.T, c.d, 16))
+    GemmMaps maps;
+    if (!make_gemm_maps(&maps, centroids, c.E, nullptr, 0, x, c.T, nullptr, 0, c.d))
       return MOE_ERR_CUDA;
-    maps[1] = maps[0];
-    maps[3] = maps[2];
     GemmArgs a{};
     a.G = 1;
     a.E = 1;
@@ -231,16 +228,10 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   const int grid = num_sms();
 
   // gate/up + SwiGLU: A = W13 rows, B = dispatched rows (routed) or tokens (shared)
-  CUtensorMap m1[4];
-  if (!make_tmap_bf16(&m1[0], w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.d, 128) ||
-      !make_tmap_bf16(&m1[2], xp, TK, c.d, 16) || !make_tmap_bf16(&m1[3], x, c.T, c.d, 16))
+  GemmMaps m1;
+  if (!make_gemm_maps(&m1, w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.S > 0 ? ws13 : nullptr,
+                      static_cast<uint64_t>(c.S) * 2 * c.I, xp, TK, x, c.T, c.d))
     return MOE_ERR_CUDA;
-  if (c.S > 0) {
-    if (!make_tmap_bf16(&m1[1], ws13, static_cast<uint64_t>(c.S) * 2 * c.I, c.d, 128))
-      return MOE_ERR_CUDA;
-  } else {
-    m1[1] = m1[0];
-  }
   GemmArgs a{};
   a.gt = GroupTable{rows, brow, orow, bs, bstart};
   a.G = G;
@@ -260,17 +251,10 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   if (s != MOE_OK) return s;
 
   // down: A = W2 rows (two 128-row boxes), B = activations
-  CUtensorMap m2[4];
-  if (!make_tmap_bf16(&m2[0], w2, static_cast<uint64_t>(c.E) * c.d, c.I, 128) ||
-      !make_tmap_bf16(&m2[2], act, R, c.I, 16))
+  GemmMaps m2;
+  if (!make_gemm_maps(&m2, w2, static_cast<uint64_t>(c.E) * c.d, c.S > 0 ? ws2 : nullptr,
+                      static_cast<uint64_t>(c.S) * c.d, act, R, nullptr, 0, c.I))
     return MOE_ERR_CUDA;
-  if (c.S > 0) {
-    if (!make_tmap_bf16(&m2[1], ws2, static_cast<uint64_t>(c.S) * c.d, c.I, 128))
-      return MOE_ERR_CUDA;
-  } else {
-    m2[1] = m2[0];
-  }
-  m2[3] = m2[2];
   GemmArgs b = a;
   b.gt = GroupTable{rows, orow, orow, bs, bstart};
   b.m_blocks = ceil_div(c.d, 256);

@@ -16,8 +16,9 @@
 //           writes fp32 partial logits of one K split
 //
 // Warp roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: A0, A1 (128x64 each) and the token rows (16-row
-//               boxes) of one 64-wide K block per pipeline stage
+//   warp 0      TMA producer: A0, A1 (128x64 each) and the token rows (at most
+//               five boxes of 256/128/64/32/16 rows) of one 64-wide K block per
+//               pipeline stage
 //   warp 1      TMEM owner and MMA issuer (one thread issues tcgen05.mma
 //               M=128, N=tokens, K=16, twice per K step)
 //   warps 2..5  epilogue: tcgen05.ld from TMEM (warp w reads lanes 32*(w%4)..)
@@ -40,9 +41,8 @@ constexpr int BM = 128;              // weight rows per accumulator (MMA M)
 constexpr int BN_MAX = 256;          // tokens per tile (MMA N, <= 256)
 constexpr int BK = 64;               // K elements per stage = one 128-byte row
 constexpr int STAGES = 3;
-constexpr int B_BOX_ROWS = 16;
 constexpr uint32_t A_BOX_BYTES = BM * BK * 2;             // 16 KB
-constexpr uint32_t B_BOX_BYTES = B_BOX_ROWS * BK * 2;     // 2 KB
+constexpr uint32_t B_ROW_BYTES = BK * 2;                  // 128 B per token row
 constexpr uint32_t STAGE_BYTES = 2 * A_BOX_BYTES + BN_MAX * BK * 2;  // 64 KB
 constexpr uint32_t TMEM_COLS = 512;  // acc0 at column 0, acc1 at column 256
 constexpr int NUM_THREADS = 192;
@@ -112,10 +112,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0,
-                   const __grid_constant__ CUtensorMap tmA1,
-                   const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+    gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -141,11 +138,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tc::tma_prefetch_desc(&tmA0);
-    tc::tma_prefetch_desc(&tmA1);
-    tc::tma_prefetch_desc(&tmB0);
-    tc::tma_prefetch_desc(&tmB1);
+  if (warp == 0 && lane < 2 + 2 * kTokBoxes) {
+    const CUtensorMap* m = lane < 2 ? &maps.a[lane] : &maps.b[(lane - 2) / kTokBoxes][(lane - 2) % kTokBoxes];
+    tc::tma_prefetch_desc(m);
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -170,8 +165,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Tile t;
       decode_tile(args, MODE, tile, t);
       const bool second = (MODE != GM_ROUTER) && (t.g >= args.E);
-      const CUtensorMap* mA = second ? &tmA1 : &tmA0;
-      const CUtensorMap* mB = second ? &tmB1 : &tmB0;
+      const CUtensorMap* mA = &maps.a[second ? 1 : 0];
+      const CUtensorMap* mB = maps.b[second ? 1 : 0];
       const int gl = second ? t.g - args.E : t.g;
       int a_row0, b_row;
       if (MODE == GM_ROUTER) {
@@ -182,8 +177,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         b_row = __ldg(args.gt.brow + t.g) + t.tok0;
       }
       const int a_row1 = a_row0 + args.a1_off;
-      const int nbox = t.nmma / B_BOX_ROWS;
-      const uint32_t bytes = 2 * A_BOX_BYTES + nbox * B_BOX_BYTES;
+      const uint32_t bytes = 2 * A_BOX_BYTES + t.nmma * B_ROW_BYTES;
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
         if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
         if (lane == 0) {
@@ -191,9 +185,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc::mbar_arrive_expect_tx(full + stage, bytes);
           tc::tma_load_2d(sa, mA, full + stage, kb * BK, a_row0);
           tc::tma_load_2d(sa + A_BOX_BYTES, mA, full + stage, kb * BK, a_row1);
-          for (int b = 0; b < nbox; ++b)
-            tc::tma_load_2d(sa + 2 * A_BOX_BYTES + b * B_BOX_BYTES, mB, full + stage, kb * BK,
-                            b_row + b * B_BOX_ROWS);
+          // token rows: one box per set bit of nmma / 16, largest first
+          int done = 0;
+#pragma unroll
+          for (int bi = kTokBoxes - 1; bi >= 0; --bi) {
+            const int h = 16 << bi;
+            if (t.nmma & h) {
+              tc::tma_load_2d(sa + 2 * A_BOX_BYTES + done * B_ROW_BYTES, mB + bi, full + stage,
+                              kb * BK, b_row + done);
+              done += h;
+            }
+          }
         }
         issued_phase[stage] = static_cast<int>(phase);
         __syncwarp();
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, 
 }
 
 template <int MODE>
-moe_status_t launch_mode(const CUtensorMap* maps, const GemmArgs& args, int grid,
+moe_status_t launch_mode(const GemmMaps& maps, const GemmArgs& args, int grid,
                          cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -393,8 +395,7 @@ moe_status_t launch_mode(const CUtensorMap* maps, const GemmArgs& args, int grid
   }
   static const char* names[3] = {"gemm_gateup_swiglu", "gemm_down", "gemm_router"};
   TraceScope tr(stream, names[MODE]);
-  gemm_tc_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2],
-                                                                   maps[3], args);
+  gemm_tc_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps, args);
   return launch_status();
 }
 
@@ -428,7 +429,27 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
-moe_status_t launch_gemm_tc(int mode, const CUtensorMap* maps, const GemmArgs& args, int grid,
+bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
+                    uint64_t a1_rows, const void* b0, uint64_t b0_rows, const void* b1,
+                    uint64_t b1_rows, uint64_t k) {
+  if (!make_tmap_bf16(&m->a[0], a0, a0_rows, k, BM)) return false;
+  if (a1) {
+    if (!make_tmap_bf16(&m->a[1], a1, a1_rows, k, BM)) return false;
+  } else {
+    m->a[1] = m->a[0];
+  }
+  for (int i = 0; i < kTokBoxes; ++i) {
+    if (!make_tmap_bf16(&m->b[0][i], b0, b0_rows, k, 16u << i)) return false;
+    if (b1) {
+      if (!make_tmap_bf16(&m->b[1][i], b1, b1_rows, k, 16u << i)) return false;
+    } else {
+      m->b[1][i] = m->b[0][i];
+    }
+  }
+  return true;
+}
+
+moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
                             cudaStream_t stream) {
   if (grid <= 0) return MOE_OK;
   switch (mode) {

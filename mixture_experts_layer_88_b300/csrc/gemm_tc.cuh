@@ -43,9 +43,24 @@ struct GemmArgs {
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
-// Launches the persistent grouped GEMM.  maps = {A0, A1, B0, B1}.
-moe_status_t launch_gemm_tc(int mode, const CUtensorMap* maps, const GemmArgs& args,
-                            int grid, cudaStream_t stream);
+// Token-operand boxes come in heights 16, 32, 64, 128, 256 rows, so any token
+// block (a multiple of 16, at most 256) is fetched with at most five TMA loads.
+constexpr int kTokBoxes = 5;
+
+struct GemmMaps {
+  CUtensorMap a[2];               // weight operand: routed (0) / shared (1), 128-row boxes
+  CUtensorMap b[2][kTokBoxes];    // token operand: routed (0) / shared (1), box 16 << i rows
+};
+
+// Fills `m`: a[i] over the [a_rows[i], k] weight matrices, b[i][*] over the
+// [b_rows[i], k] token matrices (a null pointer reuses entry 0).
+bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
+                    uint64_t a1_rows, const void* b0, uint64_t b0_rows, const void* b1,
+                    uint64_t b1_rows, uint64_t k);
+
+// Launches the persistent grouped GEMM.
+moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
+                            cudaStream_t stream);
 
 // Builds the group table of the expert GEMMs from the dispatch offsets:
 // groups 0..E-1 are routed experts (rows = counts), E..E+S-1 the shared
