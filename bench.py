@@ -293,19 +293,20 @@ def main():
     ms_step = ms_max / args.steps
     value = ws * cfg.T / (ms_step / 1e3)
 
-    # ---- end to end: pinned host tokens in, pinned host output back, every step
+    # ---- end to end: every step copies its tokens in from pinned host memory
+    # and its output back to pinned host memory (HostPipeline overlaps the
+    # copies of neighbouring steps with the compute)
     x_host = x.cpu().pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
-    x_dev = torch.empty_like(x)
-    for _ in range(args.warmup):
-        layer.step_host(x_host, out_host, x_dev, out)
+    out_hosts = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
+    pipe = m.HostPipeline(layer, x)
+    pipe.run([x_host] * args.warmup, [out_hosts[i & 1] for i in range(args.warmup)])
+    torch.cuda.synchronize()
     _barrier(dist, device)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        layer.step_host(x_host, out_host, x_dev, out)
-    e1.record(stream)
+    pipe.run([x_host] * args.steps, [out_hosts[i & 1] for i in range(args.steps)], stream)
+    e1.record(pipe.d2h)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1), device) / args.steps
     e2e_value = ws * cfg.T / (e2e_ms / 1e3)

@@ -9,8 +9,8 @@ from ._lib import (MoeCfg, MoeError, make_cfg, cfg_from_layer, workspace_size, c
                    get_status, trace_enable, trace_read_all, version, MOE_F32, MOE_BF16,
                    MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX, MOE_WS_ROUTE, MOE_WS_DISPATCH,
                    MOE_WS_EXPERTS, MOE_WS_FORWARD)
-from .layer import MoeLayer
+from .layer import MoeLayer, HostPipeline
 
-__all__ = ["MoeCfg", "MoeError", "MoeLayer", "make_cfg", "cfg_from_layer", "workspace_size",
+__all__ = ["MoeCfg", "MoeError", "MoeLayer", "HostPipeline", "make_cfg", "cfg_from_layer", "workspace_size",
            "check_cfg", "alloc_workspace", "route", "dispatch", "experts", "combine",
            "update_bias", "forward", "get_status", "trace_enable", "trace_read_all", "version"]

@@ -166,7 +166,8 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
     const RouterPlan p = router_plan(c);
     float* partial = static_cast<float*>(ws);
     GemmMaps maps;
-    if (!make_gemm_maps(&maps, centroids, c.E, nullptr, 0, x, c.T, nullptr, 0, c.d))
+    if (!make_gemm_maps(&maps, centroids, c.E, nullptr, 0, x, c.T, nullptr, 0, c.d,
+                        kTokBox0Single))
       return MOE_ERR_CUDA;
     GemmArgs a{};
     a.G = 1;
@@ -230,13 +231,13 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   // gate/up + SwiGLU: A = W13 rows, B = dispatched rows (routed) or tokens (shared)
   GemmMaps m1;
   if (!make_gemm_maps(&m1, w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.S > 0 ? ws13 : nullptr,
-                      static_cast<uint64_t>(c.S) * 2 * c.I, xp, TK, x, c.T, c.d))
+                      static_cast<uint64_t>(c.S) * 2 * c.I, xp, TK, x, c.T, c.d, kTokBox0Pair))
     return MOE_ERR_CUDA;
   GemmArgs a{};
   a.gt = GroupTable{rows, brow, orow, bs, bstart};
   a.G = G;
   a.E = c.E;
-  a.m_blocks = c.I / 128;
+  a.m_blocks = ceil_div(c.I, 256);   // 256 gate rows (and their up rows) per CTA pair
   a.a_rows_per_group = 2 * c.I;
   a.a1_off = c.I;
   a.k_blocks = c.d / 64;
@@ -253,13 +254,13 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   // down: A = W2 rows (two 128-row boxes), B = activations
   GemmMaps m2;
   if (!make_gemm_maps(&m2, w2, static_cast<uint64_t>(c.E) * c.d, c.S > 0 ? ws2 : nullptr,
-                      static_cast<uint64_t>(c.S) * c.d, act, R, nullptr, 0, c.I))
+                      static_cast<uint64_t>(c.S) * c.d, act, R, nullptr, 0, c.I, kTokBox0Pair))
     return MOE_ERR_CUDA;
   GemmArgs b = a;
   b.gt = GroupTable{rows, orow, orow, bs, bstart};
-  b.m_blocks = ceil_div(c.d, 256);
+  b.m_blocks = ceil_div(c.d, 512);   // 2 x 256 rows of W2 per CTA pair
   b.a_rows_per_group = c.d;
-  b.a1_off = 128;
+  b.a1_off = 256;
   b.k_blocks = c.I / 64;
   b.k_per_split = b.k_blocks;
   b.out_ld = c.d;

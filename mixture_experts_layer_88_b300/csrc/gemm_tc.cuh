@@ -21,9 +21,9 @@ struct GemmArgs {
   GroupTable gt;
   int G;                     // groups (grouped modes)
   int E;                     // groups g < E read A/B map 0, others map 1
-  int m_blocks;              // weight-row blocks per group
+  int m_blocks;              // weight-row blocks per group (a block spans the CTA pair)
   int a_rows_per_group;      // rows of A per group (2I or d; 0 in router mode)
-  int a1_off;                // row offset of the second A box
+  int a1_off;                // row offset of the second A box (I, 256 or 128)
   int k_blocks;              // K / 64
   int k_splits;              // router mode: K splits (1 otherwise)
   int k_per_split;           // k-blocks per split
@@ -43,9 +43,13 @@ struct GemmArgs {
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
-// Token-operand boxes come in heights 16, 32, 64, 128, 256 rows, so any token
-// block (a multiple of 16, at most 256) is fetched with at most five TMA loads.
+// Token-operand boxes come in five heights h0 << i, so a CTA's share of a
+// token block is fetched with at most five TMA loads: h0 = 16 (16..256 rows)
+// when one CTA loads the whole block (router), h0 = 8 (8..128 rows) when
+// each CTA of a pair loads half of a block (expert GEMMs).
 constexpr int kTokBoxes = 5;
+constexpr uint32_t kTokBox0Single = 16;
+constexpr uint32_t kTokBox0Pair = 8;
 
 struct GemmMaps {
   CUtensorMap a[2];               // weight operand: routed (0) / shared (1), 128-row boxes
@@ -53,12 +57,14 @@ struct GemmMaps {
 };
 
 // Fills `m`: a[i] over the [a_rows[i], k] weight matrices, b[i][*] over the
-// [b_rows[i], k] token matrices (a null pointer reuses entry 0).
+// [b_rows[i], k] token matrices in boxes of tok_box0 << j rows (a null pointer
+// reuses entry 0).
 bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
                     uint64_t a1_rows, const void* b0, uint64_t b0_rows, const void* b1,
-                    uint64_t b1_rows, uint64_t k);
+                    uint64_t b1_rows, uint64_t k, uint32_t tok_box0);
 
-// Launches the persistent grouped GEMM.
+// Launches the persistent grouped GEMM: GATEUP and DOWN on CTA pairs
+// (clusters of two; grid rounded down to even), ROUTER on single CTAs.
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
                             cudaStream_t stream);
 

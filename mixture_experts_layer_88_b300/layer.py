@@ -63,3 +63,51 @@ class MoeLayer:
         self.step(x_dev, out_dev, stream)
         out_host.copy_(out_dev, non_blocking=True)
         return out_host
+
+
+class HostPipeline:
+    """Runs a layer over a sequence of batches that live in pinned host memory.
+
+    Step i copies its tokens host->device on one copy stream, runs the layer
+    (forward + bias update) on the compute stream, and copies its output
+    device->host on a second copy stream.  Two device buffers alternate, so
+    the copies of step i+1 (in) and step i-1 (out) overlap the compute of
+    step i; the compute of step i still sees the bias left by step i-1.
+    """
+
+    def __init__(self, layer: MoeLayer, like: torch.Tensor):
+        self.layer = layer
+        dev = layer.device
+        self.x_dev = [torch.empty_like(like, device=dev) for _ in range(2)]
+        self.out_dev = [torch.empty_like(like, device=dev) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+        self.x_ready, self.done, self.out_free = ev(), ev(), ev()
+        self._used = [False, False]
+
+    def run(self, x_hosts, out_hosts, stream=None):
+        """Processes batch i = x_hosts[i] into out_hosts[i] for every i;
+        returns once all work is queued (synchronise the streams to wait)."""
+        comp = stream or torch.cuda.current_stream(self.layer.device)
+        for i, (xh, oh) in enumerate(zip(x_hosts, out_hosts)):
+            b = i & 1
+            with torch.cuda.stream(self.h2d):
+                if self._used[b]:
+                    self.h2d.wait_event(self.done[b])      # compute of step i-2 read x[b]
+                self.x_dev[b].copy_(xh, non_blocking=True)
+                self.x_ready[b].record(self.h2d)
+            comp.wait_event(self.x_ready[b])
+            if self._used[b]:
+                comp.wait_event(self.out_free[b])           # step i-2's output copied out
+            self.layer.step(self.x_dev[b], self.out_dev[b], comp)
+            self.done[b].record(comp)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.done[b])
+                oh.copy_(self.out_dev[b], non_blocking=True)
+                self.out_free[b].record(self.d2h)
+            self._used[b] = True
+        return out_hosts
+
+    def synchronize(self):
+        self.d2h.synchronize()
