@@ -132,6 +132,11 @@ def _barrier(dist, device):
             dist.barrier()
 
 
+# FP8 tensor-core peak = the measured bf16 peak x the nominal fp8 : bf16
+# ratio of B300 (4.5 : 2.25 dense PFLOP/s)
+FP8_OVER_BF16 = 2.0
+
+
 def kernel_roofline(cfg, traces, peaks):
     """Per-kernel algorithmic work / measured average launch time."""
     T, d, E, K, S, I = cfg.T, cfg.d, cfg.E, cfg.K, cfg.S, cfg.I
@@ -141,10 +146,15 @@ def kernel_roofline(cfg, traces, peaks):
         # flops
         "gemm_gateup_swiglu": ("TFLOP/s", 2.0 * R * d * 2 * I),
         "gemm_down": ("TFLOP/s", 2.0 * R * I * d),
+        "gemm_fp8_gateup_swiglu": ("TFLOP/s fp8", 2.0 * R * d * 2 * I),
+        "gemm_fp8_down": ("TFLOP/s fp8", 2.0 * R * I * d),
         # bytes: algorithmic traffic (inputs read once, outputs written once)
         "gemm_router": ("GB/s", es * (T * d + E * d) + 4.0 * T * E),
         "router_topk": ("GB/s", 4.0 * T * E + 8.0 * T * K),
         "dispatch_scatter": ("GB/s", es * (T * d + T * K * d) + 4.0 * T * K),
+        # bf16 tokens in, e4m3 rows + fp32 1x128 scales out (K routed + S>0 shared copies)
+        "dispatch_scatter_fp8": ("GB/s", es * T * d + (T * K + (T if S else 0)) *
+                                 (d + 4.0 * d / 128) + 4.0 * T * K),
         "combine": ("GB/s", es * (R * d + 2 * T * d) + 8.0 * T * K),
     }
     out = {}
@@ -152,9 +162,9 @@ def kernel_roofline(cfg, traces, peaks):
         if name in work and launches > 0:
             unit, amount = work[name]
             avg_s = ms / launches / 1e3
-            if unit == "TFLOP/s":
+            if unit.startswith("TFLOP/s"):
                 ach = amount / avg_s / 1e12
-                peak = peaks["bf16_tflops_sustained"]
+                peak = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if "fp8" in unit else 1)
             else:
                 ach = amount / avg_s / 1e9
                 peak = peaks["hbm_gbs"]
@@ -186,6 +196,10 @@ def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7):
     host = {"x": x_host, "centroids": inp["centroids"].cpu(), "bias": inp["bias"].cpu(),
             "w13": _Experts(inp["w13"], used), "w2": _Experts(inp["w2"], used),
             "ws13": inp["ws13"].cpu(), "ws2": inp["ws2"].cpu()}
+    for k in ("w13", "w2"):
+        if k + "_scale" in inp:                       # FP8 layer: block scales too
+            host[k + "_scale"] = _Experts(inp[k + "_scale"], used)
+            host["s" + k + "_scale"] = inp["s" + k + "_scale"].cpu()
     t0 = time.perf_counter()
     O.moe_layer(host, cfg.K, cfg.normalize, cfg.score_func, cfg.add_residual)
     dt = time.perf_counter() - t0
@@ -239,6 +253,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=1,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--balance-steps", type=int, default=20,
+                    help="skewed layers: bias-update steps of the balancing run")
     ap.add_argument("--override", default="",
                     help="comma-separated shape overrides, e.g. T=1024,E=32 (profiling cases)")
     args = ap.parse_args()
@@ -317,9 +333,13 @@ def main():
         return
 
     roof = kernel_roofline(cfg, traces, peaks)
-    top = roof.get("gemm_gateup_swiglu")
+    fp8 = cfg.wgt == "e4m3"
+    top_name = "gemm_fp8_gateup_swiglu" if fp8 else "gemm_gateup_swiglu"
+    top = roof.get(top_name)
     gemm_flops = cfg.gemm_flops()
-    gemm_ms = sum(t[2] for t in traces if t[0] in ("gemm_gateup_swiglu", "gemm_down"))
+    gemm_names = (("gemm_fp8_gateup_swiglu", "gemm_fp8_down") if fp8
+                  else ("gemm_gateup_swiglu", "gemm_down"))
+    gemm_ms = sum(t[2] for t in traces if t[0] in gemm_names)
     gemm_ms_step = gemm_ms / args.steps if gemm_ms else None
     gemm_tflops = gemm_flops / (gemm_ms_step / 1e3) / 1e12 if gemm_ms_step else None
     launches = sum(t[1] for t in traces)
@@ -329,10 +349,12 @@ def main():
         with open(tfile) as f:
             traffic = json.load(f).get(cfg.name, {}).get("gemm_gateup_swiglu")
 
+    gemm_peak = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if fp8 else 1)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 (fp32 promotion), bf16 tokens" if fp8 else "bf16",
         "data": "synthetic (seeded random tokens and random-init weights of the layer's shape)",
         "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
                    "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
@@ -340,15 +362,20 @@ def main():
                    "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
                          if cfg.name.startswith("v3") else "inputs larger than L2"},
         "grouped_gemm": {"tflops": round(gemm_tflops, 1) if gemm_tflops else None,
-                         "frac_of_peak": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4)
+                         "frac_of_peak": round(gemm_tflops / gemm_peak, 4)
                          if gemm_tflops else None,
-                         "peak_tflops": peaks["bf16_tflops_sustained"],
-                         "peak_kind": f"bf16 sustained, {peaks['source']}",
+                         "peak_tflops": gemm_peak,
+                         "peak_kind": (f"fp8 = 2 x bf16 sustained, {peaks['source']}" if fp8
+                                       else f"bf16 sustained, {peaks['source']}"),
+                         "frac_of_burst_bf16": round(gemm_tflops / peaks["bf16_tflops"], 4)
+                         if gemm_tflops and not fp8 else None,
                          "ms_per_step": round(gemm_ms_step, 4) if gemm_ms_step else None},
-        "roofline": ({"kernel": "gemm_gateup_swiglu", "bound": "tensor",
+        "roofline": ({"kernel": top_name, "bound": "tensor",
                       "achieved": top["achieved"], "peak": top["peak"], "unit": "TFLOP/s",
                       "frac": top["frac"], "traffic": traffic,
-                      "peak_kind": f"bf16 sustained, {peaks['source']}"} if top else None),
+                      "peak_kind": (f"fp8 = 2 x bf16 sustained, {peaks['source']}" if fp8
+                                    else f"bf16 sustained, {peaks['source']}")}
+                     if top else None),
         "kernels": roof,
         "gpu_launches": launches,
         "device_status": st,
@@ -358,6 +385,18 @@ def main():
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
                 "ms_per_step": round(e2e_ms, 4)},
     }
+    if cfg.zipf_s > 0:
+        # balancing run of the skewed layer: fresh tokens every step, bias
+        # from 0, one sign update per step; max / mean expert load per step
+        from moe_inputs import make_tokens
+        layer.bias.zero_()
+        loads = []
+        for step in range(args.balance_steps):
+            xb = make_tokens(cfg, device, seed=rank, step=step + 1)
+            layer.forward(xb, out)
+            loads.append(round(float(layer.update_bias()[0].item()), 3))
+        line["balance"] = {"steps": args.balance_steps, "gamma": cfg.gamma,
+                           "max_over_mean_load": loads}
     if not args.no_cpu_baseline:
         rate, secs, cores = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens)
         line["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores,

@@ -21,7 +21,9 @@
  *     library allocates nothing on any call below.
  *   - Floating tensors use cfg->act_dtype (tokens, activations, outputs) or
  *     cfg->wgt_dtype (centroids, expert weights).  Supported pairs:
- *     (MOE_F32, MOE_F32) and (MOE_BF16, MOE_BF16).  Bias, gates and load
+ *     (MOE_F32, MOE_F32), (MOE_BF16, MOE_BF16) and (MOE_BF16, MOE_E4M3); the
+ *     last is the FP8 layer (block-scaled e4m3 expert weights, bf16 tokens
+ *     and centroids) served by the *_fp8 entry points.  Bias, gates and load
  *     statistics are always fp32; indices, counts, offsets are int32.
  *   - For MOE_BF16, d and I must be multiples of 128 and every pointer must be
  *     16-byte aligned.  Limits: 1 <= K <= min(E, 32), E <= 1024, S <= 64,
@@ -208,6 +210,75 @@ moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centro
                          const void* ws13, const void* ws2, int32_t* idx,
                          float* gates, int32_t* counts, void* out,
                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * FP8 layers (V3 section 4.3): expert weights in e4m3 with one fp32 scale per
+ * 128 x 128 block (w = q * scale), activations quantised inside the layer to
+ * e4m3 in 1 x 128 tiles along K (scale = max|x| / 448), and tensor-core
+ * partial sums promoted to fp32 on the CUDA cores every 128 elements of K.
+ * cfg: act_dtype MOE_BF16, wgt_dtype MOE_E4M3; d and I multiples of 128.
+ * Centroids are bf16 (the router is not quantised).
+ */
+typedef struct {
+  const void* w13;  const float* w13_scale;   /* [E,2I,d] e4m3; [E, 2I/128, d/128] */
+  const void* w2;   const float* w2_scale;    /* [E,d,I]  e4m3; [E, d/128, I/128]  */
+  const void* ws13; const float* ws13_scale;  /* [S,2I,d] e4m3; [S, 2I/128, d/128] (NULL if S == 0) */
+  const void* ws2;  const float* ws2_scale;   /* [S,d,I]  e4m3; [S, d/128, I/128]  */
+} moe_fp8_weights_t;
+
+/*
+ * Row layout of the FP8 buffers.  Rows of expert e start at offsets[e], a
+ * multiple of 4; the shared experts read their tokens from rows
+ * shared_row .. shared_row + T - 1 of xq and write their outputs from row
+ * shared_row + s * round_up(T, 4) of act / y.  rows_in: rows of xq (and
+ * columns of xq_scale); rows_out: rows of act and y (columns of act_scale).
+ */
+moe_status_t moe_fp8_rows(const moe_cfg_t* cfg, int64_t* rows_in, int64_t* rows_out,
+                          int64_t* shared_row);
+
+/*
+ * moe_dispatch_fp8 - moe_dispatch for FP8 layers: the same counts, pos and
+ * perm_tok (expert rows in ascending token order), but offsets[e] is the
+ * prefix sum of counts rounded up to 4 rows, and the rows are written
+ * quantised:
+ *   xq       [rows_in, d]         e4m3 out  q = rne_sat(x * 448 / max|tile|)
+ *   xq_scale [d/128, rows_in]     fp32 out  max|tile| / 448 (K-block major)
+ *   perm_tok [shared_row]         int32 out  source token of each routed row
+ * Rows of routed expert e: offsets[e] .. + counts[e]; shared-expert input:
+ * rows shared_row .. + T (moe_fp8_rows).  Other rows (and their perm_tok
+ * entries) are left unwritten.
+ */
+moe_status_t moe_dispatch_fp8(const moe_cfg_t* cfg, const void* x, const int32_t* idx,
+                              int32_t* counts, int32_t* offsets, void* xq, float* xq_scale,
+                              int32_t* perm_tok, int32_t* pos, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * moe_experts_fp8 - moe_experts for FP8 layers on the moe_dispatch_fp8 rows.
+ *   act       [rows_out, I]        e4m3 out  SiLU(gate) * up, 1 x 128 tiles
+ *   act_scale [I/128, rows_out]    fp32 out
+ *   y         [rows_out, d]        bf16 out  expert outputs (routed at
+ *                                  offsets[e] + r, shared expert s at
+ *                                  shared_row + s * round_up(T, 4) + t)
+ * ws: MOE_WS_EXPERTS bytes.  Accumulation is fp32 (promotion every 128 K).
+ */
+moe_status_t moe_experts_fp8(const moe_cfg_t* cfg, const void* xq, const float* xq_scale,
+                             const int32_t* offsets, const int32_t* counts,
+                             const moe_fp8_weights_t* w, void* act, float* act_scale, void* y,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward_fp8 - the FP8 layer: moe_route -> moe_dispatch_fp8 ->
+ * moe_experts_fp8 -> moe_combine on one stream, no host synchronisation;
+ * arguments as moe_forward with the weights in `w`.  moe_combine and
+ * moe_update_bias take FP8 cfgs as they are (moe_combine reads the FP8 row
+ * layout); moe_dispatch, moe_experts, moe_experts_static and moe_forward
+ * return MOE_ERR_UNSUPPORTED for them.
+ */
+moe_status_t moe_forward_fp8(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                             const float* bias, const moe_fp8_weights_t* w, int32_t* idx,
+                             float* gates, int32_t* counts, void* out, void* ws,
+                             size_t ws_bytes, void* stream);
 
 /* Waits for `stream`, then returns and clears this device's error word
  * (MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS) or MOE_ERR_CUDA. */

@@ -6,6 +6,8 @@ include/moe.h); this package only marshals torch tensors into it.
 from . import _lib
 from ._lib import (MoeCfg, MoeError, make_cfg, cfg_from_layer, workspace_size, check_cfg,
                    alloc_workspace, route, dispatch, experts, combine, update_bias, forward,
+                   Fp8Weights, fp8_weights, fp8_rows, dispatch_fp8, experts_fp8, forward_fp8,
+                   MOE_E4M3,
                    get_status, trace_enable, trace_read_all, version, MOE_F32, MOE_BF16,
                    MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX, MOE_WS_ROUTE, MOE_WS_DISPATCH,
                    MOE_WS_EXPERTS, MOE_WS_FORWARD)
@@ -13,4 +15,6 @@ from .layer import MoeLayer, HostPipeline
 
 __all__ = ["MoeCfg", "MoeError", "MoeLayer", "HostPipeline", "make_cfg", "cfg_from_layer", "workspace_size",
            "check_cfg", "alloc_workspace", "route", "dispatch", "experts", "combine",
-           "update_bias", "forward", "get_status", "trace_enable", "trace_read_all", "version"]
+           "update_bias", "forward", "Fp8Weights", "fp8_weights", "fp8_rows", "dispatch_fp8",
+           "experts_fp8", "forward_fp8", "get_status", "trace_enable", "trace_read_all",
+           "version"]

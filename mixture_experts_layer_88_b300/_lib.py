@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # every symbol include/moe.h declares
 SYMBOLS = ["moe_workspace_size", "moe_check_cfg", "moe_route", "moe_dispatch", "moe_experts",
            "moe_experts_static",
-           "moe_combine", "moe_update_bias", "moe_forward", "moe_get_status",
+           "moe_combine", "moe_update_bias", "moe_forward", "moe_fp8_rows", "moe_dispatch_fp8",
+           "moe_experts_fp8", "moe_forward_fp8", "moe_get_status",
            "moe_status_string", "moe_trace_enable", "moe_trace_read", "moe_version"]
 
 
@@ -41,6 +42,14 @@ class MoeCfg(ctypes.Structure):
                 ("act_dtype", ctypes.c_int32), ("wgt_dtype", ctypes.c_int32),
                 ("score_func", ctypes.c_int32), ("normalize", ctypes.c_int32),
                 ("add_residual", ctypes.c_int32), ("gamma", ctypes.c_float)]
+
+
+class Fp8Weights(ctypes.Structure):
+    """moe_fp8_weights_t: e4m3 expert weights and their 128 x 128 block scales."""
+    _fields_ = [("w13", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
+                ("ws13", ctypes.c_void_p), ("ws13_scale", ctypes.c_void_p),
+                ("ws2", ctypes.c_void_p), ("ws2_scale", ctypes.c_void_p)]
 
 
 class KernelTime(ctypes.Structure):
@@ -65,6 +74,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P]),
         "moe_update_bias": (I32, [cfgp, P, P, P, P]),
         "moe_forward": (I32, [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_fp8_rows": (I32, [cfgp, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                               ctypes.POINTER(ctypes.c_int64)]),
+        "moe_dispatch_fp8": (I32, [cfgp, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_experts_fp8": (I32, [cfgp, P, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, P, SZ,
+                                  P]),
+        "moe_forward_fp8": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, P, P, SZ,
+                                  P]),
         "moe_get_status": (I32, [P]),
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_trace_enable": (I32, [I32]),
@@ -174,6 +190,44 @@ def forward(cfg, x, centroids, bias, w13, w2, ws13, ws2, idx, gates, counts, out
     _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(centroids), _p(bias), _p(w13),
                              _p(w2), _p(ws13), _p(ws2), _p(idx), _p(gates), _p(counts),
                              _p(out), _p(ws), ws.numel(), _stream(stream)), "moe_forward")
+
+
+def fp8_weights(w: dict) -> Fp8Weights:
+    """Fp8Weights from a dict with w13, w13_scale, w2, w2_scale and (when the
+    layer has shared experts) ws13, ws13_scale, ws2, ws2_scale tensors."""
+    def g(k):
+        t = w.get(k)
+        return None if t is None or t.numel() == 0 else t.data_ptr()
+    return Fp8Weights(g("w13"), g("w13_scale"), g("w2"), g("w2_scale"), g("ws13"),
+                      g("ws13_scale"), g("ws2"), g("ws2_scale"))
+
+
+def fp8_rows(cfg) -> tuple:
+    """(rows_in, rows_out, shared_row) of the FP8 row layout."""
+    a, b, c = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib().moe_fp8_rows(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(b),
+                              ctypes.byref(c)), "moe_fp8_rows")
+    return a.value, b.value, c.value
+
+
+def dispatch_fp8(cfg, x, idx, counts, offsets, xq, xq_scale, perm_tok, pos, ws, stream=None):
+    _check(lib().moe_dispatch_fp8(ctypes.byref(cfg), _p(x), _p(idx), _p(counts), _p(offsets),
+                                  _p(xq), _p(xq_scale), _p(perm_tok), _p(pos), _p(ws),
+                                  ws.numel(), _stream(stream)), "moe_dispatch_fp8")
+
+
+def experts_fp8(cfg, xq, xq_scale, offsets, counts, weights: Fp8Weights, act, act_scale, y, ws,
+                stream=None):
+    _check(lib().moe_experts_fp8(ctypes.byref(cfg), _p(xq), _p(xq_scale), _p(offsets),
+                                 _p(counts), ctypes.byref(weights), _p(act), _p(act_scale),
+                                 _p(y), _p(ws), ws.numel(), _stream(stream)), "moe_experts_fp8")
+
+
+def forward_fp8(cfg, x, centroids, bias, weights: Fp8Weights, idx, gates, counts, out, ws,
+                stream=None):
+    _check(lib().moe_forward_fp8(ctypes.byref(cfg), _p(x), _p(centroids), _p(bias),
+                                 ctypes.byref(weights), _p(idx), _p(gates), _p(counts), _p(out),
+                                 _p(ws), ws.numel(), _stream(stream)), "moe_forward_fp8")
 
 
 def get_status(stream=None) -> int:

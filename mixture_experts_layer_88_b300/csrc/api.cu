@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "gemm_fp8.cuh"
 #include "gemm_tc.cuh"
 #include "kernels.cuh"
 
@@ -104,8 +105,29 @@ size_t experts_ws(const moe_cfg_t& c) {
   return align_up(5 * (G + 1) * sizeof(int32_t), 256);
 }
 
+// FP8 layers: rows of expert e start at offsets[e], a multiple of 4 (the
+// scales of a token block are a 16-byte aligned fp32 run); the shared
+// experts' input rows sit at a fixed row P after every routed row, and their
+// outputs at P + s * Tp.
+struct Fp8Rows {
+  long long P, Tp, rows_in, rows_out;
+};
+
+bool is_fp8(const moe_cfg_t& c) { return c.wgt_dtype == MOE_E4M3; }
+
+Fp8Rows fp8_rows(const moe_cfg_t& c) {
+  Fp8Rows r;
+  const long long TK = static_cast<long long>(c.T) * c.K;
+  r.P = (TK + 3LL * c.E + 3) / 4 * 4;
+  r.Tp = (c.T + 3LL) / 4 * 4;
+  r.rows_in = r.P + r.Tp;
+  r.rows_out = r.P + c.S * r.Tp;
+  return r;
+}
+
 struct ForwardLayout {
   size_t route, dispatch, experts, offsets, perm, pos, xp, act, y, total;
+  size_t xs, act_s;   // FP8 layers: activation scales
 };
 
 ForwardLayout forward_layout(const moe_cfg_t& c) {
@@ -123,11 +145,21 @@ ForwardLayout forward_layout(const moe_cfg_t& c) {
   L.dispatch = take(dispatch_ws(c));
   L.experts = take(experts_ws(c));
   L.offsets = take((c.E + 1) * sizeof(int32_t));
-  L.perm = take(TK * sizeof(int32_t));
+  // perm_tok spans the row space of the routed rows (padded in FP8 layers)
+  L.perm = take((is_fp8(c) ? static_cast<size_t>(fp8_rows(c).P) : TK) * sizeof(int32_t));
   L.pos = take(TK * sizeof(int32_t));
-  L.xp = take(TK * c.d * es);
-  L.act = take(R * c.I * es);
-  L.y = take(R * c.d * es);
+  if (is_fp8(c)) {
+    const Fp8Rows fr = fp8_rows(c);
+    L.xp = take(static_cast<size_t>(fr.rows_in) * c.d);
+    L.xs = take(static_cast<size_t>(fr.rows_in) * (c.d / 128) * sizeof(float));
+    L.act = take(static_cast<size_t>(fr.rows_out) * c.I);
+    L.act_s = take(static_cast<size_t>(fr.rows_out) * (c.I / 128) * sizeof(float));
+    L.y = take(static_cast<size_t>(fr.rows_out) * c.d * 2);
+  } else {
+    L.xp = take(TK * c.d * es);
+    L.act = take(R * c.I * es);
+    L.y = take(R * c.d * es);
+  }
   L.total = off;
   return L;
 }
@@ -166,7 +198,7 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
     const RouterPlan p = router_plan(c);
     float* partial = static_cast<float*>(ws);
     GemmMaps maps;
-    if (!make_gemm_maps(&maps, centroids, c.E, nullptr, 0, x, c.T, nullptr, 0, c.d,
+    if (!make_gemm_maps(&maps, centroids, c.E, nullptr, 0, 128, x, c.T, nullptr, 0, c.d,
                         kTokBox0Single))
       return MOE_ERR_CUDA;
     GemmArgs a{};
@@ -221,8 +253,9 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   int32_t* orow = brow + (G + 1);
   int32_t* bs = orow + (G + 1);
   int32_t* bstart = bs + (G + 1);
-  moe_status_t s = launch_build_groups(offsets, c.T, c.K, c.E, c.S, rows, brow, orow, bs, bstart,
-                                       st);
+  const GroupLayout lay{0, c.T * c.K, c.T, 256};
+  moe_status_t s = launch_build_groups(offsets, nullptr, c.T, c.E, c.S, lay, rows, brow, orow, bs,
+                                       bstart, st);
   if (s != MOE_OK) return s;
   const long long TK = static_cast<long long>(c.T) * c.K;
   const long long R = TK + static_cast<long long>(c.S) * c.T;
@@ -231,13 +264,14 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   // gate/up + SwiGLU: A = W13 rows, B = dispatched rows (routed) or tokens (shared)
   GemmMaps m1;
   if (!make_gemm_maps(&m1, w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.S > 0 ? ws13 : nullptr,
-                      static_cast<uint64_t>(c.S) * 2 * c.I, xp, TK, x, c.T, c.d, kTokBox0Pair))
+                      static_cast<uint64_t>(c.S) * 2 * c.I, 128, xp, TK, x, c.T, c.d,
+                      kTokBox0Pair))
     return MOE_ERR_CUDA;
   GemmArgs a{};
   a.gt = GroupTable{rows, brow, orow, bs, bstart};
   a.G = G;
   a.E = c.E;
-  a.m_blocks = ceil_div(c.I, 256);   // 256 gate rows (and their up rows) per CTA pair
+  a.m_blocks = ceil_div(c.I, 256);   // 256 gate rows and their up rows per CTA pair
   a.a_rows_per_group = 2 * c.I;
   a.a1_off = c.I;
   a.k_blocks = c.d / 64;
@@ -254,11 +288,12 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   // down: A = W2 rows (two 128-row boxes), B = activations
   GemmMaps m2;
   if (!make_gemm_maps(&m2, w2, static_cast<uint64_t>(c.E) * c.d, c.S > 0 ? ws2 : nullptr,
-                      static_cast<uint64_t>(c.S) * c.d, act, R, nullptr, 0, c.I, kTokBox0Pair))
+                      static_cast<uint64_t>(c.S) * c.d, 128, act, R, nullptr, 0, c.I,
+                      kTokBox0Pair))
     return MOE_ERR_CUDA;
   GemmArgs b = a;
   b.gt = GroupTable{rows, orow, orow, bs, bstart};
-  b.m_blocks = ceil_div(c.d, 512);   // 2 x 256 rows of W2 per CTA pair
+  b.m_blocks = ceil_div(c.d, 512);   // 512 rows of W2 per CTA pair
   b.a_rows_per_group = c.d;
   b.a1_off = 256;
   b.k_blocks = c.I / 64;
@@ -267,6 +302,87 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   b.out_cols = c.d;
   b.out = y;
   return launch_gemm_tc(GM_DOWN, m2, b, grid, st);
+}
+
+moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,
+                            const int32_t* offsets, const int32_t* counts,
+                            const moe_fp8_weights_t& w, void* act, float* act_s, void* y,
+                            void* ws, cudaStream_t st) {
+  const int G = c.E + c.S;
+  const Fp8Rows fr = fp8_rows(c);
+  int32_t* tab = static_cast<int32_t*>(ws);
+  int32_t* rows = tab;
+  int32_t* brow = rows + (G + 1);
+  int32_t* orow = brow + (G + 1);
+  int32_t* bs = orow + (G + 1);
+  int32_t* bstart = bs + (G + 1);
+  const GroupLayout lay{static_cast<int>(fr.P), static_cast<int>(fr.P), static_cast<int>(fr.Tp),
+                        128};
+  moe_status_t s = launch_build_groups(offsets, counts, c.T, c.E, c.S, lay, rows, brow, orow, bs,
+                                       bstart, st);
+  if (s != MOE_OK) return s;
+  const bool sh = c.S > 0;
+
+  // gate/up + SwiGLU + e4m3 quantisation of act (1 x 128 along I)
+  Fp8GemmMaps m1;
+  if (!make_fp8_maps(&m1, w.w13, static_cast<uint64_t>(c.E) * 2 * c.I, sh ? w.ws13 : nullptr,
+                     static_cast<uint64_t>(c.S) * 2 * c.I, xq, fr.rows_in, xs, c.d))
+    return MOE_ERR_CUDA;
+  Fp8GemmArgs a{};
+  a.gt = GroupTable{rows, brow, orow, bs, bstart};
+  a.G = G;
+  a.E = c.E;
+  a.m_blocks = c.I / 128;
+  a.a_rows_per_group = 2 * c.I;
+  a.a1_off = c.I;
+  a.k_blocks = c.d / 128;
+  a.w_scale[0] = w.w13_scale;
+  a.w_scale[1] = sh ? w.ws13_scale : w.w13_scale;
+  a.out_ld = c.I;
+  a.out_cols = c.I;
+  a.out = act;
+  a.out_scale = act_s;
+  a.out_scale_ld = fr.rows_out;
+  a.status = device_status_word();
+  a.timeout_ns = kWaitTimeoutNs;
+  if ((s = launch_fp8_gemm(GM_GATEUP, m1, a, st)) != MOE_OK) return s;
+
+  // down: A = W2 blocks, B = quantised activations
+  Fp8GemmMaps m2;
+  if (!make_fp8_maps(&m2, w.w2, static_cast<uint64_t>(c.E) * c.d, sh ? w.ws2 : nullptr,
+                     static_cast<uint64_t>(c.S) * c.d, act, fr.rows_out, act_s, c.I))
+    return MOE_ERR_CUDA;
+  Fp8GemmArgs b = a;
+  b.gt = GroupTable{rows, orow, orow, bs, bstart};
+  b.m_blocks = ceil_div(c.d, 256);
+  b.a_rows_per_group = c.d;
+  b.a1_off = 128;
+  b.k_blocks = c.I / 128;
+  b.w_scale[0] = w.w2_scale;
+  b.w_scale[1] = sh ? w.ws2_scale : w.w2_scale;
+  b.out_ld = c.d;
+  b.out_cols = c.d;
+  b.out = y;
+  b.out_scale = nullptr;
+  b.out_scale_ld = 0;
+  return launch_fp8_gemm(GM_DOWN, m2, b, st);
+}
+
+moe_status_t check_fp8_weights(const moe_cfg_t& c, const moe_fp8_weights_t* w) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (!w->w13 || !w->w2 || !w->w13_scale || !w->w2_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->w13) || !aligned16(w->w2)) return MOE_ERR_INVALID_ARG;
+  if (c.S > 0 && (!w->ws13 || !w->ws2 || !w->ws13_scale || !w->ws2_scale ||
+                  !aligned16(w->ws13) || !aligned16(w->ws2)))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+long long combine_shared0(const moe_cfg_t& c) {
+  return is_fp8(c) ? fp8_rows(c).P : static_cast<long long>(c.T) * c.K;
+}
+long long combine_shared_stride(const moe_cfg_t& c) {
+  return is_fp8(c) ? fp8_rows(c).Tp : c.T;
 }
 
 }  // namespace
@@ -289,8 +405,10 @@ moe_status_t moe_check_cfg(const moe_cfg_t* cfg) {
   if (c.act_dtype < MOE_F32 || c.act_dtype > MOE_E4M3 || c.wgt_dtype < MOE_F32 ||
       c.wgt_dtype > MOE_E4M3)
     return MOE_ERR_INVALID_ARG;
-  if (c.act_dtype != c.wgt_dtype || c.act_dtype == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
-  const long long rows = static_cast<long long>(c.T) * c.K + static_cast<long long>(c.S) * c.T;
+  const bool fp8 = c.act_dtype == MOE_BF16 && c.wgt_dtype == MOE_E4M3;
+  if ((c.act_dtype != c.wgt_dtype && !fp8) || c.act_dtype == MOE_E4M3) return MOE_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(c.T) * c.K + static_cast<long long>(c.S) * c.T +
+                         4LL * c.E + 4LL * (c.S + 1);
   if (rows >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
   if (c.act_dtype == MOE_BF16 && (c.d % 128 != 0 || c.I % 128 != 0)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -326,6 +444,7 @@ moe_status_t moe_dispatch(const moe_cfg_t* cfg, const void* x, const int32_t* id
   moe_status_t s = moe_check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_cfg_t& c = *cfg;
+  if (is_fp8(c)) return MOE_ERR_UNSUPPORTED;   // FP8 layers: the *_fp8 entry points
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (c.T > 0) {
     if ((s = check_ptrs(c, {x, xp}, {idx, perm_tok, pos})) != MOE_OK) return s;
@@ -343,6 +462,7 @@ moe_status_t moe_experts(const moe_cfg_t* cfg, const void* xp, const void* x,
   moe_status_t s = moe_check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_cfg_t& c = *cfg;
+  if (is_fp8(c)) return MOE_ERR_UNSUPPORTED;   // FP8 layers: the *_fp8 entry points
   if (c.T == 0) return MOE_OK;
   if ((s = check_ptrs(c, {xp, x, w13, w2, act, y}, {offsets})) != MOE_OK) return s;
   if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
@@ -392,6 +512,7 @@ moe_status_t moe_experts_static(const moe_cfg_t* cfg, const void* xp, const void
   moe_status_t s = moe_check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_cfg_t& c = *cfg;
+  if (is_fp8(c)) return MOE_ERR_UNSUPPORTED;   // FP8 layers: the *_fp8 entry points
   if (c.E + c.S > kStaticMaxGroups) return MOE_ERR_INVALID_ARG;
   if (c.T == 0) return MOE_OK;
   if ((s = check_ptrs(c, {xp, x, w13, w2, act, y}, {offsets})) != MOE_OK) return s;
@@ -410,7 +531,8 @@ moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y, const float* gates
   if (c.T == 0) return MOE_OK;
   if ((s = check_ptrs(c, {y, out}, {gates, pos})) != MOE_OK) return s;
   if (c.add_residual && (s = check_ptrs(c, {x}, {})) != MOE_OK) return s;
-  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d, c.add_residual,
+  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d,
+                        combine_shared0(c), combine_shared_stride(c), c.add_residual,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -432,6 +554,7 @@ moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centro
   moe_status_t s = moe_check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_cfg_t& c = *cfg;
+  if (is_fp8(c)) return MOE_ERR_UNSUPPORTED;   // FP8 layers: the *_fp8 entry points
   if (!counts) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c.T == 0) {
@@ -458,8 +581,100 @@ moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centro
   if ((s = do_experts(c, xp, x, offsets, w13, w2, ws13, ws2, act, y, at<void>(ws, L.experts),
                       st)) != MOE_OK)
     return s;
-  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d, c.add_residual,
+  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d,
+                        static_cast<long long>(c.T) * c.K, c.T, c.add_residual,
                         st);
+}
+
+moe_status_t moe_fp8_rows(const moe_cfg_t* cfg, int64_t* rows_in, int64_t* rows_out,
+                          int64_t* shared_row) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!is_fp8(*cfg)) return MOE_ERR_INVALID_ARG;
+  const Fp8Rows r = fp8_rows(*cfg);
+  if (rows_in) *rows_in = r.rows_in;
+  if (rows_out) *rows_out = r.rows_out;
+  if (shared_row) *shared_row = r.P;
+  return MOE_OK;
+}
+
+moe_status_t moe_dispatch_fp8(const moe_cfg_t* cfg, const void* x, const int32_t* idx,
+                              int32_t* counts, int32_t* offsets, void* xq, float* xq_scale,
+                              int32_t* perm_tok, int32_t* pos, void* ws, size_t ws_bytes,
+                              void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!is_fp8(c)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0) {
+    if ((s = check_ptrs(c, {x, xq}, {idx, perm_tok, pos, xq_scale})) != MOE_OK) return s;
+  }
+  if ((s = check_ws(ws, ws_bytes, dispatch_ws(c))) != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = launch_dispatch_index(idx, c.T, c.K, c.E, 4, counts, offsets, perm_tok, pos,
+                                 static_cast<int32_t*>(ws), st)) != MOE_OK)
+    return s;
+  const Fp8Rows fr = fp8_rows(c);
+  return launch_scatter_quant(x, c.T, c.K, c.d, pos, c.S > 0 ? static_cast<int>(fr.P) : -1, xq,
+                              xq_scale, fr.rows_in, st);
+}
+
+moe_status_t moe_experts_fp8(const moe_cfg_t* cfg, const void* xq, const float* xq_scale,
+                             const int32_t* offsets, const int32_t* counts,
+                             const moe_fp8_weights_t* w, void* act, float* act_scale, void* y,
+                             void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!is_fp8(c)) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if ((s = check_ptrs(c, {xq, act, y}, {xq_scale, offsets, counts, act_scale})) != MOE_OK)
+    return s;
+  if ((s = check_fp8_weights(c, w)) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, experts_ws(c))) != MOE_OK) return s;
+  return do_experts_fp8(c, xq, xq_scale, offsets, counts, *w, act, act_scale, y, ws,
+                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_forward_fp8(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                             const float* bias, const moe_fp8_weights_t* w, int32_t* idx,
+                             float* gates, int32_t* counts, void* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!is_fp8(c)) return MOE_ERR_INVALID_ARG;
+  if (!counts) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) {
+    TraceScope tr(st, "forward_empty");
+    cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
+    return launch_status();
+  }
+  if ((s = check_ptrs(c, {x, centroids, out}, {bias, idx, gates})) != MOE_OK) return s;
+  if ((s = check_fp8_weights(c, w)) != MOE_OK) return s;
+  const ForwardLayout L = forward_layout(c);
+  if ((s = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return s;
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  const Fp8Rows fr = fp8_rows(c);
+  if ((s = do_route(c, x, centroids, bias, idx, gates, at<void>(ws, L.route), st)) != MOE_OK)
+    return s;
+  if ((s = launch_dispatch_index(idx, c.T, c.K, c.E, 4, counts, offsets, perm, pos,
+                                 at<int32_t>(ws, L.dispatch), st)) != MOE_OK)
+    return s;
+  if ((s = launch_scatter_quant(x, c.T, c.K, c.d, pos, c.S > 0 ? static_cast<int>(fr.P) : -1,
+                                at<void>(ws, L.xp), at<float>(ws, L.xs), fr.rows_in, st)) !=
+      MOE_OK)
+    return s;
+  if ((s = do_experts_fp8(c, at<void>(ws, L.xp), at<float>(ws, L.xs), offsets, counts, *w,
+                          at<void>(ws, L.act), at<float>(ws, L.act_s), at<void>(ws, L.y),
+                          at<void>(ws, L.experts), st)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, at<void>(ws, L.y), gates, pos, x, out, c.T, c.K, c.S, c.d,
+                        fr.P, fr.Tp, c.add_residual, st);
 }
 
 moe_status_t moe_get_status(void* stream) {

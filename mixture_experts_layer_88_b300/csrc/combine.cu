@@ -1,7 +1,9 @@
 // Gate-weighted combine and the balancing-bias update of a DeepSeekMoE layer.
 //
 // Combine ("DeepSeekMoE架构解析", section 3.1: output = u + shared + routed):
-//   out_t = sum_k g_{t,k} y[pos[t,k]] + sum_s y[T*K + s*T + t] (+ u_t)
+//   out_t = sum_k g_{t,k} y[pos[t,k]] + sum_s y[shared0 + s*stride + t] (+ u_t)
+// (shared rows: shared0 = T*K, stride = T in the bf16/fp32 layout; the FP8
+// layout places them after the padded routed rows)
 // summed in fp32 in that fixed order.  One thread owns 8 consecutive
 // channels (one 16-byte vector) of one token: the K + S + 1 source rows are
 // gathered with 16-byte loads, the output written with one 16-byte store.
@@ -37,7 +39,7 @@ __device__ __forceinline__ void bf16x8_add(float (&acc)[8], const uint4& v) {
 __global__ void __launch_bounds__(128) combine_bf16_kernel(
     const uint4* __restrict__ y, const float* __restrict__ gates, const int32_t* __restrict__ pos,
     const uint4* __restrict__ x, uint4* __restrict__ out, int T, int K, int S, int vpr,
-    int add_residual) {
+    long long shared0, long long shared_stride, int add_residual) {
   const int v = blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= vpr) return;
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
@@ -49,9 +51,8 @@ __global__ void __launch_bounds__(128) combine_bf16_kernel(
     const float g = __ldg(gates + static_cast<size_t>(t) * K + k);
     bf16x8_fma(acc, __ldg(y + static_cast<size_t>(r) * vpr + v), g);
   }
-  const size_t shared0 = static_cast<size_t>(T) * K;
   for (int s = 0; s < S; ++s)
-    bf16x8_add(acc, __ldg(y + (shared0 + static_cast<size_t>(s) * T + t) * vpr + v));
+    bf16x8_add(acc, __ldg(y + static_cast<size_t>(shared0 + s * shared_stride + t) * vpr + v));
   if (add_residual) bf16x8_add(acc, __ldg(x + static_cast<size_t>(t) * vpr + v));
   uint4 o;
   __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(128) combine_bf16_kernel(
 __global__ void __launch_bounds__(128) combine_f32_kernel(
     const float* __restrict__ y, const float* __restrict__ gates, const int32_t* __restrict__ pos,
     const float* __restrict__ x, float* __restrict__ out, int T, int K, int S, int d,
-    int add_residual) {
+    long long shared0, long long shared_stride, int add_residual) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= d) return;
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
@@ -73,8 +74,8 @@ __global__ void __launch_bounds__(128) combine_f32_kernel(
     const int r = __ldg(pos + static_cast<size_t>(t) * K + k);
     acc = fmaf(__ldg(gates + static_cast<size_t>(t) * K + k), __ldg(y + static_cast<size_t>(r) * d + c), acc);
   }
-  const size_t shared0 = static_cast<size_t>(T) * K;
-  for (int s = 0; s < S; ++s) acc += __ldg(y + (shared0 + static_cast<size_t>(s) * T + t) * d + c);
+  for (int s = 0; s < S; ++s)
+    acc += __ldg(y + static_cast<size_t>(shared0 + s * shared_stride + t) * d + c);
   if (add_residual) acc += __ldg(x + static_cast<size_t>(t) * d + c);
   out[static_cast<size_t>(t) * d + c] = acc;
   }
@@ -123,7 +124,8 @@ __global__ void __launch_bounds__(1024) update_bias_kernel(const int32_t* __rest
 
 moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, const int32_t* pos,
                             const void* x, void* out, int T, int K, int S, int d,
-                            int add_residual, cudaStream_t stream) {
+                            long long shared0, long long shared_stride, int add_residual,
+                            cudaStream_t stream) {
   if (T <= 0) return MOE_OK;
   TraceScope tr(stream, "combine");
   if (act_dtype == MOE_BF16) {
@@ -131,13 +133,13 @@ moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, co
     dim3 grid(ceil_div(vpr, 128), T < 65535 ? T : 65535);
     combine_bf16_kernel<<<grid, 128, 0, stream>>>(
         static_cast<const uint4*>(y), gates, pos, static_cast<const uint4*>(x),
-        static_cast<uint4*>(out), T, K, S, vpr, add_residual);
+        static_cast<uint4*>(out), T, K, S, vpr, shared0, shared_stride, add_residual);
   } else {
     dim3 grid(ceil_div(d, 128), T < 65535 ? T : 65535);
     combine_f32_kernel<<<grid, 128, 0, stream>>>(static_cast<const float*>(y), gates, pos,
                                                   static_cast<const float*>(x),
                                                   static_cast<float*>(out), T, K, S, d,
-                                                  add_residual);
+                                                  shared0, shared_stride, add_residual);
   }
   return launch_status();
 }

@@ -12,6 +12,8 @@
 //           ascending token order; writes pos and perm_tok
 //   scatter each token row is read once (16-byte vectors) and written to its
 //           K destination rows of xp
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -54,8 +56,11 @@ __global__ void __launch_bounds__(kDispatchChunk) count_kernel(const int32_t* __
   }
 }
 
+// offsets = exclusive prefix over experts of counts rounded up to `pad` rows
+// (pad = 1: dense; pad = 4: every expert's rows start 16-byte aligned for the
+// fp32 scale runs of the FP8 path)
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int nchunks,
-                                                    int E, int32_t* __restrict__ counts,
+                                                    int E, int pad, int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets) {
   __shared__ int warp_sums[32];
   const int e = threadIdx.x;
@@ -79,9 +84,10 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
       running += h;
     }
   }
-  // exclusive scan of counts over experts
+  // exclusive scan of the (padded) counts over experts
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int x = running;
+  const int span = (running + pad - 1) / pad * pad;
+  int x = span;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -99,11 +105,11 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
     warp_sums[lane] = s;
   }
   __syncthreads();
-  const int before = (w > 0 ? warp_sums[w - 1] : 0) + x - running;
+  const int before = (w > 0 ? warp_sums[w - 1] : 0) + x - span;
   if (e < E) {
     counts[e] = running;
     offsets[e] = before;
-    if (e == E - 1) offsets[E] = before + running;
+    if (e == E - 1) offsets[E] = before + span;
   }
 }
 
@@ -154,7 +160,101 @@ __global__ void __launch_bounds__(256) scatter_kernel(const V* __restrict__ x, i
   }
 }
 
+// FP8 dispatch: each token row is read once (bf16), cut into 1 x 128 tiles
+// (V3 walk-through, section 4.3), each tile scaled by 448 / max|x| and
+// rounded to e4m3, and written to the token's K expert rows and to its
+// shared-expert row.  Scales (max|x| / 448) go K-block-major:
+// xs[kb * ld_s + row].  Sixteen threads hold one tile (8 values each).
+__global__ void __launch_bounds__(256) scatter_quant_kernel(
+    const uint4* __restrict__ x, int T, int K, int d, const int32_t* __restrict__ pos,
+    int shared_row, uint2* __restrict__ xq, float* __restrict__ xs, long long ld_s) {
+  const int t = blockIdx.x;
+  if (t >= T) return;
+  __shared__ int dst[kMaxK + 1];
+  for (int k = threadIdx.x; k < K; k += blockDim.x) dst[k] = __ldg(pos + static_cast<size_t>(t) * K + k);
+  if (threadIdx.x == 0) dst[K] = shared_row >= 0 ? shared_row + t : -1;
+  __syncthreads();
+  const int vpr = d / 8;                        // 8-element vectors per row
+  for (int base = 0; base < vpr; base += blockDim.x) {
+    const int v = base + threadIdx.x;
+    const bool in = v < vpr;                    // a 16-lane group is all in or all out
+    float f[8];
+    if (in) {
+      const uint4 raw = __ldg(x + static_cast<size_t>(t) * vpr + v);
+      const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 ff = __bfloat1622float2(hb[i]);
+        f[2 * i] = ff.x;
+        f[2 * i + 1] = ff.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (!in) continue;
+    const float inv = m > 0.f ? 448.0f / m : 0.f;
+    uint2 q;
+    uint16_t* qh = reinterpret_cast<uint16_t*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      qh[i] = __nv_cvt_float2_to_fp8x2(make_float2(f[2 * i] * inv, f[2 * i + 1] * inv),
+                                       __NV_SATFINITE, __NV_E4M3);
+    const int kb = v >> 4;
+    for (int k = 0; k <= K; ++k) {
+      const int r = dst[k];
+      if (r < 0) continue;
+      xq[static_cast<size_t>(r) * vpr + v] = q;
+      if ((threadIdx.x & 15) == 0) xs[kb * ld_s + r] = m / 448.0f;
+    }
+  }
+}
+
 }  // namespace
+
+moe_status_t launch_scatter_quant(const void* x, int T, int K, int d, const int32_t* pos,
+                                  int shared_row, void* xq, float* xs, long long ld_s,
+                                  cudaStream_t stream) {
+  if (T <= 0) return MOE_OK;
+  TraceScope tr(stream, "dispatch_scatter_fp8");
+  scatter_quant_kernel<<<T, 256, 0, stream>>>(static_cast<const uint4*>(x), T, K, d, pos,
+                                              shared_row, static_cast<uint2*>(xq), xs, ld_s);
+  return launch_status();
+}
+
+moe_status_t launch_dispatch_index(const int32_t* idx, int T, int K, int E, int pad,
+                                   int32_t* counts, int32_t* offsets, int32_t* perm_tok,
+                                   int32_t* pos, int32_t* hist, cudaStream_t stream) {
+  if (T <= 0) {
+    TraceScope tr(stream, "dispatch_empty");
+    cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
+    cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), stream);
+    return launch_status();
+  }
+  const int nchunks = ceil_div(T, kDispatchChunk);
+  const size_t mask_bytes = sizeof(uint32_t) * WARPS * E;
+  {
+    TraceScope tr(stream, "dispatch_count");
+    count_kernel<<<nchunks, kDispatchChunk, mask_bytes, stream>>>(idx, T, K, E, hist,
+                                                                  device_status_word());
+  }
+  {
+    TraceScope tr(stream, "dispatch_scan");
+    scan_kernel<<<1, 1024, 0, stream>>>(hist, nchunks, E, pad, counts, offsets);
+  }
+  {
+    TraceScope tr(stream, "dispatch_rank");
+    rank_kernel<<<nchunks, kDispatchChunk, mask_bytes, stream>>>(idx, T, K, E, hist, offsets,
+                                                                 pos, perm_tok,
+                                                                 device_status_word());
+  }
+  return launch_status();
+}
 
 moe_status_t launch_dispatch(const void* x, size_t row_bytes, const int32_t* idx, int T, int K,
                              int E, int32_t* counts, int32_t* offsets, void* xp,
@@ -175,7 +275,7 @@ moe_status_t launch_dispatch(const void* x, size_t row_bytes, const int32_t* idx
   }
   {
     TraceScope tr(stream, "dispatch_scan");
-    scan_kernel<<<1, 1024, 0, stream>>>(hist, nchunks, E, counts, offsets);
+    scan_kernel<<<1, 1024, 0, stream>>>(hist, nchunks, E, 1, counts, offsets);
   }
   {
     TraceScope tr(stream, "dispatch_rank");

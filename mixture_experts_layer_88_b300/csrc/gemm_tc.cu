@@ -1,4 +1,4 @@
-// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMA +
+// Persistent grouped GEMMs on the 5th-generation tensor cores (tcgen05 + TMA +
 // TMEM) for the expert FFNs and the router of a DeepSeekMoE layer.
 //
 // Weights sit in the MMA's M slot and tokens in its N slot ("swap-AB"):
@@ -6,33 +6,34 @@
 // so a ragged expert group costs at most 15 padded token columns instead of a
 // partly empty 128-row tile, and small decode batches still use M = 128.
 //
-// The expert GEMMs run on CTA pairs (clusters of two, tcgen05 cta_group::2):
-// one MMA of M = 256 weight rows spans both CTAs, each CTA holding 128 rows of
-// A and of the accumulator and half of the token rows of B.  Per CTA that is
-// 48 KB of operands per 64-wide K step instead of 64 KB for the same FLOPs,
-// which is what bounds this GEMM: the bytes each SM takes in per FLOP.
-// The router runs the single-CTA form (CG = 1) of the same kernel.
+// Expert GEMMs (expert_gemm_kernel) run on CTA pairs: clusters of two CTAs and
+// tcgen05 cta_group::2, so one MMA of M = 256 weight rows spans both CTAs;
+// each CTA holds 128 rows of A and of the accumulator and half of the tile's
+// token rows of B.  One tile = one group g, one weight-row block and one
+// token block of N <= 256 tokens; each CTA runs two accumulators of 128 lanes
+// x N fp32 columns (all 512 TMEM columns) that share the token operand:
+//   GATEUP: a pair covers 256 intermediate columns c0..c0+255.  CTA r: acc0 =
+//           gate rows c0+128r .. +127, acc1 = the matching up rows (offset I);
+//           the epilogue writes act = SiLU(acc0) * acc1   (SwiGLU)
+//   DOWN:   a pair covers 512 rows m..m+511 of W2.  CTA r: acc0 = rows
+//           m+128r .., acc1 = rows m+256+128r ..; the epilogue writes y (bf16)
+// Per CTA that is 48 KB of operands per 64-wide K step for 8.4 MFLOP.  The
+// two accumulators fill TMEM, so a tile's MMAs wait for the previous tile's
+// epilogue; eight epilogue warps keep that drain short.
 //
-// One tile = one group g, one weight-row block and one token block (<= 256
-// tokens).  Each tile runs two accumulators that share the token operand:
-//   GATEUP: acc0 = gate rows of W13_g, acc1 = the matching up rows (offset I);
-//           epilogue writes act = SiLU(acc0) * acc1   (SwiGLU)
-//   DOWN:   acc0 / acc1 = two row blocks of W2_g; epilogue writes y (bf16)
-//   ROUTER: acc0 / acc1 = centroids [m, m+128) / [m+128, m+256); epilogue
-//           writes fp32 partial logits of one K split
-// CTA r of a pair owns accumulator rows [r*128, r*128+128) of each M = 256
-// block, so each CTA's epilogue is independent.
+// The router GEMM (router_gemm_kernel) runs one CTA per tile: two 128-row
+// centroid boxes, one token block, one K split; fp32 partial logits out.
 //
-// Warp roles (192 threads per CTA):
-//   warp 0      TMA producer: its CTA's two 128x64 weight boxes and its half
-//               of the token rows (at most five boxes) per pipeline stage; both
+// Warp roles of the expert kernel (320 threads per CTA):
+//   warp 0      TMA producer: per 64-wide K step, this CTA's two 128-row weight
+//               boxes and its half of the token rows (at most five boxes); both
 //               CTAs' bytes are counted on the even CTA's "full" barrier
 //   warp 1      TMEM owner; in the even CTA also the MMA issuer (one thread
-//               issues tcgen05.mma K=16, twice per K step, and commits to
-//               both CTAs' barriers)
-//   warps 2..5  epilogue: tcgen05.ld from this CTA's TMEM (warp w reads lanes
-//               32*(w%4)..), then one arrival per warp on the even CTA's
-//               "tmem empty" barrier
+//               issues tcgen05.mma M=256 N=tokens K=16 twice per K step and
+//               commits to both CTAs)
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. of its CTA, the
+//               four warps of each half take alternate 16-column chunks, then
+//               one arrival per warp on the even CTA's "tmem empty" barrier
 //
 // Every barrier wait is bounded: after `timeout_ns` without progress the CTA
 // raises an abort flag, lets the TMA loads it issued land, waits for its own
@@ -48,72 +49,48 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128;              // weight rows per accumulator per CTA (MMA M / CG)
-constexpr int BN_MAX = 256;          // tokens per tile (MMA N, <= 256)
-constexpr int BK = 64;               // K elements per stage = one 128-byte row
-constexpr uint32_t A_BOX_BYTES = BM * BK * 2;             // 16 KB
-constexpr uint32_t B_ROW_BYTES = BK * 2;                  // 128 B per token row
-constexpr uint32_t TMEM_COLS = 512;  // acc0 at column 0, acc1 at column 256
-constexpr int NUM_THREADS = 192;
-
-template <int CG> struct Cfg {
-  static constexpr int STAGES = CG == 1 ? 3 : 4;
-  // two weight boxes + this CTA's share of the token rows
-  static constexpr uint32_t STAGE_BYTES = 2 * A_BOX_BYTES + (BN_MAX / CG) * BK * 2;
-  static constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-  static constexpr int TOK_BOX0 = 16 / CG;   // smallest token box height
-};
+constexpr int BK = 64;                        // K elements per stage = one 128-byte row
+constexpr uint32_t ROW_BYTES = BK * 2;        // 128 B per operand row per stage
+constexpr uint32_t TMEM_COLS = 512;
 
 struct Tile {
   int g, mb, tok0, ntok, nmma, kb0, kb1, split;
 };
 
-__device__ __forceinline__ int total_tiles(const GemmArgs& a, int mode) {
-  if (mode == GM_ROUTER) return a.router_nb * a.m_blocks * a.k_splits;
-  return a.gt.bstart[a.G] * a.m_blocks;
-}
-
-__device__ __forceinline__ void decode_tile(const GemmArgs& a, int mode, int tile, Tile& t) {
-  if (mode == GM_ROUTER) {
-    const int per_split = a.router_nb * a.m_blocks;
-    t.split = tile / per_split;
-    const int rem = tile - t.split * per_split;
-    t.mb = rem / a.router_nb;
-    const int nb = rem - t.mb * a.router_nb;
-    t.g = 0;
-    t.tok0 = nb * a.router_bs;
-    t.ntok = min(a.router_bs, a.router_T - t.tok0);
-    t.kb0 = t.split * a.k_per_split;
-    t.kb1 = min(a.k_blocks, t.kb0 + a.k_per_split);
-  } else {
-    // largest g with bstart[g] * m_blocks <= tile (groups with no blocks are skipped)
-    int lo = 0, hi = a.G - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(a.gt.bstart + mid) * a.m_blocks <= tile) lo = mid; else hi = mid - 1;
-    }
-    t.g = lo;
-    const int b0 = __ldg(a.gt.bstart + lo);
-    const int nbk = __ldg(a.gt.bstart + lo + 1) - b0;
-    const int local = tile - b0 * a.m_blocks;
-    t.mb = local / nbk;
-    const int nb = local - t.mb * nbk;
-    const int bs = __ldg(a.gt.bs + lo);
-    t.tok0 = nb * bs;
-    t.ntok = min(bs, __ldg(a.gt.rows + lo) - t.tok0);
-    t.split = 0;
-    t.kb0 = 0;
-    t.kb1 = a.k_blocks;
+__device__ __forceinline__ void decode_group_tile(const GemmArgs& a, int tile, Tile& t) {
+  // largest g with bstart[g] * m_blocks <= tile (groups with no blocks are skipped)
+  int lo = 0, hi = a.G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.gt.bstart + mid) * a.m_blocks <= tile) lo = mid; else hi = mid - 1;
   }
+  t.g = lo;
+  const int b0 = __ldg(a.gt.bstart + lo);
+  const int nbk = __ldg(a.gt.bstart + lo + 1) - b0;
+  const int local = tile - b0 * a.m_blocks;
+  t.mb = local / nbk;
+  const int nb = local - t.mb * nbk;
+  const int bs = __ldg(a.gt.bs + lo);
+  t.tok0 = nb * bs;
+  t.ntok = min(bs, __ldg(a.gt.rows + lo) - t.tok0);
+  t.split = 0;
+  t.kb0 = 0;
+  t.kb1 = a.k_blocks;
   t.nmma = (t.ntok + 15) & ~15;
 }
 
-// First weight row of the tile's M block (both CTAs of a pair; CTA r then
-// adds r * 128).  GATEUP blocks are CG*128 gate rows; DOWN and ROUTER blocks
-// are 2*CG*128 rows (acc1 = the second half).
-template <int CG>
-__device__ __forceinline__ int m_block_rows(int mode) {
-  return mode == GM_GATEUP ? CG * BM : 2 * CG * BM;
+__device__ __forceinline__ void decode_router_tile(const GemmArgs& a, int tile, Tile& t) {
+  const int per_split = a.router_nb * a.m_blocks;
+  t.split = tile / per_split;
+  const int rem = tile - t.split * per_split;
+  t.mb = rem / a.router_nb;
+  const int nb = rem - t.mb * a.router_nb;
+  t.g = 0;
+  t.tok0 = nb * a.router_bs;
+  t.ntok = min(a.router_bs, a.router_T - t.tok0);
+  t.kb0 = t.split * a.k_per_split;
+  t.kb1 = min(a.k_blocks, t.kb0 + a.k_per_split);
+  t.nmma = (t.ntok + 15) & ~15;
 }
 
 // Bounded wait by lane 0, result broadcast to the warp.  CLUSTER: the
@@ -133,21 +110,52 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok != 0;
 }
 
+// SiLU(g) * u with the fast reciprocal: g * u / (1 + e^-g).
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  return g / (1.0f + __expf(-g)) * u;
+  return __fdividef(g * u, 1.0f + __expf(-g));
 }
 
-template <int MODE, int CG>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
-  constexpr int STAGES = Cfg<CG>::STAGES;
-  constexpr uint32_t STAGE_BYTES = Cfg<CG>::STAGE_BYTES;
+// Token rows of one stage: one TMA box per set bit of rows / box0, largest first.
+template <bool PAIR>
+__device__ __forceinline__ void load_token_rows(uint8_t* dst, const CUtensorMap* maps,
+                                                uint32_t box0, int rows, uint64_t* bar,
+                                                uint32_t bar_caddr, int k0, int row0) {
+  int done = 0;
+#pragma unroll
+  for (int bi = kTokBoxes - 1; bi >= 0; --bi) {
+    const int h = static_cast<int>(box0) << bi;
+    if (rows & h) {
+      if constexpr (PAIR)
+        tc::tma_load_2d_pair(dst + done * ROW_BYTES, maps + bi, bar_caddr, k0, row0 + done);
+      else
+        tc::tma_load_2d(dst + done * ROW_BYTES, maps + bi, bar, k0, row0 + done);
+      done += h;
+    }
+  }
+}
+
+// ============================================================================
+// Expert GEMMs on CTA pairs
+// ============================================================================
+
+constexpr int EX_STAGES = 4;
+constexpr uint32_t EX_A_BOX_BYTES = 128 * ROW_BYTES;      // 16 KB: one 128-row weight box
+constexpr uint32_t EX_B_BYTES = 128 * ROW_BYTES;          // 16 KB: up to 128 token rows
+constexpr uint32_t EX_STAGE_BYTES = 2 * EX_A_BOX_BYTES + EX_B_BYTES;
+constexpr int EX_EPI_WARPS = 8;
+constexpr int EX_THREADS = 64 + 32 * EX_EPI_WARPS;
+constexpr size_t EX_SMEM_BYTES = EX_STAGES * EX_STAGE_BYTES + 1024 + 256;
+static_assert(EX_SMEM_BYTES <= 227 * 1024, "expert GEMM shared memory");
+
+template <int MODE>
+__global__ void __launch_bounds__(EX_THREADS, 1)
+    expert_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + EX_STAGES * EX_STAGE_BYTES);
+  uint64_t* empty = full + EX_STAGES;
+  uint64_t* tfull = empty + EX_STAGES;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -155,33 +163,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = CG == 2 ? tc::cluster_ctarank() : 0u;
-  const int cluster = blockIdx.x / CG, nclusters = gridDim.x / CG;
+  const uint32_t rank = tc::cluster_ctarank();
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < EX_STAGES; ++s) {
       tc::mbar_init(full + s, 1);     // the even CTA expects both CTAs' bytes
       tc::mbar_init(empty + s, 1);
     }
     tc::mbar_init(tfull, 1);
-    tc::mbar_init(tempty, CG * 4);    // every epilogue warp of the pair
+    tc::mbar_init(tempty, 2 * EX_EPI_WARPS);  // every epilogue warp of the pair
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   if (warp == 0 && lane < 2 + 2 * kTokBoxes) {
-    const CUtensorMap* m = lane < 2 ? &maps.a[lane] : &maps.b[(lane - 2) / kTokBoxes][(lane - 2) % kTokBoxes];
+    const CUtensorMap* m =
+        lane < 2 ? &maps.a[lane] : &maps.b[(lane - 2) / kTokBoxes][(lane - 2) % kTokBoxes];
     tc::tma_prefetch_desc(m);
   }
   if (warp == 1) {
-    tc::tmem_alloc<CG>(tmem_slot, TMEM_COLS);
-    tc::tmem_relinquish<CG>();
+    tc::tmem_alloc<2>(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish<2>();
   }
   tc::tc_fence_before();
-  if constexpr (CG == 2) tc::cluster_sync_all(); else __syncthreads();
+  tc::cluster_sync_all();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = total_tiles(args, MODE);
+  const int ntiles = args.gt.bstart[args.G] * args.m_blocks;
   const unsigned long long tmo = args.timeout_ns;
 
   if (warp == 0) {
@@ -192,187 +201,311 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
       Tile t;
-      decode_tile(args, MODE, tile, t);
-      const bool second = (MODE != GM_ROUTER) && (t.g >= args.E);
+      decode_group_tile(args, tile, t);
+      const bool second = t.g >= args.E;
       const CUtensorMap* mA = &maps.a[second ? 1 : 0];
       const CUtensorMap* mB = maps.b[second ? 1 : 0];
       const int gl = second ? t.g - args.E : t.g;
-      const int half = t.nmma / CG;                // token rows this CTA loads
-      int a_row0, b_row;
-      if (MODE == GM_ROUTER) {
-        a_row0 = t.mb * 2 * BM;
-        b_row = t.tok0;
-      } else {
-        a_row0 = gl * args.a_rows_per_group + t.mb * m_block_rows<CG>(MODE) + rank * BM;
-        b_row = __ldg(args.gt.brow + t.g) + t.tok0 + rank * half;
-      }
+      const int half = t.nmma >> 1;                // token rows this CTA loads
+      // GATEUP: gate rows of this CTA and the matching up rows (+I);
+      // DOWN: W2 rows of this CTA in the two 256-row halves of the block
+      const int a_row0 = gl * args.a_rows_per_group +
+                         t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128;
       const int a_row1 = a_row0 + args.a1_off;
-      const uint32_t bytes = 2 * A_BOX_BYTES + half * B_ROW_BYTES;
+      const int b_row = __ldg(args.gt.brow + t.g) + t.tok0 + static_cast<int>(rank) * half;
+      const uint32_t bytes = 2 * EX_A_BOX_BYTES + half * ROW_BYTES;
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
         if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
         if (lane == 0) {
-          uint8_t* sa = smem + stage * STAGE_BYTES;
-          if constexpr (CG == 1) {
-            tc::mbar_arrive_expect_tx(full + stage, bytes);
-            tc::tma_load_2d(sa, mA, full + stage, kb * BK, a_row0);
-            tc::tma_load_2d(sa + A_BOX_BYTES, mA, full + stage, kb * BK, a_row1);
-          } else {
-            // Only the even CTA arrives, expecting the bytes of both CTAs; the
-            // odd CTA's loads just count their bytes on the even CTA's barrier.
-            // (The odd CTA reuses stage s only after the MMAs that consumed it
-            // completed, so its bytes always land in the phase they belong to.)
-            const uint32_t fb = tc::mapa_shared(tc::smem_u32(full + stage), 0);
-            if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, CG * bytes);
-            tc::tma_load_2d_pair(sa, mA, fb, kb * BK, a_row0);
-            tc::tma_load_2d_pair(sa + A_BOX_BYTES, mA, fb, kb * BK, a_row1);
-          }
-          // token rows: one box per set bit of half / TOK_BOX0, largest first
-          int done = 0;
-#pragma unroll
-          for (int bi = kTokBoxes - 1; bi >= 0; --bi) {
-            const int h = Cfg<CG>::TOK_BOX0 << bi;
-            if (half & h) {
-              uint8_t* dst = sa + 2 * A_BOX_BYTES + done * B_ROW_BYTES;
-              if constexpr (CG == 1)
-                tc::tma_load_2d(dst, mB + bi, full + stage, kb * BK, b_row + done);
-              else
-                tc::tma_load_2d_pair(dst, mB + bi, tc::mapa_shared(tc::smem_u32(full + stage), 0),
-                                     kb * BK, b_row + done);
-              done += h;
-            }
-          }
+          uint8_t* sa = smem + stage * EX_STAGE_BYTES;
+          // Only the even CTA arrives, expecting the bytes of both CTAs; the
+          // odd CTA's loads just count their bytes on the even CTA's barrier.
+          // (The odd CTA reuses stage s only after the MMAs that consumed it
+          // completed, so its bytes always land in the phase they belong to.)
+          const uint32_t fb = tc::mapa_shared(tc::smem_u32(full + stage), 0);
+          if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, 2 * bytes);
+          tc::tma_load_2d_pair(sa, mA, fb, kb * BK, a_row0);
+          tc::tma_load_2d_pair(sa + EX_A_BOX_BYTES, mA, fb, kb * BK, a_row1);
+          load_token_rows<true>(sa + 2 * EX_A_BOX_BYTES, mB, kTokBox0Pair, half, nullptr, fb,
+                                kb * BK, b_row);
         }
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == EX_STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok && (CG == 1 || rank == 0)) {
+    if (!ok && rank == 0) {
       // abort: let every load counted on this CTA's barriers land before exit
-      for (int s = 0; s < STAGES; ++s)
-        if (issued & (1u << s))
-          warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+      for (int s = 0; s < EX_STAGES; ++s)
+        if (issued & (1u << s)) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (CG == 1 || rank == 0) {
+    if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0, tphase = 0;
       bool ok = true, issued_any = false;
       for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
         Tile t;
-        decode_tile(args, MODE, tile, t);
-        if (!warp_wait<CG == 2>(tempty, tphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        decode_group_tile(args, tile, t);
+        if (!warp_wait<true>(tempty, tphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
         tc::tc_fence_after();
-        const uint32_t idesc = tc::idesc_bf16_f32(BM * CG, t.nmma);
+        const uint32_t idesc = tc::idesc_bf16_f32(256, t.nmma);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
           tc::tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t sa = tc::smem_u32(smem + stage * EX_STAGE_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t da0 = tc::smem_desc_sw128(sa + kk * 32);
-              const uint64_t da1 = tc::smem_desc_sw128(sa + A_BOX_BYTES + kk * 32);
-              const uint64_t db = tc::smem_desc_sw128(sa + 2 * A_BOX_BYTES + kk * 32);
+              const uint64_t da1 = tc::smem_desc_sw128(sa + EX_A_BOX_BYTES + kk * 32);
+              const uint64_t db = tc::smem_desc_sw128(sa + 2 * EX_A_BOX_BYTES + kk * 32);
               const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
-              tc::mma_bf16<CG>(tmem_base, da0, db, idesc, acc);
-              tc::mma_bf16<CG>(tmem_base + 256, da1, db, idesc, acc);
+              tc::mma_bf16<2>(tmem_base, da0, db, idesc, acc);
+              tc::mma_bf16<2>(tmem_base + 256, da1, db, idesc, acc);
             }
-            tc::mma_commit<CG>(empty + stage);   // frees the stage in both CTAs
+            tc::mma_commit<2>(empty + stage);   // frees the stage in both CTAs
           }
           issued_any = true;
           __syncwarp();
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == EX_STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        if (lane == 0) tc::mma_commit<CG>(tfull);  // accumulators complete, both CTAs
+        if (lane == 0) tc::mma_commit<2>(tfull);  // accumulators complete, both CTAs
         __syncwarp();
         tphase ^= 1u;
       }
       if (!ok && issued_any) {
-        if (lane == 0) tc::mma_commit<CG>(drain, 0x1);
+        if (lane == 0) tc::mma_commit<2>(drain, 0x1);
         __syncwarp();
         warp_wait(drain, 0, abort_flag, tmo);
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int row = q * 32 + lane;       // accumulator row = weight row in the box
-    const uint32_t tempty_addr =
-        CG == 2 ? tc::mapa_shared(tc::smem_u32(tempty), 0) : tc::smem_u32(tempty);
+    const int q = warp & 3;                      // TMEM lane quadrant of this warp
+    const int h = (warp - 2) >> 2;               // which alternate 16-column chunks
+    const uint32_t tempty_addr = tc::mapa_shared(tc::smem_u32(tempty), 0);
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t tphase = 0;
     for (int tile = cluster; tile < ntiles; tile += nclusters) {
       Tile t;
-      decode_tile(args, MODE, tile, t);
+      decode_group_tile(args, tile, t);
       if (!warp_wait(tfull, tphase, abort_flag, tmo)) break;
       tc::tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      int out_row0, col0, col1;
-      if (MODE == GM_ROUTER) {
-        out_row0 = t.tok0;
-        col0 = t.mb * 2 * BM + row;
-        col1 = col0 + BM;
-      } else {
-        out_row0 = __ldg(args.gt.orow + t.g) + t.tok0;
-        col0 = t.mb * m_block_rows<CG>(MODE) + static_cast<int>(rank) * BM + row;
-        col1 = col0 + CG * BM;   // DOWN: acc1 rows
-      }
-      const bool c0ok = col0 < args.out_cols, c1ok = col1 < args.out_cols;
-      for (int j0 = 0; j0 < t.nmma; j0 += 16) {
+      const size_t out_row0 = static_cast<size_t>(__ldg(args.gt.orow + t.g) + t.tok0);
+      // GATEUP: act column of acc0 (gate) and acc1 (up) of this lane
+      // DOWN:   y columns of acc0 and acc1 (256 rows apart)
+      const int col0 = t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128 +
+                       q * 32 + lane;
+      const int col1 = col0 + 256;
+      const bool c0ok = col0 < args.out_cols;
+      const bool c1ok = MODE == GM_DOWN && col1 < args.out_cols;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+      for (int j0 = h * 16; j0 < t.nmma; j0 += 32) {
         uint32_t r0[16], r1[16];
         tc::tmem_ld16(taddr + j0, r0);
         tc::tmem_ld16(taddr + 256 + j0, r1);
         tc::tmem_wait_ld(r0, r1);
-        const int jn = min(16, t.ntok - j0);
-        // fully unrolled with a predicate, so r0/r1 stay in registers
+        __nv_bfloat16* o = out + (out_row0 + j0) * args.out_ld;
+        const int jn = t.ntok - j0;
         if (MODE == GM_GATEUP) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
-                               static_cast<size_t>(out_row0 + j0) * args.out_ld + col0;
+          if (c0ok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0ok && j < jn)
-              out[static_cast<size_t>(j) * args.out_ld] = __float2bfloat16_rn(
-                  silu_mul(__uint_as_float(r0[j]), __uint_as_float(r1[j])));
-        } else if (MODE == GM_DOWN) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
-                               static_cast<size_t>(out_row0 + j0) * args.out_ld;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (j < jn) {
-              __nv_bfloat16* o = out + static_cast<size_t>(j) * args.out_ld;
-              if (c0ok) o[col0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
-              if (c1ok) o[col1] = __float2bfloat16_rn(__uint_as_float(r1[j]));
-            }
+            for (int j = 0; j < 16; ++j)
+              if (j < jn)
+                o[static_cast<size_t>(j) * args.out_ld + col0] = __float2bfloat16_rn(
+                    silu_mul(__uint_as_float(r0[j]), __uint_as_float(r1[j])));
           }
         } else {
-          float* out = static_cast<float*>(args.out) + t.split * args.out_split_stride +
-                       static_cast<size_t>(out_row0 + j0) * args.out_ld;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (j < jn) {
-              float* o = out + static_cast<size_t>(j) * args.out_ld;
-              if (c0ok) o[col0] = __uint_as_float(r0[j]);
-              if (c1ok) o[col1] = __uint_as_float(r1[j]);
+              __nv_bfloat16* oj = o + static_cast<size_t>(j) * args.out_ld;
+              if (c0ok) oj[col0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
+              if (c1ok) oj[col1] = __float2bfloat16_rn(__uint_as_float(r1[j]));
             }
           }
         }
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (CG == 2) tc::mbar_arrive_cluster(tempty_addr); else tc::mbar_arrive(tempty);
-      }
+      if (lane == 0) tc::mbar_arrive_cluster(tempty_addr);
       tphase ^= 1u;
     }
   }
 
   tc::tc_fence_before();
-  if constexpr (CG == 2) tc::cluster_sync_all(); else __syncthreads();
+  tc::cluster_sync_all();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc<CG>(tmem_base, TMEM_COLS);
+  if (warp == 1) tc::tmem_dealloc<2>(tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(args.status, ERRBIT_TIMEOUT);
+}
+
+// ============================================================================
+// Router GEMM: one CTA per tile
+// ============================================================================
+
+constexpr int RT_STAGES = 3;
+constexpr uint32_t RT_A_BOX_BYTES = 128 * ROW_BYTES;                     // 16 KB
+constexpr uint32_t RT_STAGE_BYTES = 2 * RT_A_BOX_BYTES + 256 * ROW_BYTES;  // 64 KB
+constexpr int RT_THREADS = 192;
+constexpr size_t RT_SMEM_BYTES = RT_STAGES * RT_STAGE_BYTES + 1024 + 256;
+
+__global__ void __launch_bounds__(RT_THREADS, 1)
+    router_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RT_STAGES * RT_STAGE_BYTES);
+  uint64_t* empty = full + RT_STAGES;
+  uint64_t* tfull = empty + RT_STAGES;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RT_STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    tc::mbar_init(tfull, 1);
+    tc::mbar_init(tempty, 4);    // one arrival per epilogue warp
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane < 1 + kTokBoxes) {
+    tc::tma_prefetch_desc(lane == 0 ? &maps.a[0] : &maps.b[0][lane - 1]);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc<1>(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish<1>();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = args.router_nb * args.m_blocks * args.k_splits;
+  const unsigned long long tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      Tile t;
+      decode_router_tile(args, tile, t);
+      const int a_row0 = t.mb * 256;
+      const uint32_t bytes = 2 * RT_A_BOX_BYTES + t.nmma * ROW_BYTES;
+      for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        if (lane == 0) {
+          uint8_t* sa = smem + stage * RT_STAGE_BYTES;
+          tc::mbar_arrive_expect_tx(full + stage, bytes);
+          tc::tma_load_2d(sa, &maps.a[0], full + stage, kb * BK, a_row0);
+          tc::tma_load_2d(sa + RT_A_BOX_BYTES, &maps.a[0], full + stage, kb * BK, a_row0 + 128);
+          load_token_rows<false>(sa + 2 * RT_A_BOX_BYTES, maps.b[0], kTokBox0Single, t.nmma,
+                                 full + stage, 0, kb * BK, t.tok0);
+        }
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        __syncwarp();
+        if (++stage == RT_STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) {
+      for (int s = 0; s < RT_STAGES; ++s)
+        if (issued & (1u << s)) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0, tphase = 0;
+    bool ok = true, issued_any = false;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      Tile t;
+      decode_router_tile(args, tile, t);
+      if (!warp_wait(tempty, tphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t idesc = tc::idesc_bf16_f32(128, t.nmma);
+      for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+        tc::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sa = tc::smem_u32(smem + stage * RT_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t da0 = tc::smem_desc_sw128(sa + kk * 32);
+            const uint64_t da1 = tc::smem_desc_sw128(sa + RT_A_BOX_BYTES + kk * 32);
+            const uint64_t db = tc::smem_desc_sw128(sa + 2 * RT_A_BOX_BYTES + kk * 32);
+            const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+            tc::mma_bf16<1>(tmem_base, da0, db, idesc, acc);
+            tc::mma_bf16<1>(tmem_base + 256, da1, db, idesc, acc);
+          }
+          tc::mma_commit<1>(empty + stage);
+        }
+        issued_any = true;
+        __syncwarp();
+        if (++stage == RT_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) tc::mma_commit<1>(tfull);
+      __syncwarp();
+      tphase ^= 1u;
+    }
+    if (!ok && issued_any) {
+      if (lane == 0) tc::mma_commit<1>(drain);
+      __syncwarp();
+      warp_wait(drain, 0, abort_flag, tmo);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    uint32_t tphase = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      Tile t;
+      decode_router_tile(args, tile, t);
+      if (!warp_wait(tfull, tphase, abort_flag, tmo)) break;
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const int col0 = t.mb * 256 + row, col1 = col0 + 128;
+      const bool c0ok = col0 < args.out_cols, c1ok = col1 < args.out_cols;
+      for (int j0 = 0; j0 < t.nmma; j0 += 16) {
+        uint32_t r0[16], r1[16];
+        tc::tmem_ld16(taddr + j0, r0);
+        tc::tmem_ld16(taddr + 256 + j0, r1);
+        tc::tmem_wait_ld(r0, r1);
+        float* o = static_cast<float*>(args.out) + t.split * args.out_split_stride +
+                   static_cast<size_t>(t.tok0 + j0) * args.out_ld;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (j0 + j < t.ntok) {
+            if (c0ok) o[static_cast<size_t>(j) * args.out_ld + col0] = __uint_as_float(r0[j]);
+            if (c1ok) o[static_cast<size_t>(j) * args.out_ld + col1] = __uint_as_float(r1[j]);
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tempty);
+      tphase ^= 1u;
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc<1>(tmem_base, TMEM_COLS);
   if (threadIdx.x == 0 && *abort_flag) atomicOr(args.status, ERRBIT_TIMEOUT);
 }
 
@@ -404,10 +537,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return before;
 }
 
-__global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, int T, int K,
-                                                            int E, int S, int* rows,
-                                                            int* brow_gu, int* orow, int* bs,
-                                                            int* bstart) {
+__global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, const int* counts,
+                                                            int T, int E, int S, GroupLayout lay,
+                                                            int* rows, int* brow, int* orow,
+                                                            int* bs, int* bstart) {
   __shared__ int warp_sums[32];
   const int G = E + S;
   // each thread owns two consecutive groups (G <= kMaxE + kMaxS <= 2048)
@@ -420,17 +553,17 @@ __global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, 
       int r, br, orw;
       if (g < E) {
         br = offsets[g];
-        r = offsets[g + 1] - br;
+        r = counts ? counts[g] : offsets[g + 1] - br;
         orw = br;
       } else {
         r = T;
-        br = 0;
-        orw = T * K + (g - E) * T;
+        br = lay.shared_src;
+        orw = lay.shared_out0 + (g - E) * lay.shared_stride;
       }
       int b;
-      token_blocks(r, &b, &nb);
+      token_blocks(r, &b, &nb, lay.max_bs);
       rows[g] = r;
-      brow_gu[g] = br;
+      brow[g] = br;
       orow[g] = orw;
       bs[g] = b;
     }
@@ -445,49 +578,62 @@ __global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, 
   if (threadIdx.x == 0) bstart[G] = total;
 }
 
-template <int MODE, int CG>
-moe_status_t launch_mode(const GemmMaps& maps, const GemmArgs& args, int grid,
-                         cudaStream_t stream) {
-  constexpr size_t smem = Cfg<CG>::SMEM_BYTES;
-  static bool attr_set[64] = {false};
+// Grid of a persistent kernel: at most one CTA (or pair) per SM, and no more
+// clusters than can be resident at once.
+template <typename Kern>
+int persistent_ctas(Kern kern, int cluster, size_t smem, int threads, int want) {
+  static int cached[2][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<MODE, CG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+  int& c = cached[cluster == 2 ? 1 : 0][dev < 64 ? dev : 0];
+  if (c == 0) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(num_sms() / cluster * cluster), 1, 1);
+    lc.blockDim = dim3(threads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess || n <= 0) return 0;
+    c = n * cluster;
+  }
+  const int g = want < c ? want : c;
+  return g / cluster * cluster;
+}
+
+template <typename Kern>
+moe_status_t launch_persistent(Kern kern, const char* name, int cluster, size_t smem,
+                               int threads, int want, const GemmMaps& maps, const GemmArgs& args,
+                               cudaStream_t stream, bool* attr_done) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MOE_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_done[dev] = true;
   }
-  static const char* names[3] = {"gemm_gateup_swiglu", "gemm_down", "gemm_router"};
-  TraceScope tr(stream, names[MODE]);
+  const int grid = persistent_ctas(kern, cluster, smem, threads, want);
+  if (grid <= 0) return MOE_ERR_CUDA;
+  TraceScope tr(stream, name);
   cudaLaunchConfig_t lc = {};
-  lc.blockDim = dim3(NUM_THREADS, 1, 1);
+  lc.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  lc.blockDim = dim3(threads, 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  // persistent: no more clusters than can be resident at once
-  static int max_clusters[64] = {0};
-  if (dev < 64 && max_clusters[dev] == 0) {
-    lc.gridDim = dim3(static_cast<unsigned>(num_sms() / CG * CG), 1, 1);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<MODE, CG>, &lc) != cudaSuccess ||
-        n <= 0)
-      return MOE_ERR_CUDA;
-    max_clusters[dev] = n;
-  }
-  int clusters = grid / CG;
-  if (dev < 64 && clusters > max_clusters[dev]) clusters = max_clusters[dev];
-  if (clusters < 1) clusters = 1;
-  lc.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
-  if (cudaLaunchKernelEx(&lc, gemm_tc_kernel<MODE, CG>, maps, args) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&lc, kern, maps, args) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_status();
 }
 
@@ -522,11 +668,11 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 }
 
 bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
-                    uint64_t a1_rows, const void* b0, uint64_t b0_rows, const void* b1,
-                    uint64_t b1_rows, uint64_t k, uint32_t tok_box0) {
-  if (!make_tmap_bf16(&m->a[0], a0, a0_rows, k, BM)) return false;
+                    uint64_t a1_rows, uint32_t a_box_rows, const void* b0, uint64_t b0_rows,
+                    const void* b1, uint64_t b1_rows, uint64_t k, uint32_t tok_box0) {
+  if (!make_tmap_bf16(&m->a[0], a0, a0_rows, k, a_box_rows)) return false;
   if (a1) {
-    if (!make_tmap_bf16(&m->a[1], a1, a1_rows, k, BM)) return false;
+    if (!make_tmap_bf16(&m->a[1], a1, a1_rows, k, a_box_rows)) return false;
   } else {
     m->a[1] = m->a[0];
   }
@@ -544,20 +690,27 @@ bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
                             cudaStream_t stream) {
   if (grid <= 0) return MOE_OK;
+  static bool attr_gu[64], attr_dn[64], attr_rt[64];
   switch (mode) {
-    case GM_GATEUP: return launch_mode<GM_GATEUP, 2>(maps, args, grid, stream);
-    case GM_DOWN: return launch_mode<GM_DOWN, 2>(maps, args, grid, stream);
-    case GM_ROUTER: return launch_mode<GM_ROUTER, 1>(maps, args, grid, stream);
+    case GM_GATEUP:
+      return launch_persistent(expert_gemm_kernel<GM_GATEUP>, "gemm_gateup_swiglu", 2,
+                               EX_SMEM_BYTES, EX_THREADS, grid, maps, args, stream, attr_gu);
+    case GM_DOWN:
+      return launch_persistent(expert_gemm_kernel<GM_DOWN>, "gemm_down", 2, EX_SMEM_BYTES,
+                               EX_THREADS, grid, maps, args, stream, attr_dn);
+    case GM_ROUTER:
+      return launch_persistent(router_gemm_kernel, "gemm_router", 1, RT_SMEM_BYTES, RT_THREADS,
+                               grid, maps, args, stream, attr_rt);
     default: return MOE_ERR_INVALID_ARG;
   }
 }
 
-moe_status_t launch_build_groups(const int* offsets, int T, int K, int E, int S, int* rows,
-                                 int* brow_gu, int* orow, int* bs, int* bstart,
-                                 cudaStream_t stream) {
+moe_status_t launch_build_groups(const int* offsets, const int* counts, int T, int E, int S,
+                                 GroupLayout lay, int* rows, int* brow, int* orow, int* bs,
+                                 int* bstart, cudaStream_t stream) {
   TraceScope tr(stream, "build_groups");
-  build_groups_kernel<<<1, 1024, 0, stream>>>(offsets, T, K, E, S, rows, brow_gu, orow, bs,
-                                              bstart);
+  build_groups_kernel<<<1, 1024, 0, stream>>>(offsets, counts, T, E, S, lay, rows, brow, orow,
+                                              bs, bstart);
   return launch_status();
 }
 

@@ -23,7 +23,7 @@ struct GemmArgs {
   int E;                     // groups g < E read A/B map 0, others map 1
   int m_blocks;              // weight-row blocks per group (a block spans the CTA pair)
   int a_rows_per_group;      // rows of A per group (2I or d; 0 in router mode)
-  int a1_off;                // row offset of the second A box (I, 256 or 128)
+  int a1_off;                // GATEUP: row offset of the up rows (I)
   int k_blocks;              // K / 64
   int k_splits;              // router mode: K splits (1 otherwise)
   int k_per_split;           // k-blocks per split
@@ -56,32 +56,42 @@ struct GemmMaps {
   CUtensorMap b[2][kTokBoxes];    // token operand: routed (0) / shared (1), box 16 << i rows
 };
 
-// Fills `m`: a[i] over the [a_rows[i], k] weight matrices, b[i][*] over the
-// [b_rows[i], k] token matrices in boxes of tok_box0 << j rows (a null pointer
-// reuses entry 0).
+// Fills `m`: a[i] over the [a_rows[i], k] weight matrices in boxes of
+// a_box_rows rows, b[i][*] over the [b_rows[i], k] token matrices in boxes of
+// tok_box0 << j rows (a null pointer reuses entry 0).
 bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
-                    uint64_t a1_rows, const void* b0, uint64_t b0_rows, const void* b1,
-                    uint64_t b1_rows, uint64_t k, uint32_t tok_box0);
+                    uint64_t a1_rows, uint32_t a_box_rows, const void* b0, uint64_t b0_rows,
+                    const void* b1, uint64_t b1_rows, uint64_t k, uint32_t tok_box0);
 
-// Launches the persistent grouped GEMM: GATEUP and DOWN on CTA pairs
-// (clusters of two; grid rounded down to even), ROUTER on single CTAs.
+// Launches a persistent grouped GEMM on at most `grid` CTAs: GATEUP and DOWN
+// on CTA pairs (clusters of two), ROUTER on single CTAs.
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
                             cudaStream_t stream);
 
-// Builds the group table of the expert GEMMs from the dispatch offsets:
-// groups 0..E-1 are routed experts (rows = counts), E..E+S-1 the shared
-// experts (rows = T).  Writes rows, brow (gate/up source row), orow, bs, bstart.
-moe_status_t launch_build_groups(const int* offsets, int T, int K, int E, int S, int* rows,
-                                 int* brow_gu, int* orow, int* bs, int* bstart,
-                                 cudaStream_t stream);
+// Where the rows of each group live.  Routed group g < E: counts[g] rows
+// starting at offsets[g] in both the token source and the outputs.  Shared
+// expert s: T rows read from source row shared_src and written from output
+// row shared_out0 + s * shared_stride.  Token blocks hold at most max_bs rows.
+struct GroupLayout {
+  int shared_src, shared_out0, shared_stride, max_bs;
+};
+
+// Builds the group table of the expert GEMMs from the dispatch offsets (E+1
+// entries; group g has counts[g] rows, or offsets[g+1] - offsets[g] when
+// counts is NULL):
+// groups 0..E-1 are routed experts, E..E+S-1 the shared experts.  Writes
+// rows, brow (token source row), orow (output row), bs, bstart.
+moe_status_t launch_build_groups(const int* offsets, const int* counts, int T, int E, int S,
+                                 GroupLayout lay, int* rows, int* brow, int* orow, int* bs,
+                                 int* bstart, cudaStream_t stream);
 
 int num_sms();
 
-// Token-block size and count for `rows` tokens: blocks of at most 256 tokens,
-// balanced, each a multiple of 16.
-__host__ __device__ inline void token_blocks(int rows, int* bs, int* nb) {
+// Token-block size and count for `rows` tokens: blocks of at most max_bs
+// (256 or 128) tokens, balanced, each a multiple of 16.
+__host__ __device__ inline void token_blocks(int rows, int* bs, int* nb, int max_bs = 256) {
   if (rows <= 0) { *bs = 16; *nb = 0; return; }
-  int n0 = (rows + 255) / 256;
+  int n0 = (rows + max_bs - 1) / max_bs;
   int b = ((rows + n0 - 1) / n0 + 15) / 16 * 16;
   *bs = b;
   *nb = (rows + b - 1) / b;

@@ -20,9 +20,22 @@ moe_status_t launch_dispatch(const void* x, size_t row_bytes, const int32_t* idx
                              int32_t* perm_tok, int32_t* pos, int32_t* hist,
                              cudaStream_t stream);
 
+// counts, offsets (padded to `pad` rows per expert), perm_tok, pos only
+moe_status_t launch_dispatch_index(const int32_t* idx, int T, int K, int E, int pad,
+                                   int32_t* counts, int32_t* offsets, int32_t* perm_tok,
+                                   int32_t* pos, int32_t* hist, cudaStream_t stream);
+
+// FP8 rows: xq row pos[t,k] and row shared_row + t (if shared_row >= 0) get
+// token t in e4m3, 1 x 128 tiles; scales xs[kb * ld_s + row].
+moe_status_t launch_scatter_quant(const void* x, int T, int K, int d, const int32_t* pos,
+                                  int shared_row, void* xq, float* xs, long long ld_s,
+                                  cudaStream_t stream);
+
+// out_t = sum_k g y[pos[t,k]] + sum_s y[shared0 + s*shared_stride + t] (+ x_t)
 moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, const int32_t* pos,
                             const void* x, void* out, int T, int K, int S, int d,
-                            int add_residual, cudaStream_t stream);
+                            long long shared0, long long shared_stride, int add_residual,
+                            cudaStream_t stream);
 
 moe_status_t launch_update_bias(const int32_t* counts, float* bias, float* stats, int E, int T,
                                 int K, float gamma, cudaStream_t stream);

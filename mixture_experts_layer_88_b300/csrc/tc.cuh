@@ -257,5 +257,14 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&a)[16], uint32_t (&b)[16
                : "memory");
 }
 
+__device__ __forceinline__ void tmem_wait_ld1(uint32_t (&a)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
+                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
+               :
+               : "memory");
+}
+
 }  // namespace tc
 }  // namespace moe

@@ -11,7 +11,9 @@ class MoeLayer:
     """One DeepSeekMoE layer resident on a CUDA device.
 
     weights: dict with centroids [E,d], bias [E] fp32, w13 [E,2I,d], w2 [E,d,I],
-    ws13 [S,2I,d], ws2 [S,d,I] (device tensors, layouts of include/moe.h).
+    ws13 [S,2I,d], ws2 [S,d,I] (device tensors, layouts of include/moe.h).  FP8
+    layers (cfg.wgt_dtype == MOE_E4M3) also carry w13_scale, w2_scale,
+    ws13_scale, ws2_scale and run through moe_forward_fp8.
     """
 
     def __init__(self, cfg: _lib.MoeCfg, weights: dict, device="cuda"):
@@ -19,6 +21,8 @@ class MoeLayer:
         self.device = torch.device(device)
         self.w = weights
         self.bias = weights["bias"]
+        self.fp8 = cfg.wgt_dtype == _lib.MOE_E4M3
+        self._fp8w = _lib.fp8_weights(weights) if self.fp8 else None
         self._ws = None
         self._T = None
 
@@ -40,8 +44,13 @@ class MoeLayer:
         if out is None:
             out = torch.empty_like(x)
         w = self.w
-        _lib.forward(self.cfg, x, w["centroids"], self.bias, w["w13"], w["w2"], w.get("ws13"),
-                     w.get("ws2"), self.idx, self.gates, self.counts, out, self._ws, stream)
+        if self.fp8:
+            _lib.forward_fp8(self.cfg, x, w["centroids"], self.bias, self._fp8w, self.idx,
+                             self.gates, self.counts, out, self._ws, stream)
+        else:
+            _lib.forward(self.cfg, x, w["centroids"], self.bias, w["w13"], w["w2"],
+                         w.get("ws13"), w.get("ws2"), self.idx, self.gates, self.counts, out,
+                         self._ws, stream)
         return out
 
     def update_bias(self, stream=None) -> torch.Tensor:

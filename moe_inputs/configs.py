@@ -40,6 +40,7 @@ class LayerCfg:
     add_residual: int = 1
     gamma: float = 1e-3
     seed: int = 0
+    zipf_s: float = 0.0          # > 0: expert popularity ~ rank^-zipf_s (see gen.py)
 
     def with_(self, **kw) -> "LayerCfg":
         return replace(self, **kw)
@@ -69,7 +70,8 @@ CONFIGS = {
                            act=BF16, wgt=BF16, w_std=0.006, bias_range=0.01),
     # V3 layer with Zipf-skewed expert popularity and FP8 block-scaled weights
     "v3_skewed_fp8": LayerCfg("v3_skewed_fp8", T=16384, d=7168, E=256, K=8, S=1, I=2048,
-                              act=BF16, wgt=E4M3, w_std=0.006, bias_range=0.0),
+                              act=BF16, wgt=E4M3, w_std=0.006, bias_range=0.0,
+                              zipf_s=1.1),
     # DeepSeekMoE-16B-shaped layer, softmax scores, no renormalisation
     "dsmoe16b": LayerCfg("dsmoe16b", T=32768, d=2048, E=64, K=6, S=2, I=1408,
                          act=BF16, wgt=BF16, w_std=0.02, bias_range=0.0,
@@ -99,4 +101,10 @@ def small_cases() -> dict:
                            w_std=0.03, bias_range=0.01),
         "tiny_f32_ragged": CONFIGS["tiny"].with_(name="tiny_f32_ragged", T=37, d=96,
                                                  E=8, K=3, S=2, I=40),
+        # FP8 block-scaled experts, Zipf-skewed routing (one expert takes every token)
+        "small_fp8": CONFIGS["v3_skewed_fp8"].with_(name="small_fp8", T=600, d=512, E=32,
+                                                    K=4, S=1, I=384, w_std=0.03),
+        "ragged_fp8": CONFIGS["v3_skewed_fp8"].with_(name="ragged_fp8", T=301, d=384, E=24,
+                                                     K=3, S=2, I=256, w_std=0.03, zipf_s=0.0,
+                                                     bias_range=0.02),
     }

@@ -149,6 +149,23 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
+def dequantize_blocks(q, scale, block: int = 128) -> np.ndarray:
+    """Block-wise FP8 weight of the V3 walk-through, section 4.3 (128 x 128
+    blocks, one fp32 scale each): w[r, c] = q[r, c] * scale[r // 128, c // 128],
+    in fp64.  ``q`` holds e4m3 values (decoded exactly by the upcast)."""
+    qv = _f64(q)
+    sc = _f64(scale)
+    return qv * np.repeat(np.repeat(sc, block, axis=0), block, axis=1)
+
+
+def _expert_weight(inp: dict, key: str, e: int):
+    """Weight ``key`` of expert e, dequantised when the layer stores FP8 blocks."""
+    w = inp[key][e]
+    if key + "_scale" in inp:
+        return dequantize_blocks(w, inp[key + "_scale"][e])
+    return w
+
+
 def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
     """One expert: W2 (SiLU(Wg u) * (Wu u)); w13 [2I, d] = [Wg; Wu], w2 [d, I].
     u [n, d] fp64 -> [n, d] fp64."""
@@ -164,9 +181,10 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
-    ``inp`` holds x, centroids, bias, w13, w2, ws13, ws2 (see moe_inputs).
-    Expert weights are read one expert at a time, so large layers can be
-    evaluated on a token sample.  Returns out (fp64), delta = out - residual,
+    ``inp`` holds x, centroids, bias, w13, w2, ws13, ws2 (see moe_inputs), and
+    for FP8 layers their 128 x 128 block scales (``*_scale``); activations are
+    used as stored (bf16), unquantised.  Expert weights are read one expert at
+    a time, so large layers can be evaluated on a token sample.  Returns out (fp64), delta = out - residual,
     idx, gates, margin."""
     x = inp["x"]
     if tokens is not None:
@@ -180,11 +198,12 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     delta = np.zeros((n, d))
     S = inp["ws13"].shape[0]
     for s in range(S):
-        delta += swiglu_ffn(u, inp["ws13"][s], inp["ws2"][s])
+        delta += swiglu_ffn(u, _expert_weight(inp, "ws13", s), _expert_weight(inp, "ws2", s))
     routed = np.zeros((n, K, d))
     for e in np.unique(idx):
         rows, slots = np.nonzero(idx == e)
-        routed[rows, slots] = swiglu_ffn(u[rows], inp["w13"][int(e)], inp["w2"][int(e)])
+        routed[rows, slots] = swiglu_ffn(u[rows], _expert_weight(inp, "w13", int(e)),
+                                         _expert_weight(inp, "w2", int(e)))
     for k in range(K):
         delta += gates[:, k:k + 1] * routed[:, k]
     out = delta + u if add_residual else delta.copy()

@@ -291,3 +291,90 @@ def test_token_subset_equals_full_batch():
     sub = O.moe_layer(inp, cfg.K, tokens=tok)
     np.testing.assert_array_equal(sub["idx"], full["idx"][tok])
     np.testing.assert_allclose(sub["out"], full["out"][tok], rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- FP8 weights
+
+def _read_fp8_fixture():
+    codes, elems, scale = [], [], None
+    with open(os.path.join(GOLDEN, "fp8_dequant_hand.txt")) as f:
+        for ln in f:
+            ln = ln.strip()
+            if not ln or ln.startswith("#"):
+                continue
+            key, rest = ln.split(":", 1)
+            if key == "code":
+                b, v = rest.split()
+                codes.append((int(b, 16), float(v)))
+            elif key == "scale":
+                scale = [[float(v) for v in row.split()] for row in rest.split("|")]
+            elif key == "elem":
+                r, c, b, v = rest.split()
+                elems.append((int(r), int(c), int(b, 16), float(v)))
+    return codes, np.array(scale), elems
+
+
+def test_golden_fp8_codes_decode():
+    """The oracle's upcast of e4m3 codes gives the values the E4M3 definition fixes."""
+    codes, _, _ = _read_fp8_fixture()
+    bits = torch.tensor([b for b, _ in codes], dtype=torch.uint8).view(torch.float8_e4m3fn)
+    got = O._f64(bits)
+    want = np.array([v for _, v in codes])
+    assert np.array_equal(got, want)
+
+
+def test_golden_fp8_block_scales():
+    """dequantize_blocks applies the scale of each element's own 128 x 128 block."""
+    _, scale, elems = _read_fp8_fixture()
+    q = torch.zeros((256, 256), dtype=torch.uint8)
+    for r, c, b, _ in elems:
+        q[r, c] = b
+    w = O.dequantize_blocks(q.view(torch.float8_e4m3fn), scale)
+    for r, c, _, v in elems:
+        assert w[r, c] == v, (r, c, w[r, c], v)
+    mask = np.ones((256, 256), bool)
+    for r, c, _, _ in elems:
+        mask[r, c] = False
+    assert np.all(w[mask] == 0.0)
+
+
+def test_fp8_layer_equals_layer_on_dequantised_weights():
+    """An FP8 layer is the same layer on the weights q * scale (the activations
+    enter unquantised): the oracle's FP8 path agrees bit for bit with its
+    plain path fed the dequantised fp64 weights."""
+    cfg = small_cases()["ragged_fp8"]
+    inp = make_inputs(cfg, "cpu")
+    plain = {k: inp[k] for k in ("x", "centroids", "bias")}
+    for k in ("w13", "w2", "ws13", "ws2"):
+        plain[k] = np.stack([O.dequantize_blocks(inp[k][e], inp[k + "_scale"][e])
+                             for e in range(inp[k].shape[0])])
+    a = O.moe_layer(inp, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    b = O.moe_layer(plain, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    assert np.array_equal(a["delta"], b["delta"])
+    assert np.array_equal(a["idx"], b["idx"])
+
+
+def test_fp8_generator_round_trip():
+    """Generator check: q * scale reproduces the fp32 draw within e4m3 rounding
+    (relative 2^-4, or 2^-10 * scale in the subnormal range), and every block's
+    largest |q| is 448."""
+    from moe_inputs.gen import _quantize_blocks
+    g = torch.Generator().manual_seed(3)
+    w = torch.randn((2, 256, 384), generator=g) * 0.01
+    q, sc = _quantize_blocks(w)
+    deq = O.dequantize_blocks(q[1], sc[1])
+    ref = w[1].double().numpy()
+    tol = np.abs(ref) * 2.0 ** -4 + np.repeat(np.repeat(sc[1].double().numpy(), 128, 0), 128, 1) * 2.0 ** -10
+    assert np.all(np.abs(deq - ref) <= tol * (1 + 1e-6))
+    qa = q.float().abs().reshape(2, 2, 128, 3, 128).amax(dim=(2, 4))
+    assert torch.all(qa == 448.0)
+
+
+def test_zipf_targets_capped_and_sum_to_k():
+    from moe_inputs.gen import zipf_targets
+    f = zipf_targets(256, 8, 1.1)
+    assert abs(float(f.sum()) - 8.0) < 1e-9 and float(f.max()) <= 1.0 + 1e-12
+    free = f < 1.0 - 1e-12
+    r = torch.arange(1, 257, dtype=torch.float64)[free]
+    ratio = f[free] * r ** 1.1
+    assert float(ratio.max() - ratio.min()) < 1e-9 * float(ratio.max())
