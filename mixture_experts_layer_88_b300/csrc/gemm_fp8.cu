@@ -14,7 +14,8 @@
 //
 // Layout is swap-AB as in the bf16 kernel: weights in the MMA's M slot,
 // tokens in N.  One tile = group g, two 128-row weight boxes, one token block
-// of N <= 128 tokens:
+// of N <= 96 tokens (each epilogue thread keeps 2 x 48 fp32 accumulators in
+// registers; with ten warps a thread can hold at most 168 registers):
 //   GATEUP: acc0 = gate rows [128 mb, +128) of W13_g, acc1 = the up rows (+I);
 //           the tile ends with act = SiLU(acc0) * acc1 quantised to e4m3 per
 //           token over its 128 columns (one 1 x 128 tile of the down GEMM's K)
@@ -29,7 +30,7 @@
 //   warp 0      TMA producer: weight boxes, token rows, token scales per stage
 //   warp 1      TMEM owner and MMA issuer
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. and
-//               columns [64 h, 64 h + 64), h = (w - 2) / 4
+//               columns [48 h, 48 h + 48), h = (w - 2) / 4
 // Every barrier wait is bounded (abort flag, device error word), as in the
 // bf16 kernel.
 #include <cudaTypedefs.h>
@@ -49,6 +50,7 @@ constexpr int STAGES = 4;
 constexpr uint32_t A_BOX = 128 * ROW;         // 16 KB
 constexpr uint32_t STAGE_BYTES = 2 * A_BOX + 128 * ROW;   // 48 KB
 constexpr int EPI_WARPS = 8;
+constexpr int CW = 48;                        // token columns per epilogue warp (N <= 2 CW)
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 // shared memory after the stages: token scales per stage, per-warp
@@ -134,6 +136,17 @@ __device__ __forceinline__ void warp_colmax64(float (&v)[64], int lane) {
       v[i] = fmaxf(keep, got);
     }
   }
+}
+
+// acc{0,1} += p{0,1} * s{0,1} as one packed two-lane fp32 FMA (f32x2).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float p0, float p1, float s0,
+                                      float s1) {
+  uint64_t acc, p, s;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(p0), "f"(p1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(s) : "f"(s0), "f"(s1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(s));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
 }
 
 template <int MODE>
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const int ew = warp - 2;
-    float* my_ps = psc + ew * 128;                 // [2][64]: gate/acc0, up/acc1 scales
+    float* my_ps = psc + ew * 128;                 // [2][64]: acc0 and acc1 scales
     const uint32_t tl = static_cast<uint32_t>(q * 32) << 16;
     uint32_t kc = 0;
     int tcount = 0;
@@ -291,17 +304,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       decode(args, tile, t);
       const bool second = t.g >= args.E;
       const int gl = second ? t.g - args.E : t.g;
-      wsc = args.w_scale[second ? 1 : 0];
+      wsc = second ? args.w_scale[1] : args.w_scale[0];
       // weight-scale rows of acc0 / acc1 in [groups][row blocks][k blocks]
       const int rb = args.a_rows_per_group / 128;
       const int rb0 = gl * rb + t.mb * (MODE == GM_GATEUP ? 1 : 2);
       const int rb1 = rb0 + (MODE == GM_GATEUP ? args.a1_off / 128 : 1);
       const bool rb1ok = MODE == GM_GATEUP || t.mb * 2 + 1 < rb;
-      const int c0 = h * 64;
+      const int c0 = h * CW;
       const bool active = c0 < t.nmma;
-      float a0[64], a1[64];
+      float a0[CW], a1[CW];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) { a0[i] = 0.f; a1[i] = 0.f; }
+      for (int i = 0; i < CW; ++i) { a0[i] = 0.f; a1[i] = 0.f; }
       for (int kb = 0; kb < nkb; ++kb, ++kc) {
         const int stage = kc % STAGES;
         const int pb = kc & 1;
@@ -313,23 +326,35 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float sw1 = rb1ok ? __ldg(wsc + static_cast<size_t>(rb1) * nkb + kb) : 0.f;
           const float* sx = sc_stage + stage * 128 + c0;
           my_ps[lane] = sw0 * sx[lane];
-          my_ps[lane + 32] = sw0 * sx[lane + 32];
           my_ps[64 + lane] = sw1 * sx[lane];
-          my_ps[64 + lane + 32] = sw1 * sx[lane + 32];
+          if (lane + 32 < CW) {
+            my_ps[lane + 32] = sw0 * sx[lane + 32];
+            my_ps[64 + lane + 32] = sw1 * sx[lane + 32];
+          }
           __syncwarp();
           const uint32_t tb = tmem_base + pb * 256 + tl + c0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < CW / 16; ++j) {
             if (c0 + 16 * j < t.nmma) {
               uint32_t p0[16], p1[16];
               tc::tmem_ld16(tb + 16 * j, p0);
               tc::tmem_ld16(tb + 128 + 16 * j, p1);
               tc::tmem_wait_ld(p0, p1);
+              const float4* s0v = reinterpret_cast<const float4*>(my_ps + 16 * j);
+              const float4* s1v = reinterpret_cast<const float4*>(my_ps + 64 + 16 * j);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                a0[16 * j + i] = fmaf(__uint_as_float(p0[i]), my_ps[16 * j + i], a0[16 * j + i]);
-                a1[16 * j + i] =
-                    fmaf(__uint_as_float(p1[i]), my_ps[64 + 16 * j + i], a1[16 * j + i]);
+              for (int i = 0; i < 4; ++i) {
+                const float4 s0 = s0v[i], s1 = s1v[i];
+                float* x0 = a0 + 16 * j + 4 * i;
+                float* x1 = a1 + 16 * j + 4 * i;
+                ffma2(x0[0], x0[1], __uint_as_float(p0[4 * i]), __uint_as_float(p0[4 * i + 1]),
+                      s0.x, s0.y);
+                ffma2(x0[2], x0[3], __uint_as_float(p0[4 * i + 2]),
+                      __uint_as_float(p0[4 * i + 3]), s0.z, s0.w);
+                ffma2(x1[0], x1[1], __uint_as_float(p1[4 * i]), __uint_as_float(p1[4 * i + 1]),
+                      s1.x, s1.y);
+                ffma2(x1[2], x1[3], __uint_as_float(p1[4 * i + 2]),
+                      __uint_as_float(p1[4 * i + 3]), s1.z, s1.w);
               }
             }
           }
@@ -350,18 +375,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         // columns.  All four warps of a half take part in the amax exchange
         // on every tile (inactive ones with nothing to store), so its
         // barrier phases and buffer parity stay in step.
+        float v[64];
         if (active) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) a0[i] = silu_mul(a0[i], a1[i]);
+          for (int i = 0; i < CW; ++i) a0[i] = silu_mul(a0[i], a1[i]);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) a1[i] = fabsf(a0[i]);
-          warp_colmax64(a1, lane);                 // a1[0..1]: warp max of cols 2l, 2l+1
+          for (int i = 0; i < 64; ++i) v[i] = i < CW ? fabsf(a0[i]) : 0.f;
+          warp_colmax64(v, lane);                  // v[0..1]: warp max of cols 2l, 2l+1
         }
         const int par = tcount & 1;
         float* am = amx + (par * 2 + h) * 4 * 64;
         if (active) {
-          am[q * 64 + 2 * lane] = a1[0];
-          am[q * 64 + 2 * lane + 1] = a1[1];
+          am[q * 64 + 2 * lane] = v[0];
+          am[q * 64 + 2 * lane + 1] = v[1];
         }
         uint64_t* xb = xam + par * 2 + h;
         tc::mbar_arrive(xb);
@@ -372,7 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int col = t.mb * 128 + q * 32 + lane;
           uint8_t* oq = static_cast<uint8_t*>(args.out) + orow0 * args.out_ld + col;
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
+          for (int i = 0; i < CW; ++i) {
             const float m = fmaxf(fmaxf(am[i], am[64 + i]), fmaxf(am[128 + i], am[192 + i]));
             const float inv = m > 0.f ? 448.0f / m : 0.f;
             if (c0 + i < t.ntok) {
@@ -387,7 +413,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int u = 0; u < 2; ++u) {
               const int i = 2 * lane + u;
               const float m = fmaxf(fmaxf(am[i], am[64 + i]), fmaxf(am[128 + i], am[192 + i]));
-              if (c0 + i < t.ntok)
+              if (i < CW && c0 + i < t.ntok)
                 args.out_scale[static_cast<size_t>(t.mb) * args.out_scale_ld + orow0 + i] =
                     m / 448.0f;
             }
@@ -398,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int col0 = t.mb * 256 + q * 32 + lane, col1 = col0 + 128;
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) + orow0 * args.out_ld;
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
+          for (int i = 0; i < CW; ++i) {
             if (c0 + i < t.ntok) {
               if (col0 < args.out_cols)
                 o[static_cast<size_t>(i) * args.out_ld + col0] = __float2bfloat16_rn(a0[i]);

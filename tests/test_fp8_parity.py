@@ -157,7 +157,7 @@ def test_fp8_stepwise_equals_forward(name):
 
 
 def test_fp8_hot_expert_many_token_blocks():
-    """One expert chosen by every token: its group spans many 128-token blocks."""
+    """One expert chosen by every token: its group spans many token blocks."""
     cfg = small_cases()["small_fp8"].with_(name="hot_fp8", T=900, E=8, K=2)
     g, c = gpu_inputs(cfg)
     g["bias"] = torch.zeros(cfg.E, device="cuda")
