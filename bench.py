@@ -174,6 +174,27 @@ def kernel_roofline(cfg, traces, peaks):
     return out
 
 
+def dram_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload`, from the
+    ncu capture recorded in profiles/dram_traffic.json, or None when there is
+    none or the kernel's source file changed since (sha256 recorded with it)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(workload, {}).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "mixture_experts_layer_88_b300", "csrc", rec["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+            return None
+    return rec["bytes_per_launch"]
+
+
 def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7):
     """Times the CPU oracle on n_tokens tokens of the workload (weights of the
     experts those tokens use are copied to host first, untimed)."""
@@ -182,7 +203,7 @@ def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7):
     tok = np.sort(rng.choice(cfg.T, n_tokens, replace=False))
     x_host = inp["x"][torch.as_tensor(tok, device=inp["x"].device)].cpu()
     idx, _, _, _ = O.route(x_host, inp["centroids"].cpu(), inp["bias"].cpu(), cfg.K,
-                           cfg.score_func, cfg.normalize)
+                           cfg.score_func, cfg.normalize, cfg.n_groups, cfg.topk_groups)
     used = sorted(set(int(e) for e in idx.reshape(-1)))
 
     class _Experts:
@@ -201,7 +222,8 @@ def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7):
             host[k + "_scale"] = _Experts(inp[k + "_scale"], used)
             host["s" + k + "_scale"] = inp["s" + k + "_scale"].cpu()
     t0 = time.perf_counter()
-    O.moe_layer(host, cfg.K, cfg.normalize, cfg.score_func, cfg.add_residual)
+    O.moe_layer(host, cfg.K, cfg.normalize, cfg.score_func, cfg.add_residual,
+                n_groups=cfg.n_groups, topk_groups=cfg.topk_groups)
     dt = time.perf_counter() - t0
     try:
         from threadpoolctl import threadpool_info
@@ -343,11 +365,7 @@ def main():
     gemm_ms_step = gemm_ms / args.steps if gemm_ms else None
     gemm_tflops = gemm_flops / (gemm_ms_step / 1e3) / 1e12 if gemm_ms_step else None
     launches = sum(t[1] for t in traces)
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    if os.path.exists(tfile):
-        with open(tfile) as f:
-            traffic = json.load(f).get(cfg.name, {}).get("gemm_gateup_swiglu")
+    traffic = dram_traffic(cfg.name, top_name)
 
     gemm_peak = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if fp8 else 1)
     line = {

@@ -75,6 +75,15 @@ typedef struct {
   int32_t normalize;    /* 1: g = g'/sum g' (V3 eq. 13); 0: g = s (course section 4) */
   int32_t add_residual; /* 1: out = u + ... (V3 section 3.1); 0: MoE term only */
   float gamma;          /* bias update speed, 0.001 in V3 section 2.2 */
+  int32_t n_groups;     /* node-limited routing (V3 section 2.3): 0 = off, else the
+                           experts form n_groups groups of E / n_groups consecutive
+                           indices (a multiple of 32, or a power of two below 32;
+                           n_groups <= 32) */
+  int32_t topk_groups;  /* groups kept per token, ranked by the sum of their
+                           experts' scores s (equal sums: lower group); top-K then
+                           runs over the kept groups' experts only.  0 when
+                           n_groups is 0, else 1..n_groups with K <= topk_groups *
+                           E / n_groups */
 } moe_cfg_t;
 
 /* Which call a workspace is sized for. */

@@ -41,7 +41,8 @@ class MoeCfg(ctypes.Structure):
                 ("K", ctypes.c_int32), ("S", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("act_dtype", ctypes.c_int32), ("wgt_dtype", ctypes.c_int32),
                 ("score_func", ctypes.c_int32), ("normalize", ctypes.c_int32),
-                ("add_residual", ctypes.c_int32), ("gamma", ctypes.c_float)]
+                ("add_residual", ctypes.c_int32), ("gamma", ctypes.c_float),
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32)]
 
 
 class Fp8Weights(ctypes.Structure):
@@ -107,8 +108,9 @@ _DT = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16}
 
 
 def make_cfg(T, d, E, K, S, I, dtype=MOE_BF16, score_func=MOE_SCORE_SIGMOID, normalize=1,
-             add_residual=1, gamma=1e-3) -> MoeCfg:
-    return MoeCfg(T, d, E, K, S, I, dtype, dtype, score_func, normalize, add_residual, gamma)
+             add_residual=1, gamma=1e-3, n_groups=0, topk_groups=0) -> MoeCfg:
+    return MoeCfg(T, d, E, K, S, I, dtype, dtype, score_func, normalize, add_residual, gamma,
+                  n_groups, topk_groups)
 
 
 def cfg_from_layer(layer_cfg, T=None) -> MoeCfg:
@@ -116,7 +118,8 @@ def cfg_from_layer(layer_cfg, T=None) -> MoeCfg:
     dt = {"f32": MOE_F32, "bf16": MOE_BF16, "e4m3": MOE_E4M3}
     c = layer_cfg
     return MoeCfg(c.T if T is None else T, c.d, c.E, c.K, c.S, c.I, dt[c.act], dt[c.wgt],
-                  c.score_func, c.normalize, c.add_residual, c.gamma)
+                  c.score_func, c.normalize, c.add_residual, c.gamma,
+                  getattr(c, "n_groups", 0), getattr(c, "topk_groups", 0))
 
 
 def _p(t):

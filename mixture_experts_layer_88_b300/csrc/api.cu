@@ -224,15 +224,15 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
     moe_status_t s = launch_gemm_tc(GM_ROUTER, maps, a, grid, st);
     if (s != MOE_OK) return s;
     return launch_topk(partial, p.splits, a.out_split_stride, bias, c.T, c.E, c.K, c.score_func,
-                       c.normalize, idx, gates, st);
+                       c.normalize, c.n_groups, c.topk_groups, idx, gates, st);
   }
   float* logits = static_cast<float*>(ws);
   moe_status_t s = launch_logits_f32(static_cast<const float*>(x),
                                      static_cast<const float*>(centroids), c.T, c.d, c.E, logits,
                                      st);
   if (s != MOE_OK) return s;
-  return launch_topk(logits, 1, 0, bias, c.T, c.E, c.K, c.score_func, c.normalize, idx, gates,
-                     st);
+  return launch_topk(logits, 1, 0, bias, c.T, c.E, c.K, c.score_func, c.normalize, c.n_groups,
+                     c.topk_groups, idx, gates, st);
 }
 
 moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
@@ -402,6 +402,17 @@ moe_status_t moe_check_cfg(const moe_cfg_t* cfg) {
     return MOE_ERR_INVALID_ARG;
   if ((c.normalize != 0 && c.normalize != 1) || (c.add_residual != 0 && c.add_residual != 1))
     return MOE_ERR_INVALID_ARG;
+  if (c.n_groups == 0) {
+    if (c.topk_groups != 0) return MOE_ERR_INVALID_ARG;
+  } else {
+    // node-limited routing: equal groups of a power-of-two size below 32 or a
+    // multiple of 32 experts, at most 32 groups, enough experts for K
+    if (c.n_groups < 1 || c.n_groups > 32 || c.E % c.n_groups != 0) return MOE_ERR_INVALID_ARG;
+    const int gs = c.E / c.n_groups;
+    if (!(gs % 32 == 0 || (gs < 32 && (gs & (gs - 1)) == 0))) return MOE_ERR_INVALID_ARG;
+    if (c.topk_groups < 1 || c.topk_groups > c.n_groups || c.K > c.topk_groups * gs)
+      return MOE_ERR_INVALID_ARG;
+  }
   if (c.act_dtype < MOE_F32 || c.act_dtype > MOE_E4M3 || c.wgt_dtype < MOE_F32 ||
       c.wgt_dtype > MOE_E4M3)
     return MOE_ERR_INVALID_ARG;

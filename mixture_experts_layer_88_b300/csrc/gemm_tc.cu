@@ -66,10 +66,22 @@ __device__ __forceinline__ void decode_group_tile(const GemmArgs& a, int tile, T
   }
   t.g = lo;
   const int b0 = __ldg(a.gt.bstart + lo);
-  const int nbk = __ldg(a.gt.bstart + lo + 1) - b0;
+  // Order inside a group.  Routed experts: weight-block-major, so the tiles
+  // that share a weight block (its token blocks) are neighbours and stream it
+  // from DRAM once, in step.  Shared experts (T tokens, up to 117 MB of token
+  // operand): token-block-major, so a token block stays in L2 while all its
+  // weight blocks pass over it instead of streaming the whole batch again for
+  // every weight block.
   const int local = tile - b0 * a.m_blocks;
-  t.mb = local / nbk;
-  const int nb = local - t.mb * nbk;
+  int nb;
+  if (lo < a.E) {
+    const int nbk = __ldg(a.gt.bstart + lo + 1) - b0;
+    t.mb = local / nbk;
+    nb = local - t.mb * nbk;
+  } else {
+    nb = local / a.m_blocks;
+    t.mb = local - nb * a.m_blocks;
+  }
   const int bs = __ldg(a.gt.bs + lo);
   t.tok0 = nb * bs;
   t.ntok = min(bs, __ldg(a.gt.rows + lo) - t.tok0);
@@ -132,6 +144,34 @@ __device__ __forceinline__ void load_token_rows(uint8_t* dst, const CUtensorMap*
       done += h;
     }
   }
+}
+
+// In-place 8x8 transpose within each group of 8 lanes: on entry lane 8g+i
+// holds column i of the group in v[0..7] (8 tokens); on exit it holds token i
+// with the group's 8 columns in v[0..7].  Three butterfly stages; every lane
+// of the warp must take part.
+__device__ __forceinline__ void transpose8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (r & m) continue;
+      const int rh = r | m;
+      const float send = hi ? v[r] : v[rh];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+      if (hi) v[r] = recv; else v[rh] = recv;
+    }
+  }
+}
+
+// Eight fp32 values rounded to bf16 and written as one 16-byte store.
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, const float (&v)[8]) {
+  uint4 o;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(dst) = o;
 }
 
 // ============================================================================
@@ -300,33 +340,39 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
       // DOWN:   y columns of acc0 and acc1 (256 rows apart)
       const int col0 = t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128 +
                        q * 32 + lane;
-      const int col1 = col0 + 256;
-      const bool c0ok = col0 < args.out_cols;
-      const bool c1ok = MODE == GM_DOWN && col1 < args.out_cols;
+      // after the 8x8 transposes lane 8g+i holds token i of a half-chunk and
+      // the 8 columns [col_base + 8g, +8): one 16-byte store per lane
+      const int colg0 = col0 - (lane & 7);
+      const int colg1 = colg0 + 256;
+      const bool c0ok = colg0 < args.out_cols;
+      const bool c1ok = MODE == GM_DOWN && colg1 < args.out_cols;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
       for (int j0 = h * 16; j0 < t.nmma; j0 += 32) {
         uint32_t r0[16], r1[16];
         tc::tmem_ld16(taddr + j0, r0);
         tc::tmem_ld16(taddr + 256 + j0, r1);
         tc::tmem_wait_ld(r0, r1);
-        __nv_bfloat16* o = out + (out_row0 + j0) * args.out_ld;
-        const int jn = t.ntok - j0;
-        if (MODE == GM_GATEUP) {
-          if (c0ok) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j < jn)
-                o[static_cast<size_t>(j) * args.out_ld + col0] = __float2bfloat16_rn(
-                    silu_mul(__uint_as_float(r0[j]), __uint_as_float(r1[j])));
-          }
-        } else {
+        for (int hf = 0; hf < 2; ++hf) {
+          const int tok = j0 + 8 * hf + (lane & 7);
+          const bool tok_ok = tok < t.ntok;
+          __nv_bfloat16* orow = out + (out_row0 + tok) * args.out_ld;
+          float v[8];
+          if (MODE == GM_GATEUP) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (j < jn) {
-              __nv_bfloat16* oj = o + static_cast<size_t>(j) * args.out_ld;
-              if (c0ok) oj[col0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
-              if (c1ok) oj[col1] = __float2bfloat16_rn(__uint_as_float(r1[j]));
-            }
+            for (int i = 0; i < 8; ++i)
+              v[i] = silu_mul(__uint_as_float(r0[8 * hf + i]), __uint_as_float(r1[8 * hf + i]));
+            transpose8(v, lane);
+            if (c0ok && tok_ok) store_bf16x8(orow + colg0, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r0[8 * hf + i]);
+            transpose8(v, lane);
+            if (c0ok && tok_ok) store_bf16x8(orow + colg0, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r1[8 * hf + i]);
+            transpose8(v, lane);
+            if (c1ok && tok_ok) store_bf16x8(orow + colg1, v);
           }
         }
       }

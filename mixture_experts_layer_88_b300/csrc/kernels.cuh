@@ -8,9 +8,11 @@ namespace moe {
 
 constexpr int kDispatchChunk = 256;   // tokens per count/rank CTA (8 warps x 32)
 
+// n_groups > 0: node-limited routing over topk_groups of n_groups groups
 moe_status_t launch_topk(const float* logits, int splits, long long split_stride,
                          const float* bias, int T, int E, int K, int score_func, int normalize,
-                         int32_t* idx, float* gates, cudaStream_t stream);
+                         int n_groups, int topk_groups, int32_t* idx, float* gates,
+                         cudaStream_t stream);
 moe_status_t launch_logits_f32(const float* x, const float* c, int T, int d, int E, float* out,
                                cudaStream_t stream);
 

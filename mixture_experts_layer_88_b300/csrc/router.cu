@@ -5,6 +5,11 @@
 //   g_i = s_i / sum of chosen s     (or g_i = s_i without renormalisation)
 // One warp per token: the logits of its E experts sit in registers, E/32 per
 // lane, and K rounds of a 64-bit (key, index) warp argmax pick the experts.
+// Node-limited routing (same page, section 2.3): with n_groups > 0 the experts
+// form n_groups groups of consecutive indices; each group's score is the sum
+// of its experts' s (summed in a fixed order: within a slot by a butterfly,
+// then over slots); the topk_groups best groups (equal sums to the lower
+// group) are kept and the K rounds only see their experts.
 // Also the fp32 SIMT logits kernel used when tokens are fp32.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -17,11 +22,60 @@ __device__ __forceinline__ uint32_t orderable(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Bit mask of the kept groups for this warp's token.  Experts per group gs is
+// a multiple of 32 or a power of two below 32 (checked by the caller).
+template <int NPL>
+__device__ __forceinline__ uint32_t kept_groups(const float (&s)[NPL], int E, int n_groups,
+                                                int topk_groups, int lane) {
+  const int gs = E / n_groups;
+  const int seg = gs < 32 ? gs : 32;
+  float part[NPL];   // per slot: sum over this lane's segment of seg lanes
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    float v = (j * 32 + lane < E) ? s[j] : 0.f;
+    for (int o = 1; o < seg; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    part[j] = v;
+  }
+  // lane g (< n_groups) gathers group g's score
+  float gsum = -INFINITY;
+  if (gs >= 32) {
+    const int spg = gs >> 5;           // slots per group
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+      if (j / spg == lane) acc += part[j];
+    if (lane < n_groups) gsum = acc;
+  } else {
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      // group g = j * (32 / gs) + lane / gs lives in slot j, lanes [g*gs % 32, +gs)
+      const int g = lane;
+      const int src = (g * gs) & 31;
+      const float v = __shfl_sync(0xffffffffu, part[j], src);
+      if (g < n_groups && (g * gs) >> 5 == j) gsum = v;
+    }
+  }
+  uint32_t mask = 0;
+  for (int m = 0; m < topk_groups; ++m) {
+    unsigned long long c = 0ull;
+    if (lane < n_groups && !((mask >> lane) & 1u))
+      c = (static_cast<unsigned long long>(orderable(gsum)) << 32) | (0xFFFFFFFFu - lane);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, c, o);
+      c = other > c ? other : c;
+    }
+    mask |= 1u << (0xFFFFFFFFu - static_cast<uint32_t>(c & 0xFFFFFFFFull));
+  }
+  return mask;
+}
+
 template <int NPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int splits,
                                                    long long split_stride,
                                                    const float* __restrict__ bias, int T, int E,
                                                    int K, int score_func, int normalize,
+                                                   int n_groups, int topk_groups,
                                                    int32_t* __restrict__ idx,
                                                    float* __restrict__ gates) {
   const int lane = threadIdx.x & 31;
@@ -66,7 +120,16 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     const int e = j * 32 + lane;
     keyo[j] = (e < E) ? orderable(s[j] + __ldg(bias + e)) : 0u;
   }
-  uint32_t taken = 0;
+  uint32_t taken = 0;   // per slot: already chosen, or outside the kept groups
+  if (n_groups > 0) {
+    const uint32_t gm = kept_groups<NPL>(s, E, n_groups, topk_groups, lane);
+    const int gs = E / n_groups;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = j * 32 + lane;
+      if (e < E && !((gm >> (e / gs)) & 1u)) taken |= 1u << j;
+    }
+  }
   int my_e = 0;
   float my_s = 0.f, sum_sel = 0.f;
   for (int k = 0; k < K; ++k) {
@@ -127,13 +190,15 @@ __global__ void logits_f32_kernel(const float* __restrict__ x, const float* __re
 
 moe_status_t launch_topk(const float* logits, int splits, long long split_stride,
                          const float* bias, int T, int E, int K, int score_func, int normalize,
-                         int32_t* idx, float* gates, cudaStream_t stream) {
+                         int n_groups, int topk_groups, int32_t* idx, float* gates,
+                         cudaStream_t stream) {
   if (T <= 0) return MOE_OK;
   TraceScope tr(stream, "router_topk");
   const int grid = ceil_div(T, 8);
 #define MOE_TOPK(NPL)                                                                      \
   topk_kernel<NPL><<<grid, 256, 0, stream>>>(logits, splits, split_stride, bias, T, E, K, \
-                                             score_func, normalize, idx, gates)
+                                             score_func, normalize, n_groups, topk_groups, idx, \
+                                             gates)
   if (E <= 32) MOE_TOPK(1);
   else if (E <= 64) MOE_TOPK(2);
   else if (E <= 128) MOE_TOPK(4);

@@ -41,6 +41,8 @@ class LayerCfg:
     gamma: float = 1e-3
     seed: int = 0
     zipf_s: float = 0.0          # > 0: expert popularity ~ rank^-zipf_s (see gen.py)
+    n_groups: int = 0            # node-limited routing: expert groups (0 = off)
+    topk_groups: int = 0         # groups kept per token
 
     def with_(self, **kw) -> "LayerCfg":
         return replace(self, **kw)
@@ -101,6 +103,9 @@ def small_cases() -> dict:
                            w_std=0.03, bias_range=0.01),
         "tiny_f32_ragged": CONFIGS["tiny"].with_(name="tiny_f32_ragged", T=37, d=96,
                                                  E=8, K=3, S=2, I=40),
+        # node-limited routing: 8 groups of 4 experts, 3 kept (V3 uses 8 nodes, 4 kept)
+        "grouped_bf16": v3.with_(name="grouped_bf16", T=512, d=512, E=32, K=4, S=1, I=256,
+                                 w_std=0.03, bias_range=0.01, n_groups=8, topk_groups=3),
         # FP8 block-scaled experts, Zipf-skewed routing (one expert takes every token)
         "small_fp8": CONFIGS["v3_skewed_fp8"].with_(name="small_fp8", T=600, d=512, E=32,
                                                     K=4, S=1, I=384, w_std=0.03),

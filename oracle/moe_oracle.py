@@ -30,6 +30,9 @@ Readings where the pages are silent (all also listed in the design doc):
 - "Overloaded" means count_i * E > T * K (exactly above the mean load); equal
   to the mean leaves b_i unchanged.  The update is float32 arithmetic.
 - Softmax mode (2024 layer) normalises over all E experts before selection.
+- Node-limited routing ranks groups by the sum of the unbiased scores s of
+  all their experts (the page's "affinity scores"); the bias then acts only
+  inside the kept groups.
 - If the chosen scores sum to 0 the renormalised gates are 0.
 """
 from __future__ import annotations
@@ -99,6 +102,28 @@ def select_topk(keys: np.ndarray, K: int):
     return idx, margin
 
 
+def select_groups(s: np.ndarray, n_groups: int, topk_groups: int):
+    """Node-limited routing (V3 walk-through, section 2.3): the experts are split
+    into n_groups equal groups of consecutive indices (one group per node); a
+    group's score is the sum of the affinity scores s of all its experts; the
+    topk_groups best groups are kept (equal scores to the lower group index).
+    Scores are summed in fp64 from the fp32-rounded s.  Returns the allowed
+    mask [T, E] and the margin between the M-th and (M+1)-th group score."""
+    T, E = s.shape
+    gs = E // n_groups
+    gscore = s.astype(np.float32).astype(np.float64).reshape(T, n_groups, gs).sum(axis=2)
+    allowed = np.zeros((T, E), dtype=bool)
+    margin = np.full(T, np.inf)
+    groups = np.arange(n_groups)
+    for t in range(T):
+        order = np.lexsort((groups, -gscore[t]))
+        for g in order[:topk_groups]:
+            allowed[t, g * gs:(g + 1) * gs] = True
+        if topk_groups < n_groups:
+            margin[t] = gscore[t, order[topk_groups - 1]] - gscore[t, order[topk_groups]]
+    return allowed, margin
+
+
 def gate_values(s: np.ndarray, idx: np.ndarray, normalize: int) -> np.ndarray:
     """g'_{i,t} = s_{i,t} for the chosen experts (eq. 14; the bias is not used),
     then g = g' / sum_j g'_j over the chosen experts (eq. 13) when ``normalize``."""
@@ -109,10 +134,21 @@ def gate_values(s: np.ndarray, idx: np.ndarray, normalize: int) -> np.ndarray:
     return g
 
 
-def route(u, centroids, bias, K: int, score_func: int = SIGMOID, normalize: int = 1):
-    """Whole router for the given tokens: idx, gates (fp64), margins, scores."""
+def route(u, centroids, bias, K: int, score_func: int = SIGMOID, normalize: int = 1,
+          n_groups: int = 0, topk_groups: int = 0):
+    """Whole router for the given tokens: idx, gates (fp64), margins, scores.
+    With n_groups > 0 the top-K runs only over the experts of the topk_groups
+    best groups (select_groups); the returned margin is then the smaller of
+    the group margin and the expert margin inside the kept groups."""
     s = expert_scores(affinity_logits(u, centroids), score_func)
-    idx, margin = select_topk(selection_keys(s, bias), K)
+    keys = selection_keys(s, bias)
+    gmargin = None
+    if n_groups > 0:
+        allowed, gmargin = select_groups(s, n_groups, topk_groups)
+        keys = np.where(allowed, keys, np.float32(-np.inf)).astype(np.float32)
+    idx, margin = select_topk(keys, K)
+    if gmargin is not None:
+        margin = np.minimum(margin, gmargin)
     return idx, gate_values(s, idx, normalize), margin, s
 
 
@@ -177,7 +213,8 @@ def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
 
 
 def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
-              add_residual: int = 1, tokens=None) -> dict:
+              add_residual: int = 1, tokens=None, n_groups: int = 0,
+              topk_groups: int = 0) -> dict:
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
@@ -193,7 +230,7 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     u = _f64(x)
     n = u.shape[0]
     idx, gates, margin, _ = route(u, inp["centroids"], inp["bias"], K, score_func,
-                                  normalize)
+                                  normalize, n_groups, topk_groups)
     d = u.shape[1]
     delta = np.zeros((n, d))
     S = inp["ws13"].shape[0]

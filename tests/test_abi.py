@@ -57,9 +57,24 @@ def _cfg(**kw):
     (dict(I=96), 1),                        # bf16 needs I % 128 == 0
     (dict(score_func=2), 1), (dict(normalize=2), 1),
     (dict(act_dtype=0, wgt_dtype=1), 2),    # mixed pair not built
-    (dict(act_dtype=2, wgt_dtype=2), 2),    # fp8 not built yet
+    (dict(act_dtype=2, wgt_dtype=2), 2),    # e4m3 tokens: not a layer dtype
+    (dict(act_dtype=1, wgt_dtype=2), 0),    # FP8 layer: bf16 tokens, e4m3 experts
+    (dict(act_dtype=0, wgt_dtype=2), 2),    # fp32 tokens with e4m3 experts: not built
     (dict(act_dtype=0, wgt_dtype=0, d=96, I=40), 0),   # fp32 takes any d, I
     (dict(T=0), 0),
+    # node-limited routing
+    (dict(n_groups=4, topk_groups=2), 0),   # 4 groups of 4 experts, K=4 <= 2*4
+    (dict(n_groups=4, topk_groups=1), 0),   # K=4 <= 1*4
+    (dict(n_groups=8, topk_groups=1), 1),   # K=4 > 1*2 experts
+    (dict(n_groups=4, topk_groups=5), 1),   # more kept than groups
+    (dict(n_groups=4, topk_groups=0), 1),
+    (dict(n_groups=0, topk_groups=2), 1),
+    (dict(n_groups=3, topk_groups=1, E=48, K=4), 0),   # groups of 16
+    (dict(n_groups=4, topk_groups=1, E=48, K=4), 1),   # groups of 12: not a power of two
+    (dict(n_groups=2, topk_groups=1, E=96, K=4), 1),   # groups of 48: not a multiple of 32
+    (dict(n_groups=2, topk_groups=1, E=128, K=4), 0),  # groups of 64
+    (dict(n_groups=5, topk_groups=2, E=16), 1),        # 16 experts do not split in 5
+    (dict(n_groups=64, topk_groups=8, E=1024, K=8), 1),  # more than 32 groups
 ])
 def test_check_cfg(kw, code):
     assert m.check_cfg(_cfg(**kw)) == code

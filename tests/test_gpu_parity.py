@@ -29,7 +29,13 @@ def _cfg(name):
 
 def _route_oracle(cfg, c, tokens=None):
     x = c["x"] if tokens is None else c["x"][torch.as_tensor(tokens, device=c["x"].device)]
-    return O.route(x, c["centroids"], c["bias"], cfg.K, cfg.score_func, cfg.normalize)
+    return O.route(x, c["centroids"], c["bias"], cfg.K, cfg.score_func, cfg.normalize,
+                   cfg.n_groups, cfg.topk_groups)
+
+
+def _layer(cfg, c, **kw):
+    return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, n_groups=cfg.n_groups,
+                       topk_groups=cfg.topk_groups, **kw)
 
 
 def _check_routing(cfg, idx_g, gates_g, idx_o, gates_o, margin, keys_o=None):
@@ -93,6 +99,22 @@ def test_route_bias_forces_expert_and_keeps_gate():
     _check_routing(cfg, idx, run.gates.cpu().numpy(), idx_o, gates_o, margin, _keys(cfg, cb, s))
 
 
+def test_route_group_limited_v3_full_size():
+    """Node-limited routing on the V3 prefill layer: 8 groups of 32 experts
+    (one per node of the V3 deployment), 4 kept per token (V3 walk-through,
+    section 2.3); all 8192 tokens against the oracle."""
+    cfg = get_config("v3_prefill").with_(name="v3_grouped", n_groups=8, topk_groups=4)
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g)
+    run.route()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    idx_g = run.idx.cpu().numpy()
+    assert max(len(set((r // 32).tolist())) for r in idx_g) <= 4
+    idx_o, gates_o, margin, s = _route_oracle(cfg, c)
+    _check_routing(cfg, idx_g, run.gates.cpu().numpy(), idx_o, gates_o, margin)
+
+
 # ---------------------------------------------------------------- dispatch
 
 @pytest.mark.parametrize("name", SMALL + FULL)
@@ -123,7 +145,7 @@ def test_experts_combine_on_oracle_routing(name):
     cfg = _cfg(name)
     g, c = gpu_inputs(cfg)
     run = GpuRun(m, cfg, g, add_residual=0)
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    ref = _layer(cfg, c, add_residual=0)
     run.dispatch(torch.as_tensor(ref["idx"], dtype=torch.int32, device="cuda"))
     run.experts()
     gates = torch.as_tensor(ref["gates"], dtype=torch.float32, device="cuda")
@@ -167,7 +189,7 @@ def test_forward_parity_all_tokens(name):
     run.forward()
     torch.cuda.synchronize()
     assert run.status() == 0
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    ref = _layer(cfg, c, add_residual=0)
     keep, _ = _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), ref["idx"],
                              ref["gates"], ref["margin"])
     assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, f"{name} forward")
@@ -184,7 +206,7 @@ def test_forward_with_residual(name):
     run = GpuRun(m, cfg, g, add_residual=1)
     run.forward()
     torch.cuda.synchronize()
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=1)
+    ref = _layer(cfg, c, add_residual=1)
     keep = ref["margin"] >= MARGIN_EXCLUDE
     assert_close(to_np(run.out)[keep], ref["out"][keep], cfg.act, f"{name} out")
 
@@ -244,7 +266,7 @@ def test_forward_full_size_sampled(name):
     tok = np.sort(rng.choice(cfg.T, SAMPLES[name], replace=False))
     tok[0] = 0
     tok[-1] = cfg.T - 1                       # first and last token (ragged tail)
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0, tokens=tok)
+    ref = _layer(cfg, c, add_residual=0, tokens=tok)
     keep = ref["margin"] >= MARGIN_EXCLUDE
     np.testing.assert_array_equal(np.sort(idx_g[tok], 1)[keep], np.sort(ref["idx"], 1)[keep])
     out = to_np(run.out)[tok]
@@ -270,7 +292,7 @@ def test_edge_cases(name):
     run.forward()
     torch.cuda.synchronize()
     assert run.status() == 0
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    ref = _layer(cfg, c, add_residual=0)
     keep, _ = _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), ref["idx"],
                              ref["gates"], ref["margin"])
     assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, name)
@@ -289,7 +311,7 @@ def test_hot_expert_spans_several_token_blocks():
     run.forward()
     torch.cuda.synchronize()
     assert run.counts[3].item() == 600
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0)
+    ref = _layer(cfg, c, add_residual=0)
     keep = ref["margin"] >= MARGIN_EXCLUDE
     assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, "hot expert")
 

@@ -378,3 +378,72 @@ def test_zipf_targets_capped_and_sum_to_k():
     r = torch.arange(1, 257, dtype=torch.float64)[free]
     ratio = f[free] * r ** 1.1
     assert float(ratio.max() - ratio.min()) < 1e-9 * float(ratio.max())
+
+
+# ---------------------------------------------------------------- node-limited routing
+
+def test_golden_group_limited_routing():
+    with open(os.path.join(GOLDEN, "routing_groups_hand.txt")) as f:
+        lines = [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+    sv = np.array([[float(v) for v in lines[0].split(":")[1].split()]])
+    for ln in lines[1:]:
+        spec, want = ln.split(":", 1)[1].split("->")
+        kv = dict(item.split("=") for item in spec.split())
+        M, K = int(kv["M"]), int(kv["K"])
+        bias = np.array([float(v) for v in kv["bias"].split(",")], dtype=np.float32)
+        allowed, _ = O.select_groups(sv, 2, M)
+        keys = np.where(allowed, O.selection_keys(sv, bias), np.float32(-np.inf))
+        idx, _ = O.select_topk(keys.astype(np.float32), K)
+        assert idx[0].tolist() == [int(v) for v in want.split(",")], ln
+
+
+@pytest.mark.parametrize("E,G,M,K", [(8, 4, 2, 3), (12, 3, 2, 4), (16, 8, 3, 5), (8, 2, 1, 4)])
+def test_group_limited_routing_brute_force(E, G, M, K):
+    """The kept groups are the M-subset with the largest total group score
+    (scores distinct), and the chosen experts are the K-subset of the kept
+    experts with the largest total key."""
+    rng = np.random.default_rng(E * 100 + G * 10 + M)
+    gs = E // G
+    for _ in range(30):
+        s = rng.random((1, E))
+        bias = (rng.random(E) * 0.2 - 0.1).astype(np.float32)
+        allowed, _ = O.select_groups(s, G, M)
+        gscore = s.astype(np.float32).astype(np.float64).reshape(G, gs).sum(axis=1)
+        best = max(itertools.combinations(range(G), M), key=lambda c: sum(gscore[list(c)]))
+        want_allowed = np.zeros(E, bool)
+        for g in best:
+            want_allowed[g * gs:(g + 1) * gs] = True
+        assert np.array_equal(allowed[0], want_allowed)
+        keys = O.selection_keys(s, bias)[0].astype(np.float64)
+        cand = np.nonzero(want_allowed)[0]
+        bestk = max(itertools.combinations(cand, K), key=lambda c: sum(keys[list(c)]))
+        idx, _, _, _ = _route_with_scores(s, bias, K, G, M)
+        assert sorted(idx[0].tolist()) == sorted(int(e) for e in bestk)
+
+
+def _route_with_scores(s, bias, K, G, M):
+    allowed, gm = O.select_groups(s, G, M)
+    keys = np.where(allowed, O.selection_keys(s, bias), np.float32(-np.inf)).astype(np.float32)
+    idx, margin = O.select_topk(keys, K)
+    return idx, O.gate_values(s, idx, 1), np.minimum(margin, gm), s
+
+
+def test_group_limit_with_all_groups_is_plain_topk():
+    cfg = small_cases()["small_bf16"]
+    inp = make_inputs(cfg, "cpu")
+    a = O.route(inp["x"], inp["centroids"], inp["bias"], cfg.K)
+    b = O.route(inp["x"], inp["centroids"], inp["bias"], cfg.K, n_groups=4, topk_groups=4)
+    c = O.route(inp["x"], inp["centroids"], inp["bias"], cfg.K, n_groups=1, topk_groups=1)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[0], c[0])
+    assert np.array_equal(a[1], b[1])
+
+
+def test_group_limit_keeps_experts_in_m_groups():
+    cfg = small_cases()["small_bf16"]
+    inp = make_inputs(cfg, "cpu")
+    idx, gates, _, _ = O.route(inp["x"], inp["centroids"], inp["bias"], cfg.K, n_groups=8,
+                               topk_groups=2)
+    gs = cfg.E // 8
+    for row in idx:
+        assert len(set((row // gs).tolist())) <= 2
+    np.testing.assert_allclose(gates.sum(axis=1), 1.0, atol=1e-12)
