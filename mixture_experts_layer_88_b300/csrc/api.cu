@@ -79,8 +79,9 @@ RouterPlan router_plan(const moe_cfg_t& c) {
   token_blocks(c.T, &p.bs, &p.nb);
   p.eb = ceil_div(c.E, 256);
   p.k_blocks = c.d / 64;
+  // K splits: as many as keep every tile in one wave (tiles <= SMs)
   const int base = p.nb * p.eb > 0 ? p.nb * p.eb : 1;
-  int s = ceil_div(kRouterTargetCtas, base);
+  int s = kRouterTargetCtas / base;
   s = s < 1 ? 1 : s;
   s = s > 16 ? 16 : s;
   s = s > p.k_blocks ? p.k_blocks : s;

@@ -81,17 +81,19 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
+  // sum of the K-split partial logits, split by split in a fixed order; the
+  // NPL loads of one split are independent, so they are in flight together
   float L[NPL];
 #pragma unroll
-  for (int j = 0; j < NPL; ++j) {
-    const int e = j * 32 + lane;
-    float acc = -INFINITY;
-    if (e < E) {
-      acc = 0.f;
-      const float* p = logits + static_cast<size_t>(t) * E + e;
-      for (int sp = 0; sp < splits; ++sp) acc += __ldg(p + sp * split_stride);  // fixed order
-    }
-    L[j] = acc;
+  for (int j = 0; j < NPL; ++j) L[j] = (j * 32 + lane < E) ? 0.f : -INFINITY;
+  const float* row = logits + static_cast<size_t>(t) * E + lane;
+  for (int sp = 0; sp < splits; ++sp) {
+    float v[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+      v[j] = (j * 32 + lane < E) ? __ldg(row + sp * split_stride + j * 32) : 0.f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) L[j] += v[j];
   }
   float s[NPL];
   if (score_func == MOE_SCORE_SOFTMAX) {
