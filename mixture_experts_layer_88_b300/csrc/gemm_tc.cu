@@ -357,22 +357,26 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
           const int tok = j0 + 8 * hf + (lane & 7);
           const bool tok_ok = tok < t.ntok;
           __nv_bfloat16* orow = out + (out_row0 + tok) * args.out_ld;
-          float v[8];
           if (MODE == GM_GATEUP) {
+            float v[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               v[i] = silu_mul(__uint_as_float(r0[8 * hf + i]), __uint_as_float(r1[8 * hf + i]));
             transpose8(v, lane);
             if (c0ok && tok_ok) store_bf16x8(orow + colg0, v);
           } else {
+            // two independent outputs per element: plain 2-byte stores (32
+            // lanes write 64 contiguous bytes) cost less than two transposes
+            const int jb = j0 + 8 * hf;
+            __nv_bfloat16* o = out + (out_row0 + jb) * args.out_ld;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r0[8 * hf + i]);
-            transpose8(v, lane);
-            if (c0ok && tok_ok) store_bf16x8(orow + colg0, v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r1[8 * hf + i]);
-            transpose8(v, lane);
-            if (c1ok && tok_ok) store_bf16x8(orow + colg1, v);
+            for (int i = 0; i < 8; ++i) {
+              if (jb + i < t.ntok) {
+                __nv_bfloat16* oi = o + static_cast<size_t>(i) * args.out_ld;
+                if (c0ok) oi[col0] = __float2bfloat16_rn(__uint_as_float(r0[8 * hf + i]));
+                if (c1ok) oi[col0 + 256] = __float2bfloat16_rn(__uint_as_float(r1[8 * hf + i]));
+              }
+            }
           }
         }
       }

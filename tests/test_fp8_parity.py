@@ -240,3 +240,30 @@ def test_fp8_bias_update_steps_skewed():
         if hot is None:
             hot = int(np.argmax(counts))
     assert bias_o[hot] < 0
+
+
+FP8_EDGE = {
+    "fp8_one_token": small_cases()["ragged_fp8"].with_(name="fp8_one_token", T=1),
+    "fp8_no_shared": small_cases()["ragged_fp8"].with_(name="fp8_no_shared", S=0),
+    "fp8_k_equals_e": small_cases()["ragged_fp8"].with_(name="fp8_k_equals_e", E=8, K=8, T=100),
+    "fp8_grouped": small_cases()["small_fp8"].with_(name="fp8_grouped", zipf_s=0.0, n_groups=4,
+                                                    topk_groups=2),
+}
+
+
+@pytest.mark.parametrize("name", list(FP8_EDGE))
+def test_fp8_edge_cases(name):
+    cfg = FP8_EDGE[name]
+    g, c = gpu_inputs(cfg)
+    run = Fp8Run(cfg, g)
+    run.forward()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0,
+                      n_groups=cfg.n_groups, topk_groups=cfg.topk_groups)
+    keep = ref["margin"] >= MARGIN_EXCLUDE
+    idx = run.idx.cpu().numpy()
+    np.testing.assert_array_equal(np.sort(idx, 1)[keep], np.sort(ref["idx"], 1)[keep])
+    got = run.out.double().cpu().numpy()
+    if keep.any():
+        assert rel_frob(got[keep], ref["delta"][keep]) <= FP8_TOL
