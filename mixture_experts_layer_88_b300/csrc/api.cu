@@ -103,7 +103,8 @@ size_t dispatch_ws(const moe_cfg_t& c) {
 }
 size_t experts_ws(const moe_cfg_t& c) {
   const size_t G = static_cast<size_t>(c.E) + c.S;
-  return align_up(5 * (G + 1) * sizeof(int32_t), 256);
+  // group table (5 x (G+1) int32) + two tile counters after bstart
+  return align_up((5 * (G + 1) + 2) * sizeof(int32_t), 256);
 }
 
 // FP8 layers: rows of expert e start at offsets[e], a multiple of 4 (the
@@ -281,6 +282,7 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   a.out_ld = c.I;
   a.out_cols = c.I;
   a.out = act;
+  a.tile_counter = bstart + G + 1;
   a.status = device_status_word();
   a.timeout_ns = kWaitTimeoutNs;
   s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st);
@@ -302,6 +304,7 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   b.out_ld = c.d;
   b.out_cols = c.d;
   b.out = y;
+  b.tile_counter = bstart + G + 2;
   return launch_gemm_tc(GM_DOWN, m2, b, grid, st);
 }
 
@@ -487,7 +490,8 @@ moe_status_t moe_experts(const moe_cfg_t* cfg, const void* xp, const void* x,
 // The expert FFNs for callers that cannot allocate device memory: the group
 // table that moe_experts keeps in the caller's workspace lives here in a
 // module-scope device array instead.  Capacity: E + S <= kStaticMaxGroups
-// groups (5 int32 arrays of kStaticMaxGroups + 1 entries, about 22 KB), which
+// groups (5 int32 arrays of kStaticMaxGroups + 1 entries and the two GEMMs'
+// tile counters, about 22 KB), which
 // every device that loads this library keeps until the process exits.  The
 // array's address is looked up once per device (cudaGetSymbolAddress) on that
 // device's first call.  All calls share the one array and keep the last
@@ -500,7 +504,7 @@ namespace {
 constexpr int kStaticMaxGroups = kMaxE + kMaxS;
 }  // namespace
 
-static __device__ __align__(256) int32_t g_static_group_table[5 * (kStaticMaxGroups + 1)];
+static __device__ __align__(256) int32_t g_static_group_table[5 * (kStaticMaxGroups + 1) + 2];
 
 namespace {
 int32_t* static_group_table() {

@@ -184,8 +184,63 @@ constexpr uint32_t EX_B_BYTES = 128 * ROW_BYTES;          // 16 KB: up to 128 to
 constexpr uint32_t EX_STAGE_BYTES = 2 * EX_A_BOX_BYTES + EX_B_BYTES;
 constexpr int EX_EPI_WARPS = 8;
 constexpr int EX_THREADS = 64 + 32 * EX_EPI_WARPS;
-constexpr size_t EX_SMEM_BYTES = EX_STAGES * EX_STAGE_BYTES + 1024 + 256;
+constexpr int EX_QUEUE = 4;                               // tile indices in flight
+// readers of each published tile index: the MMA warp and the epilogue warps of
+// the even CTA, the producer and the epilogue warps of the odd CTA
+constexpr int kQueueConsumers = 2 + 2 * EX_EPI_WARPS;
+constexpr size_t EX_SMEM_BYTES = EX_STAGES * EX_STAGE_BYTES + 1024 + 512;
 static_assert(EX_SMEM_BYTES <= 227 * 1024, "expert GEMM shared memory");
+
+// Dynamic tile scheduling for a CTA pair.  The even CTA's producer takes the
+// next tile from a global counter (atomicAdd) and publishes it in slot
+// i % EX_QUEUE of a small queue held in both CTAs' shared memory; every other
+// role reads the same sequence from its own CTA's copy.  An index >= ntiles
+// ends the sequence.  Waits are bounded like all others.
+struct TileQueue {
+  uint64_t* qfull;
+  uint64_t* qempty;
+  volatile int* tq;
+  uint32_t rank;
+  volatile int* abort_flag;
+  unsigned long long tmo;
+  int* counter;
+  int i = 0;
+
+  // even CTA, producer warp, lane 0: claim a tile (the value is needed only
+  // by the publish that follows, so the atomic's latency overlaps the loads
+  // issued in between)
+  __device__ __forceinline__ int take() const {
+    return (threadIdx.x & 31) == 0 ? atomicAdd(counter, 1) : 0;
+  }
+  // even CTA, producer warp: publish a claimed tile to both CTAs; every lane
+  // gets it back
+  __device__ __forceinline__ bool publish(int t, int& tile) {
+    const int s = i % EX_QUEUE;
+    const uint32_t ph = static_cast<uint32_t>(i / EX_QUEUE) & 1u;
+    if (!warp_wait<true>(qempty + s, ph ^ 1u, abort_flag, tmo)) return false;
+    if ((threadIdx.x & 31) == 0) {
+      tq[s] = t;
+      tc::st_shared_cluster_u32(tc::mapa_shared(tc::smem_u32(const_cast<int*>(tq) + s), 1),
+                                static_cast<uint32_t>(t));
+      tc::mbar_arrive(qfull + s);
+      tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(qfull + s), 1));
+    }
+    tile = __shfl_sync(0xffffffffu, t, 0);
+    ++i;
+    return true;
+  }
+  // any other role: read the next published tile and release the slot
+  __device__ __forceinline__ bool next(int& tile) {
+    const int s = i % EX_QUEUE;
+    const uint32_t ph = static_cast<uint32_t>(i / EX_QUEUE) & 1u;
+    if (!warp_wait<true>(qfull + s, ph, abort_flag, tmo)) return false;
+    tile = tq[s];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(qempty + s), 0));
+    ++i;
+    return true;
+  }
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(EX_THREADS, 1)
@@ -198,13 +253,15 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
   uint64_t* tfull = empty + EX_STAGES;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* qfull = drain + 1;           // [EX_QUEUE]: tile index published
+  uint64_t* qempty = qfull + EX_QUEUE;   // [EX_QUEUE]: read by every consumer
+  volatile int* tq = reinterpret_cast<volatile int*>(qempty + EX_QUEUE);   // [EX_QUEUE]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tq) + EX_QUEUE);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_ctarank();
-  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < EX_STAGES; ++s) {
@@ -214,6 +271,10 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
     tc::mbar_init(tfull, 1);
     tc::mbar_init(tempty, 2 * EX_EPI_WARPS);  // every epilogue warp of the pair
     tc::mbar_init(drain, 1);
+    for (int s = 0; s < EX_QUEUE; ++s) {
+      tc::mbar_init(qfull + s, 1);
+      tc::mbar_init(qempty + s, kQueueConsumers);
+    }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -233,13 +294,17 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
   const int ntiles = args.gt.bstart[args.G] * args.m_blocks;
   const unsigned long long tmo = args.timeout_ns;
 
+  TileQueue queue{qfull, qempty, tq, rank, abort_flag, tmo, args.tile_counter};
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, issued_par = 0;   // per stage: a load is in flight / its parity
     bool ok = true;
-    for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
+    int tile = 0;
+    ok = rank == 0 ? queue.publish(queue.take(), tile) : queue.next(tile);
+    while (ok && tile < ntiles) {
+      const int claimed = rank == 0 ? queue.take() : 0;   // the tile after this one
       Tile t;
       decode_group_tile(args, tile, t);
       const bool second = t.g >= args.E;
@@ -274,6 +339,8 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
         __syncwarp();
         if (++stage == EX_STAGES) { stage = 0; phase ^= 1u; }
       }
+      if (!ok) break;
+      ok = rank == 0 ? queue.publish(claimed, tile) : queue.next(tile);
     }
     if (!ok && rank == 0) {
       // abort: let every load counted on this CTA's barriers land before exit
@@ -286,7 +353,10 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, tphase = 0;
       bool ok = true, issued_any = false;
-      for (int tile = cluster; tile < ntiles && ok; tile += nclusters) {
+      for (;;) {
+        int tile;
+        if (!queue.next(tile)) { ok = false; break; }
+        if (tile >= ntiles) break;
         Tile t;
         decode_group_tile(args, tile, t);
         if (!warp_wait<true>(tempty, tphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
@@ -330,7 +400,9 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
     const uint32_t tempty_addr = tc::mapa_shared(tc::smem_u32(tempty), 0);
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t tphase = 0;
-    for (int tile = cluster; tile < ntiles; tile += nclusters) {
+    for (;;) {
+      int tile;
+      if (!queue.next(tile) || tile >= ntiles) break;
       Tile t;
       decode_group_tile(args, tile, t);
       if (!warp_wait(tfull, tphase, abort_flag, tmo)) break;
@@ -625,7 +697,11 @@ __global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, 
   const int g0 = threadIdx.x * 2;
   if (g0 < G) bstart[g0] = before;
   if (g0 + 1 < G) bstart[g0 + 1] = before + nb_pair[0];
-  if (threadIdx.x == 0) bstart[G] = total;
+  if (threadIdx.x == 0) {
+    bstart[G] = total;
+    bstart[G + 1] = 0;   // tile counter of the gate/up GEMM
+    bstart[G + 2] = 0;   // tile counter of the down GEMM
+  }
 }
 
 // Grid of a persistent kernel: at most one CTA (or pair) per SM, and no more

@@ -34,6 +34,7 @@ struct GemmArgs {
   int out_cols;              // valid output columns
   long long out_split_stride;  // router mode: elements between split partials
   void* out;
+  int* tile_counter;         // expert GEMMs: next tile to hand out, 0 at launch
   unsigned* status;
   unsigned long long timeout_ns;  // bound of every barrier wait
 };
@@ -78,7 +79,8 @@ struct GroupLayout {
 
 // Builds the group table of the expert GEMMs from the dispatch offsets (E+1
 // entries; group g has counts[g] rows, or offsets[g+1] - offsets[g] when
-// counts is NULL):
+// counts is NULL), and zeroes the two tile counters (gate/up, down) that
+// follow bstart (bstart[G + 1], bstart[G + 2]):
 // groups 0..E-1 are routed experts, E..E+S-1 the shared experts.  Writes
 // rows, brow (token source row), orow (output row), bs, bstart.
 moe_status_t launch_build_groups(const int* offsets, const int* counts, int T, int E, int S,
