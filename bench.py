@@ -376,7 +376,8 @@ def main():
         "data": "synthetic (seeded random tokens and random-init weights of the layer's shape)",
         "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
                    "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
-                   "parallelism": f"replicas x{ws}",
+                   "parallelism": (f"data parallel x{ws}, load counts all-reduced for the "
+                                   f"bias update" if ws > 1 else "one replica"),
                    "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
                          if cfg.name.startswith("v3") else "inputs larger than L2"},
         "grouped_gemm": {"tflops": round(gemm_tflops, 1) if gemm_tflops else None,

@@ -225,7 +225,7 @@ moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centro
  * 128 x 128 block (w = q * scale), activations quantised inside the layer to
  * e4m3 in 1 x 128 tiles along K (scale = max|x| / 448), and tensor-core
  * partial sums promoted to fp32 on the CUDA cores every 128 elements of K.
- * cfg: act_dtype MOE_BF16, wgt_dtype MOE_E4M3; d and I multiples of 128.
+ * cfg: act_dtype MOE_BF16, wgt_dtype MOE_E4M3; d and I multiples of 128, at most 8192.
  * Centroids are bf16 (the router is not quantised).
  */
 typedef struct {

@@ -426,6 +426,8 @@ moe_status_t moe_check_cfg(const moe_cfg_t* cfg) {
                          4LL * c.E + 4LL * (c.S + 1);
   if (rows >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
   if (c.act_dtype == MOE_BF16 && (c.d % 128 != 0 || c.I % 128 != 0)) return MOE_ERR_INVALID_ARG;
+  // FP8 GEMMs keep a tile's weight scales in shared memory: at most 64 K blocks
+  if (fp8 && (c.d > 8192 || c.I > 8192)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 

@@ -27,7 +27,9 @@
 // the operands.  Group rows start on multiples of 4 (16 bytes of scales).
 //
 // Warp roles (320 threads, one CTA per SM):
-//   warp 0      TMA producer: weight boxes, token rows, token scales per stage
+//   warp 0      TMA producer: weight boxes and token rows per stage, the token
+//               scales of the same K block into an 8-slot ring (freed by the
+//               promotion, while the stage is freed by the MMAs)
 //   warp 1      TMEM owner and MMA issuer
 //   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. and
 //               columns [48 h, 48 h + 48), h = (w - 2) / 4
@@ -53,12 +55,17 @@ constexpr int EPI_WARPS = 8;
 constexpr int CW = 48;                        // token columns per epilogue warp (N <= 2 CW)
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-// shared memory after the stages: token scales per stage, per-warp
-// premultiplied scales, amax exchange, barriers
+// shared memory after the stages: token-scale ring, per-warp premultiplied
+// scales, amax exchange, per-warp weight scales, barriers
+// token scales ride in their own, deeper ring: an operand stage is freed as soon
+// as its MMAs finish, while the scales of that K block stay until promoted
+constexpr int SC_SLOTS = 8;
 constexpr uint32_t SC_OFF = STAGES * STAGE_BYTES;
-constexpr uint32_t PS_OFF = SC_OFF + STAGES * 128 * 4;
+constexpr uint32_t PS_OFF = SC_OFF + SC_SLOTS * 128 * 4;
 constexpr uint32_t AM_OFF = PS_OFF + EPI_WARPS * 2 * 64 * 4;
-constexpr uint32_t BAR_OFF = AM_OFF + 2 * 2 * 4 * 64 * 4;
+constexpr uint32_t WS_OFF = AM_OFF + 2 * 2 * 4 * 64 * 4;   // per warp: the tile's weight scales
+constexpr int MAX_KB = 64;                                  // K blocks per tile (K <= 8192)
+constexpr uint32_t BAR_OFF = WS_OFF + EPI_WARPS * 2 * MAX_KB * 4;
 constexpr size_t SMEM_BYTES = BAR_OFF + 256 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "fp8 GEMM shared memory");
 
@@ -155,15 +162,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* sc_stage = reinterpret_cast<float*>(smem + SC_OFF);    // [STAGES][128]
+  float* sc_ring = reinterpret_cast<float*>(smem + SC_OFF);     // [SC_SLOTS][128]
   float* psc = reinterpret_cast<float*>(smem + PS_OFF);         // [EPI_WARPS][2][64]
   float* amx = reinterpret_cast<float*>(smem + AM_OFF);         // [2 par][2 h][4 q][64]
+  float* wsm = reinterpret_cast<float*>(smem + WS_OFF);         // [EPI_WARPS][2][MAX_KB]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* pfull = empty + STAGES;     // [2]
   uint64_t* pempty = pfull + 2;         // [2]
   uint64_t* xam = pempty + 2;           // [2 par][2 h]
-  uint64_t* drain = xam + 4;
+  uint64_t* sempty = xam + 4;           // [SC_SLOTS]: scales promoted by every epilogue warp
+  uint64_t* drain = sempty + SC_SLOTS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -173,13 +182,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1 + EPI_WARPS);   // MMAs done + scales read
+      tc::mbar_init(empty + s, 1);               // MMAs done
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(pfull + b, 1);
       tc::mbar_init(pempty + b, EPI_WARPS);
     }
     for (int i = 0; i < 4; ++i) tc::mbar_init(xam + i, 128);
+    for (int i = 0; i < SC_SLOTS; ++i) tc::mbar_init(sempty + i, EPI_WARPS);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -221,7 +231,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int kb = 0; kb < nkb; ++kb, ++kc) {
         const int stage = kc % STAGES;
         const uint32_t phase = (kc / STAGES) & 1u;
+        const int slot = kc % SC_SLOTS;
         if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        if (!warp_wait(sempty + slot, ((kc / SC_SLOTS) & 1u) ^ 1u, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
         if (lane == 0) {
           uint8_t* sa = smem + stage * STAGE_BYTES;
           tc::mbar_arrive_expect_tx(full + stage, bytes);
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
           // 128 token scales of block kb starting at the tile's first row
-          tc::tma_load_2d(sc_stage + stage * 128, &maps.sx, full + stage, b_row, kb);
+          tc::tma_load_2d(sc_ring + slot * 128, &maps.sx, full + stage, b_row, kb);
         }
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -312,19 +327,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool rb1ok = MODE == GM_GATEUP || t.mb * 2 + 1 < rb;
       const int c0 = h * CW;
       const bool active = c0 < t.nmma;
+      // the tile's weight scales, one read per tile instead of one per K block
+      float* my_ws = wsm + ew * 2 * MAX_KB;
+      for (int k = lane; k < nkb; k += 32) {
+        my_ws[k] = __ldg(wsc + static_cast<size_t>(rb0) * nkb + k);
+        my_ws[MAX_KB + k] = rb1ok ? __ldg(wsc + static_cast<size_t>(rb1) * nkb + k) : 0.f;
+      }
+      __syncwarp();
       float a0[CW], a1[CW];
 #pragma unroll
       for (int i = 0; i < CW; ++i) { a0[i] = 0.f; a1[i] = 0.f; }
       for (int kb = 0; kb < nkb; ++kb, ++kc) {
-        const int stage = kc % STAGES;
         const int pb = kc & 1;
         const uint32_t puse = (kc >> 1) & 1u;
         if (!warp_wait(pfull + pb, puse, abort_flag, tmo)) { ok = false; break; }
         tc::tc_fence_after();
         if (active) {
-          const float sw0 = __ldg(wsc + static_cast<size_t>(rb0) * nkb + kb);
-          const float sw1 = rb1ok ? __ldg(wsc + static_cast<size_t>(rb1) * nkb + kb) : 0.f;
-          const float* sx = sc_stage + stage * 128 + c0;
+          const float sw0 = my_ws[kb];
+          const float sw1 = my_ws[MAX_KB + kb];
+          const float* sx = sc_ring + (kc % SC_SLOTS) * 128 + c0;
           my_ps[lane] = sw0 * sx[lane];
           my_ps[64 + lane] = sw1 * sx[lane];
           if (lane + 32 < CW) {
@@ -364,7 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           tc::mbar_arrive(pempty + pb);
-          tc::mbar_arrive(empty + stage);
+          tc::mbar_arrive(sempty + kc % SC_SLOTS);
         }
       }
       if (!ok) break;

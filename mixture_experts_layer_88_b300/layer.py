@@ -4,7 +4,7 @@ from __future__ import annotations
 
 import torch
 
-from . import _lib
+from . import _lib, parallel
 
 
 class MoeLayer:
@@ -53,10 +53,15 @@ class MoeLayer:
                          self._ws, stream)
         return out
 
-    def update_bias(self, stream=None) -> torch.Tensor:
-        """Sign update of the balancing bias from the last forward's counts."""
-        _lib.update_bias(self.cfg, self.counts, self.bias, self.load_stats, stream)
-        return self.load_stats
+    def update_bias(self, stream=None, group=None) -> torch.Tensor:
+        """Sign update of the balancing bias from the last forward's counts.
+        Under torch.distributed with more than one rank the counts are first
+        summed over `group` (data-parallel replicas balance on the global
+        batch; see parallel.py)."""
+        def upd(cfg, counts, bias):
+            _lib.update_bias(cfg, counts, bias, self.load_stats, stream)
+            return self.load_stats
+        return parallel.balance_step(self.cfg, self.counts, self.bias, upd, group)
 
     def step(self, x: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
         """One batch of the layer: forward, then the bias update for the next batch."""

@@ -60,6 +60,7 @@ def _cfg(**kw):
     (dict(act_dtype=2, wgt_dtype=2), 2),    # e4m3 tokens: not a layer dtype
     (dict(act_dtype=1, wgt_dtype=2), 0),    # FP8 layer: bf16 tokens, e4m3 experts
     (dict(act_dtype=0, wgt_dtype=2), 2),    # fp32 tokens with e4m3 experts: not built
+    (dict(act_dtype=1, wgt_dtype=2, d=8320), 1),   # FP8 layers: d, I <= 8192
     (dict(act_dtype=0, wgt_dtype=0, d=96, I=40), 0),   # fp32 takes any d, I
     (dict(T=0), 0),
     # node-limited routing

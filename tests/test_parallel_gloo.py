@@ -1,0 +1,80 @@
+"""The data-parallel exchange on CPU: two gloo ranks, each with its own batch,
+sum their load counts and apply the same sign update against the global mean
+load, so their biases stay equal and match one rank holding both batches.
+The update here is the oracle's (no GPU); the GPU layer passes the C-ABI
+update through the same mixture_experts_layer_88_b300.parallel.balance_step."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from oracle import moe_oracle as O
+
+E, K, T_LOCAL = 16, 4, 64
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+class _Cfg:
+    def __init__(self, T):
+        self.T, self.K, self.E, self.gamma = T, K, E, 1e-3
+
+
+def _rank_counts(rank):
+    rng = np.random.default_rng(100 + rank)
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T_LOCAL)])
+    return np.bincount(idx.reshape(-1), minlength=E).astype(np.int32)
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from mixture_experts_layer_88_b300 import parallel
+    counts = torch.from_numpy(_rank_counts(rank))
+    bias = torch.full((E,), 0.25, dtype=torch.float32)
+    seen = {}
+
+    def update(cfg, c, b):
+        seen["T"] = cfg.T
+        nb, _ = O.update_bias(c.numpy(), b.numpy(), cfg.T, cfg.K, cfg.gamma)
+        b.copy_(torch.from_numpy(nb))
+        return b
+
+    parallel.balance_step(_Cfg(T_LOCAL), counts, bias, update)
+    out[rank] = (counts.numpy().copy(), bias.numpy().copy(), seen["T"])
+    dist.destroy_process_group()
+
+
+def test_two_rank_balance_step_keeps_biases_equal():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+            assert p.exitcode == 0
+        res = dict(out)
+    c0, b0, t0 = res[0]
+    c1, b1, t1 = res[1]
+    total = _rank_counts(0) + _rank_counts(1)
+    np.testing.assert_array_equal(c0, total)
+    np.testing.assert_array_equal(c1, total)
+    assert t0 == t1 == 2 * T_LOCAL
+    assert np.array_equal(b0.view(np.uint32), b1.view(np.uint32))
+    # equals one process updating on the whole batch
+    want, _ = O.update_bias(total, np.full(E, 0.25, np.float32), 2 * T_LOCAL, K, 1e-3)
+    assert np.array_equal(b0.view(np.uint32), want.view(np.uint32))
+    # and differs from what rank 0 alone would have done on its half
+    alone, _ = O.update_bias(_rank_counts(0), np.full(E, 0.25, np.float32), T_LOCAL, K, 1e-3)
+    assert not np.array_equal(alone, want)
