@@ -74,19 +74,37 @@ struct RouterPlan {
   int bs, nb, eb, k_blocks, splits, kps;
 };
 
+// Router tiles: token blocks x expert blocks x K splits, chosen to fill the
+// SMs in one wave: the most tiles that fit, then the largest token blocks
+// (fewer re-reads of the centroids), then the fewest splits (fewer partials).
 RouterPlan router_plan(const moe_cfg_t& c) {
   RouterPlan p{};
-  token_blocks(c.T, &p.bs, &p.nb);
   p.eb = ceil_div(c.E, 256);
   p.k_blocks = c.d / 64;
-  // K splits: as many as keep every tile in one wave (tiles <= SMs)
-  const int base = p.nb * p.eb > 0 ? p.nb * p.eb : 1;
-  int s = kRouterTargetCtas / base;
-  s = s < 1 ? 1 : s;
-  s = s > 16 ? 16 : s;
-  s = s > p.k_blocks ? p.k_blocks : s;
-  p.kps = ceil_div(p.k_blocks, s);
-  p.splits = ceil_div(p.k_blocks, p.kps);
+  const int sms = kRouterTargetCtas;
+  int best_tiles = -1;
+  for (int s = 1; s <= 16 && s <= p.k_blocks; ++s) {
+    const int nb_max = sms / (p.eb * s);
+    if (nb_max < 1) break;
+    int bs = round_up(ceil_div(c.T > 0 ? c.T : 1, nb_max), 16);
+    if (bs > 256) continue;                 // too few blocks for T with s splits
+    const int nb = ceil_div(c.T > 0 ? c.T : 1, bs);
+    const int kps = ceil_div(p.k_blocks, s);
+    const int splits = ceil_div(p.k_blocks, kps);
+    const int tiles = nb * p.eb * splits;
+    if (tiles > best_tiles || (tiles == best_tiles && bs > p.bs)) {
+      best_tiles = tiles;
+      p.bs = bs;
+      p.nb = nb;
+      p.kps = kps;
+      p.splits = splits;
+    }
+  }
+  if (best_tiles < 0) {                     // more tokens than one wave holds
+    token_blocks(c.T, &p.bs, &p.nb);
+    p.kps = p.k_blocks;
+    p.splits = 1;
+  }
   return p;
 }
 
