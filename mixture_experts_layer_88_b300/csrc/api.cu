@@ -217,7 +217,7 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
   if (c.act_dtype == MOE_BF16) {
     const RouterPlan p = router_plan(c);
     float* partial = static_cast<float*>(ws);
-    GemmMaps maps;
+    GemmMaps maps{};
     if (!make_gemm_maps(&maps, centroids, c.E, nullptr, 0, 128, x, c.T, nullptr, 0, c.d,
                         kTokBox0Single))
       return MOE_ERR_CUDA;
@@ -285,7 +285,8 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   GemmMaps m1;
   if (!make_gemm_maps(&m1, w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.S > 0 ? ws13 : nullptr,
                       static_cast<uint64_t>(c.S) * 2 * c.I, 128, xp, TK, x, c.T, c.d,
-                      kTokBox0Pair))
+                      kTokBox0Pair) ||
+      !make_store_map(&m1.out, act, R, c.I))
     return MOE_ERR_CUDA;
   GemmArgs a{};
   a.gt = GroupTable{rows, brow, orow, bs, bstart};
@@ -310,7 +311,8 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   GemmMaps m2;
   if (!make_gemm_maps(&m2, w2, static_cast<uint64_t>(c.E) * c.d, c.S > 0 ? ws2 : nullptr,
                       static_cast<uint64_t>(c.S) * c.d, 128, act, R, nullptr, 0, c.I,
-                      kTokBox0Pair))
+                      kTokBox0Pair) ||
+      !make_store_map(&m2.out, y, R, c.d))
     return MOE_ERR_CUDA;
   GemmArgs b = a;
   b.gt = GroupTable{rows, orow, orow, bs, bstart};

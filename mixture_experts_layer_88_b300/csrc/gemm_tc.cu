@@ -32,8 +32,10 @@
 //               issues tcgen05.mma M=256 N=tokens K=16 twice per K step and
 //               commits to both CTAs)
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. of its CTA, the
-//               four warps of each half take alternate 16-column chunks, then
-//               one arrival per warp on the even CTA's "tmem empty" barrier
+//               two warps of a lane quadrant take alternate 16-token chunks;
+//               each chunk is rounded to bf16, written token-major into a
+//               shared-memory box (stmatrix.trans) and stored by TMA; then one
+//               arrival per warp on the even CTA's "tmem empty" barrier
 //
 // Every barrier wait is bounded: after `timeout_ns` without progress the CTA
 // raises an abort flag, lets the TMA loads it issued land, waits for its own
@@ -127,6 +129,31 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g * u, 1.0f + __expf(-g));
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Rounds a 16-lane x 16-column TMEM fragment (tcgen05.ld 16x256b.x2 layout)
+// to bf16 and stores it token-major at this lane's stmatrix row address.
+__device__ __forceinline__ void stage_bf16(uint32_t saddr, const uint32_t (&r)[8]) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  tc::stmatrix_x4_trans(saddr, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                        pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+// Same for SiLU(gate) * up of two fragments at the same TMEM positions.
+__device__ __forceinline__ void stage_swiglu(uint32_t saddr, const uint32_t (&g)[8],
+                                             const uint32_t (&u)[8]) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
+  tc::stmatrix_x4_trans(saddr, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                        pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
 // Token rows of one stage: one TMA box per set bit of rows / box0, largest first.
 template <bool PAIR>
 __device__ __forceinline__ void load_token_rows(uint8_t* dst, const CUtensorMap* maps,
@@ -146,34 +173,6 @@ __device__ __forceinline__ void load_token_rows(uint8_t* dst, const CUtensorMap*
   }
 }
 
-// In-place 8x8 transpose within each group of 8 lanes: on entry lane 8g+i
-// holds column i of the group in v[0..7] (8 tokens); on exit it holds token i
-// with the group's 8 columns in v[0..7].  Three butterfly stages; every lane
-// of the warp must take part.
-__device__ __forceinline__ void transpose8(float (&v)[8], int lane) {
-#pragma unroll
-  for (int m = 4; m >= 1; m >>= 1) {
-    const bool hi = (lane & m) != 0;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if (r & m) continue;
-      const int rh = r | m;
-      const float send = hi ? v[r] : v[rh];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, m);
-      if (hi) v[r] = recv; else v[rh] = recv;
-    }
-  }
-}
-
-// Eight fp32 values rounded to bf16 and written as one 16-byte store.
-__device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, const float (&v)[8]) {
-  uint4 o;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-  *reinterpret_cast<uint4*>(dst) = o;
-}
-
 // ============================================================================
 // Expert GEMMs on CTA pairs
 // ============================================================================
@@ -188,8 +187,16 @@ constexpr int EX_QUEUE = 4;                               // tile indices in fli
 // readers of each published tile index: the MMA warp and the epilogue warps of
 // the even CTA, the producer and the epilogue warps of the odd CTA
 constexpr int kQueueConsumers = 2 + 2 * EX_EPI_WARPS;
-constexpr size_t EX_SMEM_BYTES = EX_STAGES * EX_STAGE_BYTES + 1024 + 512;
-static_assert(EX_SMEM_BYTES <= 227 * 1024, "expert GEMM shared memory");
+// Epilogue staging: per warp, two buffers of NOUT output boxes (16 tokens x 32
+// columns of bf16, 64-byte rows in the TMA 64B swizzle), 1024-byte aligned,
+// after the operand ring and a 1 KB block of barriers.
+constexpr uint32_t EX_STG_OFF = EX_STAGES * EX_STAGE_BYTES + 1024;
+constexpr uint32_t EX_STG_BOX = 16 * 64;
+constexpr int ex_nout(int mode) { return mode == GM_GATEUP ? 1 : 2; }
+constexpr size_t ex_smem_bytes(int mode) {
+  return EX_STG_OFF + EX_EPI_WARPS * 2 * ex_nout(mode) * EX_STG_BOX + 1024;
+}
+static_assert(ex_smem_bytes(GM_DOWN) <= 227 * 1024, "expert GEMM shared memory");
 
 // Dynamic tile scheduling for a CTA pair.  The even CTA's producer takes the
 // next tile from a global counter (atomicAdd) and publishes it in slot
@@ -278,9 +285,11 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 0 && lane < 2 + 2 * kTokBoxes) {
-    const CUtensorMap* m =
-        lane < 2 ? &maps.a[lane] : &maps.b[(lane - 2) / kTokBoxes][(lane - 2) % kTokBoxes];
+  if (warp == 0 && lane < 3 + 2 * kTokBoxes) {
+    const CUtensorMap* m = lane < 2                   ? &maps.a[lane]
+                           : lane < 2 + 2 * kTokBoxes ? &maps.b[(lane - 2) / kTokBoxes]
+                                                               [(lane - 2) % kTokBoxes]
+                                                      : &maps.out;
     tc::tma_prefetch_desc(m);
   }
   if (warp == 1) {
@@ -395,68 +404,103 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                      // TMEM lane quadrant of this warp
-    const int h = (warp - 2) >> 2;               // which alternate 16-column chunks
+    // Warp w drains TMEM lanes 32*(w%4).. (its quadrant: 32 output columns of
+    // this CTA) in 16-token chunks, alternate chunks per warp of a quadrant.
+    // tcgen05.ld 16x256b yields the 8x8 fragment layout that stmatrix.trans
+    // writes token-major into a staging box; one TMA store per box then writes
+    // 16 tokens x 64 bytes (a ragged last chunk is copied row by row instead).
+    constexpr int NOUT = ex_nout(MODE);
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     const uint32_t tempty_addr = tc::mapa_shared(tc::smem_u32(tempty), 0);
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    constexpr uint32_t kLanes16 = 16u << 16;     // TMEM lane offset of the upper 16 lanes
+    uint8_t* stg_p = smem + EX_STG_OFF + (warp - 2) * (2 * NOUT * EX_STG_BOX);
+    const uint32_t stg = tc::smem_u32(stg_p);
+    // stmatrix: lane 8i+j addresses row j of matrix i; matrices 0/1 hold
+    // tokens 0..7 and 2/3 tokens 8..15, odd ones the upper 8 columns of a
+    // 16-lane half; the box row r keeps 16-byte chunk c at c ^ ((r >> 1) & 3)
+    const int srow = (lane & 7) + 8 * (lane >> 4);
+    uint32_t soff[2];
+#pragma unroll
+    for (int lh = 0; lh < 2; ++lh) {
+      const int chunk = 2 * lh + ((lane >> 3) & 1);
+      soff[lh] = static_cast<uint32_t>(srow * 64 + ((chunk ^ ((srow >> 1) & 3)) << 4));
+    }
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+    int sbuf = 0;
     uint32_t tphase = 0;
     for (;;) {
       int tile;
       if (!queue.next(tile) || tile >= ntiles) break;
       Tile t;
       decode_group_tile(args, tile, t);
+      const int out_row0 = __ldg(args.gt.orow + t.g) + t.tok0;
+      // GATEUP: act columns (SiLU(acc0) * acc1); DOWN: y columns of acc0 and,
+      // 256 further, of acc1
+      const int colbase = t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128 +
+                          q * 32;
       if (!warp_wait(tfull, tphase, abort_flag, tmo)) break;
       tc::tc_fence_after();
-      const size_t out_row0 = static_cast<size_t>(__ldg(args.gt.orow + t.g) + t.tok0);
-      // GATEUP: act column of acc0 (gate) and acc1 (up) of this lane
-      // DOWN:   y columns of acc0 and acc1 (256 rows apart)
-      const int col0 = t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128 +
-                       q * 32 + lane;
-      // after the 8x8 transposes lane 8g+i holds token i of a half-chunk and
-      // the 8 columns [col_base + 8g, +8): one 16-byte store per lane
-      const int colg0 = col0 - (lane & 7);
-      const int colg1 = colg0 + 256;
-      const bool c0ok = colg0 < args.out_cols;
-      const bool c1ok = MODE == GM_DOWN && colg1 < args.out_cols;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
       for (int j0 = h * 16; j0 < t.nmma; j0 += 32) {
-        uint32_t r0[16], r1[16];
-        tc::tmem_ld16(taddr + j0, r0);
-        tc::tmem_ld16(taddr + 256 + j0, r1);
-        tc::tmem_wait_ld(r0, r1);
+        uint32_t g0[8], g1[8], u0[8], u1[8];      // acc0 / acc1, lanes 0..15 / 16..31
+        tc::tmem_ld16x256_x2(taddr + j0, g0);
+        tc::tmem_ld16x256_x2(taddr + kLanes16 + j0, g1);
+        tc::tmem_ld16x256_x2(taddr + 256 + j0, u0);
+        tc::tmem_ld16x256_x2(taddr + kLanes16 + 256 + j0, u1);
+        tc::tmem_wait_ld4(g0, g1, u0, u1);
+        // the buffer written now was last stored from two chunks ago
+        if (lane == 0) tc::bulk_wait_read<1>();
+        __syncwarp();
+        const uint32_t buf = stg + sbuf * (NOUT * EX_STG_BOX);
+        if (MODE == GM_GATEUP) {
+          stage_swiglu(buf + soff[0], g0, u0);
+          stage_swiglu(buf + soff[1], g1, u1);
+        } else {
+          stage_bf16(buf + soff[0], g0);
+          stage_bf16(buf + soff[1], g1);
+          stage_bf16(buf + EX_STG_BOX + soff[0], u0);
+          stage_bf16(buf + EX_STG_BOX + soff[1], u1);
+        }
+        const int nv = min(16, t.ntok - j0);
+        if (nv == 16) {
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int tok = j0 + 8 * hf + (lane & 7);
-          const bool tok_ok = tok < t.ntok;
-          __nv_bfloat16* orow = out + (out_row0 + tok) * args.out_ld;
-          if (MODE == GM_GATEUP) {
-            float v[8];
+            for (int o = 0; o < NOUT; ++o)
+              if (colbase + 256 * o < args.out_cols)
+                tc::tma_store_2d(&maps.out, buf + o * EX_STG_BOX, colbase + 256 * o,
+                                 out_row0 + j0);
+          }
+        } else {
+          __syncwarp();
+          const uint8_t* bp = stg_p + sbuf * (NOUT * EX_STG_BOX);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              v[i] = silu_mul(__uint_as_float(r0[8 * hf + i]), __uint_as_float(r1[8 * hf + i]));
-            transpose8(v, lane);
-            if (c0ok && tok_ok) store_bf16x8(orow + colg0, v);
-          } else {
-            // two independent outputs per element: plain 2-byte stores (32
-            // lanes write 64 contiguous bytes) cost less than two transposes
-            const int jb = j0 + 8 * hf;
-            __nv_bfloat16* o = out + (out_row0 + jb) * args.out_ld;
+          for (int o = 0; o < NOUT; ++o) {
+            const int col = colbase + 256 * o;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (jb + i < t.ntok) {
-                __nv_bfloat16* oi = o + static_cast<size_t>(i) * args.out_ld;
-                if (c0ok) oi[col0] = __float2bfloat16_rn(__uint_as_float(r0[8 * hf + i]));
-                if (c1ok) oi[col0 + 256] = __float2bfloat16_rn(__uint_as_float(r1[8 * hf + i]));
+            for (int u = lane; u < 64; u += 32) {
+              const int r = u >> 2, c = u & 3;
+              if (r < nv && col < args.out_cols) {
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    bp + o * EX_STG_BOX + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+                *reinterpret_cast<uint4*>(
+                    out + static_cast<size_t>(out_row0 + j0 + r) * args.out_ld + col + 8 * c) = v;
               }
             }
           }
         }
+        if (lane == 0) tc::bulk_commit();
+        sbuf ^= 1;
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(tempty_addr);
       tphase ^= 1u;
     }
+    if (lane == 0) tc::bulk_wait_all();
+    __syncwarp();
   }
 
   tc::tc_fence_before();
@@ -793,6 +837,19 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool make_store_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc || !base || rows == 0 || cols == 0) return false;
+  const cuuint64_t gdim[2] = {cols, rows};
+  const cuuint64_t gstride[1] = {cols * 2};
+  const cuuint32_t box[2] = {32, 16};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
                     uint64_t a1_rows, uint32_t a_box_rows, const void* b0, uint64_t b0_rows,
                     const void* b1, uint64_t b1_rows, uint64_t k, uint32_t tok_box0) {
@@ -820,10 +877,12 @@ moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args
   switch (mode) {
     case GM_GATEUP:
       return launch_persistent(expert_gemm_kernel<GM_GATEUP>, "gemm_gateup_swiglu", 2,
-                               EX_SMEM_BYTES, EX_THREADS, grid, maps, args, stream, attr_gu);
+                               ex_smem_bytes(GM_GATEUP), EX_THREADS, grid, maps, args, stream,
+                               attr_gu);
     case GM_DOWN:
-      return launch_persistent(expert_gemm_kernel<GM_DOWN>, "gemm_down", 2, EX_SMEM_BYTES,
-                               EX_THREADS, grid, maps, args, stream, attr_dn);
+      return launch_persistent(expert_gemm_kernel<GM_DOWN>, "gemm_down", 2,
+                               ex_smem_bytes(GM_DOWN), EX_THREADS, grid, maps, args, stream,
+                               attr_dn);
     case GM_ROUTER:
       return launch_persistent(router_gemm_kernel, "gemm_router", 1, RT_SMEM_BYTES, RT_THREADS,
                                grid, maps, args, stream, attr_rt);
