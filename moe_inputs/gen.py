@@ -13,6 +13,7 @@ Layout (row-major, K-contiguous, as the C ABI expects):
     w2         [E, d, I]         down projection
     ws13       [S, 2I, d]        shared experts, same layout
     ws2        [S, d, I]
+    norm_w     [d]     fp32      weight of the RMSNorm in front of the layer
 
 FP8 (e4m3) layers store every expert weight as e4m3 values plus one fp32 scale
 per 128 x 128 block ("block-wise" quantisation of the V3 walk-through,
@@ -162,4 +163,14 @@ def make_inputs(cfg: LayerCfg, device="cpu", seed=None) -> dict:
             out[k], out[k + "_scale"] = _normal_e4m3(shp, cfg.w_std, device, s * 1000 + 3 + j)
         else:
             out[k] = _normal(shp, cfg.w_std, wdt, device, s * 1000 + 3 + j, slab_rows=8)
+    out["norm_w"] = make_norm_weight(cfg, device, s)
     return out
+
+
+def make_norm_weight(cfg: LayerCfg, device="cpu", seed=None) -> torch.Tensor:
+    """Per-channel weight of the RMSNorm in front of the layer, fp32 [d]:
+    U(0.5, 1.5), a spread around the initial value 1 so that a dropped or
+    misplaced weight changes the result."""
+    s = cfg.seed if seed is None else seed
+    g = _gen(device, s * 1000 + 7)
+    return 0.5 + torch.rand((cfg.d,), generator=g, device=device, dtype=torch.float32)

@@ -34,6 +34,10 @@ Readings where the pages are silent (all also listed in the design doc):
   all their experts (the page's "affinity scores"); the bias then acts only
   inside the kept groups.
 - If the chosen scores sum to 0 the renormalised gates are 0.
+- The RMSNorm in front of the layer (V3 walk-through, section 4.1, eps 1e-6) is
+  the standard one with a per-channel weight, x * w / sqrt(mean(x^2) + eps);
+  its output is held in the activation type like every stored activation, and
+  the residual adds the un-normalised x.
 """
 from __future__ import annotations
 
@@ -56,6 +60,35 @@ def _f32(a) -> np.ndarray:
         import torch
         return a.detach().to("cpu", torch.float32).numpy()
     return np.asarray(a, dtype=np.float32)
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm in front of the layer (V3 walk-through, section 4.1: an RMSNorm before
+# and after the MoE layer, eps = 1e-6)
+# ----------------------------------------------------------------------------
+
+def rmsnorm(x, w, eps: float = 1e-6):
+    """Root-mean-square normalisation of each token row, then the per-channel
+    weight: inv_rms_t = 1 / sqrt(mean_j x_tj^2 + eps), xn_tj = x_tj * inv_rms_t
+    * w_j.  x [T, d], w [d] -> (xn [T, d] fp64, inv_rms [T] fp64)."""
+    xv = _f64(x)
+    inv_rms = 1.0 / np.sqrt(np.mean(xv * xv, axis=1) + eps)
+    return xv * inv_rms[:, None] * _f64(w)[None, :], inv_rms
+
+
+def round_bf16(v) -> np.ndarray:
+    """Round to the nearest bfloat16 value (8 significant bits), ties to even,
+    from the exact fp64 value (one rounding).  Normal-range values only."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)                     # v = m * 2**e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def round_act(v, act: str) -> np.ndarray:
+    """Rounding of a stored activation: 'bf16' or 'f32'."""
+    if act == "bf16":
+        return round_bf16(v)
+    return np.asarray(v, dtype=np.float32).astype(np.float64)
 
 
 # ----------------------------------------------------------------------------
@@ -214,20 +247,30 @@ def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
 
 def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
               add_residual: int = 1, tokens=None, n_groups: int = 0,
-              topk_groups: int = 0) -> dict:
+              topk_groups: int = 0, norm_w=None, norm_eps: float = 1e-6,
+              act: str = "bf16") -> dict:
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
     ``inp`` holds x, centroids, bias, w13, w2, ws13, ws2 (see moe_inputs), and
     for FP8 layers their 128 x 128 block scales (``*_scale``); activations are
     used as stored (bf16), unquantised.  Expert weights are read one expert at
-    a time, so large layers can be evaluated on a token sample.  Returns out (fp64), delta = out - residual,
-    idx, gates, margin."""
+    a time, so large layers can be evaluated on a token sample.
+
+    With ``norm_w`` the layer sits behind its RMSNorm: the router and the
+    experts read u = RMSNorm(x) held in the activation type ``act`` (rounded
+    once), and the residual adds x itself (h = x + MoE(RMSNorm(x))).
+
+    Returns out (fp64), delta = out - residual, idx, gates, margin."""
     x = inp["x"]
     if tokens is not None:
         tokens = np.asarray(tokens, dtype=np.int64)
         x = x[tokens] if not hasattr(x, "detach") else x[_torch_index(tokens, x)]
-    u = _f64(x)
+    resid = _f64(x)
+    if norm_w is not None:
+        u = round_act(rmsnorm(resid, norm_w, norm_eps)[0], act)
+    else:
+        u = resid
     n = u.shape[0]
     idx, gates, margin, _ = route(u, inp["centroids"], inp["bias"], K, score_func,
                                   normalize, n_groups, topk_groups)
@@ -243,7 +286,7 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
                                          _expert_weight(inp, "w2", int(e)))
     for k in range(K):
         delta += gates[:, k:k + 1] * routed[:, k]
-    out = delta + u if add_residual else delta.copy()
+    out = delta + resid if add_residual else delta.copy()
     return {"out": out, "delta": delta, "idx": idx, "gates": gates, "margin": margin}
 
 

@@ -447,3 +447,75 @@ def test_group_limit_keeps_experts_in_m_groups():
     for row in idx:
         assert len(set((row // gs).tolist())) <= 2
     np.testing.assert_allclose(gates.sum(axis=1), 1.0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- RMSNorm in front of the layer
+
+def test_golden_rmsnorm():
+    kv = dict(_read("rmsnorm_hand.txt"))
+    for c in ("a", "b"):
+        x = np.array([_rows(kv[c + "_x"])[0]])
+        w = np.array(_rows(kv[c + "_w"])[0])
+        xn, inv = O.rmsnorm(x, w, _num(kv[c + "_eps"]))
+        np.testing.assert_allclose(inv, [_num(kv[c + "_inv_rms"])], rtol=1e-15, atol=0)
+        np.testing.assert_allclose(xn[0], _rows(kv[c + "_xn"])[0], rtol=1e-15, atol=0)
+
+
+def test_rmsnorm_closed_forms():
+    rng = np.random.default_rng(5)
+    d = 96
+    w = rng.uniform(0.5, 1.5, d)
+    # constant row c: inv_rms = 1 / sqrt(c^2 + eps), xn = c * w * inv_rms
+    for cval, eps in ((0.5, 1e-6), (-3.0, 1e-6), (1e-3, 1e-6), (2.0, 0.0)):
+        xn, inv = O.rmsnorm(np.full((1, d), cval), w, eps)
+        np.testing.assert_allclose(inv[0], 1.0 / math.sqrt(cval * cval + eps), rtol=1e-14)
+        np.testing.assert_allclose(xn[0], cval * w / math.sqrt(cval * cval + eps), rtol=1e-14)
+    # eps = 0: invariant under positive scaling of the row, sign flips with the row
+    x = rng.standard_normal((4, d))
+    xn0, _ = O.rmsnorm(x, w, 0.0)
+    for a in (1e-3, 0.25, 7.0):
+        np.testing.assert_allclose(O.rmsnorm(a * x, w, 0.0)[0], xn0, rtol=1e-13, atol=0)
+    np.testing.assert_allclose(O.rmsnorm(-x, w, 0.0)[0], -xn0, rtol=0, atol=0)
+    # the normalised row (before w) has mean square ms / (ms + eps)
+    eps = 0.05
+    xn, inv = O.rmsnorm(x, w, eps)
+    ms = np.mean(x * x, axis=1)
+    np.testing.assert_allclose(np.mean((xn / w) ** 2, axis=1), ms / (ms + eps), rtol=1e-13)
+
+
+def test_round_bf16_ties_and_library():
+    # spacing of bfloat16 near 1 is 2^-7: halfway cases go to the even neighbour
+    v = np.array([1.0, 1 + 2.0**-8, 1 + 3 * 2.0**-8, -(1 + 3 * 2.0**-8), 1 + 2.0**-8 + 2.0**-20,
+                  0.75 + 2.0**-10])
+    want = np.array([1.0, 1.0, 1 + 2.0**-6, -(1 + 2.0**-6), 1 + 2.0**-7, 0.75])
+    np.testing.assert_array_equal(O.round_bf16(v), want)
+    # float32-representable values: one rounding, equal to torch's conversion
+    r = np.random.default_rng(6).standard_normal(200000).astype(np.float32)
+    t = torch.from_numpy(r).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_bf16(r.astype(np.float64)), t)
+
+
+def test_prenorm_layer_is_layer_of_normalised_tokens():
+    """h = x + MoE(RMSNorm(x)).  With w = 1, eps = 0 and rows of +-4 entries,
+    RMSNorm(x) = x / 4 exactly, so the pre-normed layer must equal the plain
+    layer on x / 4 for the routing and the MoE term, while the residual adds
+    x itself (not x / 4)."""
+    cfg = small_cases()["tiny"]
+    inp = make_inputs(cfg)
+    rng = np.random.default_rng(7)
+    sgn = rng.choice([-4.0, 4.0], size=tuple(inp["x"].shape))
+    x = torch.from_numpy(sgn).to(inp["x"].dtype)
+    plain = dict(inp, x=x / 4)
+    normed = dict(inp, x=x)
+    ones = np.ones(cfg.d)
+    r0 = O.moe_layer(plain, cfg.K, cfg.normalize, cfg.score_func, add_residual=1)
+    r1 = O.moe_layer(normed, cfg.K, cfg.normalize, cfg.score_func, add_residual=1,
+                     norm_w=ones, norm_eps=0.0, act="f32")
+    np.testing.assert_array_equal(r1["idx"], r0["idx"])
+    np.testing.assert_array_equal(r1["gates"], r0["gates"])
+    np.testing.assert_array_equal(r1["delta"], r0["delta"])
+    np.testing.assert_array_equal(r1["out"], r1["delta"] + sgn)
+    # a non-trivial weight changes the routed input: the MoE term must move
+    r2 = O.moe_layer(normed, cfg.K, cfg.normalize, cfg.score_func, add_residual=1,
+                     norm_w=np.linspace(0.5, 1.5, cfg.d), norm_eps=0.0, act="f32")
+    assert not np.allclose(r2["delta"], r0["delta"])
