@@ -141,7 +141,7 @@ def kernel_roofline(cfg, traces, peaks):
     """Per-kernel algorithmic work / measured average launch time."""
     T, d, E, K, S, I = cfg.T, cfg.d, cfg.E, cfg.K, cfg.S, cfg.I
     R = T * K + S * T
-    es = 2
+    es = 4 if cfg.act == "f32" else 2
     work = {
         # flops
         "gemm_gateup_swiglu": ("TFLOP/s", 2.0 * R * d * 2 * I),
@@ -156,6 +156,8 @@ def kernel_roofline(cfg, traces, peaks):
         "dispatch_scatter_fp8": ("GB/s", es * T * d + (T * K + (T if S else 0)) *
                                  (d + 4.0 * d / 128) + 4.0 * T * K),
         "combine": ("GB/s", es * (R * d + 2 * T * d) + 8.0 * T * K),
+        # x read once, xn written once, the weight row
+        "rmsnorm": ("GB/s", es * 2.0 * T * d + 4.0 * d),
     }
     out = {}
     for name, launches, ms in traces:
@@ -195,14 +197,16 @@ def dram_traffic(workload: str, kernel: str):
     return rec["bytes_per_launch"]
 
 
-def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7):
+def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7, prenorm: bool = False):
     """Times the CPU oracle on n_tokens tokens of the workload (weights of the
     experts those tokens use are copied to host first, untimed)."""
     from oracle import moe_oracle as O
     rng = np.random.default_rng(seed)
     tok = np.sort(rng.choice(cfg.T, n_tokens, replace=False))
     x_host = inp["x"][torch.as_tensor(tok, device=inp["x"].device)].cpu()
-    idx, _, _, _ = O.route(x_host, inp["centroids"].cpu(), inp["bias"].cpu(), cfg.K,
+    norm_w = inp["norm_w"].cpu() if prenorm else None
+    u = (O.round_act(O.rmsnorm(x_host, norm_w, NORM_EPS)[0], cfg.act) if prenorm else x_host)
+    idx, _, _, _ = O.route(u, inp["centroids"].cpu(), inp["bias"].cpu(), cfg.K,
                            cfg.score_func, cfg.normalize, cfg.n_groups, cfg.topk_groups)
     used = sorted(set(int(e) for e in idx.reshape(-1)))
 
@@ -223,7 +227,8 @@ def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7):
             host["s" + k + "_scale"] = inp["s" + k + "_scale"].cpu()
     t0 = time.perf_counter()
     O.moe_layer(host, cfg.K, cfg.normalize, cfg.score_func, cfg.add_residual,
-                n_groups=cfg.n_groups, topk_groups=cfg.topk_groups)
+                n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, norm_w=norm_w,
+                norm_eps=NORM_EPS, act=cfg.act)
     dt = time.perf_counter() - t0
     try:
         from threadpoolctl import threadpool_info
@@ -242,7 +247,8 @@ def run_reference(args, cfg, dist, rank, ws, device):
     rates = []
     cores = None
     for i in range(args.warmup + args.steps):
-        r, dt, cores = cpu_oracle_tokens_per_s(cfg, inp, per_step, seed=100 + i)
+        r, dt, cores = cpu_oracle_tokens_per_s(cfg, inp, per_step, seed=100 + i,
+                                               prenorm=args.prenorm)
         if i >= args.warmup:
             rates.append((per_step, dt))
     tok = sum(t for t, _ in rates)
@@ -252,8 +258,8 @@ def run_reference(args, cfg, dist, rank, ws, device):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(secs / len(rates) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
-                       "S": cfg.S, "I": cfg.I, "sample_tokens_per_step": per_step},
+            "config": {"workload": _workload(cfg, args), "T": cfg.T, "d": cfg.d, "E": cfg.E,
+                       "K": cfg.K, "S": cfg.S, "I": cfg.I, "sample_tokens_per_step": per_step},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                              "kind": "oracle",
                              "sample": f"{per_step} random tokens of the {cfg.name} batch per "
@@ -261,6 +267,14 @@ def run_reference(args, cfg, dist, rank, ws, device):
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# eps of the RMSNorm in front of the layer (V3 walk-through, section 4.1)
+NORM_EPS = 1e-6
+
+
+def _workload(cfg, args) -> str:
+    return cfg.name + ("+rmsnorm" if args.prenorm else "")
 
 
 def main():
@@ -277,6 +291,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--balance-steps", type=int, default=20,
                     help="skewed layers: bias-update steps of the balancing run")
+    ap.add_argument("--prenorm", action="store_true",
+                    help="the layer behind its RMSNorm: h = x + MoE(RMSNorm(x))")
     ap.add_argument("--override", default="",
                     help="comma-separated shape overrides, e.g. T=1024,E=32 (profiling cases)")
     args = ap.parse_args()
@@ -301,7 +317,8 @@ def main():
     peaks = _peaks()
     inp = make_inputs(cfg, device, seed=rank)
     mc = m.cfg_from_layer(cfg)
-    layer = m.MoeLayer(mc, inp, device=device)
+    layer = m.MoeLayer(mc, inp, device=device,
+                       norm_w=inp["norm_w"] if args.prenorm else None, norm_eps=NORM_EPS)
     x = inp["x"]
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -374,8 +391,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 (fp32 promotion), bf16 tokens" if fp8 else "bf16",
         "data": "synthetic (seeded random tokens and random-init weights of the layer's shape)",
-        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
-                   "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
+        "config": {"workload": _workload(cfg, args), "T": cfg.T, "d": cfg.d, "E": cfg.E,
+                   "K": cfg.K, "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
                    "parallelism": (f"data parallel x{ws}, load counts all-reduced for the "
                                    f"bias update" if ws > 1 else "one replica"),
                    "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
@@ -417,7 +434,8 @@ def main():
         line["balance"] = {"steps": args.balance_steps, "gamma": cfg.gamma,
                            "max_over_mean_load": loads}
     if not args.no_cpu_baseline:
-        rate, secs, cores = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens)
+        rate, secs, cores = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens,
+                                                    prenorm=args.prenorm)
         line["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"{args.cpu_tokens} random tokens of the {cfg.name} "

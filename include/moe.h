@@ -14,6 +14,8 @@
  *   V3 section 3.1                   output = u + shared + gate-weighted routed
  *   course section 4                 2024 variant: gates not renormalised
  *   course sections 5, 6             bias applies to the next batch; no drops
+ *   V3 section 4.1                   RMSNorm in front of the layer, eps 1e-6
+ *   V3 section 4.3                   FP8: 128x128 weight blocks, 1x128 tiles
  *
  * Conventions for every entry point
  *   - All tensors are row-major, densely packed, in device memory, unless a
@@ -91,7 +93,8 @@ typedef enum {
   MOE_WS_ROUTE = 0,
   MOE_WS_DISPATCH = 1,
   MOE_WS_EXPERTS = 2,
-  MOE_WS_FORWARD = 3
+  MOE_WS_FORWARD = 3,
+  MOE_WS_FORWARD_PRENORM = 4   /* moe_forward_prenorm / moe_forward_fp8_prenorm */
 } moe_ws_kind_t;
 
 /* Bytes of scratch that `which` needs for this cfg (0 on an invalid cfg). */
@@ -221,6 +224,31 @@ moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centro
                          void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_rmsnorm - the RMSNorm in front of the MoE layer (V3 section 4.1: an
+ * RMSNorm before and after the MoE layer, eps = 1e-6), per token row:
+ *   inv_rms[t] = 1 / sqrt(sum_j x[t,j]^2 / d + eps)
+ *   xn[t,j]    = x[t,j] * inv_rms[t] * norm_w[j]
+ * in fp32, rounded once (nearest even) to act_dtype.
+ *   x [T,d] act_dtype, norm_w [d] fp32 (16-byte aligned), eps > 0;
+ *   xn [T,d] act_dtype out (may be x itself), inv_rms [T] fp32 out or NULL.
+ */
+moe_status_t moe_rmsnorm(const moe_cfg_t* cfg, const void* x, const float* norm_w, float eps,
+                         void* xn, float* inv_rms, void* stream);
+
+/*
+ * moe_forward_prenorm - the layer behind its RMSNorm, h = x + MoE(RMSNorm(x)):
+ * moe_rmsnorm(x) into the workspace, then moe_forward on the normalised
+ * tokens (router, dispatch, shared experts), with the residual (add_residual)
+ * taken from x itself.  ws: MOE_WS_FORWARD_PRENORM bytes.  Other arguments as
+ * moe_forward and moe_rmsnorm.
+ */
+moe_status_t moe_forward_prenorm(const moe_cfg_t* cfg, const void* x, const float* norm_w,
+                                 float eps, const void* centroids, const float* bias,
+                                 const void* w13, const void* w2, const void* ws13,
+                                 const void* ws2, int32_t* idx, float* gates, int32_t* counts,
+                                 void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * FP8 layers (V3 section 4.3): expert weights in e4m3 with one fp32 scale per
  * 128 x 128 block (w = q * scale), activations quantised inside the layer to
  * e4m3 in 1 x 128 tiles along K (scale = max|x| / 448), and tensor-core
@@ -288,6 +316,15 @@ moe_status_t moe_forward_fp8(const moe_cfg_t* cfg, const void* x, const void* ce
                              const float* bias, const moe_fp8_weights_t* w, int32_t* idx,
                              float* gates, int32_t* counts, void* out, void* ws,
                              size_t ws_bytes, void* stream);
+
+/* moe_forward_fp8 behind the RMSNorm, as moe_forward_prenorm: the router reads
+ * the normalised bf16 tokens, the dispatch quantises them to e4m3 1 x 128
+ * tiles in its single read, the residual is x.  ws: MOE_WS_FORWARD_PRENORM. */
+moe_status_t moe_forward_fp8_prenorm(const moe_cfg_t* cfg, const void* x, const float* norm_w,
+                                     float eps, const void* centroids, const float* bias,
+                                     const moe_fp8_weights_t* w, int32_t* idx, float* gates,
+                                     int32_t* counts, void* out, void* ws, size_t ws_bytes,
+                                     void* stream);
 
 /* Waits for `stream`, then returns and clears this device's error word
  * (MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS) or MOE_ERR_CUDA. */

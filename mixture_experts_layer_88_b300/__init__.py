@@ -7,14 +7,15 @@ from . import _lib
 from ._lib import (MoeCfg, MoeError, make_cfg, cfg_from_layer, workspace_size, check_cfg,
                    alloc_workspace, route, dispatch, experts, combine, update_bias, forward,
                    Fp8Weights, fp8_weights, fp8_rows, dispatch_fp8, experts_fp8, forward_fp8,
-                   MOE_E4M3,
+                   rmsnorm, forward_prenorm, forward_fp8_prenorm, MOE_E4M3,
                    get_status, trace_enable, trace_read_all, version, MOE_F32, MOE_BF16,
                    MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX, MOE_WS_ROUTE, MOE_WS_DISPATCH,
-                   MOE_WS_EXPERTS, MOE_WS_FORWARD)
+                   MOE_WS_EXPERTS, MOE_WS_FORWARD, MOE_WS_FORWARD_PRENORM)
 from .layer import MoeLayer, HostPipeline
 
 __all__ = ["MoeCfg", "MoeError", "MoeLayer", "HostPipeline", "make_cfg", "cfg_from_layer", "workspace_size",
            "check_cfg", "alloc_workspace", "route", "dispatch", "experts", "combine",
            "update_bias", "forward", "Fp8Weights", "fp8_weights", "fp8_rows", "dispatch_fp8",
-           "experts_fp8", "forward_fp8", "get_status", "trace_enable", "trace_read_all",
+           "experts_fp8", "forward_fp8", "rmsnorm", "forward_prenorm", "forward_fp8_prenorm",
+           "get_status", "trace_enable", "trace_read_all",
            "version"]

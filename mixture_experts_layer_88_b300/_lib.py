@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_EXPERTS, MOE_WS_FORWARD = 0, 1, 2, 3
+MOE_WS_FORWARD_PRENORM = 4
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
@@ -26,7 +27,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 SYMBOLS = ["moe_workspace_size", "moe_check_cfg", "moe_route", "moe_dispatch", "moe_experts",
            "moe_experts_static",
            "moe_combine", "moe_update_bias", "moe_forward", "moe_fp8_rows", "moe_dispatch_fp8",
-           "moe_experts_fp8", "moe_forward_fp8", "moe_get_status",
+           "moe_experts_fp8", "moe_forward_fp8", "moe_rmsnorm", "moe_forward_prenorm",
+           "moe_forward_fp8_prenorm", "moe_get_status",
            "moe_status_string", "moe_trace_enable", "moe_trace_read", "moe_version"]
 
 
@@ -63,7 +65,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         raise ImportError(f"libmoe.so not built at {path}; run "
                           "`python -m mixture_experts_layer_88_b300.build`")
     lib = ctypes.CDLL(path)
-    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    P, I32, SZ, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
     cfgp = ctypes.POINTER(MoeCfg)
     sig = {
         "moe_workspace_size": (SZ, [cfgp, I32]),
@@ -82,6 +84,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                   P]),
         "moe_forward_fp8": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, P, P, SZ,
                                   P]),
+        "moe_rmsnorm": (I32, [cfgp, P, P, F32, P, P, P]),
+        "moe_forward_prenorm": (I32, [cfgp, P, P, F32, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_forward_fp8_prenorm": (I32, [cfgp, P, P, F32, P, P, ctypes.POINTER(Fp8Weights), P,
+                                          P, P, P, P, SZ, P]),
         "moe_get_status": (I32, [P]),
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_trace_enable": (I32, [I32]),
@@ -231,6 +237,27 @@ def forward_fp8(cfg, x, centroids, bias, weights: Fp8Weights, idx, gates, counts
     _check(lib().moe_forward_fp8(ctypes.byref(cfg), _p(x), _p(centroids), _p(bias),
                                  ctypes.byref(weights), _p(idx), _p(gates), _p(counts), _p(out),
                                  _p(ws), ws.numel(), _stream(stream)), "moe_forward_fp8")
+
+
+def rmsnorm(cfg, x, norm_w, eps, xn, inv_rms=None, stream=None):
+    _check(lib().moe_rmsnorm(ctypes.byref(cfg), _p(x), _p(norm_w), float(eps), _p(xn),
+                             _p(inv_rms), _stream(stream)), "moe_rmsnorm")
+
+
+def forward_prenorm(cfg, x, norm_w, eps, centroids, bias, w13, w2, ws13, ws2, idx, gates, counts,
+                    out, ws, stream=None):
+    _check(lib().moe_forward_prenorm(ctypes.byref(cfg), _p(x), _p(norm_w), float(eps),
+                                     _p(centroids), _p(bias), _p(w13), _p(w2), _p(ws13),
+                                     _p(ws2), _p(idx), _p(gates), _p(counts), _p(out), _p(ws),
+                                     ws.numel(), _stream(stream)), "moe_forward_prenorm")
+
+
+def forward_fp8_prenorm(cfg, x, norm_w, eps, centroids, bias, weights: Fp8Weights, idx, gates,
+                        counts, out, ws, stream=None):
+    _check(lib().moe_forward_fp8_prenorm(ctypes.byref(cfg), _p(x), _p(norm_w), float(eps),
+                                         _p(centroids), _p(bias), ctypes.byref(weights), _p(idx),
+                                         _p(gates), _p(counts), _p(out), _p(ws), ws.numel(),
+                                         _stream(stream)), "moe_forward_fp8_prenorm")
 
 
 def get_status(stream=None) -> int:

@@ -184,6 +184,12 @@ ForwardLayout forward_layout(const moe_cfg_t& c) {
   return L;
 }
 
+// Pre-normed forward: the forward's workspace, then the normalised tokens.
+size_t prenorm_ws(const moe_cfg_t& c) {
+  return forward_layout(c).total +
+         align_up(static_cast<size_t>(c.T) * c.d * esize(c.act_dtype), 256);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status_t check_ptrs(const moe_cfg_t& c, std::initializer_list<const void*> dtype_ptrs,
@@ -459,6 +465,7 @@ size_t moe_workspace_size(const moe_cfg_t* cfg, int32_t which) {
     case MOE_WS_DISPATCH: return dispatch_ws(c);
     case MOE_WS_EXPERTS: return experts_ws(c);
     case MOE_WS_FORWARD: return forward_layout(c).total;
+    case MOE_WS_FORWARD_PRENORM: return prenorm_ws(c);
     default: return 0;
   }
 }
@@ -585,6 +592,76 @@ moe_status_t moe_update_bias(const moe_cfg_t* cfg, const int32_t* counts, float*
                             static_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace {
+
+// The layer on tokens xin (router and experts) with residual xres.  Arguments
+// checked by the caller; T > 0.
+moe_status_t do_forward(const moe_cfg_t& c, const void* xin, const void* xres,
+                        const void* centroids, const float* bias, const void* w13,
+                        const void* w2, const void* ws13, const void* ws2, int32_t* idx,
+                        float* gates, int32_t* counts, void* out, void* ws, cudaStream_t st) {
+  const ForwardLayout L = forward_layout(c);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  void* xp = at<void>(ws, L.xp);
+  void* act = at<void>(ws, L.act);
+  void* y = at<void>(ws, L.y);
+  moe_status_t s;
+  if ((s = do_route(c, xin, centroids, bias, idx, gates, at<void>(ws, L.route), st)) != MOE_OK)
+    return s;
+  if ((s = launch_dispatch(xin, static_cast<size_t>(c.d) * esize(c.act_dtype), idx, c.T, c.K,
+                           c.E, counts, offsets, xp, perm, pos, at<int32_t>(ws, L.dispatch),
+                           st)) != MOE_OK)
+    return s;
+  if ((s = do_experts(c, xp, xin, offsets, w13, w2, ws13, ws2, act, y, at<void>(ws, L.experts),
+                      st)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, y, gates, pos, xres, out, c.T, c.K, c.S, c.d,
+                        static_cast<long long>(c.T) * c.K, c.T, c.add_residual, st);
+}
+
+moe_status_t do_forward_fp8(const moe_cfg_t& c, const void* xin, const void* xres,
+                            const void* centroids, const float* bias,
+                            const moe_fp8_weights_t* w, int32_t* idx, float* gates,
+                            int32_t* counts, void* out, void* ws, cudaStream_t st) {
+  const ForwardLayout L = forward_layout(c);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  const Fp8Rows fr = fp8_rows(c);
+  moe_status_t s;
+  if ((s = do_route(c, xin, centroids, bias, idx, gates, at<void>(ws, L.route), st)) != MOE_OK)
+    return s;
+  if ((s = launch_dispatch_index(idx, c.T, c.K, c.E, 4, counts, offsets, perm, pos,
+                                 at<int32_t>(ws, L.dispatch), st)) != MOE_OK)
+    return s;
+  if ((s = launch_scatter_quant(xin, c.T, c.K, c.d, pos, c.S > 0 ? static_cast<int>(fr.P) : -1,
+                                at<void>(ws, L.xp), at<float>(ws, L.xs), fr.rows_in, st)) !=
+      MOE_OK)
+    return s;
+  if ((s = do_experts_fp8(c, at<void>(ws, L.xp), at<float>(ws, L.xs), offsets, counts, *w,
+                          at<void>(ws, L.act), at<float>(ws, L.act_s), at<void>(ws, L.y),
+                          at<void>(ws, L.experts), st)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, at<void>(ws, L.y), gates, pos, xres, out, c.T, c.K, c.S,
+                        c.d, fr.P, fr.Tp, c.add_residual, st);
+}
+
+moe_status_t forward_empty(const moe_cfg_t& c, int32_t* counts, cudaStream_t st) {
+  TraceScope tr(st, "forward_empty");
+  cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
+  return launch_status();
+}
+
+bool valid_eps(float eps) { return eps > 0.f && eps < 1e30f; }
+
+}  // namespace
+
+extern "C" {
+
 moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centroids,
                          const float* bias, const void* w13, const void* w2, const void* ws13,
                          const void* ws2, int32_t* idx, float* gates, int32_t* counts, void* out,
@@ -595,33 +672,68 @@ moe_status_t moe_forward(const moe_cfg_t* cfg, const void* x, const void* centro
   if (is_fp8(c)) return MOE_ERR_UNSUPPORTED;   // FP8 layers: the *_fp8 entry points
   if (!counts) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c.T == 0) {
-    TraceScope tr(st, "forward_empty");
-    cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
-    return launch_status();
-  }
+  if (c.T == 0) return forward_empty(c, counts, st);
   if ((s = check_ptrs(c, {x, centroids, w13, w2, out}, {bias, idx, gates})) != MOE_OK) return s;
   if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
-  const ForwardLayout L = forward_layout(c);
-  if ((s = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return s;
-  int32_t* offsets = at<int32_t>(ws, L.offsets);
-  int32_t* perm = at<int32_t>(ws, L.perm);
-  int32_t* pos = at<int32_t>(ws, L.pos);
-  void* xp = at<void>(ws, L.xp);
-  void* act = at<void>(ws, L.act);
-  void* y = at<void>(ws, L.y);
-  if ((s = do_route(c, x, centroids, bias, idx, gates, at<void>(ws, L.route), st)) != MOE_OK)
+  if ((s = check_ws(ws, ws_bytes, forward_layout(c).total)) != MOE_OK) return s;
+  return do_forward(c, x, x, centroids, bias, w13, w2, ws13, ws2, idx, gates, counts, out, ws,
+                    st);
+}
+
+moe_status_t moe_rmsnorm(const moe_cfg_t* cfg, const void* x, const float* norm_w, float eps,
+                         void* xn, float* inv_rms, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!valid_eps(eps)) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if ((s = check_ptrs(c, {x, xn, norm_w}, {})) != MOE_OK) return s;
+  return launch_rmsnorm(c.act_dtype, x, norm_w, eps, c.T, c.d, xn, inv_rms,
+                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_forward_prenorm(const moe_cfg_t* cfg, const void* x, const float* norm_w,
+                                 float eps, const void* centroids, const float* bias,
+                                 const void* w13, const void* w2, const void* ws13,
+                                 const void* ws2, int32_t* idx, float* gates, int32_t* counts,
+                                 void* out, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (is_fp8(c)) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !valid_eps(eps)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) return forward_empty(c, counts, st);
+  if ((s = check_ptrs(c, {x, norm_w, centroids, w13, w2, out}, {bias, idx, gates})) != MOE_OK)
     return s;
-  if ((s = launch_dispatch(x, static_cast<size_t>(c.d) * esize(c.act_dtype), idx, c.T, c.K, c.E,
-                           counts, offsets, xp, perm, pos, at<int32_t>(ws, L.dispatch), st)) !=
-      MOE_OK)
+  if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, prenorm_ws(c))) != MOE_OK) return s;
+  void* xn = at<void>(ws, forward_layout(c).total);
+  if ((s = launch_rmsnorm(c.act_dtype, x, norm_w, eps, c.T, c.d, xn, nullptr, st)) != MOE_OK)
     return s;
-  if ((s = do_experts(c, xp, x, offsets, w13, w2, ws13, ws2, act, y, at<void>(ws, L.experts),
-                      st)) != MOE_OK)
+  return do_forward(c, xn, x, centroids, bias, w13, w2, ws13, ws2, idx, gates, counts, out, ws,
+                    st);
+}
+
+moe_status_t moe_forward_fp8_prenorm(const moe_cfg_t* cfg, const void* x, const float* norm_w,
+                                     float eps, const void* centroids, const float* bias,
+                                     const moe_fp8_weights_t* w, int32_t* idx, float* gates,
+                                     int32_t* counts, void* out, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!is_fp8(c)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !valid_eps(eps)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) return forward_empty(c, counts, st);
+  if ((s = check_ptrs(c, {x, norm_w, centroids, out}, {bias, idx, gates})) != MOE_OK) return s;
+  if ((s = check_fp8_weights(c, w)) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, prenorm_ws(c))) != MOE_OK) return s;
+  void* xn = at<void>(ws, forward_layout(c).total);
+  if ((s = launch_rmsnorm(c.act_dtype, x, norm_w, eps, c.T, c.d, xn, nullptr, st)) != MOE_OK)
     return s;
-  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d,
-                        static_cast<long long>(c.T) * c.K, c.T, c.add_residual,
-                        st);
+  return do_forward_fp8(c, xn, x, centroids, bias, w, idx, gates, counts, out, ws, st);
 }
 
 moe_status_t moe_fp8_rows(const moe_cfg_t* cfg, int64_t* rows_in, int64_t* rows_out,
@@ -685,34 +797,11 @@ moe_status_t moe_forward_fp8(const moe_cfg_t* cfg, const void* x, const void* ce
   if (!is_fp8(c)) return MOE_ERR_INVALID_ARG;
   if (!counts) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c.T == 0) {
-    TraceScope tr(st, "forward_empty");
-    cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
-    return launch_status();
-  }
+  if (c.T == 0) return forward_empty(c, counts, st);
   if ((s = check_ptrs(c, {x, centroids, out}, {bias, idx, gates})) != MOE_OK) return s;
   if ((s = check_fp8_weights(c, w)) != MOE_OK) return s;
-  const ForwardLayout L = forward_layout(c);
-  if ((s = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return s;
-  int32_t* offsets = at<int32_t>(ws, L.offsets);
-  int32_t* perm = at<int32_t>(ws, L.perm);
-  int32_t* pos = at<int32_t>(ws, L.pos);
-  const Fp8Rows fr = fp8_rows(c);
-  if ((s = do_route(c, x, centroids, bias, idx, gates, at<void>(ws, L.route), st)) != MOE_OK)
-    return s;
-  if ((s = launch_dispatch_index(idx, c.T, c.K, c.E, 4, counts, offsets, perm, pos,
-                                 at<int32_t>(ws, L.dispatch), st)) != MOE_OK)
-    return s;
-  if ((s = launch_scatter_quant(x, c.T, c.K, c.d, pos, c.S > 0 ? static_cast<int>(fr.P) : -1,
-                                at<void>(ws, L.xp), at<float>(ws, L.xs), fr.rows_in, st)) !=
-      MOE_OK)
-    return s;
-  if ((s = do_experts_fp8(c, at<void>(ws, L.xp), at<float>(ws, L.xs), offsets, counts, *w,
-                          at<void>(ws, L.act), at<float>(ws, L.act_s), at<void>(ws, L.y),
-                          at<void>(ws, L.experts), st)) != MOE_OK)
-    return s;
-  return launch_combine(c.act_dtype, at<void>(ws, L.y), gates, pos, x, out, c.T, c.K, c.S, c.d,
-                        fr.P, fr.Tp, c.add_residual, st);
+  if ((s = check_ws(ws, ws_bytes, forward_layout(c).total)) != MOE_OK) return s;
+  return do_forward_fp8(c, x, x, centroids, bias, w, idx, gates, counts, out, ws, st);
 }
 
 moe_status_t moe_get_status(void* stream) {

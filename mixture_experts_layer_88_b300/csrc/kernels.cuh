@@ -1,5 +1,5 @@
 // Launchers of the SIMT kernels (router top-K, dispatch, combine, bias update,
-// fp32 expert GEMMs).  Internal.
+// RMSNorm, fp32 expert GEMMs).  Internal.
 #pragma once
 
 #include "common.cuh"
@@ -38,6 +38,10 @@ moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, co
                             const void* x, void* out, int T, int K, int S, int d,
                             long long shared0, long long shared_stride, int add_residual,
                             cudaStream_t stream);
+
+// xn = x * w / sqrt(mean(x^2) + eps) per token row; inv_rms [T] optional
+moe_status_t launch_rmsnorm(int act_dtype, const void* x, const float* w, float eps, int T, int d,
+                            void* xn, float* inv_rms, cudaStream_t stream);
 
 moe_status_t launch_update_bias(const int32_t* counts, float* bias, float* stats, int E, int T,
                                 int K, float gamma, cudaStream_t stream);

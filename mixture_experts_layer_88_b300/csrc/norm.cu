@@ -1,0 +1,102 @@
+// RMSNorm in front of the MoE layer ("DeepSeekMoE架构解析", section 4.1: an
+// RMSNorm sits before and after the MoE layer, eps = 1e-6):
+//   inv_rms_t = 1 / sqrt(mean_j x_tj^2 + eps),   xn_tj = x_tj * inv_rms_t * w_j
+// in fp32, rounded once to the activation type.
+//
+// HBM-bound: one 128-thread CTA per token row.  The first pass sums the
+// squares (16-byte loads of bf16), the CTA reduces them in a fixed order, and
+// the second pass re-reads the same row (from L1/L2, so DRAM sees it once),
+// scales it and writes it with 16-byte stores.  xn may alias x: every thread
+// reads an element before it writes it, and all reads of the first pass end
+// at the CTA barrier of the reduction.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kNormThreads = 128;
+
+// Sum over the CTA; every thread returns the same value (fixed order).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) s += red[i];
+  return s;
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_bf16_kernel(const uint4* x, const float4* __restrict__ w, float eps, int d,
+                        uint4* xn, float* __restrict__ inv_rms) {
+  __shared__ float red[kNormThreads / 32];
+  const int nv = d >> 3;                       // 8 bf16 per 16-byte vector
+  const size_t row = blockIdx.x;
+  const uint4* xr = x + row * nv;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < nv; i += kNormThreads) {
+    const uint4 v = xr[i];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      ss = fmaf(f.x, f.x, ss);
+      ss = fmaf(f.y, f.y, ss);
+    }
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  if (threadIdx.x == 0 && inv_rms) inv_rms[row] = inv;
+  uint4* orow = xn + row * nv;
+  for (int i = threadIdx.x; i < nv; i += kNormThreads) {
+    const uint4 v = xr[i];
+    const float4 w0 = __ldg(w + 2 * i), w1 = __ldg(w + 2 * i + 1);
+    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+    uint4 o;
+    __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      oh[k] = __floats2bfloat162_rn((f.x * inv) * wv[2 * k], (f.y * inv) * wv[2 * k + 1]);
+    }
+    orow[i] = o;
+  }
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_f32_kernel(const float* x, const float* __restrict__ w, float eps, int d, float* xn,
+                       float* __restrict__ inv_rms) {
+  __shared__ float red[kNormThreads / 32];
+  const size_t row = blockIdx.x;
+  const float* xr = x + row * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += kNormThreads) ss = fmaf(xr[i], xr[i], ss);
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  if (threadIdx.x == 0 && inv_rms) inv_rms[row] = inv;
+  float* orow = xn + row * d;
+  for (int i = threadIdx.x; i < d; i += kNormThreads) orow[i] = (xr[i] * inv) * __ldg(w + i);
+}
+
+}  // namespace
+
+moe_status_t launch_rmsnorm(int act_dtype, const void* x, const float* w, float eps, int T, int d,
+                            void* xn, float* inv_rms, cudaStream_t stream) {
+  if (T <= 0) return MOE_OK;
+  TraceScope tr(stream, "rmsnorm");
+  if (act_dtype == MOE_BF16) {
+    rmsnorm_bf16_kernel<<<T, kNormThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), reinterpret_cast<const float4*>(w), eps, d,
+        static_cast<uint4*>(xn), inv_rms);
+  } else {
+    rmsnorm_f32_kernel<<<T, kNormThreads, 0, stream>>>(static_cast<const float*>(x), w, eps, d,
+                                                       static_cast<float*>(xn), inv_rms);
+  }
+  return launch_status();
+}
+
+}  // namespace moe

@@ -291,12 +291,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 // 16 TMEM lanes (from taddr's lane) x 16 columns: thread t receives, for each
 // 8-column half c (registers 4c..4c+3), lane t/4 at columns 2(t%4), 2(t%4)+1
-// and lane t/4 + 8 at the same two columns.  Valid after tmem_wait_ld4().
+// and lane t/4 + 8 at the same two columns.  Valid after tmem_wait_ld2/4().
 __device__ __forceinline__ void tmem_ld16x256_x2(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[8], uint32_t (&b)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                 "+r"(a[6]), "+r"(a[7]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]),
+                 "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7])
+               :
                : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld4(uint32_t (&a)[8], uint32_t (&b)[8], uint32_t (&c)[8],

@@ -1,5 +1,5 @@
 """MoeLayer: owns one layer's weights, bias and workspace on one GPU and calls
-moe_forward / moe_update_bias through the C ABI."""
+moe_forward (or its FP8 / pre-normed forms) and moe_update_bias through the C ABI."""
 from __future__ import annotations
 
 import torch
@@ -14,22 +14,29 @@ class MoeLayer:
     ws13 [S,2I,d], ws2 [S,d,I] (device tensors, layouts of include/moe.h).  FP8
     layers (cfg.wgt_dtype == MOE_E4M3) also carry w13_scale, w2_scale,
     ws13_scale, ws2_scale and run through moe_forward_fp8.
+
+    norm_w ([d] fp32) puts the layer behind its RMSNorm: h = x + MoE(RMSNorm(x))
+    through moe_forward_prenorm / moe_forward_fp8_prenorm, with eps norm_eps.
     """
 
-    def __init__(self, cfg: _lib.MoeCfg, weights: dict, device="cuda"):
+    def __init__(self, cfg: _lib.MoeCfg, weights: dict, device="cuda", norm_w=None,
+                 norm_eps: float = 1e-6):
         self.cfg = cfg
         self.device = torch.device(device)
         self.w = weights
         self.bias = weights["bias"]
         self.fp8 = cfg.wgt_dtype == _lib.MOE_E4M3
         self._fp8w = _lib.fp8_weights(weights) if self.fp8 else None
+        self.norm_w = norm_w
+        self.norm_eps = norm_eps
         self._ws = None
         self._T = None
 
     def _buffers(self, T: int):
         if self._T != T:
             self.cfg.T = T
-            self._ws = _lib.alloc_workspace(self.cfg, _lib.MOE_WS_FORWARD, self.device)
+            kind = _lib.MOE_WS_FORWARD if self.norm_w is None else _lib.MOE_WS_FORWARD_PRENORM
+            self._ws = _lib.alloc_workspace(self.cfg, kind, self.device)
             K, E = self.cfg.K, self.cfg.E
             self.idx = torch.empty((T, K), dtype=torch.int32, device=self.device)
             self.gates = torch.empty((T, K), dtype=torch.float32, device=self.device)
@@ -44,7 +51,15 @@ class MoeLayer:
         if out is None:
             out = torch.empty_like(x)
         w = self.w
-        if self.fp8:
+        if self.norm_w is not None and self.fp8:
+            _lib.forward_fp8_prenorm(self.cfg, x, self.norm_w, self.norm_eps, w["centroids"],
+                                     self.bias, self._fp8w, self.idx, self.gates, self.counts,
+                                     out, self._ws, stream)
+        elif self.norm_w is not None:
+            _lib.forward_prenorm(self.cfg, x, self.norm_w, self.norm_eps, w["centroids"],
+                                 self.bias, w["w13"], w["w2"], w.get("ws13"), w.get("ws2"),
+                                 self.idx, self.gates, self.counts, out, self._ws, stream)
+        elif self.fp8:
             _lib.forward_fp8(self.cfg, x, w["centroids"], self.bias, self._fp8w, self.idx,
                              self.gates, self.counts, out, self._ws, stream)
         else:

@@ -109,3 +109,27 @@ def test_argument_errors_return_before_any_launch():
     assert lib.moe_route(ctypes.byref(c0), P, P, P, P, P, P, 0, P) == 0
     assert lib.moe_combine(ctypes.byref(c0), P, P, P, P, P, P) == 0
     assert lib.moe_experts(ctypes.byref(c0), P, P, P, P, P, P, P, P, P, P, 0, P) == 0
+
+
+def test_prenorm_workspace_and_argument_errors():
+    c = m.make_cfg(8192, 7168, 256, 8, 1, 2048)
+    f = m.workspace_size(c, m.MOE_WS_FORWARD)
+    # the pre-normed forward adds the normalised tokens [T, d] bf16
+    assert m.workspace_size(c, m.MOE_WS_FORWARD_PRENORM) == f + 8192 * 7168 * 2
+    lib = L.lib()
+    P = None
+    b = _cfg()
+    # eps must be positive; pointers non-null and 16-byte aligned for bf16
+    assert lib.moe_rmsnorm(ctypes.byref(b), 16, 16, 0.0, 16, P, P) == 1
+    assert lib.moe_rmsnorm(ctypes.byref(b), 16, 16, -1e-6, 16, P, P) == 1
+    assert lib.moe_rmsnorm(ctypes.byref(b), P, 16, 1e-6, 16, P, P) == 1
+    assert lib.moe_rmsnorm(ctypes.byref(b), 16, 8, 1e-6, 16, P, P) == 1
+    assert lib.moe_rmsnorm(ctypes.byref(_cfg(T=0)), P, P, 1e-6, P, P, P) == 0
+    args = [16, 16, 1e-6, 16, 16, 16, 16, 16, 16, 256, 256, 256, 16]
+    # workspace too small -> MOE_ERR_WORKSPACE before any launch
+    assert lib.moe_forward_prenorm(ctypes.byref(b), *args, 256, 64, P) == 3
+    # FP8 layers use the FP8 entry point
+    f8 = _cfg(wgt_dtype=m.MOE_E4M3)
+    assert lib.moe_forward_prenorm(ctypes.byref(f8), *args, 256, 1 << 40, P) == 2
+    assert lib.moe_forward_fp8_prenorm(ctypes.byref(b), 16, 16, 1e-6, 16, 16, P, 256, 256,
+                                       256, 16, 256, 1 << 40, P) == 1
