@@ -291,8 +291,7 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   GemmMaps m1;
   if (!make_gemm_maps(&m1, w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.S > 0 ? ws13 : nullptr,
                       static_cast<uint64_t>(c.S) * 2 * c.I, 128, xp, TK, x, c.T, c.d,
-                      kTokBox0Pair) ||
-      !make_store_map(&m1.out, act, R, c.I))
+                      kTokBox0Pair))
     return MOE_ERR_CUDA;
   GemmArgs a{};
   a.gt = GroupTable{rows, brow, orow, bs, bstart};
@@ -317,8 +316,7 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   GemmMaps m2;
   if (!make_gemm_maps(&m2, w2, static_cast<uint64_t>(c.E) * c.d, c.S > 0 ? ws2 : nullptr,
                       static_cast<uint64_t>(c.S) * c.d, 128, act, R, nullptr, 0, c.I,
-                      kTokBox0Pair) ||
-      !make_store_map(&m2.out, y, R, c.d))
+                      kTokBox0Pair))
     return MOE_ERR_CUDA;
   GemmArgs b = a;
   b.gt = GroupTable{rows, orow, orow, bs, bstart};

@@ -34,8 +34,9 @@
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. of its CTA, the
 //               two warps of a lane quadrant take alternate 16-token chunks;
 //               each chunk is rounded to bf16, written token-major into a
-//               shared-memory box (stmatrix.trans) and stored by TMA; then one
-//               arrival per warp on the even CTA's "tmem empty" barrier
+//               shared-memory box (stmatrix.trans) and copied out with
+//               16-byte stores; then one arrival per warp on the even CTA's
+//               "tmem empty" barrier
 //
 // Every barrier wait is bounded: after `timeout_ns` without progress the CTA
 // raises an abort flag, lets the TMA loads it issued land, waits for its own
@@ -188,8 +189,9 @@ constexpr int EX_QUEUE = 4;                               // tile indices in fli
 // the even CTA, the producer and the epilogue warps of the odd CTA
 constexpr int kQueueConsumers = 2 + 2 * EX_EPI_WARPS;
 // Epilogue staging: per warp, two buffers of NOUT output boxes (16 tokens x 32
-// columns of bf16, 64-byte rows in the TMA 64B swizzle), 1024-byte aligned,
-// after the operand ring and a 1 KB block of barriers.
+// columns of bf16: 64-byte rows whose 16-byte pieces are permuted by row pair,
+// so that both the stmatrix writes and the row reads are free of bank
+// conflicts), 1024-byte aligned, after the operand ring and 1 KB of barriers.
 constexpr uint32_t EX_STG_OFF = EX_STAGES * EX_STAGE_BYTES + 1024;
 constexpr uint32_t EX_STG_BOX = 16 * 64;
 constexpr int ex_nout(int mode) { return mode == GM_GATEUP ? 1 : 2; }
@@ -285,11 +287,9 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 0 && lane < 3 + 2 * kTokBoxes) {
-    const CUtensorMap* m = lane < 2                   ? &maps.a[lane]
-                           : lane < 2 + 2 * kTokBoxes ? &maps.b[(lane - 2) / kTokBoxes]
-                                                               [(lane - 2) % kTokBoxes]
-                                                      : &maps.out;
+  if (warp == 0 && lane < 2 + 2 * kTokBoxes) {
+    const CUtensorMap* m =
+        lane < 2 ? &maps.a[lane] : &maps.b[(lane - 2) / kTokBoxes][(lane - 2) % kTokBoxes];
     tc::tma_prefetch_desc(m);
   }
   if (warp == 1) {
@@ -407,8 +407,9 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
     // Warp w drains TMEM lanes 32*(w%4).. (its quadrant: 32 output columns of
     // this CTA) in 16-token chunks, alternate chunks per warp of a quadrant.
     // tcgen05.ld 16x256b yields the 8x8 fragment layout that stmatrix.trans
-    // writes token-major into a staging box; one TMA store per box then writes
-    // 16 tokens x 64 bytes (a ragged last chunk is copied row by row instead).
+    // writes token-major into a staging box (16 tokens x 64 bytes); the warp
+    // then copies the box out with 16-byte loads and stores.  (A TMA store of
+    // the box needs a proxy fence first, which cost more than the copy.)
     constexpr int NOUT = ex_nout(MODE);
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
@@ -449,9 +450,8 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
         tc::tmem_ld16x256_x2(taddr + 256 + j0, u0);
         tc::tmem_ld16x256_x2(taddr + kLanes16 + 256 + j0, u1);
         tc::tmem_wait_ld4(g0, g1, u0, u1);
-        // the buffer written now was last stored from two chunks ago
-        if (lane == 0) tc::bulk_wait_read<1>();
-        __syncwarp();
+        // buffer sbuf was last read two chunks ago, before the previous
+        // chunk's __syncwarp
         const uint32_t buf = stg + sbuf * (NOUT * EX_STG_BOX);
         if (MODE == GM_GATEUP) {
           stage_swiglu(buf + soff[0], g0, u0);
@@ -462,36 +462,25 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
           stage_bf16(buf + EX_STG_BOX + soff[0], u0);
           stage_bf16(buf + EX_STG_BOX + soff[1], u1);
         }
+        __syncwarp();
+        // each box: 16 token rows of 64 bytes, one 16-byte piece per lane
+        // and step (a quarter row), rows of tokens past the group skipped
         const int nv = min(16, t.ntok - j0);
-        if (nv == 16) {
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
+        const uint8_t* bp = stg_p + sbuf * (NOUT * EX_STG_BOX);
 #pragma unroll
-            for (int o = 0; o < NOUT; ++o)
-              if (colbase + 256 * o < args.out_cols)
-                tc::tma_store_2d(&maps.out, buf + o * EX_STG_BOX, colbase + 256 * o,
-                                 out_row0 + j0);
-          }
-        } else {
-          __syncwarp();
-          const uint8_t* bp = stg_p + sbuf * (NOUT * EX_STG_BOX);
+        for (int o = 0; o < NOUT; ++o) {
+          const int col = colbase + 256 * o;
 #pragma unroll
-          for (int o = 0; o < NOUT; ++o) {
-            const int col = colbase + 256 * o;
-#pragma unroll
-            for (int u = lane; u < 64; u += 32) {
-              const int r = u >> 2, c = u & 3;
-              if (r < nv && col < args.out_cols) {
-                const uint4 v = *reinterpret_cast<const uint4*>(
-                    bp + o * EX_STG_BOX + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-                *reinterpret_cast<uint4*>(
-                    out + static_cast<size_t>(out_row0 + j0 + r) * args.out_ld + col + 8 * c) = v;
-              }
+          for (int u = lane; u < 64; u += 32) {
+            const int r = u >> 2, c = u & 3;
+            if (r < nv && col < args.out_cols) {
+              const uint4 v = *reinterpret_cast<const uint4*>(
+                  bp + o * EX_STG_BOX + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+              *reinterpret_cast<uint4*>(
+                  out + static_cast<size_t>(out_row0 + j0 + r) * args.out_ld + col + 8 * c) = v;
             }
           }
         }
-        if (lane == 0) tc::bulk_commit();
         sbuf ^= 1;
       }
       tc::tc_fence_before();
@@ -499,8 +488,6 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
       if (lane == 0) tc::mbar_arrive_cluster(tempty_addr);
       tphase ^= 1u;
     }
-    if (lane == 0) tc::bulk_wait_all();
-    __syncwarp();
   }
 
   tc::tc_fence_before();
@@ -834,19 +821,6 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-bool make_store_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
-  if (!enc || !base || rows == 0 || cols == 0) return false;
-  const cuuint64_t gdim[2] = {cols, rows};
-  const cuuint64_t gstride[1] = {cols * 2};
-  const cuuint32_t box[2] = {32, 16};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estride,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

@@ -55,12 +55,7 @@ constexpr uint32_t kTokBox0Pair = 8;
 struct GemmMaps {
   CUtensorMap a[2];               // weight operand: routed (0) / shared (1), 128-row boxes
   CUtensorMap b[2][kTokBoxes];    // token operand: routed (0) / shared (1), box 16 << i rows
-  CUtensorMap out;                // expert GEMMs: bf16 output, see make_store_map
 };
-
-// Tensor map of the row-major bf16 output [rows, cols] written by the expert
-// GEMMs' epilogue in boxes of {32 columns, 16 rows} with 64-byte swizzle.
-bool make_store_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols);
 
 // Fills `m`: a[i] over the [a_rows[i], k] weight matrices in boxes of
 // a_box_rows rows, b[i][*] over the [b_rows[i], k] token matrices in boxes of

@@ -132,35 +132,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tma
       : "memory");
 }
 
-// 2-D tiled store of box {c0 (inner), c1} from shared memory to global memory,
-// tracked in this thread's bulk async-group.  The shared source must have been
-// made visible to the async proxy (fence_proxy_async_smem) by its writers.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t smem_src, int32_t c0,
-                                             int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(smem_src), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until at most N of this thread's bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Waits until every bulk group of this thread has completed its writes.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA) reads of them.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Four 8x8 b16 matrices stored transposed: register i of thread t holds
 // elements (t/4, 2(t%4)) (low half) and (t/4, 2(t%4)+1) of matrix i; thread
 // 8i+j gives the shared address of row j of stored matrix i, which receives
@@ -291,20 +262,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 // 16 TMEM lanes (from taddr's lane) x 16 columns: thread t receives, for each
 // 8-column half c (registers 4c..4c+3), lane t/4 at columns 2(t%4), 2(t%4)+1
-// and lane t/4 + 8 at the same two columns.  Valid after tmem_wait_ld2/4().
+// and lane t/4 + 8 at the same two columns.  Valid after tmem_wait_ld4().
 __device__ __forceinline__ void tmem_ld16x256_x2(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "r"(taddr)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[8], uint32_t (&b)[8]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
-                 "+r"(a[6]), "+r"(a[7]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]),
-                 "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7])
-               :
                : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld4(uint32_t (&a)[8], uint32_t (&b)[8], uint32_t (&c)[8],
