@@ -148,6 +148,9 @@ def kernel_roofline(cfg, traces, peaks):
         "gemm_down": ("TFLOP/s", 2.0 * R * I * d),
         "gemm_fp8_gateup_swiglu": ("TFLOP/s fp8", 2.0 * R * d * 2 * I),
         "gemm_fp8_down": ("TFLOP/s fp8", 2.0 * R * I * d),
+        # e4m3 weights dequantised in shared memory, bf16 tensor cores
+        "gemm_w8_gateup_swiglu": ("TFLOP/s", 2.0 * R * d * 2 * I),
+        "gemm_w8_down": ("TFLOP/s", 2.0 * R * I * d),
         # bytes: algorithmic traffic (inputs read once, outputs written once)
         "gemm_router": ("GB/s", es * (T * d + E * d) + 4.0 * T * E),
         "router_topk": ("GB/s", 4.0 * T * E + 8.0 * T * K),
@@ -274,7 +277,10 @@ NORM_EPS = 1e-6
 
 
 def _workload(cfg, args) -> str:
-    return cfg.name + ("+rmsnorm" if args.prenorm else "")
+    w = cfg.name + ("+rmsnorm" if args.prenorm else "")
+    if cfg.wgt == "e4m3":
+        w += "+" + args.fp8_path
+    return w
 
 
 def main():
@@ -291,6 +297,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--balance-steps", type=int, default=20,
                     help="skewed layers: bias-update steps of the balancing run")
+    ap.add_argument("--fp8-path", default="e4m3", choices=["e4m3", "w8a16"],
+                    help="FP8 layers: e4m3 x e4m3 with fp32 promotion every 128 K (e4m3) or "
+                         "e4m3 weights dequantised to bf16 on the fly (w8a16)")
     ap.add_argument("--prenorm", action="store_true",
                     help="the layer behind its RMSNorm: h = x + MoE(RMSNorm(x))")
     ap.add_argument("--override", default="",
@@ -318,7 +327,8 @@ def main():
     inp = make_inputs(cfg, device, seed=rank)
     mc = m.cfg_from_layer(cfg)
     layer = m.MoeLayer(mc, inp, device=device,
-                       norm_w=inp["norm_w"] if args.prenorm else None, norm_eps=NORM_EPS)
+                       norm_w=inp["norm_w"] if args.prenorm else None, norm_eps=NORM_EPS,
+                       fp8_path=args.fp8_path)
     x = inp["x"]
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -372,12 +382,13 @@ def main():
         return
 
     roof = kernel_roofline(cfg, traces, peaks)
-    fp8 = cfg.wgt == "e4m3"
-    top_name = "gemm_fp8_gateup_swiglu" if fp8 else "gemm_gateup_swiglu"
+    w8 = layer.w8a16                        # FP8 weights on the bf16 tensor cores
+    fp8 = cfg.wgt == "e4m3" and not w8      # e4m3 x e4m3 tensor cores
+    pre = "gemm_w8_" if w8 else "gemm_fp8_" if fp8 else "gemm_"
+    top_name = pre + "gateup_swiglu"
     top = roof.get(top_name)
     gemm_flops = cfg.gemm_flops()
-    gemm_names = (("gemm_fp8_gateup_swiglu", "gemm_fp8_down") if fp8
-                  else ("gemm_gateup_swiglu", "gemm_down"))
+    gemm_names = (top_name, pre + "down")
     gemm_ms = sum(t[2] for t in traces if t[0] in gemm_names)
     gemm_ms_step = gemm_ms / args.steps if gemm_ms else None
     gemm_tflops = gemm_flops / (gemm_ms_step / 1e3) / 1e12 if gemm_ms_step else None
@@ -389,7 +400,9 @@ def main():
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 (fp32 promotion), bf16 tokens" if fp8 else "bf16",
+        "dtype": ("e4m3 x e4m3 (fp32 promotion), bf16 tokens" if fp8 else
+                  "e4m3 weights dequantised to bf16, bf16 x bf16 (fp32 accumulate)" if w8
+                  else "bf16"),
         "data": "synthetic (seeded random tokens and random-init weights of the layer's shape)",
         "config": {"workload": _workload(cfg, args), "T": cfg.T, "d": cfg.d, "E": cfg.E,
                    "K": cfg.K, "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
@@ -405,6 +418,7 @@ def main():
                                        else f"bf16 sustained, {peaks['source']}"),
                          "frac_of_burst_bf16": round(gemm_tflops / peaks["bf16_tflops"], 4)
                          if gemm_tflops and not fp8 else None,
+                         "kernels": list(gemm_names),
                          "ms_per_step": round(gemm_ms_step, 4) if gemm_ms_step else None},
         "roofline": ({"kernel": top_name, "bound": "tensor",
                       "achieved": top["achieved"], "peak": top["peak"], "unit": "TFLOP/s",

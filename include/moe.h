@@ -94,7 +94,8 @@ typedef enum {
   MOE_WS_DISPATCH = 1,
   MOE_WS_EXPERTS = 2,
   MOE_WS_FORWARD = 3,
-  MOE_WS_FORWARD_PRENORM = 4   /* moe_forward_prenorm / moe_forward_fp8_prenorm */
+  MOE_WS_FORWARD_PRENORM = 4,  /* moe_forward_prenorm / moe_forward_fp8_prenorm */
+  MOE_WS_FORWARD_W8A16 = 5     /* moe_forward_w8a16 (FP8 layers) */
 } moe_ws_kind_t;
 
 /* Bytes of scratch that `which` needs for this cfg (0 on an invalid cfg). */
@@ -316,6 +317,28 @@ moe_status_t moe_forward_fp8(const moe_cfg_t* cfg, const void* x, const void* ce
                              const float* bias, const moe_fp8_weights_t* w, int32_t* idx,
                              float* gates, int32_t* counts, void* out, void* ws,
                              size_t ws_bytes, void* stream);
+
+/*
+ * W8A16 form of an FP8 layer: the e4m3 block-scaled expert weights meet bf16
+ * tokens and activations.  Each 64-wide slice of a weight tile is brought in
+ * as e4m3, dequantised in shared memory to bf16 (q * scale of its 128 x 128
+ * block, rounded once) and multiplied on the bf16 tensor cores with fp32
+ * accumulation over all of K; nothing else is quantised.  The rows follow the
+ * bf16 layer's layout: dispatch and combine are moe_dispatch / moe_combine
+ * called with the same cfg but wgt_dtype = MOE_BF16 (they read no weights).
+ *   moe_experts_w8a16: xp [T*K, d] bf16 (moe_dispatch), x [T, d] (shared
+ *     experts' input), offsets [E+1]; act [T*K+S*T, I] and y [T*K+S*T, d] bf16
+ *     out; ws: MOE_WS_EXPERTS bytes.
+ *   moe_forward_w8a16: route -> dispatch -> experts -> combine on one stream;
+ *     ws: MOE_WS_FORWARD_W8A16 bytes.  Other arguments as moe_forward_fp8.
+ */
+moe_status_t moe_experts_w8a16(const moe_cfg_t* cfg, const void* xp, const void* x,
+                               const int32_t* offsets, const moe_fp8_weights_t* w, void* act,
+                               void* y, void* ws, size_t ws_bytes, void* stream);
+moe_status_t moe_forward_w8a16(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                               const float* bias, const moe_fp8_weights_t* w, int32_t* idx,
+                               float* gates, int32_t* counts, void* out, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /* moe_forward_fp8 behind the RMSNorm, as moe_forward_prenorm: the router reads
  * the normalised bf16 tokens, the dispatch quantises them to e4m3 1 x 128

@@ -18,6 +18,7 @@ MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_EXPERTS, MOE_WS_FORWARD = 0, 1, 2, 3
 MOE_WS_FORWARD_PRENORM = 4
+MOE_WS_FORWARD_W8A16 = 5
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
@@ -28,7 +29,8 @@ SYMBOLS = ["moe_workspace_size", "moe_check_cfg", "moe_route", "moe_dispatch", "
            "moe_experts_static",
            "moe_combine", "moe_update_bias", "moe_forward", "moe_fp8_rows", "moe_dispatch_fp8",
            "moe_experts_fp8", "moe_forward_fp8", "moe_rmsnorm", "moe_forward_prenorm",
-           "moe_forward_fp8_prenorm", "moe_get_status",
+           "moe_forward_fp8_prenorm", "moe_experts_w8a16", "moe_forward_w8a16",
+           "moe_get_status",
            "moe_status_string", "moe_trace_enable", "moe_trace_read", "moe_version"]
 
 
@@ -88,6 +90,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward_prenorm": (I32, [cfgp, P, P, F32, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_forward_fp8_prenorm": (I32, [cfgp, P, P, F32, P, P, ctypes.POINTER(Fp8Weights), P,
                                           P, P, P, P, SZ, P]),
+        "moe_experts_w8a16": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, SZ, P]),
+        "moe_forward_w8a16": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, P, P,
+                                    SZ, P]),
         "moe_get_status": (I32, [P]),
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_trace_enable": (I32, [I32]),
@@ -258,6 +263,29 @@ def forward_fp8_prenorm(cfg, x, norm_w, eps, centroids, bias, weights: Fp8Weight
                                          _p(centroids), _p(bias), ctypes.byref(weights), _p(idx),
                                          _p(gates), _p(counts), _p(out), _p(ws), ws.numel(),
                                          _stream(stream)), "moe_forward_fp8_prenorm")
+
+
+def bf16_layout(cfg: MoeCfg) -> MoeCfg:
+    """The cfg of an FP8 layer's W8A16 path for moe_dispatch / moe_combine
+    (the bf16 layer's row layout)."""
+    v = MoeCfg()
+    ctypes.pointer(v)[0] = cfg
+    v.wgt_dtype = MOE_BF16
+    return v
+
+
+def experts_w8a16(cfg, xp, x, offsets, weights: Fp8Weights, act, y, ws, stream=None):
+    _check(lib().moe_experts_w8a16(ctypes.byref(cfg), _p(xp), _p(x), _p(offsets),
+                                   ctypes.byref(weights), _p(act), _p(y), _p(ws), ws.numel(),
+                                   _stream(stream)), "moe_experts_w8a16")
+
+
+def forward_w8a16(cfg, x, centroids, bias, weights: Fp8Weights, idx, gates, counts, out, ws,
+                  stream=None):
+    _check(lib().moe_forward_w8a16(ctypes.byref(cfg), _p(x), _p(centroids), _p(bias),
+                                   ctypes.byref(weights), _p(idx), _p(gates), _p(counts),
+                                   _p(out), _p(ws), ws.numel(), _stream(stream)),
+           "moe_forward_w8a16")
 
 
 def get_status(stream=None) -> int:

@@ -135,6 +135,14 @@ struct Fp8Rows {
 
 bool is_fp8(const moe_cfg_t& c) { return c.wgt_dtype == MOE_E4M3; }
 
+// The W8A16 path of an FP8 layer keeps every activation in bf16 and uses the
+// bf16 layer's row layout: the same cfg with bf16 weights describes it.
+moe_cfg_t bf16_layout(const moe_cfg_t& c) {
+  moe_cfg_t v = c;
+  v.wgt_dtype = MOE_BF16;
+  return v;
+}
+
 Fp8Rows fp8_rows(const moe_cfg_t& c) {
   Fp8Rows r;
   const long long TK = static_cast<long long>(c.T) * c.K;
@@ -261,10 +269,12 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
                      c.topk_groups, idx, gates, st);
 }
 
+// w8 (an FP8 layer's e4m3 weights and block scales) replaces w13..ws2: the
+// same bf16 GEMMs with the weights dequantised in shared memory.
 moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
                         const int32_t* offsets, const void* w13, const void* w2,
                         const void* ws13, const void* ws2, void* act, void* y, void* ws,
-                        cudaStream_t st) {
+                        cudaStream_t st, const moe_fp8_weights_t* w8 = nullptr) {
   if (c.act_dtype != MOE_BF16) {
     return launch_experts_f32(static_cast<const float*>(xp), static_cast<const float*>(x),
                               offsets, static_cast<const float*>(w13),
@@ -279,7 +289,8 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   int32_t* orow = brow + (G + 1);
   int32_t* bs = orow + (G + 1);
   int32_t* bstart = bs + (G + 1);
-  const GroupLayout lay{0, c.T * c.K, c.T, 256};
+  // W8 tiles keep both accumulators and two weight slots in TMEM: <= 192 tokens
+  const GroupLayout lay{0, c.T * c.K, c.T, w8 ? 192 : 256};
   moe_status_t s = launch_build_groups(offsets, nullptr, c.T, c.E, c.S, lay, rows, brow, orow, bs,
                                        bstart, st);
   if (s != MOE_OK) return s;
@@ -288,10 +299,26 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   const int grid = num_sms();
 
   // gate/up + SwiGLU: A = W13 rows, B = dispatched rows (routed) or tokens (shared)
+  const uint64_t r13 = static_cast<uint64_t>(c.E) * 2 * c.I, rs13 = static_cast<uint64_t>(c.S) * 2 * c.I;
+  const uint64_t r2 = static_cast<uint64_t>(c.E) * c.d, rs2 = static_cast<uint64_t>(c.S) * c.d;
+  // W8: e4m3 weight maps replace the bf16 ones (the token maps are the same)
+  auto w8_maps = [&](GemmMaps* m, const void* a0, uint64_t n0, const void* a1, uint64_t n1,
+                     uint64_t k) {
+    if (!make_tmap_e4m3(&m->a[0], a0, n0, k)) return false;
+    if (a1) return make_tmap_e4m3(&m->a[1], a1, n1, k);
+    m->a[1] = m->a[0];
+    return true;
+  };
+  if (w8) {
+    w13 = w8->w13;
+    w2 = w8->w2;
+    ws13 = w8->ws13;
+    ws2 = w8->ws2;
+  }
   GemmMaps m1;
-  if (!make_gemm_maps(&m1, w13, static_cast<uint64_t>(c.E) * 2 * c.I, c.S > 0 ? ws13 : nullptr,
-                      static_cast<uint64_t>(c.S) * 2 * c.I, 128, xp, TK, x, c.T, c.d,
-                      kTokBox0Pair))
+  if (!make_gemm_maps(&m1, w13, r13, c.S > 0 ? ws13 : nullptr, rs13, 128, xp, TK, x, c.T, c.d,
+                      kTokBox0Pair) ||
+      (w8 && !w8_maps(&m1, w13, r13, c.S > 0 ? ws13 : nullptr, rs13, c.d)))
     return MOE_ERR_CUDA;
   GemmArgs a{};
   a.gt = GroupTable{rows, brow, orow, bs, bstart};
@@ -309,14 +336,19 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   a.tile_counter = bstart + G + 1;
   a.status = device_status_word();
   a.timeout_ns = kWaitTimeoutNs;
-  s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st);
+  if (w8) {
+    a.w_scale[0] = w8->w13_scale;
+    a.w_scale[1] = c.S > 0 ? w8->ws13_scale : w8->w13_scale;
+    a.scale_kb = c.d / 128;
+  }
+  s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st, w8 != nullptr);
   if (s != MOE_OK) return s;
 
   // down: A = W2 rows (two 128-row boxes), B = activations
   GemmMaps m2;
-  if (!make_gemm_maps(&m2, w2, static_cast<uint64_t>(c.E) * c.d, c.S > 0 ? ws2 : nullptr,
-                      static_cast<uint64_t>(c.S) * c.d, 128, act, R, nullptr, 0, c.I,
-                      kTokBox0Pair))
+  if (!make_gemm_maps(&m2, w2, r2, c.S > 0 ? ws2 : nullptr, rs2, 128, act, R, nullptr, 0, c.I,
+                      kTokBox0Pair) ||
+      (w8 && !w8_maps(&m2, w2, r2, c.S > 0 ? ws2 : nullptr, rs2, c.I)))
     return MOE_ERR_CUDA;
   GemmArgs b = a;
   b.gt = GroupTable{rows, orow, orow, bs, bstart};
@@ -329,7 +361,12 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   b.out_cols = c.d;
   b.out = y;
   b.tile_counter = bstart + G + 2;
-  return launch_gemm_tc(GM_DOWN, m2, b, grid, st);
+  if (w8) {
+    b.w_scale[0] = w8->w2_scale;
+    b.w_scale[1] = c.S > 0 ? w8->ws2_scale : w8->w2_scale;
+    b.scale_kb = c.I / 128;
+  }
+  return launch_gemm_tc(GM_DOWN, m2, b, grid, st, w8 != nullptr);
 }
 
 moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,
@@ -464,6 +501,7 @@ size_t moe_workspace_size(const moe_cfg_t* cfg, int32_t which) {
     case MOE_WS_EXPERTS: return experts_ws(c);
     case MOE_WS_FORWARD: return forward_layout(c).total;
     case MOE_WS_FORWARD_PRENORM: return prenorm_ws(c);
+    case MOE_WS_FORWARD_W8A16: return is_fp8(c) ? forward_layout(bf16_layout(c)).total : 0;
     default: return 0;
   }
 }
@@ -732,6 +770,54 @@ moe_status_t moe_forward_fp8_prenorm(const moe_cfg_t* cfg, const void* x, const 
   if ((s = launch_rmsnorm(c.act_dtype, x, norm_w, eps, c.T, c.d, xn, nullptr, st)) != MOE_OK)
     return s;
   return do_forward_fp8(c, xn, x, centroids, bias, w, idx, gates, counts, out, ws, st);
+}
+
+moe_status_t moe_experts_w8a16(const moe_cfg_t* cfg, const void* xp, const void* x,
+                               const int32_t* offsets, const moe_fp8_weights_t* w, void* act,
+                               void* y, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!is_fp8(c)) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if ((s = check_ptrs(c, {xp, x, act, y}, {offsets})) != MOE_OK) return s;
+  if ((s = check_fp8_weights(c, w)) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, experts_ws(c))) != MOE_OK) return s;
+  return do_experts(bf16_layout(c), xp, x, offsets, nullptr, nullptr, nullptr, nullptr, act, y,
+                    ws, static_cast<cudaStream_t>(stream), w);
+}
+
+moe_status_t moe_forward_w8a16(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                               const float* bias, const moe_fp8_weights_t* w, int32_t* idx,
+                               float* gates, int32_t* counts, void* out, void* ws,
+                               size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!is_fp8(*cfg)) return MOE_ERR_INVALID_ARG;
+  const moe_cfg_t c = bf16_layout(*cfg);
+  if (!counts) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) return forward_empty(c, counts, st);
+  if ((s = check_ptrs(c, {x, centroids, out}, {bias, idx, gates})) != MOE_OK) return s;
+  if ((s = check_fp8_weights(*cfg, w)) != MOE_OK) return s;
+  const ForwardLayout L = forward_layout(c);
+  if ((s = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return s;
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  void* xp = at<void>(ws, L.xp);
+  void* act = at<void>(ws, L.act);
+  void* y = at<void>(ws, L.y);
+  if ((s = do_route(c, x, centroids, bias, idx, gates, at<void>(ws, L.route), st)) != MOE_OK)
+    return s;
+  if ((s = launch_dispatch(x, static_cast<size_t>(c.d) * 2, idx, c.T, c.K, c.E, counts, offsets,
+                           xp, at<int32_t>(ws, L.perm), pos, at<int32_t>(ws, L.dispatch), st)) !=
+      MOE_OK)
+    return s;
+  if ((s = do_experts(c, xp, x, offsets, nullptr, nullptr, nullptr, nullptr, act, y,
+                      at<void>(ws, L.experts), st, w)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, y, gates, pos, x, out, c.T, c.K, c.S, c.d,
+                        static_cast<long long>(c.T) * c.K, c.T, c.add_residual, st);
 }
 
 moe_status_t moe_fp8_rows(const moe_cfg_t* cfg, int64_t* rows_in, int64_t* rows_out,

@@ -42,6 +42,7 @@
 // raises an abort flag, lets the TMA loads it issued land, waits for its own
 // MMAs, frees TMEM, sets the device error word and returns.
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 #include <stdio.h>
 
 #include "common.cuh"
@@ -183,11 +184,38 @@ constexpr uint32_t EX_A_BOX_BYTES = 128 * ROW_BYTES;      // 16 KB: one 128-row 
 constexpr uint32_t EX_B_BYTES = 128 * ROW_BYTES;          // 16 KB: up to 128 token rows
 constexpr uint32_t EX_STAGE_BYTES = 2 * EX_A_BOX_BYTES + EX_B_BYTES;
 constexpr int EX_EPI_WARPS = 8;
-constexpr int EX_THREADS = 64 + 32 * EX_EPI_WARPS;
 constexpr int EX_QUEUE = 4;                               // tile indices in flight
+
+// W8 variant (e4m3 weights with 128x128 fp32 block scales, bf16 tokens): a
+// stage holds this CTA's two raw e4m3 weight boxes (64-byte swizzle) and its
+// token rows.  Dequantisation warps (one thread per weight row) turn a K
+// step of raw weights into bf16 (q * scale, rounded once) and write it to an
+// A slot in tensor memory with tcgen05.st; the MMAs read A from TMEM (the
+// "TS" form).  Writing A to shared memory instead needs a proxy fence per K
+// step, which cost more than the MMAs.  TMEM: acc0 at column 0, acc1 at 192
+// (token blocks of at most 192), two A slots of 2 x 32 columns at 384.  Two
+// groups of four warps take alternate K steps (slot = step % 2).
+constexpr uint32_t W8_RAW_BOX_BYTES = 128 * BK;                          // 8 KB
+constexpr uint32_t W8_STAGE_BYTES = 2 * W8_RAW_BOX_BYTES + EX_B_BYTES;   // 32 KB
+constexpr int W8_STAGES = 6;
+constexpr int W8_A_SLOTS = 2;
+constexpr int W8_DQ_GROUP = 4;                             // warps per dequantisation group
+constexpr int W8_DQ_WARPS = W8_A_SLOTS * W8_DQ_GROUP;      // one group per A slot
+constexpr uint32_t W8_ACC1_COL = 192;
+constexpr uint32_t W8_A_COL = 384;                         // slot j: columns 384 + 64 j
+constexpr int W8_MAX_BS = 192;
+static_assert(W8_STAGES * W8_STAGE_BYTES == EX_STAGES * EX_STAGE_BYTES,
+              "the W8 ring fills the bf16 ring's space");
+static_assert(W8_A_COL + W8_A_SLOTS * 64 <= TMEM_COLS && 2 * W8_MAX_BS <= W8_A_COL, "TMEM");
+constexpr int EX_MAX_STAGES = W8_STAGES;
+
+constexpr int ex_threads(bool w8) { return 64 + 32 * (EX_EPI_WARPS + (w8 ? W8_DQ_WARPS : 0)); }
 // readers of each published tile index: the MMA warp and the epilogue warps of
-// the even CTA, the producer and the epilogue warps of the odd CTA
-constexpr int kQueueConsumers = 2 + 2 * EX_EPI_WARPS;
+// the even CTA, the producer and the epilogue warps of the odd CTA, and (W8)
+// the dequantisation warps of both
+constexpr int queue_consumers(bool w8) {
+  return 2 + 2 * EX_EPI_WARPS + (w8 ? 2 * W8_DQ_WARPS : 0);
+}
 // Epilogue staging: per warp, two buffers of NOUT output boxes (16 tokens x 32
 // columns of bf16: 64-byte rows whose 16-byte pieces are permuted by row pair,
 // so that both the stmatrix writes and the row reads are free of bank
@@ -251,20 +279,33 @@ struct TileQueue {
   }
 };
 
-template <int MODE>
-__global__ void __launch_bounds__(EX_THREADS, 1)
+// e4m3 pair -> bf16 pair of q * scale (one rounding)
+__device__ __forceinline__ uint32_t dequant2(uint16_t q2, float sc) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(q2, __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  return pack_bf16x2(f.x * sc, f.y * sc);
+}
+
+template <int MODE, bool W8>
+__global__ void __launch_bounds__(ex_threads(W8), 1)
     expert_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int NST = W8 ? W8_STAGES : EX_STAGES;            // operand ring stages
+  constexpr uint32_t STB = W8 ? W8_STAGE_BYTES : EX_STAGE_BYTES;
+  constexpr uint32_t ACC1 = W8 ? W8_ACC1_COL : 256;           // TMEM column of acc1
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + EX_STAGES * EX_STAGE_BYTES);
-  uint64_t* empty = full + EX_STAGES;
-  uint64_t* tfull = empty + EX_STAGES;
+  uint64_t* empty = full + EX_MAX_STAGES;
+  uint64_t* tfull = empty + EX_MAX_STAGES;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
   uint64_t* qfull = drain + 1;           // [EX_QUEUE]: tile index published
   uint64_t* qempty = qfull + EX_QUEUE;   // [EX_QUEUE]: read by every consumer
-  volatile int* tq = reinterpret_cast<volatile int*>(qempty + EX_QUEUE);   // [EX_QUEUE]
+  uint64_t* raw_full = qempty + EX_QUEUE;      // W8 [NST]: this CTA's raw boxes landed
+  uint64_t* a_full = raw_full + EX_MAX_STAGES; // W8 [A slots]: dequantised, both CTAs (even)
+  uint64_t* a_empty = a_full + W8_A_SLOTS;     // W8 [A slots]: MMAs done with the slot
+  volatile int* tq = reinterpret_cast<volatile int*>(a_empty + W8_A_SLOTS);   // [EX_QUEUE]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tq) + EX_QUEUE);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -273,7 +314,7 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
   const uint32_t rank = tc::cluster_ctarank();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < EX_STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       tc::mbar_init(full + s, 1);     // the even CTA expects both CTAs' bytes
       tc::mbar_init(empty + s, 1);
     }
@@ -282,7 +323,14 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
     tc::mbar_init(drain, 1);
     for (int s = 0; s < EX_QUEUE; ++s) {
       tc::mbar_init(qfull + s, 1);
-      tc::mbar_init(qempty + s, kQueueConsumers);
+      tc::mbar_init(qempty + s, queue_consumers(W8));
+    }
+    if (W8) {
+      for (int s = 0; s < NST; ++s) tc::mbar_init(raw_full + s, 1);
+      for (int j = 0; j < W8_A_SLOTS; ++j) {
+        tc::mbar_init(a_full + j, 2 * W8_DQ_GROUP);   // the slot's group, both CTAs
+        tc::mbar_init(a_empty + j, 1);
+      }
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -327,40 +375,54 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
                          t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128;
       const int a_row1 = a_row0 + args.a1_off;
       const int b_row = __ldg(args.gt.brow + t.g) + t.tok0 + static_cast<int>(rank) * half;
-      const uint32_t bytes = 2 * EX_A_BOX_BYTES + half * ROW_BYTES;
+      // bytes of this CTA on the even CTA's "full" barrier (W8: token rows only;
+      // the raw weight boxes count on this CTA's own raw_full barrier)
+      const uint32_t bytes = (W8 ? 0u : 2 * EX_A_BOX_BYTES) + half * ROW_BYTES;
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
         if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
         if (lane == 0) {
-          uint8_t* sa = smem + stage * EX_STAGE_BYTES;
           // Only the even CTA arrives, expecting the bytes of both CTAs; the
           // odd CTA's loads just count their bytes on the even CTA's barrier.
           // (The odd CTA reuses stage s only after the MMAs that consumed it
           // completed, so its bytes always land in the phase they belong to.)
           const uint32_t fb = tc::mapa_shared(tc::smem_u32(full + stage), 0);
           if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, 2 * bytes);
-          tc::tma_load_2d_pair(sa, mA, fb, kb * BK, a_row0);
-          tc::tma_load_2d_pair(sa + EX_A_BOX_BYTES, mA, fb, kb * BK, a_row1);
-          load_token_rows<true>(sa + 2 * EX_A_BOX_BYTES, mB, kTokBox0Pair, half, nullptr, fb,
-                                kb * BK, b_row);
+          if (W8) {
+            uint8_t* sa = smem + stage * STB;
+            tc::mbar_arrive_expect_tx(raw_full + stage, 2 * W8_RAW_BOX_BYTES);
+            tc::tma_load_2d(sa, mA, raw_full + stage, kb * BK, a_row0);
+            tc::tma_load_2d(sa + W8_RAW_BOX_BYTES, mA, raw_full + stage, kb * BK, a_row1);
+            load_token_rows<true>(sa + 2 * W8_RAW_BOX_BYTES, mB, kTokBox0Pair, half, nullptr,
+                                  fb, kb * BK, b_row);
+          } else {
+            uint8_t* sa = smem + stage * EX_STAGE_BYTES;
+            tc::tma_load_2d_pair(sa, mA, fb, kb * BK, a_row0);
+            tc::tma_load_2d_pair(sa + EX_A_BOX_BYTES, mA, fb, kb * BK, a_row1);
+            load_token_rows<true>(sa + 2 * EX_A_BOX_BYTES, mB, kTokBox0Pair, half, nullptr, fb,
+                                  kb * BK, b_row);
+          }
         }
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         __syncwarp();
-        if (++stage == EX_STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == NST) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
       ok = rank == 0 ? queue.publish(claimed, tile) : queue.next(tile);
     }
-    if (!ok && rank == 0) {
+    if (!ok) {
       // abort: let every load counted on this CTA's barriers land before exit
-      for (int s = 0; s < EX_STAGES; ++s)
-        if (issued & (1u << s)) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+      for (int s = 0; s < NST; ++s) {
+        if (!(issued & (1u << s))) continue;
+        if (rank == 0) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+        if (W8) warp_wait(raw_full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (rank == 0) {
-      int stage = 0;
-      uint32_t phase = 0, tphase = 0;
+      int stage = 0, aslot = 0;
+      uint32_t phase = 0, tphase = 0, aphase = 0;
       bool ok = true, issued_any = false;
       for (;;) {
         int tile;
@@ -373,23 +435,39 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
         const uint32_t idesc = tc::idesc_bf16_f32(256, t.nmma);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+          // W8: the dequantised weights of both CTAs (written by threads,
+          // published with release at cluster scope)
+          if (W8 && !warp_wait<true>(a_full + aslot, aphase, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
           tc::tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = tc::smem_u32(smem + stage * EX_STAGE_BYTES);
+            const uint32_t sa = tc::smem_u32(smem + stage * STB);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t da0 = tc::smem_desc_sw128(sa + kk * 32);
-              const uint64_t da1 = tc::smem_desc_sw128(sa + EX_A_BOX_BYTES + kk * 32);
-              const uint64_t db = tc::smem_desc_sw128(sa + 2 * EX_A_BOX_BYTES + kk * 32);
               const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
-              tc::mma_bf16<2>(tmem_base, da0, db, idesc, acc);
-              tc::mma_bf16<2>(tmem_base + 256, da1, db, idesc, acc);
+              if constexpr (W8) {
+                // A from the TMEM slot: box b at +32 b, K = 16 per MMA = 8 columns
+                const uint32_t ta = tmem_base + W8_A_COL + aslot * 64 + kk * 8;
+                const uint64_t db = tc::smem_desc_sw128(sa + 2 * W8_RAW_BOX_BYTES + kk * 32);
+                tc::mma_bf16_ts<2>(tmem_base, ta, db, idesc, acc);
+                tc::mma_bf16_ts<2>(tmem_base + ACC1, ta + 32, db, idesc, acc);
+              } else {
+                const uint64_t da0 = tc::smem_desc_sw128(sa + kk * 32);
+                const uint64_t da1 = tc::smem_desc_sw128(sa + EX_A_BOX_BYTES + kk * 32);
+                const uint64_t db = tc::smem_desc_sw128(sa + 2 * EX_A_BOX_BYTES + kk * 32);
+                tc::mma_bf16<2>(tmem_base, da0, db, idesc, acc);
+                tc::mma_bf16<2>(tmem_base + ACC1, da1, db, idesc, acc);
+              }
             }
             tc::mma_commit<2>(empty + stage);   // frees the stage in both CTAs
+            if (W8) tc::mma_commit<2>(a_empty + aslot);
           }
           issued_any = true;
           __syncwarp();
-          if (++stage == EX_STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
+          if (W8 && ++aslot == W8_A_SLOTS) { aslot = 0; aphase ^= 1u; }
         }
         if (!ok) break;
         if (lane == 0) tc::mma_commit<2>(tfull);  // accumulators complete, both CTAs
@@ -401,6 +479,67 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
         __syncwarp();
         warp_wait(drain, 0, abort_flag, tmo);
       }
+    }
+  } else if (W8 && warp >= 2 + EX_EPI_WARPS) {
+    // ------------------------------------------------------------ dequantisation (W8)
+    // Group grp takes the K steps ks with ks % 2 == grp (A slot grp).  Thread
+    // = weight row r of the CTA's 128 (TMEM lane r; warp w reaches lanes
+    // 32 (w % 4)..): per box it reads the row's 64 raw bytes (four 16-byte
+    // pieces, 64-byte swizzle: conflict-free), converts them to 32 bf16 pairs
+    // and stores them to its TMEM lane in one tcgen05.st.
+    const int grp = (warp - 2 - EX_EPI_WARPS) / W8_DQ_GROUP;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t ta_lane = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                             W8_A_COL + grp * 64;
+    const uint32_t afull_c = tc::mapa_shared(tc::smem_u32(a_full + grp), 0);
+    uint32_t ks = 0;                               // K steps of the sequence so far
+    bool ok = true;
+    for (;;) {
+      int tile;
+      if (!queue.next(tile) || tile >= ntiles) break;
+      Tile t;
+      decode_group_tile(args, tile, t);
+      const bool second = t.g >= args.E;
+      const int gl = second ? t.g - args.E : t.g;
+      const int a_row0 = gl * args.a_rows_per_group +
+                         t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128;
+      const int a_row1 = a_row0 + args.a1_off;
+      // 128 x 128 block scales of the two boxes' rows, one per 128-wide K block
+      const float* scb = second ? args.w_scale[1] : args.w_scale[0];
+      const float* sc0 = scb + static_cast<size_t>(a_row0 >> 7) * args.scale_kb;
+      const float* sc1 = scb + static_cast<size_t>(a_row1 >> 7) * args.scale_kb;
+      for (int kb = t.kb0; kb < t.kb1; ++kb, ++ks) {
+        if ((ks & 1u) != static_cast<uint32_t>(grp)) continue;
+        const int stage = static_cast<int>(ks % NST);
+        const uint32_t phase = (ks / NST) & 1u;
+        const uint32_t aphase = (ks / W8_A_SLOTS) & 1u;
+        if (!warp_wait(raw_full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+        if (!warp_wait(a_empty + grp, aphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint8_t* raw = smem + stage * STB + r * 64;
+#pragma unroll
+        for (int box = 0; box < 2; ++box) {
+          const float sc = __ldg((box ? sc1 : sc0) + (kb >> 1));
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(
+                raw + box * W8_RAW_BOX_BYTES + ((c ^ ((r >> 1) & 3)) << 4));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[8 * c + 2 * i] = dequant2(static_cast<uint16_t>(wv[i] & 0xffffu), sc);
+              o[8 * c + 2 * i + 1] = dequant2(static_cast<uint16_t>(wv[i] >> 16), sc);
+            }
+          }
+          tc::tmem_st32(ta_lane + box * 32, o);
+        }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(afull_c);
+      }
+      if (!ok) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -447,8 +586,8 @@ __global__ void __launch_bounds__(EX_THREADS, 1)
         uint32_t g0[8], g1[8], u0[8], u1[8];      // acc0 / acc1, lanes 0..15 / 16..31
         tc::tmem_ld16x256_x2(taddr + j0, g0);
         tc::tmem_ld16x256_x2(taddr + kLanes16 + j0, g1);
-        tc::tmem_ld16x256_x2(taddr + 256 + j0, u0);
-        tc::tmem_ld16x256_x2(taddr + kLanes16 + 256 + j0, u1);
+        tc::tmem_ld16x256_x2(taddr + ACC1 + j0, u0);
+        tc::tmem_ld16x256_x2(taddr + kLanes16 + ACC1 + j0, u1);
         tc::tmem_wait_ld4(g0, g1, u0, u1);
         // buffer sbuf was last read two chunks ago, before the previous
         // chunk's __syncwarp
@@ -824,6 +963,19 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_e4m3(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc || !base || rows == 0 || cols == 0) return false;
+  const cuuint64_t gdim[2] = {cols, rows};
+  const cuuint64_t gstride[1] = {cols};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), 128};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
                     uint64_t a1_rows, uint32_t a_box_rows, const void* b0, uint64_t b0_rows,
                     const void* b1, uint64_t b1_rows, uint64_t k, uint32_t tok_box0) {
@@ -845,18 +997,26 @@ bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a
 }
 
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool w8) {
   if (grid <= 0) return MOE_OK;
-  static bool attr_gu[64], attr_dn[64], attr_rt[64];
+  static bool attr_gu[64], attr_dn[64], attr_rt[64], attr_gu8[64], attr_dn8[64];
   switch (mode) {
     case GM_GATEUP:
-      return launch_persistent(expert_gemm_kernel<GM_GATEUP>, "gemm_gateup_swiglu", 2,
-                               ex_smem_bytes(GM_GATEUP), EX_THREADS, grid, maps, args, stream,
-                               attr_gu);
+      if (w8)
+        return launch_persistent(expert_gemm_kernel<GM_GATEUP, true>, "gemm_w8_gateup_swiglu", 2,
+                                 ex_smem_bytes(GM_GATEUP), ex_threads(true), grid, maps, args,
+                                 stream, attr_gu8);
+      return launch_persistent(expert_gemm_kernel<GM_GATEUP, false>, "gemm_gateup_swiglu", 2,
+                               ex_smem_bytes(GM_GATEUP), ex_threads(false), grid, maps, args,
+                               stream, attr_gu);
     case GM_DOWN:
-      return launch_persistent(expert_gemm_kernel<GM_DOWN>, "gemm_down", 2,
-                               ex_smem_bytes(GM_DOWN), EX_THREADS, grid, maps, args, stream,
-                               attr_dn);
+      if (w8)
+        return launch_persistent(expert_gemm_kernel<GM_DOWN, true>, "gemm_w8_down", 2,
+                                 ex_smem_bytes(GM_DOWN), ex_threads(true), grid, maps, args,
+                                 stream, attr_dn8);
+      return launch_persistent(expert_gemm_kernel<GM_DOWN, false>, "gemm_down", 2,
+                               ex_smem_bytes(GM_DOWN), ex_threads(false), grid, maps, args,
+                               stream, attr_dn);
     case GM_ROUTER:
       return launch_persistent(router_gemm_kernel, "gemm_router", 1, RT_SMEM_BYTES, RT_THREADS,
                                grid, maps, args, stream, attr_rt);

@@ -35,6 +35,8 @@ struct GemmArgs {
   long long out_split_stride;  // router mode: elements between split partials
   void* out;
   int* tile_counter;         // expert GEMMs: next tile to hand out, 0 at launch
+  const float* w_scale[2];   // W8: routed / shared 128x128 block scales [groups, rows/128, K/128]
+  int scale_kb;              // W8: K / 128
   unsigned* status;
   unsigned long long timeout_ns;  // bound of every barrier wait
 };
@@ -65,9 +67,16 @@ bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a
                     const void* b1, uint64_t b1_rows, uint64_t k, uint32_t tok_box0);
 
 // Launches a persistent grouped GEMM on at most `grid` CTAs: GATEUP and DOWN
-// on CTA pairs (clusters of two), ROUTER on single CTAs.
+// on CTA pairs (clusters of two), ROUTER on single CTAs.  w8: the expert
+// weights are e4m3 (maps.a from make_tmap_e4m3) with args.w_scale block
+// scales, dequantised to bf16 in shared memory.
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool w8 = false);
+
+// Tensor map of a row-major e4m3 matrix [rows, cols] read in boxes of {64
+// columns, 128 rows} with 64-byte swizzle (the dequantisation warps read it,
+// one 64-byte row per thread).
+bool make_tmap_e4m3(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 
 // Where the rows of each group live.  Routed group g < E: counts[g] rows
 // starting at offsets[g] in both the token source and the outputs.  Shared

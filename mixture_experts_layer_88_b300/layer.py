@@ -17,10 +17,16 @@ class MoeLayer:
 
     norm_w ([d] fp32) puts the layer behind its RMSNorm: h = x + MoE(RMSNorm(x))
     through moe_forward_prenorm / moe_forward_fp8_prenorm, with eps norm_eps.
+
+    fp8_path picks the GEMMs of an FP8 layer: "e4m3" (moe_forward_fp8: tokens
+    and activations quantised to e4m3 1x128 tiles, e4m3 tensor cores, fp32
+    promotion every 128 K; the faster) or "w8a16" (moe_forward_w8a16: e4m3
+    weights dequantised to bf16 on the fly, bf16 tokens and activations; the
+    more accurate).
     """
 
     def __init__(self, cfg: _lib.MoeCfg, weights: dict, device="cuda", norm_w=None,
-                 norm_eps: float = 1e-6):
+                 norm_eps: float = 1e-6, fp8_path: str = "e4m3"):
         self.cfg = cfg
         self.device = torch.device(device)
         self.w = weights
@@ -29,13 +35,17 @@ class MoeLayer:
         self._fp8w = _lib.fp8_weights(weights) if self.fp8 else None
         self.norm_w = norm_w
         self.norm_eps = norm_eps
+        if fp8_path not in ("w8a16", "e4m3"):
+            raise ValueError(f"fp8_path {fp8_path!r}")
+        self.w8a16 = self.fp8 and fp8_path == "w8a16" and norm_w is None
         self._ws = None
         self._T = None
 
     def _buffers(self, T: int):
         if self._T != T:
             self.cfg.T = T
-            kind = _lib.MOE_WS_FORWARD if self.norm_w is None else _lib.MOE_WS_FORWARD_PRENORM
+            kind = (_lib.MOE_WS_FORWARD_W8A16 if self.w8a16 else
+                    _lib.MOE_WS_FORWARD if self.norm_w is None else _lib.MOE_WS_FORWARD_PRENORM)
             self._ws = _lib.alloc_workspace(self.cfg, kind, self.device)
             K, E = self.cfg.K, self.cfg.E
             self.idx = torch.empty((T, K), dtype=torch.int32, device=self.device)
@@ -51,7 +61,10 @@ class MoeLayer:
         if out is None:
             out = torch.empty_like(x)
         w = self.w
-        if self.norm_w is not None and self.fp8:
+        if self.w8a16:
+            _lib.forward_w8a16(self.cfg, x, w["centroids"], self.bias, self._fp8w, self.idx,
+                               self.gates, self.counts, out, self._ws, stream)
+        elif self.norm_w is not None and self.fp8:
             _lib.forward_fp8_prenorm(self.cfg, x, self.norm_w, self.norm_eps, w["centroids"],
                                      self.bias, self._fp8w, self.idx, self.gates, self.counts,
                                      out, self._ws, stream)

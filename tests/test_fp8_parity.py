@@ -221,7 +221,7 @@ def test_fp8_bias_update_steps_skewed():
     cfg = small_cases()["small_fp8"].with_(name="skew_steps", T=1024)
     g, _ = gpu_inputs(cfg)
     mc = m.cfg_from_layer(cfg)
-    layer = m.MoeLayer(mc, g, device="cuda")
+    layer = m.MoeLayer(mc, g, device="cuda", fp8_path="e4m3")
     bias_o = g["bias"].cpu().numpy().copy()
     hot = None
     for step in range(8):

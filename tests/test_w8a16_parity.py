@@ -1,0 +1,221 @@
+"""GPU parity of the W8A16 form of the FP8 layer (e4m3 expert weights with
+128x128 block scales, V3 walk-through section 4.3; bf16 tokens and
+activations) against the CPU oracle, through the C ABI.
+
+The kernels dequantise each weight to bf16 (q * scale, one rounding) and
+multiply on the bf16 tensor cores with fp32 accumulation; tokens and the
+SwiGLU activations stay bf16.  The oracle runs the layer on the exact
+dequantised weights with the same bf16 tokens.  The only differences are the
+bf16 rounding of the dequantised weights and of the stored activations, so the
+bf16 bar applies: relative Frobenius 1e-2 and max-abs 3e-2 on the MoE term.
+Routing, counts and the dispatch are integer results and must be exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from moe_inputs import small_cases, get_config, make_inputs
+from oracle import moe_oracle as O
+from tests._util import MARGIN_EXCLUDE, gpu_inputs, assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+m = pytest.importorskip("mixture_experts_layer_88_b300")
+
+SMALL = [k for k, c in small_cases().items() if c.wgt == "e4m3"]
+
+
+class W8Run:
+    """Buffers and calls of the W8A16 path for one FP8 config."""
+
+    def __init__(self, cfg, g, add_residual=0):
+        self.lc = cfg
+        self.cfg = m.cfg_from_layer(cfg)
+        self.cfg.add_residual = add_residual
+        self.c16 = m.bf16_layout(self.cfg)        # row layout of dispatch / combine
+        self.g = g
+        T, K, E, S, d, I = cfg.T, cfg.K, cfg.E, cfg.S, cfg.d, cfg.I
+        dev = "cuda"
+        R = T * K + S * T
+        self.idx = torch.full((T, K), -1, dtype=torch.int32, device=dev)
+        self.gates = torch.zeros((T, K), dtype=torch.float32, device=dev)
+        self.counts = torch.full((E,), -1, dtype=torch.int32, device=dev)
+        self.offsets = torch.full((E + 1,), -1, dtype=torch.int32, device=dev)
+        self.perm = torch.full((T * K,), -1, dtype=torch.int32, device=dev)
+        self.pos = torch.full((T, K), -1, dtype=torch.int32, device=dev)
+        self.xp = torch.zeros((T * K, d), dtype=torch.bfloat16, device=dev)
+        self.act = torch.zeros((R, I), dtype=torch.bfloat16, device=dev)
+        self.y = torch.zeros((R, d), dtype=torch.bfloat16, device=dev)
+        self.out = torch.zeros((T, d), dtype=torch.bfloat16, device=dev)
+        self.w = m.fp8_weights(g)
+        self.ws_fwd = m.alloc_workspace(self.cfg, m.MOE_WS_FORWARD_W8A16)
+        self.ws = {w: m.alloc_workspace(self.c16, w) for w in
+                   (m.MOE_WS_ROUTE, m.MOE_WS_DISPATCH, m.MOE_WS_EXPERTS)}
+
+    def forward(self, out=None):
+        g = self.g
+        m.forward_w8a16(self.cfg, g["x"], g["centroids"], g["bias"], self.w, self.idx, self.gates,
+                        self.counts, self.out if out is None else out, self.ws_fwd)
+
+    def stepwise(self):
+        g = self.g
+        m.route(self.c16, g["x"], g["centroids"], g["bias"], self.idx, self.gates,
+                self.ws[m.MOE_WS_ROUTE])
+        m.dispatch(self.c16, g["x"], self.idx, self.counts, self.offsets, self.xp, self.perm,
+                   self.pos, self.ws[m.MOE_WS_DISPATCH])
+        m.experts_w8a16(self.cfg, self.xp, g["x"], self.offsets, self.w, self.act, self.y,
+                        self.ws[m.MOE_WS_EXPERTS])
+        m.combine(self.c16, self.y, self.gates, self.pos, g["x"], self.out)
+
+
+def _oracle(cfg, c, tokens=None, add_residual=0):
+    return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=add_residual,
+                       tokens=tokens, n_groups=cfg.n_groups, topk_groups=cfg.topk_groups)
+
+
+def _check(cfg, run, ref, what):
+    keep = ref["margin"] >= MARGIN_EXCLUDE
+    assert int((~keep).sum()) <= max(2, cfg.T // 50)
+    idx = run.idx.cpu().numpy()
+    np.testing.assert_array_equal(np.sort(idx, 1)[keep], np.sort(ref["idx"], 1)[keep])
+    np.testing.assert_array_equal(run.counts.cpu().numpy(),
+                                  np.bincount(idx.reshape(-1), minlength=cfg.E))
+    if keep.any():
+        assert_close(to_np(run.out)[keep], ref["delta"][keep], "bf16", what)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_w8a16_layer_parity(name):
+    cfg = small_cases()[name]
+    g, c = gpu_inputs(cfg)
+    run = W8Run(cfg, g)
+    run.forward()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    _check(cfg, run, _oracle(cfg, c), f"{name} W8A16 layer")
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_w8a16_expert_rows(name):
+    """Every routed and shared row of y against the oracle's expert FFN of
+    that row's token, on the GPU's own routing (no near-tie exclusions)."""
+    cfg = small_cases()[name]
+    g, c = gpu_inputs(cfg)
+    run = W8Run(cfg, g)
+    run.stepwise()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    offsets = run.offsets.cpu().numpy()
+    perm = run.perm.cpu().numpy()
+    y = to_np(run.y)
+    x = O._f64(c["x"])
+    T, K = cfg.T, cfg.K
+    for e in range(cfg.E):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        if rows.size == 0:
+            continue
+        toks = perm[rows]
+        want = O.swiglu_ffn(x[toks], O._expert_weight(c, "w13", e), O._expert_weight(c, "w2", e))
+        assert_close(y[rows], want, "bf16", f"{name} expert {e}")
+    for s in range(cfg.S):
+        want = O.swiglu_ffn(x, O._expert_weight(c, "ws13", s), O._expert_weight(c, "ws2", s))
+        assert_close(y[T * K + s * T:T * K + (s + 1) * T], want, "bf16", f"{name} shared {s}")
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_w8a16_stepwise_equals_forward(name):
+    cfg = small_cases()[name]
+    g, _ = gpu_inputs(cfg)
+    a = W8Run(cfg, g)
+    a.forward()
+    b = W8Run(cfg, g)
+    b.stepwise()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    assert torch.equal(a.idx, b.idx) and torch.equal(a.counts, b.counts)
+    assert torch.equal(a.out, b.out)
+
+
+def test_w8a16_residual_and_layer_object():
+    cfg = small_cases()["small_fp8"]
+    g, c = gpu_inputs(cfg)
+    layer = m.MoeLayer(m.cfg_from_layer(cfg), g, device="cuda", fp8_path="w8a16")
+    layer.cfg.add_residual = 1
+    out = layer.forward(g["x"])
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    ref = _oracle(cfg, c, add_residual=1)
+    keep = ref["margin"] >= MARGIN_EXCLUDE
+    assert_close(to_np(out)[keep], ref["out"][keep], "bf16", "W8A16 with residual")
+
+
+def test_w8a16_hot_expert_many_token_blocks():
+    """One expert chosen by every token: its group spans many token blocks."""
+    cfg = small_cases()["small_fp8"].with_(name="hot_w8", T=900, E=8, K=2)
+    g, c = gpu_inputs(cfg)
+    g["bias"] = torch.zeros(cfg.E, device="cuda")
+    g["bias"][3] = 5.0
+    c = dict(c)
+    c["bias"] = g["bias"].cpu()
+    run = W8Run(cfg, g)
+    run.forward()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    assert int(run.counts[3].item()) == cfg.T
+    _check(cfg, run, _oracle(cfg, c), "W8A16 hot expert")
+
+
+W8_EDGE = {
+    "w8_one_token": small_cases()["ragged_fp8"].with_(name="w8_one_token", T=1),
+    "w8_no_shared": small_cases()["ragged_fp8"].with_(name="w8_no_shared", S=0),
+    "w8_k_equals_e": small_cases()["ragged_fp8"].with_(name="w8_k_equals_e", E=8, K=8, T=100),
+}
+
+
+@pytest.mark.parametrize("name", list(W8_EDGE))
+def test_w8a16_edge_cases(name):
+    cfg = W8_EDGE[name]
+    g, c = gpu_inputs(cfg)
+    run = W8Run(cfg, g)
+    run.forward()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    _check(cfg, run, _oracle(cfg, c), name)
+
+
+def test_w8a16_v3_skewed_full_size_sampled():
+    """The Zipf-skewed V3 FP8 layer at full size (T=16384) through the W8A16
+    path: routing and counts on every token, outputs on a token sample."""
+    cfg = get_config("v3_skewed_fp8")
+    g = make_inputs(cfg, "cuda")
+    run = W8Run(cfg, g)
+    run.forward()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    idx = run.idx.cpu().numpy()
+    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
+    np.testing.assert_array_equal(run.counts.cpu().numpy(), counts)
+    assert counts.sum() == cfg.T * cfg.K and counts.max() >= 0.9 * cfg.T
+    assert torch.isfinite(run.out.float()).all()
+    rng = np.random.default_rng(12)
+    tok = np.sort(rng.choice(cfg.T, 24, replace=False))
+    host = {k: g[k].cpu() for k in ("x", "centroids", "bias", "ws13", "ws13_scale", "ws2",
+                                    "ws2_scale")}
+
+    class _PerExpert:
+        def __init__(self, t):
+            self.t = t
+            self.shape = t.shape
+
+        def __getitem__(self, e):
+            return self.t[int(e)].cpu()
+
+    for k in ("w13", "w13_scale", "w2", "w2_scale"):
+        host[k] = _PerExpert(g[k])
+    ref = _oracle(cfg, host, tokens=tok)
+    keep = ref["margin"] >= MARGIN_EXCLUDE
+    np.testing.assert_array_equal(np.sort(idx[tok], 1)[keep], np.sort(ref["idx"], 1)[keep])
+    got = to_np(run.out[torch.as_tensor(tok, device="cuda")])
+    assert_close(got[keep], ref["delta"][keep], "bf16", "C3 W8A16 sampled tokens")
