@@ -133,3 +133,29 @@ def test_prenorm_workspace_and_argument_errors():
     assert lib.moe_forward_prenorm(ctypes.byref(f8), *args, 256, 1 << 40, P) == 2
     assert lib.moe_forward_fp8_prenorm(ctypes.byref(b), 16, 16, 1e-6, 16, 16, P, 256, 256,
                                        256, 16, 256, 1 << 40, P) == 1
+
+
+def test_w8a16_workspace_and_argument_errors():
+    c = m.make_cfg(16384, 7168, 256, 8, 1, 2048)
+    c.wgt_dtype = m.MOE_E4M3
+    # the W8A16 forward uses the bf16 layer's row layout
+    v = m.bf16_layout(c)
+    assert v.wgt_dtype == m.MOE_BF16 and c.wgt_dtype == m.MOE_E4M3
+    assert m.workspace_size(c, m.MOE_WS_FORWARD_W8A16) == m.workspace_size(v, m.MOE_WS_FORWARD)
+    assert m.workspace_size(v, m.MOE_WS_FORWARD_W8A16) == 0      # bf16 layers: not an FP8 path
+    lib = L.lib()
+    P = None
+    b = _cfg()
+    f8 = _cfg(wgt_dtype=m.MOE_E4M3)
+    w = L.Fp8Weights(16, 16, 16, 16, 16, 16, 16, 16)
+    # bf16 layers are rejected, missing weights and small workspaces too
+    assert lib.moe_forward_w8a16(ctypes.byref(b), 16, 16, 256, ctypes.byref(w), 256, 256, 256,
+                                 16, 256, 1 << 40, P) == 1
+    assert lib.moe_forward_w8a16(ctypes.byref(f8), 16, 16, 256, None, 256, 256, 256, 16, 256,
+                                 1 << 40, P) == 1
+    assert lib.moe_forward_w8a16(ctypes.byref(f8), 16, 16, 256, ctypes.byref(w), 256, 256, 256,
+                                 16, 256, 64, P) == 3
+    assert lib.moe_experts_w8a16(ctypes.byref(f8), 16, 16, 256, ctypes.byref(w), 16, 16, 256, 64,
+                                 P) == 3
+    assert lib.moe_experts_w8a16(ctypes.byref(_cfg(T=0, wgt_dtype=m.MOE_E4M3)), P, P, P, None, P,
+                                 P, P, 0, P) == 0
