@@ -38,6 +38,11 @@
 //               16-byte stores; then one arrival per warp on the even CTA's
 //               "tmem empty" barrier
 //
+// The W8 variant (FP8 layers' e4m3 weights, bf16 tokens) adds eight
+// dequantisation warps (warps 10..17): they turn each K step of raw e4m3
+// weight boxes into bf16 in TMEM, and the MMAs read A from there (see the
+// W8_* constants below).
+//
 // Every barrier wait is bounded: after `timeout_ns` without progress the CTA
 // raises an abort flag, lets the TMA loads it issued land, waits for its own
 // MMAs, frees TMEM, sets the device error word and returns.

@@ -132,12 +132,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tma
       : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads of them (TMA, tensor cores).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Four 8x8 b16 matrices stored transposed: register i of thread t holds
 // elements (t/4, 2(t%4)) (low half) and (t/4, 2(t%4)+1) of matrix i; thread
 // 8i+j gives the shared address of row j of stored matrix i, which receives
@@ -340,15 +334,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&a)[16], uint32_t (&b)[16
                  "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
                  "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]),
                  "+r"(b[14]), "+r"(b[15])
-               :
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_ld1(uint32_t (&a)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
-                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
-                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
                :
                : "memory");
 }
