@@ -300,6 +300,8 @@ def main():
     ap.add_argument("--fp8-path", default="e4m3", choices=["e4m3", "w8a16"],
                     help="FP8 layers: e4m3 x e4m3 with fp32 promotion every 128 K (e4m3) or "
                          "e4m3 weights dequantised to bf16 on the fly (w8a16)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the step from a CUDA graph captured after the warm-up")
     ap.add_argument("--prenorm", action="store_true",
                     help="the layer behind its RMSNorm: h = x + MoE(RMSNorm(x))")
     ap.add_argument("--override", default="",
@@ -338,6 +340,14 @@ def main():
         layer.step(x, out)
     torch.cuda.synchronize()
     assert m.get_status() == 0, "device error during warm-up"
+    run_step = lambda: layer.step(x, out)  # noqa: E731
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.step(x, out)
+        graph.replay()
+        torch.cuda.synchronize()
+        run_step = graph.replay
     m.trace_enable(True)
     m.trace_read_all()
     _barrier(dist, device)
@@ -346,11 +356,18 @@ def main():
     with ClockSampler(local) as clk:
         ev0.record(stream)
         for _ in range(args.steps):
-            layer.step(x, out)
+            run_step()
         ev1.record(stream)
         torch.cuda.synchronize()
     _barrier(dist, device)
     traces = m.trace_read_all()
+    if args.graph:
+        # replayed launches bypass the library's per-launch events: take the
+        # per-kernel figures from the same number of traced eager steps
+        for _ in range(args.steps):
+            layer.step(x, out)
+        torch.cuda.synchronize()
+        traces = m.trace_read_all()
     m.trace_enable(False)
     st = m.get_status()
     ms = ev0.elapsed_time(ev1)
@@ -408,6 +425,7 @@ def main():
                    "K": cfg.K, "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
                    "parallelism": (f"data parallel x{ws}, load counts all-reduced for the "
                                    f"bias update" if ws > 1 else "one replica"),
+                   "launch": "CUDA graph replay" if args.graph else "eager stream launches",
                    "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
                          if cfg.name.startswith("v3") else "inputs larger than L2"},
         "grouped_gemm": {"tflops": round(gemm_tflops, 1) if gemm_tflops else None,

@@ -881,12 +881,31 @@ __global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, 
 
 // Grid of a persistent kernel: at most one CTA (or pair) per SM, and no more
 // clusters than can be resident at once.
+// The occupancy query runs on a kernel's first launch on a device only, so
+// later launches (and CUDA graph captures after a first eager call) make no
+// host query.
 template <typename Kern>
 int persistent_ctas(Kern kern, int cluster, size_t smem, int threads, int want) {
-  static int cached[2][64] = {{0}};
+  struct Entry {
+    const void* fn;
+    int dev, ctas;
+  };
+  static Entry cache[32] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  int& c = cached[cluster == 2 ? 1 : 0][dev < 64 ? dev : 0];
+  const void* fn = reinterpret_cast<const void*>(kern);
+  int slot = -1;
+  for (int i = 0; i < 32; ++i) {
+    if (cache[i].fn == fn && cache[i].dev == dev) { slot = i; break; }
+    if (!cache[i].fn) { slot = i; break; }
+  }
+  if (slot < 0) slot = 31;                        // more kernels x devices than slots: re-query
+  int& c = cache[slot].ctas;
+  if (cache[slot].fn != fn || cache[slot].dev != dev) {
+    cache[slot].fn = fn;
+    cache[slot].dev = dev;
+    c = 0;
+  }
   if (c == 0) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(num_sms() / cluster * cluster), 1, 1);
