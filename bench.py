@@ -472,6 +472,16 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"{args.cpu_tokens} random tokens of the {cfg.name} "
                                           f"batch through the fp64 oracle ({secs:.1f} s)"}
+        # the same sample on one core (numpy's BLAS pool limited to one thread)
+        try:
+            from threadpoolctl import threadpool_limits
+            with threadpool_limits(limits=1):
+                rate1, secs1, _ = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens,
+                                                          prenorm=args.prenorm)
+            line["cpu_baseline"]["one_core"] = {"value": round(rate1, 4), "unit": UNIT,
+                                                "seconds": round(secs1, 1)}
+        except ImportError:
+            pass
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
