@@ -241,6 +241,27 @@ def cpu_oracle_tokens_per_s(cfg, inp, n_tokens: int, seed: int = 7, prenorm: boo
     return n_tokens / dt, dt, cores
 
 
+def _one_core_oracle(cfg, inp, args):
+    try:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            rate, secs, _ = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens,
+                                                    prenorm=args.prenorm)
+        how = "BLAS pool limited to one thread"
+    except ImportError:
+        if not hasattr(os, "sched_setaffinity"):
+            return None
+        cpus = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {min(cpus)})
+        try:
+            rate, secs, _ = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens,
+                                                    prenorm=args.prenorm)
+        finally:
+            os.sched_setaffinity(0, cpus)
+        how = "process pinned to one CPU"
+    return {"value": round(rate, 4), "unit": UNIT, "seconds": round(secs, 1), "how": how}
+
+
 def run_reference(args, cfg, dist, rank, ws, device):
     """Reference arm: the CPU oracle timed on bounded token samples."""
     if rank != 0:
@@ -472,16 +493,11 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"{args.cpu_tokens} random tokens of the {cfg.name} "
                                           f"batch through the fp64 oracle ({secs:.1f} s)"}
-        # the same sample on one core (numpy's BLAS pool limited to one thread)
-        try:
-            from threadpoolctl import threadpool_limits
-            with threadpool_limits(limits=1):
-                rate1, secs1, _ = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens,
-                                                          prenorm=args.prenorm)
-            line["cpu_baseline"]["one_core"] = {"value": round(rate1, 4), "unit": UNIT,
-                                                "seconds": round(secs1, 1)}
-        except ImportError:
-            pass
+        # the same sample on one core: numpy's BLAS pool limited to one thread,
+        # or (without threadpoolctl) the process pinned to one CPU meanwhile
+        one = _one_core_oracle(cfg, inp, args)
+        if one is not None:
+            line["cpu_baseline"]["one_core"] = one
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
