@@ -21,7 +21,7 @@ Sources (DeepSeekMoE pages):
   bias is updated after every batch and takes effect for the next one;
   section 6: no token is dropped.
 
-Readings where the pages are silent (all also listed in the design doc):
+Readings where the pages are silent:
 - The top-K decision is taken on float32 keys fp32(fp32(s_i) + b_i): the pages
   fix no precision, so the decision uses the CUDA kernel's.  Equal keys go to
   the lower expert index; chosen experts are listed by descending key.
