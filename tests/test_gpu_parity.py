@@ -281,6 +281,12 @@ EDGE = {
     "no_shared": small_cases()["ragged_bf16"].with_(name="no_shared", S=0),
     "k1_many_empty": small_cases()["small_bf16"].with_(name="k1_many_empty", T=20, E=64, K=1),
     "f32_one_token": small_cases()["tiny"].with_(name="f32_one_token", T=1),
+    # the ABI's limits: E = 1024 experts (four router expert blocks, group
+    # table of 1025 groups) with K = 32 (the widest top-K), and S = 64 shared
+    # experts (64 extra groups of T rows each)
+    "e1024_k32": small_cases()["small_bf16"].with_(name="e1024_k32", T=160, d=256, E=1024,
+                                                   K=32, S=1, I=128, bias_range=0.01),
+    "s64": small_cases()["small_bf16"].with_(name="s64", T=96, d=256, E=16, K=4, S=64, I=128),
 }
 
 
