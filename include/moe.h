@@ -353,6 +353,16 @@ moe_status_t moe_forward_fp8_prenorm(const moe_cfg_t* cfg, const void* x, const 
  * (MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS) or MOE_ERR_CUDA. */
 moe_status_t moe_get_status(void* stream);
 
+/*
+ * Failure-detection self-test: launches one thread that waits, with the same
+ * bounded barrier wait every GEMM role uses, on a barrier nothing arrives on.
+ * After limit_ns (1 ns .. 1 s) the wait gives up, the kernel sets the timeout
+ * bit of the device error word and returns; the next moe_get_status() on the
+ * stream reports MOE_ERR_DEVICE_TIMEOUT (and clears it).  Nothing faults or
+ * hangs; the context stays usable.
+ */
+moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* Static text for a status code. */
 const char* moe_status_string(moe_status_t st);
 

@@ -30,7 +30,7 @@ SYMBOLS = ["moe_workspace_size", "moe_check_cfg", "moe_route", "moe_dispatch", "
            "moe_combine", "moe_update_bias", "moe_forward", "moe_fp8_rows", "moe_dispatch_fp8",
            "moe_experts_fp8", "moe_forward_fp8", "moe_rmsnorm", "moe_forward_prenorm",
            "moe_forward_fp8_prenorm", "moe_experts_w8a16", "moe_forward_w8a16",
-           "moe_get_status",
+           "moe_selftest_wait_timeout", "moe_get_status",
            "moe_status_string", "moe_trace_enable", "moe_trace_read", "moe_version"]
 
 
@@ -93,6 +93,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_experts_w8a16": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, SZ, P]),
         "moe_forward_w8a16": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, P, P,
                                     SZ, P]),
+        "moe_selftest_wait_timeout": (I32, [ctypes.c_uint64, P]),
         "moe_get_status": (I32, [P]),
         "moe_status_string": (ctypes.c_char_p, [I32]),
         "moe_trace_enable": (I32, [I32]),
@@ -286,6 +287,12 @@ def forward_w8a16(cfg, x, centroids, bias, weights: Fp8Weights, idx, gates, coun
                                    ctypes.byref(weights), _p(idx), _p(gates), _p(counts),
                                    _p(out), _p(ws), ws.numel(), _stream(stream)),
            "moe_forward_w8a16")
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None):
+    """Runs out one bounded device wait after limit_ns; see include/moe.h."""
+    _check(lib().moe_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def get_status(stream=None) -> int:

@@ -888,6 +888,11 @@ moe_status_t moe_forward_fp8(const moe_cfg_t* cfg, const void* x, const void* ce
   return do_forward_fp8(c, x, x, centroids, bias, w, idx, gates, counts, out, ws, st);
 }
 
+moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return MOE_ERR_INVALID_ARG;
+  return launch_wait_timeout_selftest(limit_ns, static_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_get_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;

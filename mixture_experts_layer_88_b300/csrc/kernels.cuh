@@ -43,6 +43,10 @@ moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, co
 moe_status_t launch_rmsnorm(int act_dtype, const void* x, const float* w, float eps, int T, int d,
                             void* xn, float* inv_rms, cudaStream_t stream);
 
+// one bounded wait that runs out after limit_ns: the device error word gets
+// the timeout bit (failure-detection self-test)
+moe_status_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
 moe_status_t launch_update_bias(const int32_t* counts, float* bias, float* stats, int E, int T,
                                 int K, float gamma, cudaStream_t stream);
 

@@ -159,3 +159,9 @@ def test_w8a16_workspace_and_argument_errors():
                                  P) == 3
     assert lib.moe_experts_w8a16(ctypes.byref(_cfg(T=0, wgt_dtype=m.MOE_E4M3)), P, P, P, None, P,
                                  P, P, 0, P) == 0
+
+
+def test_selftest_limits_checked_before_any_launch():
+    lib = L.lib()
+    assert lib.moe_selftest_wait_timeout(0, None) == 1
+    assert lib.moe_selftest_wait_timeout(2_000_000_000, None) == 1
