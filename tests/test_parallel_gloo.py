@@ -78,3 +78,49 @@ def test_two_rank_balance_step_keeps_biases_equal():
     # and differs from what rank 0 alone would have done on its half
     alone, _ = O.update_bias(_rank_counts(0), np.full(E, 0.25, np.float32), T_LOCAL, K, 1e-3)
     assert not np.array_equal(alone, want)
+
+
+def _worker_peer_dies(rank, world, port, out):
+    """Rank 1 leaves between steps (before the count exchange); rank 0 must
+    get an error from its all-reduce within the process group's timeout
+    instead of waiting for ever."""
+    import datetime
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=10))
+    if rank == 1:
+        os._exit(0)                       # gone without a word, between steps
+    from mixture_experts_layer_88_b300 import parallel
+    counts = torch.from_numpy(_rank_counts(rank))
+    bias = torch.zeros((E,), dtype=torch.float32)
+    t0 = time.monotonic()
+    try:
+        parallel.balance_step(_Cfg(T_LOCAL), counts, bias, lambda cfg, c, b: b)
+        out[rank] = ("no error", time.monotonic() - t0)
+    except Exception as e:               # noqa: BLE001  (gloo raises RuntimeError)
+        out[rank] = (type(e).__name__, time.monotonic() - t0)
+    # the bias was not touched by a step that could not see the global load
+    out["bias_untouched"] = bool(torch.count_nonzero(bias).item() == 0)
+
+
+def test_peer_leaving_is_reported_not_waited_for():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_worker_peer_dies, args=(r, 2, port, out))
+                 for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+        alive = [p for p in procs if p.is_alive()]
+        for p in alive:
+            p.kill()
+        assert not alive, "a rank waited for a peer that had left"
+        res = dict(out)
+    kind, secs = res[0]
+    assert kind != "no error"
+    assert secs < 60
+    assert res["bias_untouched"]
