@@ -1,0 +1,41 @@
+"""Launch tracing (moe_trace_enable / moe_trace_read): every kernel a forward
+launches is recorded once per launch with its event-timed duration; nothing
+is recorded while tracing is off."""
+import pytest
+import torch
+
+from moe_inputs import small_cases
+from tests._util import gpu_inputs
+
+m = pytest.importorskip("mixture_experts_layer_88_b300")
+
+
+def test_trace_read_without_records_needs_no_gpu():
+    m.trace_enable(False)
+    assert m.trace_read_all() == []
+
+
+@pytest.mark.gpu
+def test_forward_kernels_traced_once_each():
+    cfg = small_cases()["small_bf16"]
+    g, _ = gpu_inputs(cfg)
+    layer = m.MoeLayer(m.cfg_from_layer(cfg), g, device="cuda")
+    layer.forward(g["x"])                     # first call outside the trace
+    torch.cuda.synchronize()
+    m.trace_enable(True)
+    m.trace_read_all()
+    layer.forward(g["x"])
+    layer.update_bias()
+    torch.cuda.synchronize()
+    rec = {name: (n, ms) for name, n, ms in m.trace_read_all()}
+    m.trace_enable(False)
+    for name in ("gemm_router", "router_topk", "dispatch_count", "dispatch_scan", "dispatch_rank",
+                 "dispatch_scatter", "build_groups",
+                 "gemm_gateup_swiglu", "gemm_down", "combine", "update_bias"):
+        assert name in rec, f"{name} not traced: {sorted(rec)}"
+        n, ms = rec[name]
+        assert n == 1 and ms > 0.0
+    assert m.trace_read_all() == []           # read clears the record
+    layer.forward(g["x"])                     # tracing off: nothing recorded
+    torch.cuda.synchronize()
+    assert m.trace_read_all() == []
