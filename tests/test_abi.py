@@ -165,3 +165,23 @@ def test_selftest_limits_checked_before_any_launch():
     lib = L.lib()
     assert lib.moe_selftest_wait_timeout(0, None) == 1
     assert lib.moe_selftest_wait_timeout(2_000_000_000, None) == 1
+
+
+def test_header_compiles_as_c99_and_links(tmp_path):
+    """include/moe.h is plain C: a C99 program compiles against it, links
+    libmoe.so and runs the checks that need no GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = os.path.join(root, "tests", "c", "abi_smoke.c")
+    exe = str(tmp_path / "abi_smoke")
+    libdir = os.path.dirname(L.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I",
+                    os.path.join(root, "include"), src, "-L", libdir, "-lmoe",
+                    f"-Wl,-rpath,{libdir}", "-o", exe], check=True)
+    res = subprocess.run([exe], capture_output=True, text=True)
+    assert res.returncode == 0, f"check {res.returncode} failed: {res.stdout}{res.stderr}"
+    assert "abi ok" in res.stdout
