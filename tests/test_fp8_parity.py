@@ -248,6 +248,9 @@ FP8_EDGE = {
     "fp8_k_equals_e": small_cases()["ragged_fp8"].with_(name="fp8_k_equals_e", E=8, K=8, T=100),
     "fp8_grouped": small_cases()["small_fp8"].with_(name="fp8_grouped", zipf_s=0.0, n_groups=4,
                                                     topk_groups=2),
+    # the ABI's limits: E = 1024 with K = 32 (3E padding rows in the FP8 row layout)
+    "fp8_e1024_k32": small_cases()["ragged_fp8"].with_(name="fp8_e1024_k32", T=160, d=256,
+                                                       E=1024, K=32, S=1, I=128),
 }
 
 

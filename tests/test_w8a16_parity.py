@@ -171,6 +171,8 @@ W8_EDGE = {
     "w8_one_token": small_cases()["ragged_fp8"].with_(name="w8_one_token", T=1),
     "w8_no_shared": small_cases()["ragged_fp8"].with_(name="w8_no_shared", S=0),
     "w8_k_equals_e": small_cases()["ragged_fp8"].with_(name="w8_k_equals_e", E=8, K=8, T=100),
+    "w8_e1024_k32": small_cases()["ragged_fp8"].with_(name="w8_e1024_k32", T=160, d=256, E=1024,
+                                                      K=32, S=1, I=128),
 }
 
 
