@@ -289,8 +289,11 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
   int32_t* orow = brow + (G + 1);
   int32_t* bs = orow + (G + 1);
   int32_t* bstart = bs + (G + 1);
-  // W8 tiles keep both accumulators and two weight slots in TMEM: <= 192 tokens
-  const GroupLayout lay{0, c.T * c.K, c.T, w8 ? 192 : 256};
+  // W8 tiles keep both accumulators and two weight slots in TMEM: <= 192 tokens.
+  // Small batches (decode: every group holds at most T rows) use token blocks
+  // of <= 64 and the kernels' deeper ring for streaming weights.
+  const bool small = !w8 && c.T <= 512;
+  const GroupLayout lay{0, c.T * c.K, c.T, w8 ? 192 : small ? 64 : 256};
   moe_status_t s = launch_build_groups(offsets, nullptr, c.T, c.E, c.S, lay, rows, brow, orow, bs,
                                        bstart, st);
   if (s != MOE_OK) return s;
@@ -341,7 +344,7 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
     a.w_scale[1] = c.S > 0 ? w8->ws13_scale : w8->w13_scale;
     a.scale_kb = c.d / 128;
   }
-  s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st, w8 != nullptr);
+  s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st, w8 != nullptr, small);
   if (s != MOE_OK) return s;
 
   // down: A = W2 rows (two 128-row boxes), B = activations
@@ -366,7 +369,7 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
     b.w_scale[1] = c.S > 0 ? w8->ws2_scale : w8->w2_scale;
     b.scale_kb = c.I / 128;
   }
-  return launch_gemm_tc(GM_DOWN, m2, b, grid, st, w8 != nullptr);
+  return launch_gemm_tc(GM_DOWN, m2, b, grid, st, w8 != nullptr, small);
 }
 
 moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,

@@ -212,6 +212,13 @@ constexpr int W8_MAX_BS = 192;
 static_assert(W8_STAGES * W8_STAGE_BYTES == EX_STAGES * EX_STAGE_BYTES,
               "the W8 ring fills the bf16 ring's space");
 static_assert(W8_A_COL + W8_A_SLOTS * 64 <= TMEM_COLS && 2 * W8_MAX_BS <= W8_A_COL, "TMEM");
+// Small batches (decode): token blocks of at most 64 tokens, so a CTA's token
+// rows take 4 KB; stages of 36 KB make a five-stage ring, with four stages of
+// weights in flight instead of three (the GEMMs only stream weights there).
+constexpr uint32_t SB_STAGE_BYTES = 2 * EX_A_BOX_BYTES + 32 * ROW_BYTES;   // 36 KB
+constexpr int SB_STAGES = 5;
+constexpr int SB_MAX_BS = 64;
+static_assert(SB_STAGES * SB_STAGE_BYTES <= EX_STAGES * EX_STAGE_BYTES, "ring space");
 constexpr int EX_MAX_STAGES = W8_STAGES;
 
 constexpr int ex_threads(bool w8) { return 64 + 32 * (EX_EPI_WARPS + (w8 ? W8_DQ_WARPS : 0)); }
@@ -291,14 +298,15 @@ __device__ __forceinline__ uint32_t dequant2(uint16_t q2, float sc) {
   return pack_bf16x2(f.x * sc, f.y * sc);
 }
 
-template <int MODE, bool W8>
+template <int MODE, bool W8, bool SMALL>
 __global__ void __launch_bounds__(ex_threads(W8), 1)
     expert_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr int NST = W8 ? W8_STAGES : EX_STAGES;            // operand ring stages
-  constexpr uint32_t STB = W8 ? W8_STAGE_BYTES : EX_STAGE_BYTES;
+  static_assert(!(W8 && SMALL), "one ring variant at a time");
+  constexpr int NST = W8 ? W8_STAGES : SMALL ? SB_STAGES : EX_STAGES;   // operand ring stages
+  constexpr uint32_t STB = W8 ? W8_STAGE_BYTES : SMALL ? SB_STAGE_BYTES : EX_STAGE_BYTES;
   constexpr uint32_t ACC1 = W8 ? W8_ACC1_COL : 256;           // TMEM column of acc1
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + EX_STAGES * EX_STAGE_BYTES);
   uint64_t* empty = full + EX_MAX_STAGES;
@@ -400,7 +408,7 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
             load_token_rows<true>(sa + 2 * W8_RAW_BOX_BYTES, mB, kTokBox0Pair, half, nullptr,
                                   fb, kb * BK, b_row);
           } else {
-            uint8_t* sa = smem + stage * EX_STAGE_BYTES;
+            uint8_t* sa = smem + stage * STB;
             tc::tma_load_2d_pair(sa, mA, fb, kb * BK, a_row0);
             tc::tma_load_2d_pair(sa + EX_A_BOX_BYTES, mA, fb, kb * BK, a_row1);
             load_token_rows<true>(sa + 2 * EX_A_BOX_BYTES, mB, kTokBox0Pair, half, nullptr, fb,
@@ -1021,24 +1029,33 @@ bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a
 }
 
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
-                            cudaStream_t stream, bool w8) {
+                            cudaStream_t stream, bool w8, bool small) {
   if (grid <= 0) return MOE_OK;
-  static bool attr_gu[64], attr_dn[64], attr_rt[64], attr_gu8[64], attr_dn8[64];
+  static bool attr_gu[64], attr_dn[64], attr_rt[64], attr_gu8[64], attr_dn8[64], attr_gus[64],
+      attr_dns[64];
   switch (mode) {
     case GM_GATEUP:
       if (w8)
-        return launch_persistent(expert_gemm_kernel<GM_GATEUP, true>, "gemm_w8_gateup_swiglu", 2,
-                                 ex_smem_bytes(GM_GATEUP), ex_threads(true), grid, maps, args,
-                                 stream, attr_gu8);
-      return launch_persistent(expert_gemm_kernel<GM_GATEUP, false>, "gemm_gateup_swiglu", 2,
-                               ex_smem_bytes(GM_GATEUP), ex_threads(false), grid, maps, args,
+        return launch_persistent(expert_gemm_kernel<GM_GATEUP, true, false>,
+                                 "gemm_w8_gateup_swiglu", 2, ex_smem_bytes(GM_GATEUP),
+                                 ex_threads(true), grid, maps, args, stream, attr_gu8);
+      if (small)
+        return launch_persistent(expert_gemm_kernel<GM_GATEUP, false, true>,
+                                 "gemm_gateup_swiglu", 2, ex_smem_bytes(GM_GATEUP),
+                                 ex_threads(false), grid, maps, args, stream, attr_gus);
+      return launch_persistent(expert_gemm_kernel<GM_GATEUP, false, false>, "gemm_gateup_swiglu",
+                               2, ex_smem_bytes(GM_GATEUP), ex_threads(false), grid, maps, args,
                                stream, attr_gu);
     case GM_DOWN:
       if (w8)
-        return launch_persistent(expert_gemm_kernel<GM_DOWN, true>, "gemm_w8_down", 2,
+        return launch_persistent(expert_gemm_kernel<GM_DOWN, true, false>, "gemm_w8_down", 2,
                                  ex_smem_bytes(GM_DOWN), ex_threads(true), grid, maps, args,
                                  stream, attr_dn8);
-      return launch_persistent(expert_gemm_kernel<GM_DOWN, false>, "gemm_down", 2,
+      if (small)
+        return launch_persistent(expert_gemm_kernel<GM_DOWN, false, true>, "gemm_down", 2,
+                                 ex_smem_bytes(GM_DOWN), ex_threads(false), grid, maps, args,
+                                 stream, attr_dns);
+      return launch_persistent(expert_gemm_kernel<GM_DOWN, false, false>, "gemm_down", 2,
                                ex_smem_bytes(GM_DOWN), ex_threads(false), grid, maps, args,
                                stream, attr_dn);
     case GM_ROUTER:

@@ -69,9 +69,10 @@ bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a
 // Launches a persistent grouped GEMM on at most `grid` CTAs: GATEUP and DOWN
 // on CTA pairs (clusters of two), ROUTER on single CTAs.  w8: the expert
 // weights are e4m3 (maps.a from make_tmap_e4m3) with args.w_scale block
-// scales, dequantised to bf16 in shared memory.
+// scales, dequantised to bf16 on the way to the tensor cores.  small: token
+// blocks of at most 64 tokens (decode batches), a deeper ring of smaller stages.
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
-                            cudaStream_t stream, bool w8 = false);
+                            cudaStream_t stream, bool w8 = false, bool small = false);
 
 // Tensor map of a row-major e4m3 matrix [rows, cols] read in boxes of {64
 // columns, 128 rows} with 64-byte swizzle (the dequantisation warps read it,
