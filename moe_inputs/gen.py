@@ -174,3 +174,12 @@ def make_norm_weight(cfg: LayerCfg, device="cpu", seed=None) -> torch.Tensor:
     s = cfg.seed if seed is None else seed
     g = _gen(device, s * 1000 + 7)
     return 0.5 + torch.rand((cfg.d,), generator=g, device=device, dtype=torch.float32)
+
+
+def make_dout(cfg: LayerCfg, device="cpu", seed=None) -> torch.Tensor:
+    """Gradient of a scalar loss with respect to the layer output, for the
+    backward pass: N(0, 1) per element in the activation dtype [T, d], drawn
+    slab by slab like the tokens."""
+    s = cfg.seed if seed is None else seed
+    return _normal((cfg.T, cfg.d), 1.0, _TORCH_DT[cfg.act], device, s * 1000 + 8,
+                   slab_rows=4096)

@@ -38,6 +38,13 @@ Readings where the pages are silent:
   the standard one with a per-channel weight, x * w / sqrt(mean(x^2) + eps);
   its output is held in the activation type like every stored activation, and
   the residual adds the un-normalised x.
+- Backward pass (no page writes it out; V3 walk-through, section 2.2, says the
+  bias only steers the selection): the gradients of a scalar loss whose
+  gradient with respect to the layer output is dout, by the chain rule through
+  the forward above.  The chosen experts (top-K, groups) are constants of the
+  backward, the bias gets no gradient, and the gradient reaches the centroids
+  and the tokens through the gates only (renormalisation, then Sigmoid or
+  Softmax).  Pinned by central finite differences of ``moe_layer``.
 """
 from __future__ import annotations
 
@@ -293,6 +300,115 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
 def _torch_index(tokens, ref):
     import torch
     return torch.as_tensor(tokens, device=ref.device)
+
+
+# ----------------------------------------------------------------------------
+# Backward pass: gradients of L with dL/d(out) = dout, chosen experts fixed
+# ----------------------------------------------------------------------------
+
+def swiglu_ffn_backward(u: np.ndarray, w13, w2, dy: np.ndarray):
+    """Gradients of one expert y = W2 a, a = SiLU(g) * v, [g; v] = W13 u, for
+    rows u [n, d] and output gradients dy [n, d]:
+      da = dy W2,  dW2 = dy^T a,
+      dg = da * v * SiLU'(g) with SiLU'(g) = sig(g) (1 + g (1 - sig(g))),
+      dv = da * SiLU(g),  dh = [dg, dv],  dW13 = dh^T u,  du = dh W13.
+    Returns du [n, d], dw13 [2I, d], dw2 [d, I], all fp64."""
+    w13 = _f64(w13)
+    w2 = _f64(w2)
+    I = w13.shape[0] // 2
+    h = u @ w13.T
+    g, v = h[:, :I], h[:, I:]
+    sig = 1.0 / (1.0 + np.exp(-g))
+    a = g * sig * v
+    da = dy @ w2
+    dw2 = dy.T @ a
+    dg = da * v * sig * (1.0 + g * (1.0 - sig))
+    dv = da * g * sig
+    dh = np.concatenate([dg, dv], axis=1)
+    return dh @ w13, dh.T @ u, dw2
+
+
+def router_backward(u: np.ndarray, centroids, s: np.ndarray, idx: np.ndarray,
+                    gates: np.ndarray, dgates: np.ndarray, normalize: int,
+                    score_func: int = SIGMOID):
+    """Gradients through eqs. (13)-(15) for fixed chosen experts idx.
+    Renormalised gates g_k = s_k / sum_j s_j (chosen j) give
+      ds_k = (dg_k - sum_j dg_j g_j) / sum_j s_j   (0 when the sum is 0),
+    otherwise ds_k = dg_k; experts not chosen get ds = 0.  Then
+      SIGMOID: dlogit_i = ds_i s_i (1 - s_i)
+      SOFTMAX: dlogit_i = s_i (ds_i - sum_j ds_j s_j)   (all E experts)
+    and logit_i = u . e_i gives du = dlogit C, dC = dlogit^T u.
+    Returns du [n, d], dcentroids [E, d], dlogit [n, E]."""
+    T, E = s.shape
+    ix = idx.astype(np.int64)
+    sc = np.take_along_axis(s, ix, axis=1)
+    if normalize:
+        tot = sc.sum(axis=1, keepdims=True)
+        inner = (dgates * gates).sum(axis=1, keepdims=True)
+        ds_c = np.where(tot > 0, (dgates - inner) / np.where(tot > 0, tot, 1.0), 0.0)
+    else:
+        ds_c = dgates
+    ds = np.zeros((T, E))
+    np.put_along_axis(ds, ix, ds_c, axis=1)
+    if score_func == SIGMOID:
+        dlogit = ds * s * (1.0 - s)
+    elif score_func == SOFTMAX:
+        dlogit = s * (ds - (ds * s).sum(axis=1, keepdims=True))
+    else:
+        raise ValueError("score_func")
+    C = _f64(centroids)
+    return dlogit @ C, dlogit.T @ u, dlogit
+
+
+def moe_layer_backward(inp: dict, K: int, dout, normalize: int = 1,
+                       score_func: int = SIGMOID, add_residual: int = 1,
+                       n_groups: int = 0, topk_groups: int = 0) -> dict:
+    """Backward of ``moe_layer`` (no RMSNorm in front) for all T tokens:
+    dout [T, d] is dL/d(out).  The routed term g_k FFN_k(u) gives
+      dgates[t, k] = dout_t . FFN_k(u_t),  dFFN_k = g_k dout_t,
+    the shared experts get dout_t itself, the residual passes dout_t to u_t,
+    and the router adds its term through the gates (router_backward).
+    Returns dx [T, d], dcentroids [E, d], dw13 [E, 2I, d], dw2 [E, d, I],
+    dws13 [S, 2I, d], dws2 [S, d, I], dgates [T, K], dlogit [T, E], idx,
+    gates, margin; every array fp64.  Weight gradients of experts that no
+    token chose are zero."""
+    u = _f64(inp["x"])
+    go = _f64(dout)
+    T, d = u.shape
+    idx, gates, margin, s = route(u, inp["centroids"], inp["bias"], K, score_func, normalize,
+                                  n_groups, topk_groups)
+    w13 = inp["w13"]
+    E = w13.shape[0]
+    I = w13.shape[1] // 2
+    S = inp["ws13"].shape[0]
+    dx = go.copy() if add_residual else np.zeros((T, d))
+    dw13 = np.zeros((E, 2 * I, d))
+    dw2 = np.zeros((E, d, I))
+    dws13 = np.zeros((S, 2 * I, d))
+    dws2 = np.zeros((S, d, I))
+    dgates = np.zeros((T, K))
+    for sx in range(S):
+        du, dw13_s, dw2_s = swiglu_ffn_backward(u, _expert_weight(inp, "ws13", sx),
+                                                _expert_weight(inp, "ws2", sx), go)
+        dx += du
+        dws13[sx] = dw13_s
+        dws2[sx] = dw2_s
+    for e in np.unique(idx):
+        rows, slots = np.nonzero(idx == e)
+        ue = u[rows]
+        w13e = _expert_weight(inp, "w13", int(e))
+        w2e = _expert_weight(inp, "w2", int(e))
+        ye = swiglu_ffn(ue, w13e, w2e)
+        dgates[rows, slots] = np.sum(go[rows] * ye, axis=1)
+        dye = gates[rows, slots][:, None] * go[rows]
+        du, dw13[e], dw2[e] = swiglu_ffn_backward(ue, w13e, w2e, dye)
+        np.add.at(dx, rows, du)
+    du_r, dcent, dlogit = router_backward(u, inp["centroids"], s, idx, gates, dgates,
+                                          normalize, score_func)
+    dx += du_r
+    return {"dx": dx, "dcentroids": dcent, "dw13": dw13, "dw2": dw2, "dws13": dws13,
+            "dws2": dws2, "dgates": dgates, "dlogit": dlogit, "idx": idx, "gates": gates,
+            "margin": margin}
 
 
 # ----------------------------------------------------------------------------
