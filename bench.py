@@ -297,6 +297,193 @@ def run_reference(args, cfg, dist, rank, ws, device):
 NORM_EPS = 1e-6
 
 
+TRAIN_METRIC = ("MoE-layer training tokens/s (forward + backward + bias update, 256e top-8, "
+                "T=8192, bf16)")
+
+
+def train_roofline(cfg, traces, peaks):
+    """Algorithmic work of the training step's kernels / measured launch time."""
+    T, d, E, K, S, I = cfg.T, cfg.d, cfg.E, cfg.K, cfg.S, cfg.I
+    R = T * K + S * T
+    es = 2
+    work = {
+        "gemm_gateup_h": ("TFLOP/s", 2.0 * R * d * 2 * I),
+        "gemm_down": ("TFLOP/s", 2.0 * R * I * d),
+        "gemm_dgrad_down": ("TFLOP/s", 2.0 * R * d * I),
+        "gemm_dgrad_gateup": ("TFLOP/s", 2.0 * R * 2 * I * d),
+        "gemm_wgrad_down": ("TFLOP/s", 2.0 * R * d * I),
+        "gemm_wgrad_gateup": ("TFLOP/s", 2.0 * R * 2 * I * d),
+        # bytes: each operand read once, each result written once
+        "swiglu_fwd": ("GB/s", es * 3.0 * R * I),
+        "combine_bwd": ("GB/s", es * (T * d + T * K * d + R * d) + 4.0 * T * K),
+        "swiglu_bwd": ("GB/s", es * 5.0 * R * I),
+        "dx_gather": ("GB/s", es * (R * d + 2.0 * T * d)),
+        "dcent_partial": ("GB/s", es * T * K * d + 4.0 * T * K),
+        "combine": ("GB/s", es * (R * d + 2 * T * d) + 8.0 * T * K),
+        "dispatch_scatter": ("GB/s", es * (T * d + T * K * d) + 4.0 * T * K),
+    }
+    out = {}
+    for name, launches, ms in traces:
+        if name in work and launches > 0:
+            unit, amount = work[name]
+            avg_s = ms / launches / 1e3
+            if unit == "TFLOP/s":
+                ach, peak = amount / avg_s / 1e12, peaks["bf16_tflops_sustained"]
+            else:
+                ach, peak = amount / avg_s / 1e9, peaks["hbm_gbs"]
+            out[name] = {"unit": unit, "achieved": round(ach, 2), "peak": peak,
+                         "frac": round(ach / peak, 4), "avg_ms": round(avg_s * 1e3, 4),
+                         "launches": launches, "total_ms": round(ms, 3)}
+    return out
+
+
+def cpu_oracle_train_tokens_per_s(cfg, inp, dout, n_tokens: int, seed: int = 7):
+    """The oracle's forward and backward of a few tokens of the full layer
+    (route, their K experts and the shared experts forward and backward, the
+    router's backward): tokens/s and seconds.  The whole-batch oracle
+    backward is not timed: its weight gradients alone are 68 GB in fp64."""
+    from oracle import moe_oracle as O
+    rng = np.random.default_rng(seed)
+    toks = rng.choice(cfg.T, n_tokens, replace=False)
+    host = {k: inp[k] for k in ("centroids", "bias")}
+    t0 = time.perf_counter()
+    for t in toks:
+        u = O._f64(inp["x"][int(t):int(t) + 1])
+        go = O._f64(dout[int(t):int(t) + 1])
+        idx, gates, _, s = O.route(u, host["centroids"], host["bias"], cfg.K, cfg.score_func,
+                                   cfg.normalize, cfg.n_groups, cfg.topk_groups)
+        dg = np.zeros((1, cfg.K))
+        for k in range(cfg.K):
+            e = int(idx[0, k])
+            w13, w2 = inp["w13"][e].cpu(), inp["w2"][e].cpu()
+            dg[0, k] = float(np.sum(go * O.swiglu_ffn(u, w13, w2)))
+            O.swiglu_ffn_backward(u, w13, w2, gates[:, k:k + 1] * go)
+        for sx in range(cfg.S):
+            O.swiglu_ffn_backward(u, inp["ws13"][sx].cpu(), inp["ws2"][sx].cpu(), go)
+        O.router_backward(u, host["centroids"], s, idx, gates, dg, cfg.normalize,
+                          cfg.score_func)
+    secs = time.perf_counter() - t0
+    return n_tokens / secs, secs
+
+
+def run_train(args, cfg, dist, rank, ws, device, peaks):
+    """Training step: moe_forward_train + moe_backward + moe_update_bias."""
+    import mixture_experts_layer_88_b300 as m
+    from moe_inputs import make_dout
+    inp = make_inputs(cfg, device, seed=rank)
+    dout = make_dout(cfg, device, seed=rank)
+    mc = m.cfg_from_layer(cfg)
+    state = m.alloc_train_state(mc, device)
+    grads = m.alloc_grads(mc, device)
+    ws_f = m.alloc_workspace(mc, m.MOE_WS_FORWARD_TRAIN, device)
+    ws_b = m.alloc_workspace(mc, m.MOE_WS_BACKWARD, device)
+    x = inp["x"]
+    out = torch.empty_like(x)
+    bias = inp["bias"].clone()
+    sh = cfg.S > 0
+    stream = torch.cuda.current_stream()
+
+    def step(xx=x, dd=dout):
+        m.forward_train(mc, xx, inp["centroids"], bias, inp["w13"], inp["w2"],
+                        inp["ws13"] if sh else None, inp["ws2"] if sh else None, state, out, ws_f)
+        m.backward(mc, dd, xx, inp["centroids"], inp["w13"], inp["w2"],
+                   inp["ws13"] if sh else None, inp["ws2"] if sh else None, state, grads, ws_b)
+        m.update_bias(mc, state["counts"], bias)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0, "device error during warm-up"
+    m.trace_enable(True)
+    m.trace_read_all()
+    _barrier(dist, device)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    _barrier(dist, device)
+    traces = m.trace_read_all()
+    m.trace_enable(False)
+    st = m.get_status()
+    ms_step = _max_over_ranks(dist, ev0.elapsed_time(ev1), device) / args.steps
+    value = ws * cfg.T / (ms_step / 1e3)
+
+    # end to end: tokens and output gradients in from pinned host memory, the
+    # layer output and the input gradients back, every step
+    x_h = x.cpu().pin_memory()
+    d_h = dout.cpu().pin_memory()
+    o_h = torch.empty_like(x_h).pin_memory()
+    dx_h = torch.empty_like(x_h).pin_memory()
+    xd, dd = torch.empty_like(x), torch.empty_like(dout)
+
+    def e2e_step():
+        xd.copy_(x_h, non_blocking=True)
+        dd.copy_(d_h, non_blocking=True)
+        step(xd, dd)
+        o_h.copy_(out, non_blocking=True)
+        dx_h.copy_(grads["dx"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(dist, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1), device) / args.steps
+    if rank != 0:
+        return
+    roof = train_roofline(cfg, traces, peaks)
+    gemms = [k for k in roof if k.startswith("gemm_")]
+    top = max(gemms, key=lambda k: roof[k]["total_ms"]) if gemms else None
+    R = cfg.T * cfg.K + cfg.S * cfg.T
+    flops = 6.0 * R * cfg.d * 2 * cfg.I          # forward 3 GEMM-halves, backward 6
+    gemm_ms = sum(roof[k]["total_ms"] for k in gemms) / args.steps
+    line = {
+        "metric": TRAIN_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random tokens, output gradients and random-init weights)",
+        "config": {"workload": cfg.name + "+train", "T": cfg.T, "d": cfg.d, "E": cfg.E,
+                   "K": cfg.K, "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
+                   "parallelism": "one replica" if ws == 1 else f"data parallel x{ws}",
+                   "launch": "eager stream launches",
+                   "l2": "inputs larger than L2 (weights, their gradients and the saved rows)"},
+        "grouped_gemm": {"tflops": round(flops / (gemm_ms / 1e3) / 1e12, 1),
+                         "frac_of_peak": round(flops / (gemm_ms / 1e3) / 1e12 /
+                                               peaks["bf16_tflops_sustained"], 4),
+                         "peak_kind": f"bf16 sustained, {peaks['source']}",
+                         "kernels": gemms, "ms_per_step": round(gemm_ms, 4)},
+        "roofline": ({"kernel": top, "bound": "tensor", "achieved": roof[top]["achieved"],
+                      "peak": roof[top]["peak"], "unit": "TFLOP/s", "frac": roof[top]["frac"],
+                      "traffic": dram_traffic(cfg.name + "+train", top),
+                      "peak_kind": f"bf16 sustained, {peaks['source']}"} if top else None),
+        "kernels": roof,
+        "gpu_launches": sum(t[1] for t in traces),
+        "device_status": st,
+        "clocks": clk.summary(),
+        "e2e": {"value": round(ws * cfg.T / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(2 * x.numel() * x.element_size()),
+                "d2h_bytes_per_step": int(2 * out.numel() * out.element_size()),
+                "ms_per_step": round(e2e_ms, 4)},
+    }
+    if not args.no_cpu_baseline:
+        n = max(1, args.cpu_tokens // 4)
+        rate, secs = cpu_oracle_train_tokens_per_s(cfg, inp, dout, n)
+        line["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT,
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{n} random tokens of the {cfg.name} batch, forward "
+                                          f"and backward through the fp64 oracle ({secs:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
 def _workload(cfg, args) -> str:
     w = cfg.name + ("+rmsnorm" if args.prenorm else "")
     if cfg.wgt == "e4m3":
@@ -325,6 +512,8 @@ def main():
                     help="replay the step from a CUDA graph captured after the warm-up")
     ap.add_argument("--prenorm", action="store_true",
                     help="the layer behind its RMSNorm: h = x + MoE(RMSNorm(x))")
+    ap.add_argument("--train", action="store_true",
+                    help="training step: forward with saved state + backward + bias update")
     ap.add_argument("--override", default="",
                     help="comma-separated shape overrides, e.g. T=1024,E=32 (profiling cases)")
     args = ap.parse_args()
@@ -347,6 +536,11 @@ def main():
 
     import mixture_experts_layer_88_b300 as m
     peaks = _peaks()
+    if args.train:
+        run_train(args, cfg, dist, rank, ws, device, peaks)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     inp = make_inputs(cfg, device, seed=rank)
     mc = m.cfg_from_layer(cfg)
     layer = m.MoeLayer(mc, inp, device=device,

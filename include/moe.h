@@ -16,6 +16,7 @@
  *   course sections 5, 6             bias applies to the next batch; no drops
  *   V3 section 4.1                   RMSNorm in front of the layer, eps 1e-6
  *   V3 section 4.3                   FP8: 128x128 weight blocks, 1x128 tiles
+ *   V3 section 2.2 + chain rule      training backward (moe_backward)
  *
  * Conventions for every entry point
  *   - All tensors are row-major, densely packed, in device memory, unless a
@@ -95,7 +96,9 @@ typedef enum {
   MOE_WS_EXPERTS = 2,
   MOE_WS_FORWARD = 3,
   MOE_WS_FORWARD_PRENORM = 4,  /* moe_forward_prenorm / moe_forward_fp8_prenorm */
-  MOE_WS_FORWARD_W8A16 = 5     /* moe_forward_w8a16 (FP8 layers) */
+  MOE_WS_FORWARD_W8A16 = 5,    /* moe_forward_w8a16 (FP8 layers) */
+  MOE_WS_FORWARD_TRAIN = 6,    /* moe_forward_train */
+  MOE_WS_BACKWARD = 7          /* moe_backward */
 } moe_ws_kind_t;
 
 /* Bytes of scratch that `which` needs for this cfg (0 on an invalid cfg). */
@@ -348,6 +351,81 @@ moe_status_t moe_forward_fp8_prenorm(const moe_cfg_t* cfg, const void* x, const 
                                      const moe_fp8_weights_t* w, int32_t* idx, float* gates,
                                      int32_t* counts, void* out, void* ws, size_t ws_bytes,
                                      void* stream);
+
+/*
+ * Training: a forward that keeps what the backward needs, and the backward.
+ * bf16 layers only (act_dtype = wgt_dtype = MOE_BF16); other cfgs return
+ * MOE_ERR_UNSUPPORTED.  No page writes the backward out: it is the chain rule
+ * through the forward of V3 sections 2.1 and 3.1 with the chosen experts held
+ * fixed; the balancing bias gets no gradient (V3 section 2.2: it only steers
+ * the choice) and is updated by moe_update_bias as in inference.
+ *
+ * moe_train_state_t - caller-owned device buffers written by moe_forward_train
+ * and read by moe_backward (R = T*K + S*T):
+ *   idx [T,K] int32, gates [T,K] fp32, scores [T,E] fp32 (s of every expert),
+ *   counts [E], offsets [E+1], perm_tok [T*K], pos [T,K] int32 (moe_dispatch),
+ *   xp [T*K, d] bf16 (dispatched rows), h [R, 2I] bf16 (gate | up
+ *   pre-activations of every row), act [R, I] bf16 (SiLU(gate) * up computed
+ *   from the stored h), y [R, d] bf16 (expert outputs).
+ */
+typedef struct {
+  int32_t* idx;
+  float* gates;
+  float* scores;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm_tok;
+  int32_t* pos;
+  void* xp;
+  void* h;
+  void* act;
+  void* y;
+} moe_train_state_t;
+
+/*
+ * moe_grads_t - caller-owned gradient outputs of moe_backward (overwritten):
+ *   dx [T,d] bf16, dcentroids [E,d] fp32, dw13 [E,2I,d], dw2 [E,d,I],
+ *   dws13 [S,2I,d], dws2 [S,d,I] bf16 (NULL when S == 0).  Experts that no
+ *   token chose get zero weight gradients.
+ */
+typedef struct {
+  void* dx;
+  float* dcentroids;
+  void* dw13;
+  void* dw2;
+  void* dws13;
+  void* dws2;
+} moe_grads_t;
+
+/*
+ * moe_forward_train - moe_forward that also fills `st`: the router writes
+ * every expert's score, the gate/up GEMM writes h instead of act, act =
+ * SiLU(gate) * up is formed from the stored bf16 h, then down and combine as
+ * in moe_forward.  out [T,d] as moe_forward.  ws: MOE_WS_FORWARD_TRAIN.
+ */
+moe_status_t moe_forward_train(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                               const float* bias, const void* w13, const void* w2,
+                               const void* ws13, const void* ws2, const moe_train_state_t* st,
+                               void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_backward - gradients of a loss L given dout = dL/d(out) [T,d] bf16, for
+ * the batch that moe_forward_train(st) ran on (same x, weights and cfg):
+ *   dgates[t,k] = dout_t . y[pos[t,k]];  expert e's output gradient on its
+ *   row is gates[t,k] * dout_t (shared experts: dout_t);
+ *   experts: da = dy W2, dW2 = dy^T act, [dgate, dup] = [da * up *
+ *   SiLU'(gate), da * SiLU(gate)], dW13 = [dgate, dup]^T u, du = [dgate, dup] W13;
+ *   router (V3 eqs. 13-15): ds = (dg - sum dg g) / sum s (renormalised gates,
+ *   else ds = dg), dlogit = ds s (1 - s) (Sigmoid) or s (ds - sum ds s)
+ *   (Softmax), dx += dlogit C, dC = dlogit^T u;  dx += dout (add_residual).
+ * Weight gradients are fp32 sums rounded once to bf16; dx sums its terms in
+ * fp32; the intermediate gradients (g * dout, da, [dgate, dup], the routed
+ * rows' du) are held in bf16.  ws: MOE_WS_BACKWARD.
+ */
+moe_status_t moe_backward(const moe_cfg_t* cfg, const void* dout, const void* x,
+                          const void* centroids, const void* w13, const void* w2,
+                          const void* ws13, const void* ws2, const moe_train_state_t* st,
+                          const moe_grads_t* grads, void* ws, size_t ws_bytes, void* stream);
 
 /* Waits for `stream`, then returns and clears this device's error word
  * (MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS) or MOE_ERR_CUDA. */

@@ -19,6 +19,8 @@ MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_EXPERTS, MOE_WS_FORWARD = 0, 1, 2, 3
 MOE_WS_FORWARD_PRENORM = 4
 MOE_WS_FORWARD_W8A16 = 5
+MOE_WS_FORWARD_TRAIN = 6
+MOE_WS_BACKWARD = 7
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
@@ -30,6 +32,7 @@ SYMBOLS = ["moe_workspace_size", "moe_check_cfg", "moe_route", "moe_dispatch", "
            "moe_combine", "moe_update_bias", "moe_forward", "moe_fp8_rows", "moe_dispatch_fp8",
            "moe_experts_fp8", "moe_forward_fp8", "moe_rmsnorm", "moe_forward_prenorm",
            "moe_forward_fp8_prenorm", "moe_experts_w8a16", "moe_forward_w8a16",
+           "moe_forward_train", "moe_backward",
            "moe_selftest_wait_timeout", "moe_get_status",
            "moe_status_string", "moe_trace_enable", "moe_trace_read", "moe_version"]
 
@@ -55,6 +58,22 @@ class Fp8Weights(ctypes.Structure):
                 ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
                 ("ws13", ctypes.c_void_p), ("ws13_scale", ctypes.c_void_p),
                 ("ws2", ctypes.c_void_p), ("ws2_scale", ctypes.c_void_p)]
+
+
+class TrainState(ctypes.Structure):
+    """moe_train_state_t: what moe_forward_train keeps for moe_backward."""
+    _fields_ = [("idx", ctypes.c_void_p), ("gates", ctypes.c_void_p),
+                ("scores", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("perm_tok", ctypes.c_void_p),
+                ("pos", ctypes.c_void_p), ("xp", ctypes.c_void_p), ("h", ctypes.c_void_p),
+                ("act", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+class Grads(ctypes.Structure):
+    """moe_grads_t: gradient outputs of moe_backward."""
+    _fields_ = [("dx", ctypes.c_void_p), ("dcentroids", ctypes.c_void_p),
+                ("dw13", ctypes.c_void_p), ("dw2", ctypes.c_void_p),
+                ("dws13", ctypes.c_void_p), ("dws2", ctypes.c_void_p)]
 
 
 class KernelTime(ctypes.Structure):
@@ -93,6 +112,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_experts_w8a16": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, SZ, P]),
         "moe_forward_w8a16": (I32, [cfgp, P, P, P, ctypes.POINTER(Fp8Weights), P, P, P, P, P,
                                     SZ, P]),
+        "moe_forward_train": (I32, [cfgp, P, P, P, P, P, P, P, ctypes.POINTER(TrainState), P, P,
+                                    SZ, P]),
+        "moe_backward": (I32, [cfgp, P, P, P, P, P, P, P, ctypes.POINTER(TrainState),
+                               ctypes.POINTER(Grads), P, SZ, P]),
         "moe_selftest_wait_timeout": (I32, [ctypes.c_uint64, P]),
         "moe_get_status": (I32, [P]),
         "moe_status_string": (ctypes.c_char_p, [I32]),
@@ -287,6 +310,65 @@ def forward_w8a16(cfg, x, centroids, bias, weights: Fp8Weights, idx, gates, coun
                                    ctypes.byref(weights), _p(idx), _p(gates), _p(counts),
                                    _p(out), _p(ws), ws.numel(), _stream(stream)),
            "moe_forward_w8a16")
+
+
+TRAIN_KEYS = ("idx", "gates", "scores", "counts", "offsets", "perm_tok", "pos", "xp", "h", "act",
+              "y")
+GRAD_KEYS = ("dx", "dcentroids", "dw13", "dw2", "dws13", "dws2")
+
+
+def alloc_train_state(cfg: MoeCfg, device="cuda") -> dict:
+    """Device buffers of moe_train_state_t for cfg (bf16 layer)."""
+    T, K, E, S, d, I = cfg.T, cfg.K, cfg.E, cfg.S, cfg.d, cfg.I
+    R = T * K + S * T
+    i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+    return {"idx": torch.empty((T, K), dtype=i32, device=device),
+            "gates": torch.empty((T, K), dtype=f32, device=device),
+            "scores": torch.empty((T, E), dtype=f32, device=device),
+            "counts": torch.empty((E,), dtype=i32, device=device),
+            "offsets": torch.empty((E + 1,), dtype=i32, device=device),
+            "perm_tok": torch.empty((T * K,), dtype=i32, device=device),
+            "pos": torch.empty((T, K), dtype=i32, device=device),
+            "xp": torch.empty((T * K, d), dtype=bf, device=device),
+            "h": torch.empty((R, 2 * I), dtype=bf, device=device),
+            "act": torch.empty((R, I), dtype=bf, device=device),
+            "y": torch.empty((R, d), dtype=bf, device=device)}
+
+
+def alloc_grads(cfg: MoeCfg, device="cuda") -> dict:
+    """Gradient buffers of moe_grads_t for cfg (bf16 layer)."""
+    T, E, S, d, I = cfg.T, cfg.E, cfg.S, cfg.d, cfg.I
+    bf = torch.bfloat16
+    return {"dx": torch.empty((T, d), dtype=bf, device=device),
+            "dcentroids": torch.empty((E, d), dtype=torch.float32, device=device),
+            "dw13": torch.empty((E, 2 * I, d), dtype=bf, device=device),
+            "dw2": torch.empty((E, d, I), dtype=bf, device=device),
+            "dws13": torch.empty((S, 2 * I, d), dtype=bf, device=device),
+            "dws2": torch.empty((S, d, I), dtype=bf, device=device)}
+
+
+def _struct(cls, keys, bufs):
+    def g(k):
+        t = bufs.get(k)
+        return None if t is None or t.numel() == 0 else t.data_ptr()
+    return cls(*[g(k) for k in keys])
+
+
+def forward_train(cfg, x, centroids, bias, w13, w2, ws13, ws2, state: dict, out, ws,
+                  stream=None):
+    st = _struct(TrainState, TRAIN_KEYS, state)
+    _check(lib().moe_forward_train(ctypes.byref(cfg), _p(x), _p(centroids), _p(bias), _p(w13),
+                                   _p(w2), _p(ws13), _p(ws2), ctypes.byref(st), _p(out), _p(ws),
+                                   ws.numel(), _stream(stream)), "moe_forward_train")
+
+
+def backward(cfg, dout, x, centroids, w13, w2, ws13, ws2, state: dict, grads: dict, ws,
+             stream=None):
+    st = _struct(TrainState, TRAIN_KEYS, state)
+    gr = _struct(Grads, GRAD_KEYS, grads)
+    _check(lib().moe_backward(ctypes.byref(cfg), _p(dout), _p(x), _p(centroids), _p(w13),
+                              _p(w2), _p(ws13), _p(ws2), ctypes.byref(st), ctypes.byref(gr),
+                              _p(ws), ws.numel(), _stream(stream)), "moe_backward")
 
 
 def selftest_wait_timeout(limit_ns: int, stream=None):

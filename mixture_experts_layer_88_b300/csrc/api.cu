@@ -227,7 +227,7 @@ P* at(void* base, size_t off) {
 
 moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
                       const float* bias, int32_t* idx, float* gates, void* ws,
-                      cudaStream_t st) {
+                      cudaStream_t st, float* scores = nullptr) {
   if (c.act_dtype == MOE_BF16) {
     const RouterPlan p = router_plan(c);
     float* partial = static_cast<float*>(ws);
@@ -258,7 +258,7 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
     moe_status_t s = launch_gemm_tc(GM_ROUTER, maps, a, grid, st);
     if (s != MOE_OK) return s;
     return launch_topk(partial, p.splits, a.out_split_stride, bias, c.T, c.E, c.K, c.score_func,
-                       c.normalize, c.n_groups, c.topk_groups, idx, gates, st);
+                       c.normalize, c.n_groups, c.topk_groups, idx, gates, st, scores);
   }
   float* logits = static_cast<float*>(ws);
   moe_status_t s = launch_logits_f32(static_cast<const float*>(x),
@@ -266,15 +266,18 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
                                      st);
   if (s != MOE_OK) return s;
   return launch_topk(logits, 1, 0, bias, c.T, c.E, c.K, c.score_func, c.normalize, c.n_groups,
-                     c.topk_groups, idx, gates, st);
+                     c.topk_groups, idx, gates, st, scores);
 }
 
 // w8 (an FP8 layer's e4m3 weights and block scales) replaces w13..ws2: the
 // same bf16 GEMMs with the weights dequantised in shared memory.
+// h (training forward, bf16 weights only): the gate/up GEMM writes the
+// pre-activations h [R, 2I] and act is formed from them.
 moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
                         const int32_t* offsets, const void* w13, const void* w2,
                         const void* ws13, const void* ws2, void* act, void* y, void* ws,
-                        cudaStream_t st, const moe_fp8_weights_t* w8 = nullptr) {
+                        cudaStream_t st, const moe_fp8_weights_t* w8 = nullptr,
+                        void* h = nullptr) {
   if (c.act_dtype != MOE_BF16) {
     return launch_experts_f32(static_cast<const float*>(xp), static_cast<const float*>(x),
                               offsets, static_cast<const float*>(w13),
@@ -344,7 +347,15 @@ moe_status_t do_experts(const moe_cfg_t& c, const void* xp, const void* x,
     a.w_scale[1] = c.S > 0 ? w8->ws13_scale : w8->w13_scale;
     a.scale_kb = c.d / 128;
   }
-  s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st, w8 != nullptr, small);
+  if (h) {
+    a.out = h;
+    a.out_ld = 2 * c.I;
+    s = launch_gemm_tc(GM_GATEUP_H, m1, a, grid, st, false, small);
+    if (s != MOE_OK) return s;
+    s = launch_swiglu_fwd(h, act, R, c.I, st);
+  } else {
+    s = launch_gemm_tc(GM_GATEUP, m1, a, grid, st, w8 != nullptr, small);
+  }
   if (s != MOE_OK) return s;
 
   // down: A = W2 rows (two 128-row boxes), B = activations
@@ -436,6 +447,227 @@ moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,
   return launch_fp8_gemm(GM_DOWN, m2, b, st);
 }
 
+// ---------------------------------------------------------------- training
+
+size_t forward_train_ws(const moe_cfg_t& c) {
+  return align_up(route_ws(c), 256) + align_up(dispatch_ws(c), 256) +
+         align_up(experts_ws(c), 256);
+}
+
+// Backward workspace: the padded row layout (see backward.cu), the input-
+// gradient GEMMs' group table, and the intermediate gradients.
+struct BackwardLayout {
+  size_t tab, dg, dlk, dlrow, dl, dxr, part, dy, dact, dh, dxp, total;
+  long long rows_max;
+  int max_blocks;
+};
+
+BackwardLayout backward_layout(const moe_cfg_t& c) {
+  BackwardLayout L{};
+  const size_t TK = static_cast<size_t>(c.T) * c.K;
+  const int G = c.E + c.S;
+  L.rows_max = static_cast<long long>(TK) + 15LL * c.E +
+               static_cast<long long>(c.S) * round_up(c.T, 16);
+  L.max_blocks = static_cast<int>(TK / 256) + c.E + 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return o;
+  };
+  L.tab = take((static_cast<size_t>(c.E) + 1 + 5 * (static_cast<size_t>(G) + 1) + 4) *
+               sizeof(int32_t));
+  L.dg = take(TK * sizeof(float));
+  const bool sm = c.score_func == MOE_SCORE_SOFTMAX;
+  L.dlk = take(sm ? 0 : TK * sizeof(float));
+  L.dlrow = take(sm ? 0 : TK * sizeof(float));
+  L.dl = take(sm ? static_cast<size_t>(c.T) * c.E * sizeof(float) : 0);
+  L.dxr = take(sm ? static_cast<size_t>(c.T) * c.d * sizeof(float) : 0);
+  L.part = take((sm ? static_cast<size_t>(ceil_div(c.T, 256)) * c.E
+                    : static_cast<size_t>(L.max_blocks)) *
+                c.d * sizeof(float));
+  const size_t R = static_cast<size_t>(L.rows_max);
+  L.dy = take(R * c.d * 2);
+  L.dact = take(R * c.I * 2);
+  L.dh = take(R * 2 * c.I * 2);
+  L.dxp = take(R * c.d * 2);
+  L.total = off;
+  return L;
+}
+
+bool is_bf16(const moe_cfg_t& c) {
+  return c.act_dtype == MOE_BF16 && c.wgt_dtype == MOE_BF16;
+}
+
+moe_status_t do_forward_train(const moe_cfg_t& c, const void* x, const void* centroids,
+                              const float* bias, const void* w13, const void* w2,
+                              const void* ws13, const void* ws2, const moe_train_state_t& t,
+                              void* out, void* ws, cudaStream_t st) {
+  const size_t o_disp = align_up(route_ws(c), 256);
+  const size_t o_exp = o_disp + align_up(dispatch_ws(c), 256);
+  moe_status_t s;
+  if ((s = do_route(c, x, centroids, bias, t.idx, t.gates, ws, st, t.scores)) != MOE_OK) return s;
+  if ((s = launch_dispatch(x, static_cast<size_t>(c.d) * 2, t.idx, c.T, c.K, c.E, t.counts,
+                           t.offsets, t.xp, t.perm_tok, t.pos, at<int32_t>(ws, o_disp), st)) !=
+      MOE_OK)
+    return s;
+  if ((s = do_experts(c, t.xp, x, t.offsets, w13, w2, ws13, ws2, t.act, t.y, at<void>(ws, o_exp),
+                      st, nullptr, t.h)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, t.y, t.gates, t.pos, x, out, c.T, c.K, c.S, c.d,
+                        static_cast<long long>(c.T) * c.K, c.T, c.add_residual, st);
+}
+
+// Weight operand of an input-gradient GEMM: the group's [K, M] matrix read
+// MN-major in boxes of 64 rows x 64 columns; token operand as the forward's.
+bool make_dgrad_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a1,
+                     uint64_t a1_rows, uint64_t a_cols, const void* b, uint64_t b_rows,
+                     uint64_t b_cols) {
+  if (!make_tmap_bf16(&m->a[0], a0, a0_rows, a_cols, 64)) return false;
+  if (a1) {
+    if (!make_tmap_bf16(&m->a[1], a1, a1_rows, a_cols, 64)) return false;
+  } else {
+    m->a[1] = m->a[0];
+  }
+  for (int i = 0; i < kTokBoxes; ++i) {
+    if (!make_tmap_bf16(&m->b[0][i], b, b_rows, b_cols, kTokBox0Pair << i)) return false;
+    m->b[1][i] = m->b[0][i];
+  }
+  return true;
+}
+
+moe_status_t do_backward(const moe_cfg_t& c, const void* dout, const void* x,
+                         const void* centroids, const void* w13, const void* w2,
+                         const void* ws13, const void* ws2, const moe_train_state_t& t,
+                         const moe_grads_t& gr, void* ws, cudaStream_t st) {
+  const BackwardLayout L = backward_layout(c);
+  const int G = c.E + c.S;
+  int32_t* poff = at<int32_t>(ws, L.tab);
+  int32_t* rows = poff + (c.E + 1);
+  int32_t* brow = rows + (G + 1);
+  int32_t* orow = brow + (G + 1);
+  int32_t* bs = orow + (G + 1);
+  int32_t* bstart = bs + (G + 1);
+  int32_t* counters = bstart + (G + 1);
+  float* dg = at<float>(ws, L.dg);
+  void* dy = at<void>(ws, L.dy);
+  void* dact = at<void>(ws, L.dact);
+  void* dh = at<void>(ws, L.dh);
+  void* dxp = at<void>(ws, L.dxp);
+  const bool sm = c.score_func == MOE_SCORE_SOFTMAX;
+  const long long TK = static_cast<long long>(c.T) * c.K;
+  const long long R = TK + static_cast<long long>(c.S) * c.T;
+  const bool sh = c.S > 0;
+  moe_status_t s;
+  if ((s = launch_build_bwd_groups(t.counts, c.T, c.E, c.S, poff, rows, brow, orow, bs, bstart,
+                                   counters, st)) != MOE_OK)
+    return s;
+  if ((s = launch_combine_bwd(dout, t.y, t.gates, t.idx, t.perm_tok, t.counts, t.offsets, poff,
+                              c.T, c.K, c.E, c.S, c.d, L.rows_max, dy, dg, st)) != MOE_OK)
+    return s;
+  if ((s = launch_router_bwd(dg, t.gates, t.idx, t.scores, t.pos, c.T, c.E, c.K, c.score_func,
+                             c.normalize, at<float>(ws, L.dlk), at<float>(ws, L.dlrow),
+                             at<float>(ws, L.dl), st)) != MOE_OK)
+    return s;
+  const int grid = num_sms();
+  GemmArgs a{};
+  a.gt = GroupTable{rows, brow, orow, bs, bstart};
+  a.G = G;
+  a.E = c.E;
+  a.k_splits = 1;
+  a.a1_off = 256;
+  a.status = device_status_word();
+  a.timeout_ns = kWaitTimeoutNs;
+  // da = dy W2: W2 of each group as [d rows (K), I columns (M)]
+  GemmMaps m1;
+  if (!make_dgrad_maps(&m1, w2, static_cast<uint64_t>(c.E) * c.d, sh ? ws2 : nullptr,
+                       static_cast<uint64_t>(c.S) * c.d, c.I, dy, L.rows_max, c.d))
+    return MOE_ERR_CUDA;
+  a.m_blocks = ceil_div(c.I, 512);
+  a.a_rows_per_group = c.d;
+  a.k_blocks = c.d / 64;
+  a.k_per_split = a.k_blocks;
+  a.out_ld = c.I;
+  a.out_cols = c.I;
+  a.out = dact;
+  a.tile_counter = counters + 0;
+  if ((s = launch_gemm_tc(GM_DGRAD, m1, a, grid, st, false, false, "gemm_dgrad_down")) != MOE_OK)
+    return s;
+  if ((s = launch_swiglu_bwd(dact, t.h, t.counts, t.offsets, poff, c.T, c.K, c.E, c.S, c.I,
+                             L.rows_max, dh, st)) != MOE_OK)
+    return s;
+  // du = dh W13: W13 of each group as [2I rows (K), d columns (M)]
+  GemmMaps m2;
+  if (!make_dgrad_maps(&m2, w13, static_cast<uint64_t>(c.E) * 2 * c.I, sh ? ws13 : nullptr,
+                       static_cast<uint64_t>(c.S) * 2 * c.I, c.d, dh, L.rows_max, 2 * c.I))
+    return MOE_ERR_CUDA;
+  a.m_blocks = ceil_div(c.d, 512);
+  a.a_rows_per_group = 2 * c.I;
+  a.k_blocks = 2 * c.I / 64;
+  a.k_per_split = a.k_blocks;
+  a.out_ld = c.d;
+  a.out_cols = c.d;
+  a.out = dxp;
+  a.tile_counter = counters + 1;
+  if ((s = launch_gemm_tc(GM_DGRAD, m2, a, grid, st, false, false, "gemm_dgrad_gateup")) !=
+      MOE_OK)
+    return s;
+  if (sm && (s = launch_router_dx_dense(at<float>(ws, L.dl), centroids, c.T, c.E, c.d,
+                                        at<float>(ws, L.dxr), st)) != MOE_OK)
+    return s;
+  if ((s = launch_dx(dxp, t.pos, t.idx, t.offsets, poff, sm ? nullptr : at<float>(ws, L.dlk),
+                     centroids, sm ? at<float>(ws, L.dxr) : nullptr, dout, gr.dx, c.T, c.K, c.E,
+                     c.S, c.d, c.add_residual, st)) != MOE_OK)
+    return s;
+  s = sm ? launch_dcent_dense(at<float>(ws, L.dl), x, c.T, c.E, c.d, at<float>(ws, L.part),
+                              gr.dcentroids, st)
+         : launch_dcent_sparse(at<float>(ws, L.dlrow), t.xp, t.counts, t.offsets, bs, bstart,
+                               c.E, c.d, L.max_blocks, at<float>(ws, L.part), gr.dcentroids, st);
+  if (s != MOE_OK) return s;
+  // dW2 = dy^T act (M = d, N = I); dW13 = dh^T u (M = 2I, N = d)
+  WgradArgs w{};
+  w.counts = t.counts;
+  w.offsets = t.offsets;
+  w.poff = poff;
+  w.E = c.E;
+  w.S = c.S;
+  w.T = c.T;
+  w.T16 = round_up(c.T, 16);
+  w.status = device_status_word();
+  w.timeout_ns = kWaitTimeoutNs;
+  WgradMaps wm;
+  if (!make_tmap_bf16(&wm.a, dy, L.rows_max, c.d, 64) ||
+      !make_tmap_bf16(&wm.b[0], t.act, R, c.I, 64))
+    return MOE_ERR_CUDA;
+  wm.b[1] = wm.b[0];
+  w.b_sh0 = static_cast<int>(TK);
+  w.b_shs = c.T;
+  w.M = c.d;
+  w.N = c.I;
+  w.m_blocks = ceil_div(c.d, 256);
+  w.n_blocks = ceil_div(c.I, 256);
+  w.out_gstride = static_cast<long long>(c.d) * c.I;
+  w.out_routed = gr.dw2;
+  w.out_shared = sh ? gr.dws2 : gr.dw2;
+  w.tile_counter = counters + 2;
+  if ((s = launch_wgrad(wm, w, st, "gemm_wgrad_down")) != MOE_OK) return s;
+  if (!make_tmap_bf16(&wm.a, dh, L.rows_max, 2 * c.I, 64) ||
+      !make_tmap_bf16(&wm.b[0], t.xp, TK, c.d, 64) ||
+      !make_tmap_bf16(&wm.b[1], x, c.T, c.d, 64))
+    return MOE_ERR_CUDA;
+  w.b_sh0 = 0;
+  w.b_shs = 0;
+  w.M = 2 * c.I;
+  w.N = c.d;
+  w.m_blocks = ceil_div(2 * c.I, 256);
+  w.n_blocks = ceil_div(c.d, 256);
+  w.out_gstride = static_cast<long long>(2 * c.I) * c.d;
+  w.out_routed = gr.dw13;
+  w.out_shared = sh ? gr.dws13 : gr.dw13;
+  w.tile_counter = counters + 3;
+  return launch_wgrad(wm, w, st, "gemm_wgrad_gateup");
+}
+
 moe_status_t check_fp8_weights(const moe_cfg_t& c, const moe_fp8_weights_t* w) {
   if (!w) return MOE_ERR_INVALID_ARG;
   if (!w->w13 || !w->w2 || !w->w13_scale || !w->w2_scale) return MOE_ERR_INVALID_ARG;
@@ -505,6 +737,8 @@ size_t moe_workspace_size(const moe_cfg_t* cfg, int32_t which) {
     case MOE_WS_FORWARD: return forward_layout(c).total;
     case MOE_WS_FORWARD_PRENORM: return prenorm_ws(c);
     case MOE_WS_FORWARD_W8A16: return is_fp8(c) ? forward_layout(bf16_layout(c)).total : 0;
+    case MOE_WS_FORWARD_TRAIN: return is_bf16(c) ? forward_train_ws(c) : 0;
+    case MOE_WS_BACKWARD: return is_bf16(c) ? backward_layout(c).total : 0;
     default: return 0;
   }
 }
@@ -889,6 +1123,60 @@ moe_status_t moe_forward_fp8(const moe_cfg_t* cfg, const void* x, const void* ce
   if ((s = check_fp8_weights(c, w)) != MOE_OK) return s;
   if ((s = check_ws(ws, ws_bytes, forward_layout(c).total)) != MOE_OK) return s;
   return do_forward_fp8(c, x, x, centroids, bias, w, idx, gates, counts, out, ws, st);
+}
+
+moe_status_t moe_forward_train(const moe_cfg_t* cfg, const void* x, const void* centroids,
+                               const float* bias, const void* w13, const void* w2,
+                               const void* ws13, const void* ws2, const moe_train_state_t* st,
+                               void* out, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!is_bf16(c)) return MOE_ERR_UNSUPPORTED;
+  if (!st || !st->counts) return MOE_ERR_INVALID_ARG;
+  cudaStream_t sm = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) return forward_empty(c, st->counts, sm);
+  if ((s = check_ptrs(c, {x, centroids, w13, w2, out, st->xp, st->h, st->act, st->y},
+                      {bias, st->idx, st->gates, st->scores, st->offsets, st->perm_tok,
+                       st->pos})) != MOE_OK)
+    return s;
+  if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, forward_train_ws(c))) != MOE_OK) return s;
+  return do_forward_train(c, x, centroids, bias, w13, w2, ws13, ws2, *st, out, ws, sm);
+}
+
+moe_status_t moe_backward(const moe_cfg_t* cfg, const void* dout, const void* x,
+                          const void* centroids, const void* w13, const void* w2,
+                          const void* ws13, const void* ws2, const moe_train_state_t* st,
+                          const moe_grads_t* grads, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = moe_check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_cfg_t& c = *cfg;
+  if (!is_bf16(c)) return MOE_ERR_UNSUPPORTED;
+  if (!st || !grads) return MOE_ERR_INVALID_ARG;
+  if ((s = check_ptrs(c, {grads->dw13, grads->dw2}, {grads->dcentroids})) != MOE_OK) return s;
+  if (c.S > 0 && (s = check_ptrs(c, {grads->dws13, grads->dws2, ws13, ws2}, {})) != MOE_OK)
+    return s;
+  cudaStream_t sm = static_cast<cudaStream_t>(stream);
+  const size_t E = static_cast<size_t>(c.E), S = static_cast<size_t>(c.S);
+  const size_t wsz = static_cast<size_t>(2) * c.I * c.d * 2;   // bytes of one expert's W13
+  if (c.T == 0) {   // no tokens: every gradient is zero
+    TraceScope tr(sm, "backward_empty");
+    cudaMemsetAsync(grads->dcentroids, 0, E * c.d * sizeof(float), sm);
+    cudaMemsetAsync(grads->dw13, 0, E * wsz, sm);
+    cudaMemsetAsync(grads->dw2, 0, E * wsz / 2, sm);
+    if (S > 0) {
+      cudaMemsetAsync(grads->dws13, 0, S * wsz, sm);
+      cudaMemsetAsync(grads->dws2, 0, S * wsz / 2, sm);
+    }
+    return launch_status();
+  }
+  if ((s = check_ptrs(c, {dout, x, centroids, w13, w2, grads->dx, st->xp, st->h, st->act, st->y},
+                      {st->idx, st->gates, st->scores, st->counts, st->offsets, st->perm_tok,
+                       st->pos})) != MOE_OK)
+    return s;
+  if ((s = check_ws(ws, ws_bytes, backward_layout(c).total)) != MOE_OK) return s;
+  return do_backward(c, dout, x, centroids, w13, w2, ws13, ws2, *st, *grads, ws, sm);
 }
 
 moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, void* stream) {

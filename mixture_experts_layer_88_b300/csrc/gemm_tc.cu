@@ -188,6 +188,7 @@ constexpr int EX_STAGES = 4;
 constexpr uint32_t EX_A_BOX_BYTES = 128 * ROW_BYTES;      // 16 KB: one 128-row weight box
 constexpr uint32_t EX_B_BYTES = 128 * ROW_BYTES;          // 16 KB: up to 128 token rows
 constexpr uint32_t EX_STAGE_BYTES = 2 * EX_A_BOX_BYTES + EX_B_BYTES;
+constexpr uint32_t kMnBoxBytes = 64 * ROW_BYTES;           // 8 KB: 64 K rows x 64 columns
 constexpr int EX_EPI_WARPS = 8;
 constexpr int EX_QUEUE = 4;                               // tile indices in flight
 
@@ -308,6 +309,10 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
   constexpr int NST = W8 ? W8_STAGES : SMALL ? SB_STAGES : EX_STAGES;   // operand ring stages
   constexpr uint32_t STB = W8 ? W8_STAGE_BYTES : SMALL ? SB_STAGE_BYTES : EX_STAGE_BYTES;
   constexpr uint32_t ACC1 = W8 ? W8_ACC1_COL : 256;           // TMEM column of acc1
+  // weight rows (or DGRAD: columns) of a tile: 256 gate rows with their up
+  // rows (GATEUP, GATEUP_H), or 512 (DOWN, DGRAD)
+  constexpr int kBlockW = (MODE == GM_GATEUP || MODE == GM_GATEUP_H) ? 256 : 512;
+  static_assert(MODE != GM_ROUTER && (!W8 || MODE == GM_GATEUP || MODE == GM_DOWN), "variant");
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + EX_STAGES * EX_STAGE_BYTES);
   uint64_t* empty = full + EX_MAX_STAGES;
   uint64_t* tfull = empty + EX_MAX_STAGES;
@@ -384,8 +389,7 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
       const int half = t.nmma >> 1;                // token rows this CTA loads
       // GATEUP: gate rows of this CTA and the matching up rows (+I);
       // DOWN: W2 rows of this CTA in the two 256-row halves of the block
-      const int a_row0 = gl * args.a_rows_per_group +
-                         t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128;
+      const int a_row0 = gl * args.a_rows_per_group + t.mb * kBlockW + static_cast<int>(rank) * 128;
       const int a_row1 = a_row0 + args.a1_off;
       const int b_row = __ldg(args.gt.brow + t.g) + t.tok0 + static_cast<int>(rank) * half;
       // bytes of this CTA on the even CTA's "full" barrier (W8: token rows only;
@@ -407,6 +411,19 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
             tc::tma_load_2d(sa + W8_RAW_BOX_BYTES, mA, raw_full + stage, kb * BK, a_row1);
             load_token_rows<true>(sa + 2 * W8_RAW_BOX_BYTES, mB, kTokBox0Pair, half, nullptr,
                                   fb, kb * BK, b_row);
+          } else if (MODE == GM_DGRAD) {
+            // MN-major weights: rows kb*64.. of the group's [K, M] matrix,
+            // columns of acc0 (this CTA's 128) and of acc1 (256 further), in
+            // boxes of 64 columns
+            uint8_t* sa = smem + stage * STB;
+            const int krow = gl * args.a_rows_per_group + kb * BK;
+            const int c0 = t.mb * 512 + static_cast<int>(rank) * 128;
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+              tc::tma_load_2d_pair(sa + bx * kMnBoxBytes, mA, fb, c0 + (bx >> 1) * 256 + (bx & 1) * 64,
+                                   krow);
+            load_token_rows<true>(sa + 2 * EX_A_BOX_BYTES, mB, kTokBox0Pair, half, nullptr, fb,
+                                  kb * BK, b_row);
           } else {
             uint8_t* sa = smem + stage * STB;
             tc::tma_load_2d_pair(sa, mA, fb, kb * BK, a_row0);
@@ -445,7 +462,7 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
         decode_group_tile(args, tile, t);
         if (!warp_wait<true>(tempty, tphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
         tc::tc_fence_after();
-        const uint32_t idesc = tc::idesc_bf16_f32(256, t.nmma);
+        const uint32_t idesc = tc::idesc_bf16_f32_mn(256, t.nmma, MODE == GM_DGRAD, false);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
           // W8: the dequantised weights of both CTAs (written by threads,
@@ -467,8 +484,17 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
                 tc::mma_bf16_ts<2>(tmem_base, ta, db, idesc, acc);
                 tc::mma_bf16_ts<2>(tmem_base + ACC1, ta + 32, db, idesc, acc);
               } else {
-                const uint64_t da0 = tc::smem_desc_sw128(sa + kk * 32);
-                const uint64_t da1 = tc::smem_desc_sw128(sa + EX_A_BOX_BYTES + kk * 32);
+                // K-major A: K = 16 is 32 bytes along the row; MN-major A: 16
+                // rows of 128 bytes, the second 64 columns one box further
+                const uint64_t da0 =
+                    MODE == GM_DGRAD
+                        ? tc::smem_desc_sw128_mn(sa + kk * 16 * ROW_BYTES, kMnBoxBytes)
+                        : tc::smem_desc_sw128(sa + kk * 32);
+                const uint64_t da1 =
+                    MODE == GM_DGRAD
+                        ? tc::smem_desc_sw128_mn(sa + 2 * kMnBoxBytes + kk * 16 * ROW_BYTES,
+                                                 kMnBoxBytes)
+                        : tc::smem_desc_sw128(sa + EX_A_BOX_BYTES + kk * 32);
                 const uint64_t db = tc::smem_desc_sw128(sa + 2 * EX_A_BOX_BYTES + kk * 32);
                 tc::mma_bf16<2>(tmem_base, da0, db, idesc, acc);
                 tc::mma_bf16<2>(tmem_base + ACC1, da1, db, idesc, acc);
@@ -514,8 +540,7 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
       decode_group_tile(args, tile, t);
       const bool second = t.g >= args.E;
       const int gl = second ? t.g - args.E : t.g;
-      const int a_row0 = gl * args.a_rows_per_group +
-                         t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128;
+      const int a_row0 = gl * args.a_rows_per_group + t.mb * kBlockW + static_cast<int>(rank) * 128;
       const int a_row1 = a_row0 + args.a1_off;
       // 128 x 128 block scales of the two boxes' rows, one per 128-wide K block
       const float* scb = second ? args.w_scale[1] : args.w_scale[0];
@@ -591,8 +616,7 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
       const int out_row0 = __ldg(args.gt.orow + t.g) + t.tok0;
       // GATEUP: act columns (SiLU(acc0) * acc1); DOWN: y columns of acc0 and,
       // 256 further, of acc1
-      const int colbase = t.mb * (MODE == GM_GATEUP ? 256 : 512) + static_cast<int>(rank) * 128 +
-                          q * 32;
+      const int colbase = t.mb * kBlockW + static_cast<int>(rank) * 128 + q * 32;
       if (!warp_wait(tfull, tphase, abort_flag, tmo)) break;
       tc::tc_fence_after();
       for (int j0 = h * 16; j0 < t.nmma; j0 += 32) {
@@ -621,11 +645,14 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
         const uint8_t* bp = stg_p + sbuf * (NOUT * EX_STG_BOX);
 #pragma unroll
         for (int o = 0; o < NOUT; ++o) {
-          const int col = colbase + 256 * o;
+          // GATEUP_H: gate column colbase.. and its up column a1_off further,
+          // both valid while colbase < I (= out_cols)
+          const int col = colbase + o * (MODE == GM_GATEUP_H ? args.a1_off : 256);
+          const int ccheck = MODE == GM_GATEUP_H ? colbase : col;
 #pragma unroll
           for (int u = lane; u < 64; u += 32) {
             const int r = u >> 2, c = u & 3;
-            if (r < nv && col < args.out_cols) {
+            if (r < nv && ccheck < args.out_cols) {
               const uint4 v = *reinterpret_cast<const uint4*>(
                   bp + o * EX_STG_BOX + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
               *reinterpret_cast<uint4*>(
@@ -639,6 +666,288 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(tempty_addr);
       tphase ^= 1u;
+    }
+  }
+
+  tc::tc_fence_before();
+  tc::cluster_sync_all();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc<2>(tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(args.status, ERRBIT_TIMEOUT);
+}
+
+// ============================================================================
+// Weight gradients on CTA pairs: dW[g] = sum over the group's tokens j of
+// A[j, :]^T B[j, :]  (dW2 = dy^T act, dW13 = dh^T u)
+// ============================================================================
+//
+// Both operands are token rows, so both are MN-major for the MMA (K = the
+// group's tokens): A rows come from the padded row layout of the output
+// gradients (rows of group g start at a 16-row boundary and the rows up to
+// the next boundary are zero), B rows from the packed forward rows.  A tile
+// is one group, 256 rows of dW (128 per CTA) and 256 columns; a K step is 64
+// tokens.  The last step issues only the MMAs of the 16-token slices that
+// hold tokens of the group; their rows past the group's end are zero in A,
+// which zeroes the product whatever B holds there.  A group without tokens
+// writes zeros without touching the tensor cores.
+//
+// With about 256 tokens per routed expert a tile has little MMA work for its
+// 128 KB of output, so the output stream sets the pace: the two 256-column
+// accumulators in TMEM alternate between consecutive tiles (the MMAs of one
+// run while the epilogue drains the other), and the epilogue writes whole
+// 128-byte lines: each warp rounds 32 rows x 64 columns to bf16 into a
+// swizzled shared-memory box, then stores it four rows per instruction.
+//
+// Warp roles as in the expert kernel (producer, MMA issuer in the even CTA,
+// eight epilogue warps: lane quadrant w % 4, column half (w - 2) / 4).
+
+struct WTile {
+  int g, mb, nb, arow, brow, kn;
+};
+
+__device__ __forceinline__ void decode_wgrad_tile(const WgradArgs& a, int tile, WTile& t) {
+  const int per = a.m_blocks * a.n_blocks;
+  const int gi = tile / per;
+  const int local = tile - gi * per;
+  t.mb = local / a.n_blocks;
+  t.nb = local - t.mb * a.n_blocks;
+  // shared experts first: their K is the whole batch, the longest tiles
+  if (gi < a.S) {
+    t.g = a.E + gi;
+    t.kn = a.T;
+    t.arow = __ldg(a.poff + a.E) + gi * a.T16;
+    t.brow = a.b_sh0 + gi * a.b_shs;
+  } else {
+    const int e = gi - a.S;
+    t.g = e;
+    t.kn = __ldg(a.counts + e);
+    t.arow = __ldg(a.poff + e);
+    t.brow = __ldg(a.offsets + e);
+  }
+}
+
+constexpr uint32_t WG_STAGE_BYTES = 4 * kMnBoxBytes;   // 32 KB: A 2 boxes, B 2 boxes
+constexpr int WG_STAGES = 6;
+constexpr uint32_t WG_STG_BYTES = 32 * 128;            // per warp: 32 rows x 64 bf16
+constexpr uint32_t WG_BAR_OFF = WG_STAGES * WG_STAGE_BYTES;
+constexpr uint32_t WG_STG_OFF = WG_BAR_OFF + 1024;
+constexpr size_t WG_SMEM_BYTES = WG_STG_OFF + EX_EPI_WARPS * WG_STG_BYTES + 1024;
+constexpr int WG_THREADS = 64 + 32 * EX_EPI_WARPS;
+static_assert(WG_SMEM_BYTES <= 227 * 1024, "wgrad shared memory");
+
+__global__ void __launch_bounds__(WG_THREADS, 1)
+    wgrad_gemm_kernel(const __grid_constant__ WgradMaps maps, const WgradArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + WG_BAR_OFF);
+  uint64_t* empty = full + WG_STAGES;
+  uint64_t* tfull = empty + WG_STAGES;     // [2] accumulator slot complete
+  uint64_t* tempty = tfull + 2;            // [2] accumulator slot drained (even CTA)
+  uint64_t* drain = tempty + 2;
+  uint64_t* qfull = drain + 1;
+  uint64_t* qempty = qfull + EX_QUEUE;
+  volatile int* tq = reinterpret_cast<volatile int*>(qempty + EX_QUEUE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tq) + EX_QUEUE);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WG_STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      tc::mbar_init(tfull + j, 1);
+      tc::mbar_init(tempty + j, 2 * EX_EPI_WARPS);
+    }
+    tc::mbar_init(drain, 1);
+    for (int s = 0; s < EX_QUEUE; ++s) {
+      tc::mbar_init(qfull + s, 1);
+      tc::mbar_init(qempty + s, queue_consumers(false));
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane < 3) tc::tma_prefetch_desc(lane == 0 ? &maps.a : &maps.b[lane - 1]);
+  if (warp == 1) {
+    tc::tmem_alloc<2>(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish<2>();
+  }
+  tc::tc_fence_before();
+  tc::cluster_sync_all();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = (args.S + args.E) * args.m_blocks * args.n_blocks;
+  const unsigned long long tmo = args.timeout_ns;
+
+  TileQueue queue{qfull, qempty, tq, rank, abort_flag, tmo, args.tile_counter};
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_par = 0;
+    bool ok = true;
+    int tile = 0;
+    ok = rank == 0 ? queue.publish(queue.take(), tile) : queue.next(tile);
+    while (ok && tile < ntiles) {
+      const int claimed = rank == 0 ? queue.take() : 0;
+      WTile t;
+      decode_wgrad_tile(args, tile, t);
+      const CUtensorMap* mB = &maps.b[t.g >= args.E ? 1 : 0];
+      const int mcol = t.mb * 256 + static_cast<int>(rank) * 128;
+      const int ncol = t.nb * 256 + static_cast<int>(rank) * 128;
+      const int nk = (t.kn + BK - 1) / BK;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t fb = tc::mapa_shared(tc::smem_u32(full + stage), 0);
+          if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, 2 * WG_STAGE_BYTES);
+          uint8_t* sa = smem + stage * WG_STAGE_BYTES;
+          const int ar = t.arow + kb * BK, br = t.brow + kb * BK;
+          tc::tma_load_2d_pair(sa, &maps.a, fb, mcol, ar);
+          tc::tma_load_2d_pair(sa + kMnBoxBytes, &maps.a, fb, mcol + 64, ar);
+          tc::tma_load_2d_pair(sa + 2 * kMnBoxBytes, mB, fb, ncol, br);
+          tc::tma_load_2d_pair(sa + 3 * kMnBoxBytes, mB, fb, ncol + 64, br);
+        }
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        __syncwarp();
+        if (++stage == WG_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      ok = rank == 0 ? queue.publish(claimed, tile) : queue.next(tile);
+    }
+    if (!ok && rank == 0) {
+      for (int s = 0; s < WG_STAGES; ++s)
+        if (issued & (1u << s)) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_n = 0;          // accumulator tiles issued so far
+      bool ok = true, issued_any = false;
+      const uint32_t idesc = tc::idesc_bf16_f32_mn(256, 256, true, true);
+      for (;;) {
+        int tile;
+        if (!queue.next(tile)) { ok = false; break; }
+        if (tile >= ntiles) break;
+        WTile t;
+        decode_wgrad_tile(args, tile, t);
+        if (t.kn <= 0) continue;               // zero tile: the epilogue writes zeros
+        const uint32_t slot = acc_n & 1u, use = acc_n >> 1;
+        if (!warp_wait<true>(tempty + slot, (use & 1u) ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t dcol = tmem_base + slot * 256;
+        const int nk = (t.kn + BK - 1) / BK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+          tc::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = tc::smem_u32(smem + stage * WG_STAGE_BYTES);
+            const int left = t.kn - kb * BK;
+            const int nmma = left >= BK ? BK / 16 : (left + 15) / 16;
+            for (int kk = 0; kk < nmma; ++kk) {
+              const uint32_t ko = kk * 16 * ROW_BYTES;
+              const uint64_t da = tc::smem_desc_sw128_mn(sa + ko, kMnBoxBytes);
+              const uint64_t db = tc::smem_desc_sw128_mn(sa + 2 * kMnBoxBytes + ko, kMnBoxBytes);
+              tc::mma_bf16<2>(dcol, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::mma_commit<2>(empty + stage);
+          }
+          issued_any = true;
+          __syncwarp();
+          if (++stage == WG_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) tc::mma_commit<2>(tfull + slot);
+        __syncwarp();
+        ++acc_n;
+      }
+      if (!ok && issued_any) {
+        if (lane == 0) tc::mma_commit<2>(drain, 0x1);
+        __syncwarp();
+        warp_wait(drain, 0, abort_flag, tmo);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // warp w: TMEM lanes 32 (w % 4).. (dW rows), columns 128 h .. of the tile
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    uint8_t* stg = smem + WG_STG_OFF + (warp - 2) * WG_STG_BYTES;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc_n = 0;
+    for (;;) {
+      int tile;
+      if (!queue.next(tile) || tile >= ntiles) break;
+      WTile t;
+      decode_wgrad_tile(args, tile, t);
+      const int row0 = t.mb * 256 + static_cast<int>(rank) * 128 + q * 32;
+      const int col0 = t.nb * 256 + h * 128;
+      const bool second = t.g >= args.E;
+      __nv_bfloat16* out =
+          static_cast<__nv_bfloat16*>(second ? args.out_shared : args.out_routed) +
+          static_cast<size_t>(second ? t.g - args.E : t.g) * args.out_gstride;
+      const bool zero = t.kn <= 0;
+      const uint32_t slot = acc_n & 1u, use = acc_n >> 1;
+      if (!zero) {
+        if (!warp_wait(tfull + slot, use & 1u, abort_flag, tmo)) break;
+        tc::tc_fence_after();
+      }
+      const uint32_t taddr = tmem_base + lane_addr + slot * 256 + h * 128;
+      for (int c0 = 0; c0 < 128; c0 += 64) {
+        // this lane's row: 64 columns -> 32 bf16 pairs -> 8 swizzled 16-byte chunks
+        uint32_t p[32];
+        if (!zero) {
+          uint32_t r0[16], r1[16], r2[16], r3[16];
+          tc::tmem_ld16(taddr + c0, r0);
+          tc::tmem_ld16(taddr + c0 + 16, r1);
+          tc::tmem_wait_ld(r0, r1);
+          tc::tmem_ld16(taddr + c0 + 32, r2);
+          tc::tmem_ld16(taddr + c0 + 48, r3);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            p[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+            p[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+          }
+          tc::tmem_wait_ld(r2, r3);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            p[16 + i] = pack_bf16x2(__uint_as_float(r2[2 * i]), __uint_as_float(r2[2 * i + 1]));
+            p[24 + i] = pack_bf16x2(__uint_as_float(r3[2 * i]), __uint_as_float(r3[2 * i + 1]));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[i] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+              make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+        __syncwarp();
+        // lane: chunk lane % 8 of rows 4 i + lane / 8 -> four whole rows per store
+        const int col = col0 + c0 + (lane & 7) * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3);
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(stg + r * 128 + (((lane & 7) ^ (r & 7)) << 4));
+          if (row0 + r < args.M && col < args.N)
+            *reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + r) * args.N + col) = v;
+        }
+        __syncwarp();
+      }
+      if (!zero) {
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(tempty + slot), 0));
+        ++acc_n;
+      }
     }
   }
 
@@ -887,6 +1196,56 @@ __global__ void __launch_bounds__(1024) build_groups_kernel(const int* offsets, 
   }
 }
 
+__global__ void __launch_bounds__(1024) build_bwd_groups_kernel(const int* counts, int T, int E,
+                                                                int S, int* poff, int* rows,
+                                                                int* brow, int* orow, int* bs,
+                                                                int* bstart, int* counters) {
+  __shared__ int warp_sums[32];
+  __shared__ int spoff[kMaxE + 1];
+  // padded offsets of the routed groups (E <= 1024: one group per thread)
+  const int e = threadIdx.x;
+  int total = 0;
+  const int before =
+      block_exclusive_scan(e < E ? (counts[e] + 15) & ~15 : 0, warp_sums, &total);
+  if (e < E) {
+    poff[e] = before;
+    spoff[e] = before;
+  }
+  if (threadIdx.x == 0) {
+    poff[E] = total;
+    spoff[E] = total;
+    for (int i = 0; i < 4; ++i) counters[i] = 0;
+  }
+  __syncthreads();
+  const int T16 = (T + 15) & ~15;
+  const int G = E + S;
+  // each thread owns two consecutive groups (G <= kMaxE + kMaxS <= 2048)
+  int nb_pair[2];
+  int local = 0;
+  for (int u = 0; u < 2; ++u) {
+    const int g = threadIdx.x * 2 + u;
+    int nb = 0;
+    if (g < G) {
+      const int r = g < E ? counts[g] : T;
+      const int br = g < E ? spoff[g] : spoff[E] + (g - E) * T16;
+      int b;
+      token_blocks(r, &b, &nb, 256);
+      rows[g] = r;
+      brow[g] = br;
+      orow[g] = br;
+      bs[g] = b;
+    }
+    nb_pair[u] = nb;
+    local += nb;
+  }
+  int tot_blocks = 0;
+  const int b0 = block_exclusive_scan(local, warp_sums, &tot_blocks);
+  const int g0 = threadIdx.x * 2;
+  if (g0 < G) bstart[g0] = b0;
+  if (g0 + 1 < G) bstart[g0 + 1] = b0 + nb_pair[0];
+  if (threadIdx.x == 0) bstart[G] = tot_blocks;
+}
+
 // Grid of a persistent kernel: at most one CTA (or pair) per SM, and no more
 // clusters than can be resident at once.
 // The occupancy query runs on a kernel's first launch on a device only, so
@@ -1029,10 +1388,10 @@ bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a
 }
 
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
-                            cudaStream_t stream, bool w8, bool small) {
+                            cudaStream_t stream, bool w8, bool small, const char* trace_name) {
   if (grid <= 0) return MOE_OK;
   static bool attr_gu[64], attr_dn[64], attr_rt[64], attr_gu8[64], attr_dn8[64], attr_gus[64],
-      attr_dns[64];
+      attr_dns[64], attr_guh[64], attr_guhs[64], attr_dg[64];
   switch (mode) {
     case GM_GATEUP:
       if (w8)
@@ -1061,6 +1420,21 @@ moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args
     case GM_ROUTER:
       return launch_persistent(router_gemm_kernel, "gemm_router", 1, RT_SMEM_BYTES, RT_THREADS,
                                grid, maps, args, stream, attr_rt);
+    case GM_GATEUP_H:
+      if (w8) return MOE_ERR_UNSUPPORTED;
+      if (small)
+        return launch_persistent(expert_gemm_kernel<GM_GATEUP_H, false, true>, "gemm_gateup_h",
+                                 2, ex_smem_bytes(GM_GATEUP_H), ex_threads(false), grid, maps,
+                                 args, stream, attr_guhs);
+      return launch_persistent(expert_gemm_kernel<GM_GATEUP_H, false, false>, "gemm_gateup_h", 2,
+                               ex_smem_bytes(GM_GATEUP_H), ex_threads(false), grid, maps, args,
+                               stream, attr_guh);
+    case GM_DGRAD:
+      if (w8 || small) return MOE_ERR_UNSUPPORTED;
+      return launch_persistent(expert_gemm_kernel<GM_DGRAD, false, false>,
+                               trace_name ? trace_name : "gemm_dgrad", 2,
+                               ex_smem_bytes(GM_DGRAD), ex_threads(false), grid, maps, args,
+                               stream, attr_dg);
     default: return MOE_ERR_INVALID_ARG;
   }
 }
@@ -1071,6 +1445,46 @@ moe_status_t launch_build_groups(const int* offsets, const int* counts, int T, i
   TraceScope tr(stream, "build_groups");
   build_groups_kernel<<<1, 1024, 0, stream>>>(offsets, counts, T, E, S, lay, rows, brow, orow,
                                               bs, bstart);
+  return launch_status();
+}
+
+moe_status_t launch_build_bwd_groups(const int* counts, int T, int E, int S, int* poff, int* rows,
+                                     int* brow, int* orow, int* bs, int* bstart, int* counters,
+                                     cudaStream_t stream) {
+  TraceScope tr(stream, "build_bwd_groups");
+  build_bwd_groups_kernel<<<1, 1024, 0, stream>>>(counts, T, E, S, poff, rows, brow, orow, bs,
+                                                  bstart, counters);
+  return launch_status();
+}
+
+moe_status_t launch_wgrad(const WgradMaps& maps, const WgradArgs& args, cudaStream_t stream,
+                          const char* trace_name) {
+  static bool attr[64];
+  const int want = num_sms();
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    if (cudaFuncSetAttribute(wgrad_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(WG_SMEM_BYTES)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr[dev] = true;
+  }
+  const int grid = persistent_ctas(wgrad_gemm_kernel, 2, WG_SMEM_BYTES, WG_THREADS, want);
+  if (grid <= 0) return MOE_ERR_CUDA;
+  TraceScope tr(stream, trace_name);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  lc.blockDim = dim3(WG_THREADS, 1, 1);
+  lc.dynamicSmemBytes = WG_SMEM_BYTES;
+  lc.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, wgrad_gemm_kernel, maps, args) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_status();
 }
 

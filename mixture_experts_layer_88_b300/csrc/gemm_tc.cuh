@@ -6,7 +6,13 @@
 
 namespace moe {
 
-enum GemmMode : int { GM_GATEUP = 0, GM_DOWN = 1, GM_ROUTER = 2 };
+// GATEUP: gate/up GEMM with the SwiGLU epilogue (act out).  DOWN: down GEMM
+// (y out).  ROUTER: router logits.  GATEUP_H: the gate/up GEMM writing the
+// pre-activations h = [gate | up] instead of act (training forward).  DGRAD:
+// the DOWN tiling with the weight operand read MN-major, for input gradients
+// (dact = dy W2 and dxp = dh W13): A is the weight matrix of a group viewed as
+// [K rows, M columns].
+enum GemmMode : int { GM_GATEUP = 0, GM_DOWN = 1, GM_ROUTER = 2, GM_GATEUP_H = 3, GM_DGRAD = 4 };
 
 // Per-group table on the device (G groups; bstart has G+1 entries).
 struct GroupTable {
@@ -72,7 +78,8 @@ bool make_gemm_maps(GemmMaps* m, const void* a0, uint64_t a0_rows, const void* a
 // scales, dequantised to bf16 on the way to the tensor cores.  small: token
 // blocks of at most 64 tokens (decode batches), a deeper ring of smaller stages.
 moe_status_t launch_gemm_tc(int mode, const GemmMaps& maps, const GemmArgs& args, int grid,
-                            cudaStream_t stream, bool w8 = false, bool small = false);
+                            cudaStream_t stream, bool w8 = false, bool small = false,
+                            const char* trace_name = nullptr);
 
 // Tensor map of a row-major e4m3 matrix [rows, cols] read in boxes of {64
 // columns, 128 rows} with 64-byte swizzle (the dequantisation warps read it,
@@ -96,6 +103,42 @@ struct GroupLayout {
 moe_status_t launch_build_groups(const int* offsets, const int* counts, int T, int E, int S,
                                  GroupLayout lay, int* rows, int* brow, int* orow, int* bs,
                                  int* bstart, cudaStream_t stream);
+
+// Weight-gradient GEMM (wgrad_gemm_kernel): dW[g] [M, N] = sum over the
+// group's tokens j of A[arow_g + j, 0..M)^T B[brow_g + j, 0..N), bf16 out.
+// Routed group e: counts[e] tokens, A rows from poff[e] (padded layout: zero
+// rows up to the next multiple of 16), B rows from offsets[e].  Shared expert
+// s: T tokens, A rows from poff[E] + s * T16, B rows from b_sh0 + s * b_shs.
+struct WgradArgs {
+  const int* counts;
+  const int* offsets;
+  const int* poff;
+  int E, S, T, T16;
+  int b_sh0, b_shs;
+  int m_blocks, n_blocks;     // ceil(M / 256), ceil(N / 256)
+  int M, N;
+  long long out_gstride;      // elements between groups' dW (M * N)
+  void* out_routed;           // [E, M, N]
+  void* out_shared;           // [S, M, N]
+  int* tile_counter;          // 0 at launch
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+struct WgradMaps {
+  CUtensorMap a;       // padded output-gradient rows [rows, M], boxes {64, 64}
+  CUtensorMap b[2];    // routed / shared forward rows [rows, N], boxes {64, 64}
+};
+moe_status_t launch_wgrad(const WgradMaps& maps, const WgradArgs& args, cudaStream_t stream,
+                          const char* trace_name = "gemm_wgrad");
+
+// Backward row layout and the input-gradient GEMMs' group table: poff[e] =
+// sum of round_up(counts[j], 16) over j < e (E+1 entries, poff[E] = start of
+// the shared segments, T16 = round_up(T, 16) rows each); group g < E has
+// counts[g] rows at brow = orow = poff[g], shared expert s has T rows at
+// poff[E] + s * T16; token blocks of at most 256.  Zeroes `counters` (4 ints).
+moe_status_t launch_build_bwd_groups(const int* counts, int T, int E, int S, int* poff, int* rows,
+                                     int* brow, int* orow, int* bs, int* bstart, int* counters,
+                                     cudaStream_t stream);
 
 int num_sms();
 

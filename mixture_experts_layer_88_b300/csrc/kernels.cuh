@@ -12,7 +12,7 @@ constexpr int kDispatchChunk = 256;   // tokens per count/rank CTA (8 warps x 32
 moe_status_t launch_topk(const float* logits, int splits, long long split_stride,
                          const float* bias, int T, int E, int K, int score_func, int normalize,
                          int n_groups, int topk_groups, int32_t* idx, float* gates,
-                         cudaStream_t stream);
+                         cudaStream_t stream, float* scores = nullptr);
 moe_status_t launch_logits_f32(const float* x, const float* c, int T, int d, int E, float* out,
                                cudaStream_t stream);
 
@@ -56,5 +56,46 @@ moe_status_t launch_experts_f32(const float* xp, const float* x, const int32_t* 
                                 const float* w13, const float* w2, const float* ws13,
                                 const float* ws2, float* act, float* y, int T, int K, int E,
                                 int S, int d, int I, cudaStream_t stream);
+
+// ---------------------------------------------------------------- training (backward.cu)
+// Padded backward rows: expert e from poff[e] (multiple of 16, zero rows up to
+// the next one), shared expert s from poff[E] + s * round_up(T, 16).
+// rows_max bounds the padded rows (T*K + 15*E + S*round_up(T, 16)).
+
+// act = SiLU(gate) * up from h = [gate | up] (rows x 2I), bf16
+moe_status_t launch_swiglu_fwd(const void* h, void* act, long long rows, int I,
+                               cudaStream_t stream);
+// dy (padded rows) and dgates [T,K] from dout and the forward's y
+moe_status_t launch_combine_bwd(const void* dout, const void* y, const float* gates,
+                                const int32_t* idx, const int32_t* perm, const int32_t* counts,
+                                const int32_t* offsets, const int32_t* poff, int T, int K, int E,
+                                int S, int d, long long rows_max, void* dy, float* dgates,
+                                cudaStream_t stream);
+// dlogits: Sigmoid -> dlk [T,K] and dlrow [T*K] (at pos); Softmax -> dl [T,E]
+moe_status_t launch_router_bwd(const float* dgates, const float* gates, const int32_t* idx,
+                               const float* scores, const int32_t* pos, int T, int E, int K,
+                               int score_func, int normalize, float* dlk, float* dlrow,
+                               float* dl, cudaStream_t stream);
+// dxr [T,d] fp32 = dl [T,E] C [E,d]
+moe_status_t launch_router_dx_dense(const float* dl, const void* cent, int T, int E, int d,
+                                    float* dxr, cudaStream_t stream);
+// dh (padded rows, 2I) from dact (padded rows, I) and the forward's h
+moe_status_t launch_swiglu_bwd(const void* dact, const void* h, const int32_t* counts,
+                               const int32_t* offsets, const int32_t* poff, int T, int K, int E,
+                               int S, int I, long long rows_max, void* dh, cudaStream_t stream);
+// dx [T,d] from dxp (padded rows), the router term (dlk with C, or dxr) and dout
+moe_status_t launch_dx(const void* dxp, const int32_t* pos, const int32_t* idx,
+                       const int32_t* offsets, const int32_t* poff, const float* dlk,
+                       const void* cent, const float* dxr, const void* dout, void* dx, int T,
+                       int K, int E, int S, int d, int add_residual, cudaStream_t stream);
+// dC [E,d] fp32 = sum over expert e's rows of dlrow * xp (blocks of the
+// input-gradient group table: bs, bstart), via part [max_blocks, d]
+moe_status_t launch_dcent_sparse(const float* dlrow, const void* xp, const int32_t* counts,
+                                 const int32_t* offsets, const int32_t* bs,
+                                 const int32_t* bstart, int E, int d, int max_blocks,
+                                 float* part, float* dc, cudaStream_t stream);
+// dC [E,d] fp32 = dl^T x, via part [ceil(T/256), E, d]
+moe_status_t launch_dcent_dense(const float* dl, const void* x, int T, int E, int d, float* part,
+                                float* dc, cudaStream_t stream);
 
 }  // namespace moe

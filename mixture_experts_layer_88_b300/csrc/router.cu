@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                                                    int K, int score_func, int normalize,
                                                    int n_groups, int topk_groups,
                                                    int32_t* __restrict__ idx,
-                                                   float* __restrict__ gates) {
+                                                   float* __restrict__ gates,
+                                                   float* __restrict__ scores) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -115,6 +116,11 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   } else {
 #pragma unroll
     for (int j = 0; j < NPL; ++j) s[j] = 1.0f / (1.0f + expf(-L[j]));
+  }
+  if (scores) {   // training forward: every expert's s for the backward
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+      if (j * 32 + lane < E) scores[static_cast<size_t>(t) * E + j * 32 + lane] = s[j];
   }
   uint32_t keyo[NPL];
 #pragma unroll
@@ -193,14 +199,14 @@ __global__ void logits_f32_kernel(const float* __restrict__ x, const float* __re
 moe_status_t launch_topk(const float* logits, int splits, long long split_stride,
                          const float* bias, int T, int E, int K, int score_func, int normalize,
                          int n_groups, int topk_groups, int32_t* idx, float* gates,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, float* scores) {
   if (T <= 0) return MOE_OK;
   TraceScope tr(stream, "router_topk");
   const int grid = ceil_div(T, 8);
 #define MOE_TOPK(NPL)                                                                      \
   topk_kernel<NPL><<<grid, 256, 0, stream>>>(logits, splits, split_stride, bias, T, E, K, \
                                              score_func, normalize, n_groups, topk_groups, idx, \
-                                             gates)
+                                             gates, scores)
   if (E <= 32) MOE_TOPK(1);
   else if (E <= 64) MOE_TOPK(2);
   else if (E <= 128) MOE_TOPK(4);

@@ -199,6 +199,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return desc;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile written by TMA
+// with 128-byte swizzle from a matrix whose rows run along K: each 128-byte
+// row holds 64 consecutive M (or N) elements of one K index, 8-row atoms
+// (8 K indices) are 1024 bytes apart (stride byte offset), and the next 64
+// M elements start `mn_stride` bytes further (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  desc |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;   // LBO: next 64 M/N
+  desc |= static_cast<uint64_t>(1024u >> 4) << 32;                    // SBO: next 8 K
+  desc |= static_cast<uint64_t>(1u) << 46;
+  desc |= static_cast<uint64_t>(2u) << 61;
+  return desc;
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32
@@ -206,6 +221,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)                                // B format: bf16
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// The same with either operand MN-major (transpose bits 15 and 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.  With CG = 2 the

@@ -362,7 +362,7 @@ def router_backward(u: np.ndarray, centroids, s: np.ndarray, idx: np.ndarray,
 
 def moe_layer_backward(inp: dict, K: int, dout, normalize: int = 1,
                        score_func: int = SIGMOID, add_residual: int = 1,
-                       n_groups: int = 0, topk_groups: int = 0) -> dict:
+                       n_groups: int = 0, topk_groups: int = 0, idx=None) -> dict:
     """Backward of ``moe_layer`` (no RMSNorm in front) for all T tokens:
     dout [T, d] is dL/d(out).  The routed term g_k FFN_k(u) gives
       dgates[t, k] = dout_t . FFN_k(u_t),  dFFN_k = g_k dout_t,
@@ -371,12 +371,20 @@ def moe_layer_backward(inp: dict, K: int, dout, normalize: int = 1,
     Returns dx [T, d], dcentroids [E, d], dw13 [E, 2I, d], dw2 [E, d, I],
     dws13 [S, 2I, d], dws2 [S, d, I], dgates [T, K], dlogit [T, E], idx,
     gates, margin; every array fp64.  Weight gradients of experts that no
-    token chose are zero."""
+    token chose are zero.  ``idx`` [T, K], when given, replaces the router's
+    own choice (another valid choice where keys tie); the gates are then
+    those of eq. (13)/(14) for that choice and the margin is NaN."""
     u = _f64(inp["x"])
     go = _f64(dout)
     T, d = u.shape
-    idx, gates, margin, s = route(u, inp["centroids"], inp["bias"], K, score_func, normalize,
-                                  n_groups, topk_groups)
+    if idx is None:
+        idx, gates, margin, s = route(u, inp["centroids"], inp["bias"], K, score_func,
+                                      normalize, n_groups, topk_groups)
+    else:
+        s = expert_scores(affinity_logits(u, inp["centroids"]), score_func)
+        idx = np.asarray(idx, dtype=np.int32)
+        gates = gate_values(s, idx, normalize)
+        margin = np.full(T, np.nan)
     w13 = inp["w13"]
     E = w13.shape[0]
     I = w13.shape[1] // 2

@@ -161,6 +161,38 @@ def test_w8a16_workspace_and_argument_errors():
                                  P, P, 0, P) == 0
 
 
+def test_training_workspace_and_argument_errors():
+    c = m.make_cfg(8192, 7168, 256, 8, 1, 2048)
+    # backward scratch holds the padded output-gradient rows dy, da, [dgate, dup], du
+    rows = 8192 * 8 + 15 * 256 + 8192
+    assert m.workspace_size(c, m.MOE_WS_BACKWARD) >= 2 * rows * (7168 + 2048 + 4096 + 7168)
+    assert 0 < m.workspace_size(c, m.MOE_WS_FORWARD_TRAIN) < m.workspace_size(c, m.MOE_WS_FORWARD)
+    # training is built for bf16 layers only
+    f32 = _cfg(act_dtype=m.MOE_F32, wgt_dtype=m.MOE_F32)
+    f8 = _cfg(wgt_dtype=m.MOE_E4M3)
+    for w in (m.MOE_WS_FORWARD_TRAIN, m.MOE_WS_BACKWARD):
+        assert m.workspace_size(f32, w) == 0 and m.workspace_size(f8, w) == 0
+    lib = L.lib()
+    P = None
+    b = _cfg()
+    st = L.TrainState(*([256] * 11))
+    gr = L.Grads(256, 256, 256, 256, 256, 256)
+    fargs = [16, 16, 256, 16, 16, 16, 16]
+    assert lib.moe_forward_train(ctypes.byref(f32), *fargs, ctypes.byref(st), 16, 256, 1 << 40,
+                                 P) == 2
+    assert lib.moe_forward_train(ctypes.byref(b), *fargs, None, 16, 256, 1 << 40, P) == 1
+    assert lib.moe_forward_train(ctypes.byref(b), *fargs, ctypes.byref(st), 16, 256, 64, P) == 3
+    bargs = [16, 16, 16, 16, 16, 16, 16]
+    assert lib.moe_backward(ctypes.byref(f8), *bargs, ctypes.byref(st), ctypes.byref(gr), 256,
+                            1 << 40, P) == 2
+    assert lib.moe_backward(ctypes.byref(b), *bargs, ctypes.byref(st), None, 256, 1 << 40,
+                            P) == 1
+    assert lib.moe_backward(ctypes.byref(b), 8, *bargs[1:], ctypes.byref(st), ctypes.byref(gr),
+                            256, 1 << 40, P) == 1          # misaligned dout
+    assert lib.moe_backward(ctypes.byref(b), *bargs, ctypes.byref(st), ctypes.byref(gr), 256, 64,
+                            P) == 3
+
+
 def test_selftest_limits_checked_before_any_launch():
     lib = L.lib()
     assert lib.moe_selftest_wait_timeout(0, None) == 1

@@ -128,3 +128,13 @@ def test_unchosen_experts_get_zero_weight_gradients():
     for e in range(8):
         if e not in chosen:
             assert not g["dw13"][e].any() and not g["dw2"][e].any()
+
+
+def test_given_choice_reproduces_router_choice():
+    """Passing the router's own choice back in changes nothing."""
+    inp = _layer(T=6, d=6, E=8, I=4, S=1, seed=12)
+    dout = np.random.default_rng(8).normal(0, 1.0, inp["x"].shape)
+    a = O.moe_layer_backward(inp, 3, dout, 1, O.SIGMOID, 1)
+    b = O.moe_layer_backward(inp, 3, dout, 1, O.SIGMOID, 1, idx=a["idx"])
+    for k in ("dx", "dcentroids", "dw13", "dw2", "dws13", "dws2", "dgates"):
+        np.testing.assert_array_equal(a[k], b[k])
