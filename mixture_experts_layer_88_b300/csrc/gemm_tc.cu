@@ -662,9 +662,11 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
         }
         sbuf ^= 1;
       }
+      // the accumulators are free once this warp's tcgen05.ld completed (waited
+      // above); a relaxed arrival does not wait for the output stores to drain
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive_cluster(tempty_addr);
+      if (lane == 0) tc::mbar_arrive_cluster_relaxed(tempty_addr);
       tphase ^= 1u;
     }
   }
@@ -684,41 +686,56 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
 // Both operands are token rows, so both are MN-major for the MMA (K = the
 // group's tokens): A rows come from the padded row layout of the output
 // gradients (rows of group g start at a 16-row boundary and the rows up to
-// the next boundary are zero), B rows from the packed forward rows.  A tile
-// is one group, 256 rows of dW (128 per CTA) and 256 columns; a K step is 64
-// tokens.  The last step issues only the MMAs of the 16-token slices that
+// the next boundary are zero), B rows from the packed forward rows.  An
+// accumulator tile is 256 rows of dW (128 per CTA) x 256 columns, a K step
+// 64 tokens.  The last step issues only the MMAs of the 16-token slices that
 // hold tokens of the group; their rows past the group's end are zero in A,
 // which zeroes the product whatever B holds there.  A group without tokens
 // writes zeros without touching the tensor cores.
 //
-// With about 256 tokens per routed expert a tile has little MMA work for its
-// 128 KB of output, so the output stream sets the pace: the two 256-column
-// accumulators in TMEM alternate between consecutive tiles (the MMAs of one
-// run while the epilogue drains the other), and the epilogue writes whole
-// 128-byte lines: each warp rounds 32 rows x 64 columns to bf16 into a
-// swizzled shared-memory box, then stores it four rows per instruction.
+// With about 256 tokens per routed expert a tile has little MMA work for the
+// operand bytes it needs, so the kernel keeps A in shared memory: a work unit
+// of a routed expert is one 256-row block of dW and ALL its column blocks;
+// A (this CTA's 128 rows x the expert's tokens, up to WG_A_SLOTS K steps) is
+// loaded once and only B streams, which halves the operand bytes per MMA.
+// Experts with more tokens and the shared experts (the whole batch) stream A
+// with B through the same slots, one column block per work unit.  The two
+// 256-column accumulators in TMEM alternate between consecutive tiles (the
+// MMAs of one run while the epilogue drains the other), and the epilogue
+// writes whole 128-byte lines: each warp rounds 32 rows x 64 columns to bf16
+// into a swizzled shared-memory box, then stores it four rows per instruction.
 //
 // Warp roles as in the expert kernel (producer, MMA issuer in the even CTA,
 // eight epilogue warps: lane quadrant w % 4, column half (w - 2) / 4).
 
 struct WTile {
-  int g, mb, nb, arow, brow, kn;
+  int g, mb, nb0, nb1, arow, brow, kn;
 };
 
+constexpr int WG_A_SLOTS = 6;                          // K steps of A held at once (384 tokens)
+constexpr int WG_B_STAGES = 6;
+
+// Work units: shared experts first (their K is the whole batch), one per
+// (expert, row block, column block); then routed experts, one per (expert,
+// row block) covering every column block.
 __device__ __forceinline__ void decode_wgrad_tile(const WgradArgs& a, int tile, WTile& t) {
-  const int per = a.m_blocks * a.n_blocks;
-  const int gi = tile / per;
-  const int local = tile - gi * per;
-  t.mb = local / a.n_blocks;
-  t.nb = local - t.mb * a.n_blocks;
-  // shared experts first: their K is the whole batch, the longest tiles
-  if (gi < a.S) {
-    t.g = a.E + gi;
+  const int nsh = a.S * a.m_blocks * a.n_blocks;
+  if (tile < nsh) {
+    const int per = a.m_blocks * a.n_blocks;
+    const int s = tile / per;
+    const int local = tile - s * per;
+    t.mb = local / a.n_blocks;
+    t.nb0 = t.nb1 = local - t.mb * a.n_blocks;
+    t.g = a.E + s;
     t.kn = a.T;
-    t.arow = __ldg(a.poff + a.E) + gi * a.T16;
-    t.brow = a.b_sh0 + gi * a.b_shs;
+    t.arow = __ldg(a.poff + a.E) + s * a.T16;
+    t.brow = a.b_sh0 + s * a.b_shs;
   } else {
-    const int e = gi - a.S;
+    const int r = tile - nsh;
+    const int e = r / a.m_blocks;
+    t.mb = r - e * a.m_blocks;
+    t.nb0 = 0;
+    t.nb1 = a.n_blocks - 1;
     t.g = e;
     t.kn = __ldg(a.counts + e);
     t.arow = __ldg(a.poff + e);
@@ -726,10 +743,14 @@ __device__ __forceinline__ void decode_wgrad_tile(const WgradArgs& a, int tile, 
   }
 }
 
-constexpr uint32_t WG_STAGE_BYTES = 4 * kMnBoxBytes;   // 32 KB: A 2 boxes, B 2 boxes
-constexpr int WG_STAGES = 6;
+__device__ __forceinline__ bool wgrad_resident(const WTile& t, int E) {
+  return t.g < E && (t.kn + BK - 1) / BK <= WG_A_SLOTS;
+}
+
+constexpr uint32_t WG_SLOT_BYTES = 2 * kMnBoxBytes;     // 16 KB: 64 tokens x 128 columns
+constexpr uint32_t WG_B_OFF = WG_A_SLOTS * WG_SLOT_BYTES;
 constexpr uint32_t WG_STG_BYTES = 32 * 128;            // per warp: 32 rows x 64 bf16
-constexpr uint32_t WG_BAR_OFF = WG_STAGES * WG_STAGE_BYTES;
+constexpr uint32_t WG_BAR_OFF = WG_B_OFF + WG_B_STAGES * WG_SLOT_BYTES;
 constexpr uint32_t WG_STG_OFF = WG_BAR_OFF + 1024;
 constexpr size_t WG_SMEM_BYTES = WG_STG_OFF + EX_EPI_WARPS * WG_STG_BYTES + 1024;
 constexpr int WG_THREADS = 64 + 32 * EX_EPI_WARPS;
@@ -740,10 +761,12 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + WG_BAR_OFF);
-  uint64_t* empty = full + WG_STAGES;
-  uint64_t* tfull = empty + WG_STAGES;     // [2] accumulator slot complete
-  uint64_t* tempty = tfull + 2;            // [2] accumulator slot drained (even CTA)
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + WG_BAR_OFF);
+  uint64_t* a_empty = a_full + WG_A_SLOTS;
+  uint64_t* b_full = a_empty + WG_A_SLOTS;
+  uint64_t* b_empty = b_full + WG_B_STAGES;
+  uint64_t* tfull = b_empty + WG_B_STAGES;   // [2] accumulator slot complete
+  uint64_t* tempty = tfull + 2;              // [2] accumulator slot drained (even CTA)
   uint64_t* drain = tempty + 2;
   uint64_t* qfull = drain + 1;
   uint64_t* qempty = qfull + EX_QUEUE;
@@ -756,9 +779,13 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   const uint32_t rank = tc::cluster_ctarank();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < WG_STAGES; ++s) {
-      tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1);
+    for (int s = 0; s < WG_A_SLOTS; ++s) {
+      tc::mbar_init(a_full + s, 1);
+      tc::mbar_init(a_empty + s, 1);
+    }
+    for (int s = 0; s < WG_B_STAGES; ++s) {
+      tc::mbar_init(b_full + s, 1);
+      tc::mbar_init(b_empty + s, 1);
     }
     for (int j = 0; j < 2; ++j) {
       tc::mbar_init(tfull + j, 1);
@@ -781,55 +808,82 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   tc::cluster_sync_all();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = (args.S + args.E) * args.m_blocks * args.n_blocks;
+  const int ntiles = args.S * args.m_blocks * args.n_blocks + args.E * args.m_blocks;
   const unsigned long long tmo = args.timeout_ns;
 
   TileQueue queue{qfull, qempty, tq, rank, abort_flag, tmo, args.tile_counter};
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t issued = 0, issued_par = 0;
+    // A loads (ai) and B loads (bi) each run through their ring of slots; a
+    // slot is refilled after the MMAs committed its "empty" barrier.
+    uint32_t ai = 0, bi = 0;
+    uint32_t a_iss = 0, a_par = 0, b_iss = 0, b_par = 0;   // per slot: load in flight, parity
     bool ok = true;
     int tile = 0;
     ok = rank == 0 ? queue.publish(queue.take(), tile) : queue.next(tile);
+    auto load_a = [&](const WTile& t, int kb) -> bool {
+      const uint32_t s = ai % WG_A_SLOTS, ph = (ai / WG_A_SLOTS) & 1u;
+      if (!warp_wait(a_empty + s, ph ^ 1u, abort_flag, tmo)) return false;
+      if (lane == 0) {
+        const uint32_t fb = tc::mapa_shared(tc::smem_u32(a_full + s), 0);
+        if (rank == 0) tc::mbar_arrive_expect_tx(a_full + s, 2 * WG_SLOT_BYTES);
+        uint8_t* sa = smem + s * WG_SLOT_BYTES;
+        const int mcol = t.mb * 256 + static_cast<int>(rank) * 128;
+        const int ar = t.arow + kb * BK;
+        tc::tma_load_2d_pair(sa, &maps.a, fb, mcol, ar);
+        tc::tma_load_2d_pair(sa + kMnBoxBytes, &maps.a, fb, mcol + 64, ar);
+      }
+      a_iss |= 1u << s;
+      a_par = (a_par & ~(1u << s)) | (ph << s);
+      __syncwarp();
+      ++ai;
+      return true;
+    };
+    auto load_b = [&](const WTile& t, int nb, int kb) -> bool {
+      const uint32_t s = bi % WG_B_STAGES, ph = (bi / WG_B_STAGES) & 1u;
+      if (!warp_wait(b_empty + s, ph ^ 1u, abort_flag, tmo)) return false;
+      if (lane == 0) {
+        const uint32_t fb = tc::mapa_shared(tc::smem_u32(b_full + s), 0);
+        if (rank == 0) tc::mbar_arrive_expect_tx(b_full + s, 2 * WG_SLOT_BYTES);
+        uint8_t* sb = smem + WG_B_OFF + s * WG_SLOT_BYTES;
+        const CUtensorMap* mB = &maps.b[t.g >= args.E ? 1 : 0];
+        const int ncol = nb * 256 + static_cast<int>(rank) * 128;
+        const int br = t.brow + kb * BK;
+        tc::tma_load_2d_pair(sb, mB, fb, ncol, br);
+        tc::tma_load_2d_pair(sb + kMnBoxBytes, mB, fb, ncol + 64, br);
+      }
+      b_iss |= 1u << s;
+      b_par = (b_par & ~(1u << s)) | (ph << s);
+      __syncwarp();
+      ++bi;
+      return true;
+    };
     while (ok && tile < ntiles) {
       const int claimed = rank == 0 ? queue.take() : 0;
       WTile t;
       decode_wgrad_tile(args, tile, t);
-      const CUtensorMap* mB = &maps.b[t.g >= args.E ? 1 : 0];
-      const int mcol = t.mb * 256 + static_cast<int>(rank) * 128;
-      const int ncol = t.nb * 256 + static_cast<int>(rank) * 128;
       const int nk = (t.kn + BK - 1) / BK;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
-        if (lane == 0) {
-          const uint32_t fb = tc::mapa_shared(tc::smem_u32(full + stage), 0);
-          if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, 2 * WG_STAGE_BYTES);
-          uint8_t* sa = smem + stage * WG_STAGE_BYTES;
-          const int ar = t.arow + kb * BK, br = t.brow + kb * BK;
-          tc::tma_load_2d_pair(sa, &maps.a, fb, mcol, ar);
-          tc::tma_load_2d_pair(sa + kMnBoxBytes, &maps.a, fb, mcol + 64, ar);
-          tc::tma_load_2d_pair(sa + 2 * kMnBoxBytes, mB, fb, ncol, br);
-          tc::tma_load_2d_pair(sa + 3 * kMnBoxBytes, mB, fb, ncol + 64, br);
+      const bool res = wgrad_resident(t, args.E);
+      for (int kb = 0; ok && res && kb < nk; ++kb) ok = load_a(t, kb);
+      for (int nb = t.nb0; ok && nb <= t.nb1 && nk > 0; ++nb)
+        for (int kb = 0; ok && kb < nk; ++kb) {
+          if (!res) ok = load_a(t, kb);
+          if (ok) ok = load_b(t, nb, kb);
         }
-        issued |= 1u << stage;
-        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-        __syncwarp();
-        if (++stage == WG_STAGES) { stage = 0; phase ^= 1u; }
-      }
       if (!ok) break;
       ok = rank == 0 ? queue.publish(claimed, tile) : queue.next(tile);
     }
     if (!ok && rank == 0) {
-      for (int s = 0; s < WG_STAGES; ++s)
-        if (issued & (1u << s)) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+      // abort: let every load counted on this CTA's barriers land before exit
+      for (int s = 0; s < WG_A_SLOTS; ++s)
+        if (a_iss & (1u << s)) warp_wait(a_full + s, (a_par >> s) & 1u, abort_flag, tmo);
+      for (int s = 0; s < WG_B_STAGES; ++s)
+        if (b_iss & (1u << s)) warp_wait(b_full + s, (b_par >> s) & 1u, abort_flag, tmo);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (rank == 0) {
-      int stage = 0;
-      uint32_t phase = 0, acc_n = 0;          // accumulator tiles issued so far
+      uint32_t ai = 0, bi = 0, acc_n = 0;
       bool ok = true, issued_any = false;
       const uint32_t idesc = tc::idesc_bf16_f32_mn(256, 256, true, true);
       for (;;) {
@@ -838,35 +892,55 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         if (tile >= ntiles) break;
         WTile t;
         decode_wgrad_tile(args, tile, t);
-        if (t.kn <= 0) continue;               // zero tile: the epilogue writes zeros
-        const uint32_t slot = acc_n & 1u, use = acc_n >> 1;
-        if (!warp_wait<true>(tempty + slot, (use & 1u) ^ 1u, abort_flag, tmo)) { ok = false; break; }
-        tc::tc_fence_after();
-        const uint32_t dcol = tmem_base + slot * 256;
         const int nk = (t.kn + BK - 1) / BK;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+        if (nk == 0) continue;                 // no tokens: the epilogue writes zeros
+        const bool res = wgrad_resident(t, args.E);
+        const uint32_t a0 = ai;                // resident: this unit's A loads a0 .. a0+nk-1
+        if (res) ai += nk;
+        for (int nb = t.nb0; ok && nb <= t.nb1; ++nb) {
+          const uint32_t slot = acc_n & 1u, use = acc_n >> 1;
+          if (!warp_wait<true>(tempty + slot, (use & 1u) ^ 1u, abort_flag, tmo)) { ok = false; break; }
           tc::tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = tc::smem_u32(smem + stage * WG_STAGE_BYTES);
-            const int left = t.kn - kb * BK;
-            const int nmma = left >= BK ? BK / 16 : (left + 15) / 16;
-            for (int kk = 0; kk < nmma; ++kk) {
-              const uint32_t ko = kk * 16 * ROW_BYTES;
-              const uint64_t da = tc::smem_desc_sw128_mn(sa + ko, kMnBoxBytes);
-              const uint64_t db = tc::smem_desc_sw128_mn(sa + 2 * kMnBoxBytes + ko, kMnBoxBytes);
-              tc::mma_bf16<2>(dcol, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t dcol = tmem_base + slot * 256;
+          for (int kb = 0; kb < nk; ++kb) {
+            const uint32_t aj = res ? a0 + kb : ai++;
+            const uint32_t as = aj % WG_A_SLOTS, bs = bi % WG_B_STAGES;
+            if (!warp_wait(a_full + as, (aj / WG_A_SLOTS) & 1u, abort_flag, tmo) ||
+                !warp_wait(b_full + bs, (bi / WG_B_STAGES) & 1u, abort_flag, tmo)) {
+              ok = false;
+              break;
             }
-            tc::mma_commit<2>(empty + stage);
+            ++bi;
+            tc::tc_fence_after();
+            if (lane == 0) {
+              const uint32_t sa = tc::smem_u32(smem + as * WG_SLOT_BYTES);
+              const uint32_t sb = tc::smem_u32(smem + WG_B_OFF + bs * WG_SLOT_BYTES);
+              const int left = t.kn - kb * BK;
+              const int nmma = left >= BK ? BK / 16 : (left + 15) / 16;
+              for (int kk = 0; kk < nmma; ++kk) {
+                const uint32_t ko = kk * 16 * ROW_BYTES;
+                tc::mma_bf16<2>(dcol, tc::smem_desc_sw128_mn(sa + ko, kMnBoxBytes),
+                                tc::smem_desc_sw128_mn(sb + ko, kMnBoxBytes), idesc,
+                                (kb > 0 || kk > 0) ? 1u : 0u);
+              }
+              tc::mma_commit<2>(b_empty + bs);
+              if (!res) tc::mma_commit<2>(a_empty + as);
+            }
+            issued_any = true;
+            __syncwarp();
           }
-          issued_any = true;
+          if (!ok) break;
+          if (lane == 0) tc::mma_commit<2>(tfull + slot);
           __syncwarp();
-          if (++stage == WG_STAGES) { stage = 0; phase ^= 1u; }
+          ++acc_n;
         }
         if (!ok) break;
-        if (lane == 0) tc::mma_commit<2>(tfull + slot);
-        __syncwarp();
-        ++acc_n;
+        if (res) {
+          // the unit's MMAs are issued: its A slots free once they complete
+          if (lane == 0)
+            for (int kb = 0; kb < nk; ++kb) tc::mma_commit<2>(a_empty + (a0 + kb) % WG_A_SLOTS);
+          __syncwarp();
+        }
       }
       if (!ok && issued_any) {
         if (lane == 0) tc::mma_commit<2>(drain, 0x1);
@@ -876,78 +950,95 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // warp w: TMEM lanes 32 (w % 4).. (dW rows), columns 128 h .. of the tile
+    // warp w: TMEM lanes 32 (w % 4).. (dW rows), columns 128 h .. of each
+    // column block.  The next unit's index is read before the stores of this
+    // unit's last tile: releasing the queue slot then has few stores to wait for.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     uint8_t* stg = smem + WG_STG_OFF + (warp - 2) * WG_STG_BYTES;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     uint32_t acc_n = 0;
-    for (;;) {
-      int tile;
-      if (!queue.next(tile) || tile >= ntiles) break;
+    int tile;
+    bool ok = queue.next(tile);
+    while (ok && tile < ntiles) {
       WTile t;
       decode_wgrad_tile(args, tile, t);
       const int row0 = t.mb * 256 + static_cast<int>(rank) * 128 + q * 32;
-      const int col0 = t.nb * 256 + h * 128;
       const bool second = t.g >= args.E;
       __nv_bfloat16* out =
           static_cast<__nv_bfloat16*>(second ? args.out_shared : args.out_routed) +
           static_cast<size_t>(second ? t.g - args.E : t.g) * args.out_gstride;
       const bool zero = t.kn <= 0;
-      const uint32_t slot = acc_n & 1u, use = acc_n >> 1;
-      if (!zero) {
-        if (!warp_wait(tfull + slot, use & 1u, abort_flag, tmo)) break;
-        tc::tc_fence_after();
-      }
-      const uint32_t taddr = tmem_base + lane_addr + slot * 256 + h * 128;
-      for (int c0 = 0; c0 < 128; c0 += 64) {
-        // this lane's row: 64 columns -> 32 bf16 pairs -> 8 swizzled 16-byte chunks
-        uint32_t p[32];
+      int next_tile = ntiles;
+      bool fetched = false;
+      for (int nb = t.nb0; nb <= t.nb1; ++nb) {
+        const int col0 = nb * 256 + h * 128;
+        const uint32_t slot = acc_n & 1u, use = acc_n >> 1;
         if (!zero) {
-          uint32_t r0[16], r1[16], r2[16], r3[16];
-          tc::tmem_ld16(taddr + c0, r0);
-          tc::tmem_ld16(taddr + c0 + 16, r1);
-          tc::tmem_wait_ld(r0, r1);
-          tc::tmem_ld16(taddr + c0 + 32, r2);
-          tc::tmem_ld16(taddr + c0 + 48, r3);
+          if (!warp_wait(tfull + slot, use & 1u, abort_flag, tmo)) { ok = false; break; }
+          tc::tc_fence_after();
+        }
+        // the next unit's index is published once the producer issued every
+        // load of this unit, which needs the MMAs (and this epilogue) to be
+        // at this unit's last tile: read it there, not earlier
+        if (nb == t.nb1) {
+          ok = queue.next(next_tile);
+          fetched = true;
+        }
+        const uint32_t taddr = tmem_base + lane_addr + slot * 256 + h * 128;
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+          // this lane's row: 64 columns -> 32 bf16 pairs -> 8 swizzled 16-byte chunks
+          uint32_t p[32];
+          if (!zero) {
+            uint32_t r0[16], r1[16], r2[16], r3[16];
+            tc::tmem_ld16(taddr + c0, r0);
+            tc::tmem_ld16(taddr + c0 + 16, r1);
+            tc::tmem_wait_ld(r0, r1);
+            tc::tmem_ld16(taddr + c0 + 32, r2);
+            tc::tmem_ld16(taddr + c0 + 48, r3);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              p[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+              p[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+            }
+            tc::tmem_wait_ld(r2, r3);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              p[16 + i] = pack_bf16x2(__uint_as_float(r2[2 * i]), __uint_as_float(r2[2 * i + 1]));
+              p[24 + i] = pack_bf16x2(__uint_as_float(r3[2 * i]), __uint_as_float(r3[2 * i + 1]));
+            }
+            if (c0 == 64) {
+              // every TMEM read of the slot is complete: hand it back to the MMAs
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0)
+                tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(tc::smem_u32(tempty + slot), 0));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) p[i] = 0u;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+          __syncwarp();
+          // lane: chunk lane % 8 of rows 4 i + lane / 8 -> four whole rows per store
+          const int col = col0 + c0 + (lane & 7) * 8;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            p[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-            p[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+            const int r = 4 * i + (lane >> 3);
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(stg + r * 128 + (((lane & 7) ^ (r & 7)) << 4));
+            if (row0 + r < args.M && col < args.N)
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + r) * args.N + col) = v;
           }
-          tc::tmem_wait_ld(r2, r3);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            p[16 + i] = pack_bf16x2(__uint_as_float(r2[2 * i]), __uint_as_float(r2[2 * i + 1]));
-            p[24 + i] = pack_bf16x2(__uint_as_float(r3[2 * i]), __uint_as_float(r3[2 * i + 1]));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p[i] = 0u;
+          __syncwarp();
         }
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-              make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
-        __syncwarp();
-        // lane: chunk lane % 8 of rows 4 i + lane / 8 -> four whole rows per store
-        const int col = col0 + c0 + (lane & 7) * 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = 4 * i + (lane >> 3);
-          const uint4 v =
-              *reinterpret_cast<const uint4*>(stg + r * 128 + (((lane & 7) ^ (r & 7)) << 4));
-          if (row0 + r < args.M && col < args.N)
-            *reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + r) * args.N + col) = v;
-        }
-        __syncwarp();
+        if (!zero) ++acc_n;
       }
-      if (!zero) {
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(tempty + slot), 0));
-        ++acc_n;
-      }
+      if (!fetched) ok = false;
+      tile = next_tile;
     }
   }
 
