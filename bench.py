@@ -6,6 +6,7 @@ tokens, on the V3-shaped prefill layer by default (T=8192, d=7168, 256 routed
 experts top-8 + 1 shared, intermediate 2048, bf16).
 
     python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl reference]
+                    [--train]   (training step: forward with saved state + backward)
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 of the layer on its own batch (replicas, weak scaling); times are the max over

@@ -1,4 +1,4 @@
-"""Data-parallel replicas of one layer: the one exchange the method has.
+"""Data-parallel replicas of one layer: the exchanges the method has.
 
 Every rank runs the whole layer on its own batch (the path shards by tokens).
 The balancing rule of the V3 walk-through (section 2.2) compares each
@@ -6,6 +6,12 @@ expert's load with the mean load of the *batch*; with a batch split over R
 ranks that is the global load, so before the sign update the [E] load counts
 are summed over the ranks (one all-reduce of E int32) and every rank applies
 the same update with T = R * T_local.  The replicas' biases then stay equal.
+
+Training adds the parameter gradients: the loss of the whole batch is the sum
+of the ranks' losses and every token's gradient depends only on that token
+(its own routing and gates), so the gradient of each shared parameter
+(centroids, routed and shared expert weights) is the sum of the ranks'
+gradients; dx stays with the rank that owns the tokens.
 """
 from __future__ import annotations
 
@@ -35,3 +41,20 @@ def balance_step(cfg, counts: torch.Tensor, bias: torch.Tensor, update, group=No
     update of every rank against the global mean load."""
     global_counts(counts, group)
     return update(global_cfg(cfg, group), counts, bias)
+
+
+PARAM_GRAD_KEYS = ("dcentroids", "dw13", "dw2", "dws13", "dws2")
+
+
+def allreduce_grads(grads: dict, group=None, keys=PARAM_GRAD_KEYS) -> dict:
+    """Sums the parameter gradients of moe_backward (a dict as from
+    alloc_grads) over the ranks of `group` in place, one all-reduce per
+    tensor in the order of `keys`; empty tensors (no shared experts) are
+    skipped.  dx is left alone."""
+    if not (dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1):
+        return grads
+    for k in keys:
+        t = grads.get(k)
+        if t is not None and t.numel() > 0:
+            dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return grads

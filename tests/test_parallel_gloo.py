@@ -124,3 +124,63 @@ def test_peer_leaving_is_reported_not_waited_for():
     assert kind != "no error"
     assert secs < 60
     assert res["bias_untouched"]
+
+
+# ---------------------------------------------------------------- training
+
+TG = dict(T=5, d=8, E=8, K=2, S=1, I=4)
+
+
+def _train_layer():
+    rng = np.random.default_rng(21)
+    E, S, d, I = TG["E"], TG["S"], TG["d"], TG["I"]
+    return {"centroids": rng.normal(0, 0.5, (E, d)),
+            "bias": rng.uniform(-0.05, 0.05, E).astype(np.float32),
+            "w13": rng.normal(0, 0.5, (E, 2 * I, d)), "w2": rng.normal(0, 0.5, (E, d, I)),
+            "ws13": rng.normal(0, 0.5, (S, 2 * I, d)), "ws2": rng.normal(0, 0.5, (S, d, I))}
+
+
+def _rank_batch(rank):
+    rng = np.random.default_rng(300 + rank)
+    return (rng.normal(0, 1.0, (TG["T"], TG["d"])), rng.normal(0, 1.0, (TG["T"], TG["d"])))
+
+
+def _worker_grads(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from mixture_experts_layer_88_b300 import parallel
+    inp = _train_layer()
+    x, dout = _rank_batch(rank)
+    inp["x"] = x
+    g = O.moe_layer_backward(inp, TG["K"], dout, 1, O.SIGMOID, 1)
+    grads = {k: torch.from_numpy(np.ascontiguousarray(g[k])) for k in
+             ("dx", "dcentroids", "dw13", "dw2", "dws13", "dws2")}
+    parallel.allreduce_grads(grads)
+    out[rank] = {k: v.numpy().copy() for k, v in grads.items()}
+    dist.destroy_process_group()
+
+
+def test_two_rank_gradient_allreduce_equals_whole_batch():
+    """Two gloo ranks, each with the oracle's backward of its own tokens: after
+    allreduce_grads every rank holds the whole batch's parameter gradients
+    (the oracle on both batches at once); dx stays each rank's own."""
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_worker_grads, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+            assert p.exitcode == 0
+        res = dict(out)
+    inp = _train_layer()
+    (x0, d0), (x1, d1) = _rank_batch(0), _rank_batch(1)
+    inp["x"] = np.concatenate([x0, x1])
+    whole = O.moe_layer_backward(inp, TG["K"], np.concatenate([d0, d1]), 1, O.SIGMOID, 1)
+    for k in ("dcentroids", "dw13", "dw2", "dws13", "dws2"):
+        for r in (0, 1):
+            np.testing.assert_allclose(res[r][k], whole[k], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(res[0]["dx"], whole["dx"][:TG["T"]], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(res[1]["dx"], whole["dx"][TG["T"]:], rtol=1e-12, atol=1e-12)
