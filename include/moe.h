@@ -1,5 +1,6 @@
 /*
- * moe.h - C ABI of the DeepSeekMoE layer forward for NVIDIA B300 (sm_103a).
+ * moe.h - C ABI of the DeepSeekMoE layer (forward, balancing, training backward)
+ * for NVIDIA B300 (sm_103a).
  *
  * One DeepSeekMoE layer: a Sigmoid router with an auxiliary-loss-free
  * balancing bias, hard top-K_r selection, renormalised gates, no-drop dispatch

@@ -21,6 +21,14 @@
 // two accumulators fill TMEM, so a tile's MMAs wait for the previous tile's
 // epilogue; eight epilogue warps keep that drain short.
 //
+// Training adds two modes of the same kernel: GATEUP_H writes the gate/up
+// pre-activations h = [gate | up] (bf16) instead of act, and DGRAD computes
+// input gradients (da = dy W2, du = dh W13) with the DOWN tiling and the
+// weight operand read MN-major (the weight matrix of a group is [K, M] in
+// memory: TMA boxes of 64 K-rows x 64 M-columns, the transpose bit of the
+// instruction descriptor).  The weight gradients (dW = A^T B over a group's
+// tokens) run in wgrad_gemm_kernel, described at its definition.
+//
 // The router GEMM (router_gemm_kernel) runs one CTA per tile: two 128-row
 // centroid boxes, one token block, one K split; fp32 partial logits out.
 //

@@ -1,4 +1,5 @@
-"""CPU oracle for the DeepSeekMoE layer forward, load count and bias update.
+"""CPU oracle for the DeepSeekMoE layer forward, load count, bias update and
+the training backward.
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check in
 ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
