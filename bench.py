@@ -271,24 +271,34 @@ def run_reference(args, cfg, dist, rank, ws, device):
     per_step = max(1, args.ref_tokens)
     rates = []
     cores = None
+    if args.train:
+        from moe_inputs import make_dout
+        dout = make_dout(cfg, device if device.type == "cuda" else "cpu")
+        cores = os.cpu_count()
     for i in range(args.warmup + args.steps):
-        r, dt, cores = cpu_oracle_tokens_per_s(cfg, inp, per_step, seed=100 + i,
-                                               prenorm=args.prenorm)
+        if args.train:
+            _, dt = cpu_oracle_train_tokens_per_s(cfg, inp, dout, per_step, seed=100 + i)
+        else:
+            _, dt, cores = cpu_oracle_tokens_per_s(cfg, inp, per_step, seed=100 + i,
+                                                   prenorm=args.prenorm)
         if i >= args.warmup:
             rates.append((per_step, dt))
     tok = sum(t for t, _ in rates)
     secs = sum(s for _, s in rates)
     value = tok / secs
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+    line = {"impl": "reference", "metric": TRAIN_METRIC if args.train else METRIC,
+            "value": round(value, 4), "unit": UNIT,
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(secs / len(rates) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": _workload(cfg, args), "T": cfg.T, "d": cfg.d, "E": cfg.E,
+            "config": {"workload": _workload(cfg, args) + ("+train" if args.train else ""),
+                       "T": cfg.T, "d": cfg.d, "E": cfg.E,
                        "K": cfg.K, "S": cfg.S, "I": cfg.I, "sample_tokens_per_step": per_step},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                              "kind": "oracle",
                              "sample": f"{per_step} random tokens of the {cfg.name} batch per "
-                                       f"step through the fp64 oracle"},
+                                       f"step through the fp64 oracle" +
+                                       (", forward and backward" if args.train else "")},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
