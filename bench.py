@@ -394,12 +394,18 @@ def run_train(args, cfg, dist, rank, ws, device, peaks):
     sh = cfg.S > 0
     stream = torch.cuda.current_stream()
 
+    from mixture_experts_layer_88_b300 import parallel
+
     def step(xx=x, dd=dout):
         m.forward_train(mc, xx, inp["centroids"], bias, inp["w13"], inp["w2"],
                         inp["ws13"] if sh else None, inp["ws2"] if sh else None, state, out, ws_f)
         m.backward(mc, dd, xx, inp["centroids"], inp["w13"], inp["w2"],
                    inp["ws13"] if sh else None, inp["ws2"] if sh else None, state, grads, ws_b)
-        m.update_bias(mc, state["counts"], bias)
+        # data parallel (N > 1): parameter gradients and load counts summed over
+        # the ranks; one rank: both are no-ops
+        parallel.allreduce_grads(grads)
+        parallel.balance_step(mc, state["counts"], bias,
+                              lambda cfg, c, b: m.update_bias(cfg, c, b))
 
     for _ in range(args.warmup):
         step()
@@ -464,7 +470,9 @@ def run_train(args, cfg, dist, rank, ws, device, peaks):
         "data": "synthetic (seeded random tokens, output gradients and random-init weights)",
         "config": {"workload": cfg.name + "+train", "T": cfg.T, "d": cfg.d, "E": cfg.E,
                    "K": cfg.K, "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
-                   "parallelism": "one replica" if ws == 1 else f"data parallel x{ws}",
+                   "parallelism": ("one replica" if ws == 1 else
+                                   f"data parallel x{ws}: parameter gradients and load "
+                                   f"counts all-reduced every step"),
                    "launch": "eager stream launches",
                    "l2": "inputs larger than L2 (weights, their gradients and the saved rows)"},
         "grouped_gemm": {"tflops": round(flops / (gemm_ms / 1e3) / 1e12, 1),
