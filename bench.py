@@ -402,7 +402,7 @@ def run_train(args, cfg, dist, rank, ws, device, peaks):
         m.backward(mc, dd, xx, inp["centroids"], inp["w13"], inp["w2"],
                    inp["ws13"] if sh else None, inp["ws2"] if sh else None, state, grads, ws_b)
         # data parallel (N > 1): parameter gradients and load counts summed over
-        # the ranks; one rank: both are no-ops
+        # the ranks before the bias update; one rank: no exchange
         parallel.allreduce_grads(grads)
         parallel.balance_step(mc, state["counts"], bias,
                               lambda cfg, c, b: m.update_bias(cfg, c, b))
