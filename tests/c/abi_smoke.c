@@ -45,6 +45,27 @@ int main(void) {
   if (moe_selftest_wait_timeout(0, NULL) != MOE_ERR_INVALID_ARG) return 9;
   if (strlen(moe_status_string(MOE_ERR_DEVICE_TIMEOUT)) == 0) return 10;
   if (strstr(moe_version(), "sm_103a") == NULL) return 11;
+  /* training: the state and gradient structs are plain C; missing ones and
+   * non-bf16 layers are refused before any launch */
+  {
+    moe_train_state_t st;
+    moe_grads_t gr;
+    memset(&st, 0, sizeof(st));
+    memset(&gr, 0, sizeof(gr));
+    if (moe_workspace_size(&c, MOE_WS_BACKWARD) == 0) return 12;
+    if (moe_workspace_size(&c, MOE_WS_FORWARD_TRAIN) == 0) return 13;
+    if (moe_backward(&c, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, &gr, NULL, 0, NULL) !=
+        MOE_ERR_INVALID_ARG)
+      return 14;
+    if (moe_forward_train(&c, NULL, NULL, NULL, NULL, NULL, NULL, NULL, &st, NULL, NULL, 0,
+                          NULL) != MOE_ERR_INVALID_ARG)
+      return 15;
+    c.wgt_dtype = MOE_E4M3;
+    if (moe_backward(&c, NULL, NULL, NULL, NULL, NULL, NULL, NULL, &st, &gr, NULL, 0, NULL) !=
+        MOE_ERR_UNSUPPORTED)
+      return 16;
+    c = v3_prefill();
+  }
   printf("abi ok: forward workspace %zu bytes\n", fwd);
   return 0;
 }
