@@ -227,6 +227,8 @@ static_assert(W8_A_COL + W8_A_SLOTS * 64 <= TMEM_COLS && 2 * W8_MAX_BS <= W8_A_C
 constexpr uint32_t SB_STAGE_BYTES = 2 * EX_A_BOX_BYTES + 32 * ROW_BYTES;   // 36 KB
 constexpr int SB_STAGES = 5;
 constexpr int SB_MAX_BS = 64;
+static_assert(SB_STAGE_BYTES == 2 * EX_A_BOX_BYTES + (SB_MAX_BS / 2) * ROW_BYTES,
+              "a small stage holds half of a token block per CTA");
 static_assert(SB_STAGES * SB_STAGE_BYTES <= EX_STAGES * EX_STAGE_BYTES, "ring space");
 constexpr int EX_MAX_STAGES = W8_STAGES;
 
