@@ -1,0 +1,32 @@
+"""The benchmark's reference arm (the oracle timed on the host cores) keeps
+the JSON contract on both metrics.  CPU only: the arm never touches a GPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*extra):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny", "--steps", "1", "--warmup", "1", *extra],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+@pytest.mark.parametrize("train", [False, True])
+def test_reference_arm_json_line(train):
+    d = _run(*(["--train"] if train else []))
+    assert d["impl"] == "reference"
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["warmup"] >= 3 and d["steps"] == 1
+    assert ("training" in d["metric"]) == train
+    assert d["config"]["workload"] == ("tiny+train" if train else "tiny")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
