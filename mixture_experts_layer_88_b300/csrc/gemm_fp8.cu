@@ -116,6 +116,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Drain wait after an abort: waits up to timeout_ns whatever the abort flag
+// says, so this CTA's own loads and MMAs complete before TMEM is freed.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
+                                           unsigned long long timeout_ns) {
+  if ((threadIdx.x & 31) == 0)
+    tc::mbar_wait_deadline(bar, parity, tc::globaltimer_ns() + timeout_ns);
+  __syncwarp();
+}
+
 __device__ __forceinline__ bool lane_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned long long timeout_ns) {
   if (tc::mbar_try_wait(bar, parity)) return true;
@@ -262,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (!ok) {
       for (int s = 0; s < STAGES; ++s)
-        if (issued & (1u << s)) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+        if (issued & (1u << s)) drain_wait(full + s, (issued_par >> s) & 1u, tmo);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (!ok && issued_any) {
       if (lane == 0) tc::mma_commit<1>(drain);
       __syncwarp();
-      warp_wait(drain, 0, abort_flag, tmo);
+      drain_wait(drain, 0, tmo);
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue

@@ -139,6 +139,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok != 0;
 }
 
+// Drain wait after an abort: lane 0 waits up to timeout_ns whatever the abort
+// flag says, so the loads and MMAs this CTA issued complete before TMEM is
+// freed and the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
+                                           unsigned long long timeout_ns) {
+  if ((threadIdx.x & 31) == 0)
+    tc::mbar_wait_deadline(bar, parity, tc::globaltimer_ns() + timeout_ns);
+  __syncwarp();
+}
+
 // SiLU(g) * u with the fast reciprocal: g * u / (1 + e^-g).
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g * u, 1.0f + __expf(-g));
@@ -454,8 +464,8 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
       // abort: let every load counted on this CTA's barriers land before exit
       for (int s = 0; s < NST; ++s) {
         if (!(issued & (1u << s))) continue;
-        if (rank == 0) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
-        if (W8) warp_wait(raw_full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+        if (rank == 0) drain_wait(full + s, (issued_par >> s) & 1u, tmo);
+        if (W8) drain_wait(raw_full + s, (issued_par >> s) & 1u, tmo);
       }
     }
   } else if (warp == 1) {
@@ -526,7 +536,7 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
       if (!ok && issued_any) {
         if (lane == 0) tc::mma_commit<2>(drain, 0x1);
         __syncwarp();
-        warp_wait(drain, 0, abort_flag, tmo);
+        drain_wait(drain, 0, tmo);
       }
     }
   } else if (W8 && warp >= 2 + EX_EPI_WARPS) {
@@ -886,9 +896,9 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     if (!ok && rank == 0) {
       // abort: let every load counted on this CTA's barriers land before exit
       for (int s = 0; s < WG_A_SLOTS; ++s)
-        if (a_iss & (1u << s)) warp_wait(a_full + s, (a_par >> s) & 1u, abort_flag, tmo);
+        if (a_iss & (1u << s)) drain_wait(a_full + s, (a_par >> s) & 1u, tmo);
       for (int s = 0; s < WG_B_STAGES; ++s)
-        if (b_iss & (1u << s)) warp_wait(b_full + s, (b_par >> s) & 1u, abort_flag, tmo);
+        if (b_iss & (1u << s)) drain_wait(b_full + s, (b_par >> s) & 1u, tmo);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -955,7 +965,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
       if (!ok && issued_any) {
         if (lane == 0) tc::mma_commit<2>(drain, 0x1);
         __syncwarp();
-        warp_wait(drain, 0, abort_flag, tmo);
+        drain_wait(drain, 0, tmo);
       }
     }
   } else {
@@ -1139,7 +1149,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     }
     if (!ok) {
       for (int s = 0; s < RT_STAGES; ++s)
-        if (issued & (1u << s)) warp_wait(full + s, (issued_par >> s) & 1u, abort_flag, tmo);
+        if (issued & (1u << s)) drain_wait(full + s, (issued_par >> s) & 1u, tmo);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -1180,7 +1190,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     if (!ok && issued_any) {
       if (lane == 0) tc::mma_commit<1>(drain);
       __syncwarp();
-      warp_wait(drain, 0, abort_flag, tmo);
+      drain_wait(drain, 0, tmo);
     }
   } else {
     // ------------------------------------------------------------ epilogue

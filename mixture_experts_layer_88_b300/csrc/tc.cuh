@@ -113,6 +113,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Bounded wait that ignores the abort flag: for draining after an abort, where
+// the CTA must still let its own TMA loads land and its own MMAs finish before
+// it frees TMEM and exits.  Returns false only when `deadline_ns` passes.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait_deadline(uint64_t* bar, uint32_t parity,
+                                                   uint64_t deadline_ns) {
+  uint32_t polls = 0;
+  while (!(CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))) {
+    if ((++polls & 255u) == 0 && globaltimer_ns() > deadline_ns) return false;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
