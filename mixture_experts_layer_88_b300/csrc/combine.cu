@@ -4,9 +4,11 @@
 //   out_t = sum_k g_{t,k} y[pos[t,k]] + sum_s y[shared0 + s*stride + t] (+ u_t)
 // (shared rows: shared0 = T*K, stride = T in the bf16/fp32 layout; the FP8
 // layout places them after the padded routed rows)
-// summed in fp32 in that fixed order.  One thread owns 8 consecutive
-// channels (one 16-byte vector) of one token: the K + S + 1 source rows are
-// gathered with 16-byte loads, the output written with one 16-byte store.
+// summed in fp32 in that fixed order.  A (t, k) whose pos is negative (an
+// expert id the dispatch rejected and flagged) adds nothing.  One thread owns
+// 8 consecutive channels (one 16-byte vector) of one token: the K + S + 1
+// source rows are gathered with 16-byte loads, the output written with one
+// 16-byte store.
 //
 // Bias update (same page, section 2.2; applied for the next batch per the
 // course chapter "MoE", section 5): b_i -= gamma when c_i * E > T * K,
@@ -48,6 +50,7 @@ __global__ void __launch_bounds__(128) combine_bf16_kernel(
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   for (int k = 0; k < K; ++k) {
     const int r = __ldg(pos + static_cast<size_t>(t) * K + k);
+    if (r < 0) continue;   // a (t, k) the dispatch rejected (flagged there)
     const float g = __ldg(gates + static_cast<size_t>(t) * K + k);
     bf16x8_fma(acc, __ldg(y + static_cast<size_t>(r) * vpr + v), g);
   }
@@ -72,6 +75,7 @@ __global__ void __launch_bounds__(128) combine_f32_kernel(
   float acc = 0.f;
   for (int k = 0; k < K; ++k) {
     const int r = __ldg(pos + static_cast<size_t>(t) * K + k);
+    if (r < 0) continue;   // a (t, k) the dispatch rejected (flagged there)
     acc = fmaf(__ldg(gates + static_cast<size_t>(t) * K + k), __ldg(y + static_cast<size_t>(r) * d + c), acc);
   }
   for (int s = 0; s < S; ++s)

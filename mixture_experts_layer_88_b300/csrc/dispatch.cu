@@ -22,7 +22,18 @@ namespace {
 
 constexpr int WARPS = kDispatchChunk / 32;
 
-// Expert ids outside [0, E) are skipped and flagged in the device error word.
+// True when expert id e is invalid for entry k of a token's idx row: outside
+// [0, E), or equal to an earlier entry of the same row (a token reaches each
+// chosen expert once).  Such entries get no row and raise the bounds bit.
+__device__ __forceinline__ bool bad_entry(const int32_t* __restrict__ row, int k, int e, int E) {
+  if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) return true;
+  for (int j = 0; j < k; ++j)
+    if (__ldg(row + j) == e) return true;
+  return false;
+}
+
+// Expert ids outside [0, E) and repeats within a token are skipped and
+// flagged in the device error word.
 __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, int T, int K, int E,
                                             uint32_t* mask, unsigned* status) {
   for (int i = threadIdx.x; i < WARPS * E; i += blockDim.x) mask[i] = 0u;
@@ -30,9 +41,10 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, int
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kDispatchChunk + warp * 32 + lane;
   if (t < T) {
+    const int32_t* row = idx + static_cast<size_t>(t) * K;
     for (int k = 0; k < K; ++k) {
-      const int e = __ldg(idx + static_cast<size_t>(t) * K + k);
-      if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+      const int e = __ldg(row + k);
+      if (bad_entry(row, k, e, E)) {
         atomicOr(status, ERRBIT_BOUNDS);
         continue;
       }
@@ -123,9 +135,10 @@ __global__ void __launch_bounds__(kDispatchChunk) rank_kernel(
   const int t = blockIdx.x * kDispatchChunk + warp * 32 + lane;
   if (t >= T) return;
   const uint32_t below = (1u << lane) - 1u;
+  const int32_t* row = idx + static_cast<size_t>(t) * K;
   for (int k = 0; k < K; ++k) {
-    const int e = __ldg(idx + static_cast<size_t>(t) * K + k);
-    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+    const int e = __ldg(row + k);
+    if (bad_entry(row, k, e, E)) {
       pos[static_cast<size_t>(t) * K + k] = -1;
       continue;
     }
