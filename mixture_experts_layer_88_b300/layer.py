@@ -40,6 +40,9 @@ class MoeLayer:
         self.w8a16 = self.fp8 and fp8_path == "w8a16" and norm_w is None
         self._ws = None
         self._T = None
+        # tokens of the whole data-parallel batch, when every rank's batch size
+        # is known up front (saves the host read that summing them costs)
+        self.T_global = None
 
     def _buffers(self, T: int):
         if self._T != T:
@@ -85,11 +88,13 @@ class MoeLayer:
         """Sign update of the balancing bias from the last forward's counts.
         Under torch.distributed with more than one rank the counts are first
         summed over `group` (data-parallel replicas balance on the global
-        batch; see parallel.py)."""
+        batch; see parallel.py), against the tokens of all ranks
+        (self.T_global if set, else summed over the ranks)."""
         def upd(cfg, counts, bias):
             _lib.update_bias(cfg, counts, bias, self.load_stats, stream)
             return self.load_stats
-        return parallel.balance_step(self.cfg, self.counts, self.bias, upd, group)
+        return parallel.balance_step(self.cfg, self.counts, self.bias, upd, group,
+                                     T_global=self.T_global)
 
     def step(self, x: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
         """One batch of the layer: forward, then the bias update for the next batch."""

@@ -17,6 +17,11 @@ from oracle import moe_oracle as O
 E, K, T_LOCAL = 16, 4, 64
 
 
+def _rank_T(rank):
+    """Ranks hold batches of different sizes (64 and 96 tokens)."""
+    return T_LOCAL + 32 * rank
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
@@ -30,7 +35,7 @@ class _Cfg:
 
 def _rank_counts(rank):
     rng = np.random.default_rng(100 + rank)
-    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T_LOCAL)])
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(_rank_T(rank))])
     return np.bincount(idx.reshape(-1), minlength=E).astype(np.int32)
 
 
@@ -48,7 +53,7 @@ def _worker(rank, world, port, out):
         b.copy_(torch.from_numpy(nb))
         return b
 
-    parallel.balance_step(_Cfg(T_LOCAL), counts, bias, update)
+    parallel.balance_step(_Cfg(_rank_T(rank)), counts, bias, update)
     out[rank] = (counts.numpy().copy(), bias.numpy().copy(), seen["T"])
     dist.destroy_process_group()
 
@@ -70,13 +75,14 @@ def test_two_rank_balance_step_keeps_biases_equal():
     total = _rank_counts(0) + _rank_counts(1)
     np.testing.assert_array_equal(c0, total)
     np.testing.assert_array_equal(c1, total)
-    assert t0 == t1 == 2 * T_LOCAL
+    T_all = _rank_T(0) + _rank_T(1)
+    assert t0 == t1 == T_all
     assert np.array_equal(b0.view(np.uint32), b1.view(np.uint32))
     # equals one process updating on the whole batch
-    want, _ = O.update_bias(total, np.full(E, 0.25, np.float32), 2 * T_LOCAL, K, 1e-3)
+    want, _ = O.update_bias(total, np.full(E, 0.25, np.float32), T_all, K, 1e-3)
     assert np.array_equal(b0.view(np.uint32), want.view(np.uint32))
     # and differs from what rank 0 alone would have done on its half
-    alone, _ = O.update_bias(_rank_counts(0), np.full(E, 0.25, np.float32), T_LOCAL, K, 1e-3)
+    alone, _ = O.update_bias(_rank_counts(0), np.full(E, 0.25, np.float32), _rank_T(0), K, 1e-3)
     assert not np.array_equal(alone, want)
 
 
@@ -96,7 +102,7 @@ def _worker_peer_dies(rank, world, port, out):
     bias = torch.zeros((E,), dtype=torch.float32)
     t0 = time.monotonic()
     try:
-        parallel.balance_step(_Cfg(T_LOCAL), counts, bias, lambda cfg, c, b: b)
+        parallel.balance_step(_Cfg(T_LOCAL), counts, bias, lambda cfg, c, b: b, T_global=2 * T_LOCAL)
         out[rank] = ("no error", time.monotonic() - t0)
     except Exception as e:               # noqa: BLE001  (gloo raises RuntimeError)
         out[rank] = (type(e).__name__, time.monotonic() - t0)
