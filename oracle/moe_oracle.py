@@ -256,7 +256,7 @@ def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
 def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
               add_residual: int = 1, tokens=None, n_groups: int = 0,
               topk_groups: int = 0, norm_w=None, norm_eps: float = 1e-6,
-              act: str = "bf16") -> dict:
+              act: str = "bf16", idx=None) -> dict:
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
@@ -269,7 +269,12 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     experts read u = RMSNorm(x) held in the activation type ``act`` (rounded
     once), and the residual adds x itself (h = x + MoE(RMSNorm(x))).
 
-    Returns out (fp64), delta = out - residual, idx, gates, margin."""
+    ``idx`` [n, K], when given, replaces the router's own choice for these
+    tokens (another valid top-K where keys tie within rounding); the gates
+    are then those of eq. (13)/(14) for that choice and the margin is NaN.
+
+    Returns out (fp64), delta = out - residual, idx, gates, margin, and the
+    scores s [n, E] of every expert."""
     x = inp["x"]
     if tokens is not None:
         tokens = np.asarray(tokens, dtype=np.int64)
@@ -280,8 +285,14 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     else:
         u = resid
     n = u.shape[0]
-    idx, gates, margin, _ = route(u, inp["centroids"], inp["bias"], K, score_func,
-                                  normalize, n_groups, topk_groups)
+    if idx is None:
+        idx, gates, margin, scores = route(u, inp["centroids"], inp["bias"], K, score_func,
+                                           normalize, n_groups, topk_groups)
+    else:
+        scores = expert_scores(affinity_logits(u, inp["centroids"]), score_func)
+        idx = np.asarray(idx, dtype=np.int32).reshape(n, K)
+        gates = gate_values(scores, idx, normalize)
+        margin = np.full(n, np.nan)
     d = u.shape[1]
     delta = np.zeros((n, d))
     S = inp["ws13"].shape[0]
@@ -295,7 +306,8 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     for k in range(K):
         delta += gates[:, k:k + 1] * routed[:, k]
     out = delta + resid if add_residual else delta.copy()
-    return {"out": out, "delta": delta, "idx": idx, "gates": gates, "margin": margin}
+    return {"out": out, "delta": delta, "idx": idx, "gates": gates, "margin": margin,
+            "scores": scores}
 
 
 def _torch_index(tokens, ref):

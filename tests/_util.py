@@ -27,6 +27,93 @@ def gpu_inputs(cfg, seed=None):
     return g, c
 
 
+def valid_topk_choice(chosen, keys, K, gscore=None, topk_groups=0, tol=MARGIN_EXCLUDE):
+    """True when `chosen` (the K expert ids a kernel picked for one token) is a
+    top-K of the oracle's fp32 keys [E] that rounding could have produced:
+    K distinct ids, and no unchosen key above the smallest chosen key by more
+    than tol.  With node-limited routing (gscore [G] = the oracle's group
+    scores, topk_groups = M) the kept groups are unknown, so every M-subset G*
+    of the groups that is itself a valid top-M within tol (min over G* >= max
+    outside - tol) is tried: the choice is valid if for one such G* every
+    chosen expert lies in G* and is a top-K within tol of G*'s experts."""
+    chosen = np.asarray(chosen, dtype=np.int64)
+    E = keys.shape[0]
+    if len(set(chosen.tolist())) != K or chosen.min() < 0 or chosen.max() >= E:
+        return False
+    keys = np.asarray(keys, dtype=np.float64)
+
+    def topk_ok(allowed):
+        if not allowed[chosen].all():
+            return False
+        rest = allowed.copy()
+        rest[chosen] = False
+        return (not rest.any()) or keys[chosen].min() >= keys[rest].max() - tol
+
+    if gscore is None:
+        return topk_ok(np.ones(E, dtype=bool))
+    G = gscore.shape[0]
+    gs = E // G
+    order = np.sort(gscore)[::-1]
+    thr = order[topk_groups - 1]
+    cand = [g for g in range(G) if gscore[g] >= thr - tol]
+    assert len(cand) <= topk_groups + 6, "too many groups within tol to enumerate"
+    import itertools
+    for sub in itertools.combinations(cand, topk_groups):
+        inside = np.zeros(G, dtype=bool)
+        inside[list(sub)] = True
+        if (~inside).any() and gscore[inside].min() < gscore[~inside].max() - tol:
+            continue
+        if topk_ok(np.repeat(inside, gs)):
+            return True
+    return False
+
+
+def check_near_ties(cfg, idx_g, margin, scores, bias, gates_g=None, tol=MARGIN_EXCLUDE):
+    """Tokens whose K-th vs (K+1)-th key margin (or group margin) in the oracle
+    is below tol are excluded from the bit-exact comparison; each of them must
+    still carry a valid choice (valid_topk_choice on the oracle's fp32 keys
+    and, with node-limited routing, its group scores), and, when gates_g is
+    given, the gates of eq. (13)/(14) for that choice within GATE_ATOL.
+    Returns (keep, n_excluded): keep marks the tokens compared bit-exactly."""
+    from oracle import moe_oracle as O
+    keep = np.asarray(margin) >= tol
+    excl = np.nonzero(~keep)[0]
+    if excl.size:
+        s = np.asarray(scores)[excl]
+        if gates_g is not None:
+            want = O.gate_values(s, np.asarray(idx_g)[excl], cfg.normalize)
+            np.testing.assert_allclose(np.asarray(gates_g)[excl], want, rtol=0, atol=GATE_ATOL)
+        keys = O.selection_keys(s, bias).astype(np.float64)
+        gsc = None
+        if cfg.n_groups:
+            gs = cfg.E // cfg.n_groups
+            gsc = s.astype(np.float32).astype(np.float64).reshape(len(excl), cfg.n_groups,
+                                                                  gs).sum(axis=2)
+        for j, t in enumerate(excl):
+            assert valid_topk_choice(idx_g[t], keys[j], cfg.K,
+                                     None if gsc is None else gsc[j], cfg.topk_groups, tol), \
+                f"token {t}: chosen {sorted(idx_g[t].tolist())} is not a top-{cfg.K} " \
+                f"within {tol} of the oracle's keys"
+    return keep, int(excl.size)
+
+
+def with_gpu_choice(ref, idx_g, keep, rerun):
+    """The oracle result `ref` (a moe_layer dict over some tokens) with the
+    rows of the excluded tokens (~keep, already validated by check_near_ties)
+    recomputed by the oracle on the kernel's own choice of experts:
+    rerun(rows, idx) must return moe_layer(..., tokens=<those rows' token
+    ids>, idx=idx).  Every token is then comparable."""
+    rows = np.nonzero(~np.asarray(keep))[0]
+    if rows.size == 0:
+        return ref
+    sub = rerun(rows, np.asarray(idx_g)[rows])
+    out = dict(ref)
+    for k in ("out", "delta", "idx", "gates"):
+        out[k] = np.array(ref[k], copy=True)
+        out[k][rows] = sub[k]
+    return out
+
+
 def rel_frob(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)

@@ -1,10 +1,14 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
 Routing: expert indices bit-exact and gates within 1e-5, except tokens whose
-K-th vs (K+1)-th biased-key margin is below 1e-5 (excluded and counted).
+K-th vs (K+1)-th biased-key margin is below 1e-5 (excluded and counted); each
+excluded token must still hold a valid top-K of the oracle's keys within 1e-5
+and the gates of that choice, and its output is compared with the oracle's
+layer on that choice.
 Dispatch: counts, offsets, perm_tok, pos bit-exact on the same indices;
 dispatched rows byte-equal to their token rows.  Layer outputs: relative
-Frobenius and max-abs error of the MoE term within the dtype's bar."""
+Frobenius and max-abs error of the MoE term within the dtype's bar, on every
+token."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +16,7 @@ import torch
 from moe_inputs import small_cases, get_config, make_inputs
 from oracle import moe_oracle as O
 from tests._util import (GpuRun, gpu_inputs, assert_close, to_np, GATE_ATOL, MARGIN_EXCLUDE,
-                         rel_frob)
+                         rel_frob, check_near_ties, with_gpu_choice)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,16 +42,17 @@ def _layer(cfg, c, **kw):
                        topk_groups=cfg.topk_groups, **kw)
 
 
-def _check_routing(cfg, idx_g, gates_g, idx_o, gates_o, margin, keys_o=None):
+def _check_routing(cfg, idx_g, gates_g, idx_o, gates_o, margin, scores, bias, keys_o=None):
     """Chosen sets bit-exact and gates within 1e-5 on tokens whose K-th vs
     (K+1)-th key margin is >= 1e-5.  The listing order (by descending key) must
     match wherever adjacent keys differ by >= 1e-5; closer keys may come in
-    either order but must still be non-increasing within 1e-5."""
+    either order but must still be non-increasing within 1e-5.  Every
+    excluded (near-tie) token must hold a valid top-K of the oracle's keys
+    within 1e-5 and the gates of that choice (check_near_ties)."""
     T, K, E = idx_g.shape[0], cfg.K, cfg.E
     assert np.all((idx_g >= 0) & (idx_g < E))
     assert all(len(set(r.tolist())) == K for r in idx_g)          # K distinct, no drop
-    keep = margin >= MARGIN_EXCLUDE
-    n_excl = int((~keep).sum())
+    keep, n_excl = check_near_ties(cfg, idx_g, margin, scores, bias, gates_g)
     assert n_excl <= max(2, T // 50), f"{n_excl} near-tie tokens excluded of {T}"
     og = np.argsort(idx_g, axis=1, kind="stable")
     oo = np.argsort(idx_o, axis=1, kind="stable")
@@ -69,6 +74,15 @@ def _keys(cfg, c, s):
     return s + O._f64(c["bias"])[None, :]
 
 
+def _ties_on_gpu_choice(cfg, c, ref, idx_g, keep, tokens=None, **kw):
+    """ref with the near-tie tokens' rows recomputed by the oracle on the GPU's
+    (validated) choice, so that every token's output is compared.  idx_g and
+    keep are indexed like ref's rows; tokens maps them to token ids."""
+    tok = np.arange(len(keep)) if tokens is None else np.asarray(tokens)
+    return with_gpu_choice(ref, idx_g, keep,
+                           lambda rows, idx: _layer(cfg, c, tokens=tok[rows], idx=idx, **kw))
+
+
 # ---------------------------------------------------------------- router
 
 @pytest.mark.parametrize("name", SMALL + FULL)
@@ -81,7 +95,7 @@ def test_route_parity(name):
     assert run.status() == 0
     idx_o, gates_o, margin, s = _route_oracle(cfg, c)
     _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), idx_o, gates_o, margin,
-                   _keys(cfg, c, s))
+                   s, c["bias"], _keys(cfg, c, s))
 
 
 def test_route_bias_forces_expert_and_keeps_gate():
@@ -96,7 +110,8 @@ def test_route_bias_forces_expert_and_keeps_gate():
     cb = dict(c)
     cb["bias"] = g["bias"].cpu()
     idx_o, gates_o, margin, s = _route_oracle(cfg, cb)
-    _check_routing(cfg, idx, run.gates.cpu().numpy(), idx_o, gates_o, margin, _keys(cfg, cb, s))
+    _check_routing(cfg, idx, run.gates.cpu().numpy(), idx_o, gates_o, margin, s, cb["bias"],
+                   _keys(cfg, cb, s))
 
 
 def test_route_group_limited_v3_full_size():
@@ -112,7 +127,7 @@ def test_route_group_limited_v3_full_size():
     idx_g = run.idx.cpu().numpy()
     assert max(len(set((r // 32).tolist())) for r in idx_g) <= 4
     idx_o, gates_o, margin, s = _route_oracle(cfg, c)
-    _check_routing(cfg, idx_g, run.gates.cpu().numpy(), idx_o, gates_o, margin)
+    _check_routing(cfg, idx_g, run.gates.cpu().numpy(), idx_o, gates_o, margin, s, c["bias"])
 
 
 # ---------------------------------------------------------------- dispatch
@@ -190,9 +205,11 @@ def test_forward_parity_all_tokens(name):
     torch.cuda.synchronize()
     assert run.status() == 0
     ref = _layer(cfg, c, add_residual=0)
-    keep, _ = _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), ref["idx"],
-                             ref["gates"], ref["margin"])
-    assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, f"{name} forward")
+    idx_g = run.idx.cpu().numpy()
+    keep, _ = _check_routing(cfg, idx_g, run.gates.cpu().numpy(), ref["idx"], ref["gates"],
+                             ref["margin"], ref["scores"], c["bias"])
+    ref = _ties_on_gpu_choice(cfg, c, ref, idx_g, keep, add_residual=0)
+    assert_close(to_np(run.out), ref["delta"], cfg.act, f"{name} forward")
     # counts of the forward are the histogram of its own indices
     np.testing.assert_array_equal(run.counts.cpu().numpy(),
                                   np.bincount(run.idx.cpu().numpy().reshape(-1),
@@ -207,8 +224,11 @@ def test_forward_with_residual(name):
     run.forward()
     torch.cuda.synchronize()
     ref = _layer(cfg, c, add_residual=1)
-    keep = ref["margin"] >= MARGIN_EXCLUDE
-    assert_close(to_np(run.out)[keep], ref["out"][keep], cfg.act, f"{name} out")
+    idx_g = run.idx.cpu().numpy()
+    keep, _ = _check_routing(cfg, idx_g, run.gates.cpu().numpy(), ref["idx"], ref["gates"],
+                             ref["margin"], ref["scores"], c["bias"])
+    ref = _ties_on_gpu_choice(cfg, c, ref, idx_g, keep, add_residual=1)
+    assert_close(to_np(run.out), ref["out"], cfg.act, f"{name} out")
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -267,10 +287,11 @@ def test_forward_full_size_sampled(name):
     tok[0] = 0
     tok[-1] = cfg.T - 1                       # first and last token (ragged tail)
     ref = _layer(cfg, c, add_residual=0, tokens=tok)
-    keep = ref["margin"] >= MARGIN_EXCLUDE
-    np.testing.assert_array_equal(np.sort(idx_g[tok], 1)[keep], np.sort(ref["idx"], 1)[keep])
+    keep, _ = _check_routing(cfg, idx_g[tok], run.gates.cpu().numpy()[tok], ref["idx"],
+                             ref["gates"], ref["margin"], ref["scores"], c["bias"])
+    ref = _ties_on_gpu_choice(cfg, c, ref, idx_g[tok], keep, tokens=tok, add_residual=0)
     out = to_np(run.out)[tok]
-    assert_close(out[keep], ref["delta"][keep], cfg.act, f"{name} sampled tokens")
+    assert_close(out, ref["delta"], cfg.act, f"{name} sampled tokens")
 
 
 # ---------------------------------------------------------------- edge cases
@@ -299,9 +320,11 @@ def test_edge_cases(name):
     torch.cuda.synchronize()
     assert run.status() == 0
     ref = _layer(cfg, c, add_residual=0)
-    keep, _ = _check_routing(cfg, run.idx.cpu().numpy(), run.gates.cpu().numpy(), ref["idx"],
-                             ref["gates"], ref["margin"])
-    assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, name)
+    idx_g = run.idx.cpu().numpy()
+    keep, _ = _check_routing(cfg, idx_g, run.gates.cpu().numpy(), ref["idx"], ref["gates"],
+                             ref["margin"], ref["scores"], c["bias"])
+    ref = _ties_on_gpu_choice(cfg, c, ref, idx_g, keep, add_residual=0)
+    assert_close(to_np(run.out), ref["delta"], cfg.act, name)
 
 
 def test_hot_expert_spans_several_token_blocks():
@@ -318,8 +341,40 @@ def test_hot_expert_spans_several_token_blocks():
     torch.cuda.synchronize()
     assert run.counts[3].item() == 600
     ref = _layer(cfg, c, add_residual=0)
-    keep = ref["margin"] >= MARGIN_EXCLUDE
-    assert_close(to_np(run.out)[keep], ref["delta"][keep], cfg.act, "hot expert")
+    idx_g = run.idx.cpu().numpy()
+    keep, _ = _check_routing(cfg, idx_g, run.gates.cpu().numpy(), ref["idx"], ref["gates"],
+                             ref["margin"], ref["scores"], c["bias"])
+    ref = _ties_on_gpu_choice(cfg, c, ref, idx_g, keep, add_residual=0)
+    assert_close(to_np(run.out), ref["delta"], cfg.act, "hot expert")
+
+
+def test_bad_expert_ids_are_flagged_and_skipped():
+    """An idx row handed to moe_dispatch with an out-of-range expert id and a
+    repeated id: both (t, k) get pos = -1 and no row, the device error word
+    reports MOE_ERR_DEVICE_BOUNDS, moe_combine adds nothing for them, and
+    every other token still matches the oracle."""
+    cfg = small_cases()["small_bf16"]
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=0)
+    ref = _layer(cfg, c, add_residual=0)
+    idx = ref["idx"].astype(np.int32).copy()
+    idx[5, 1] = cfg.E + 3                     # outside [0, E)
+    idx[9, 2] = idx[9, 0]                     # the same expert twice
+    run.dispatch(torch.as_tensor(idx, device="cuda"))
+    run.experts()
+    run.combine(gates=torch.as_tensor(ref["gates"], dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert run.status() == 6                  # MOE_ERR_DEVICE_BOUNDS, then cleared
+    assert run.status() == 0
+    pos = run.pos.cpu().numpy()
+    assert pos[5, 1] == -1 and pos[9, 2] == -1
+    assert int(run.counts.cpu().numpy().sum()) == cfg.T * cfg.K - 2
+    want = ref["delta"].copy()
+    u = O._f64(c["x"])
+    for t, k in ((5, 1), (9, 2)):             # those slots contribute nothing
+        e = int(ref["idx"][t, k])
+        want[t] -= ref["gates"][t, k] * O.swiglu_ffn(u[t:t + 1], c["w13"][e], c["w2"][e])[0]
+    assert_close(to_np(run.out), want, cfg.act, "layer with rejected slots")
 
 
 def test_empty_batch():

@@ -88,6 +88,33 @@ def test_golden_swiglu():
     np.testing.assert_allclose(y[0], _rows(kv["y"])[0], rtol=0, atol=1e-14)
 
 
+def test_golden_layer_two_distinct_experts():
+    """The gate of each chosen expert multiplies that expert's own output
+    (V3 walk-through, section 3.1 with eqs. (13)-(15)): a hand-worked layer
+    whose two chosen experts differ and whose gates are unequal."""
+    kv = dict(_read("layer_two_experts_hand.txt"))
+    w13 = np.array([_rows(kv[f"w13_{e}"]) for e in range(3)])
+    w2 = np.array([_rows(kv[f"w2_{e}"]) for e in range(3)])
+    inp = {"x": np.array(_rows(kv["x"])), "centroids": np.array(_rows(kv["centroids"])),
+           "bias": np.zeros(3, np.float32), "w13": w13, "w2": w2,
+           "ws13": np.zeros((0, 2, 2)), "ws2": np.zeros((0, 2, 1))}
+    r = O.moe_layer(inp, 2, normalize=1, add_residual=0)
+    np.testing.assert_array_equal(r["idx"], np.array(_rows(kv["idx"], int)))
+    np.testing.assert_allclose(r["gates"], np.array(_rows(kv["gates"])), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["delta"], np.array(_rows(kv["out"])), rtol=0, atol=1e-12)
+    # the same choice given explicitly reproduces the layer exactly
+    r2 = O.moe_layer(inp, 2, normalize=1, add_residual=0, idx=r["idx"])
+    np.testing.assert_array_equal(r2["delta"], r["delta"])
+    assert np.all(np.isnan(r2["margin"]))
+    # another (valid-looking) choice gives that choice's gates and outputs:
+    # token 0 on experts 1 and 0 (same set, other listing order) is unchanged
+    # up to the slot order; on experts 0 and 2 it uses expert 2's output
+    r3 = O.moe_layer(inp, 2, normalize=1, add_residual=0, idx=np.array([[1, 0], [2, 1]]))
+    np.testing.assert_allclose(r3["delta"], r["delta"], rtol=0, atol=1e-14)
+    r4 = O.moe_layer(inp, 2, normalize=1, add_residual=0, idx=np.array([[0, 2], [2, 1]]))
+    assert not np.allclose(r4["delta"][0], r["delta"][0])
+
+
 # ---------------------------------------------------------------- brute force
 
 def _brute_topk(keys_row, K):

@@ -11,6 +11,9 @@ elements off.  A token whose normalised row differs that way sees routing
 keys that differ by ~1e-5, so the layer's strict routing checks (exact sets,
 gates within 1e-5) cover the tokens whose rows agree; the others must still
 pick the same experts when their K-th vs (K+1)-th margin is above 1e-3.
+Every token left out of those checks must hold a valid top-K of the oracle's
+keys (within 1e-5, or 1e-3 where its normalised row differs), and its output
+is compared with the oracle's layer on that choice.
 """
 from __future__ import annotations
 
@@ -21,7 +24,7 @@ import torch
 from moe_inputs import small_cases, get_config
 from oracle import moe_oracle as O
 from tests._util import (GpuRun, gpu_inputs, assert_close, to_np, GATE_ATOL, MARGIN_EXCLUDE,
-                         rel_frob)
+                         rel_frob, valid_topk_choice, with_gpu_choice)
 
 pytestmark = pytest.mark.gpu
 
@@ -138,7 +141,23 @@ def test_forward_prenorm_is_forward_of_normalised_tokens(name):
     assert torch.equal(a.out, b.out)
 
 
-def _check_prenorm_layer(cfg, run, ref, same_row, tol_check):
+def _validate_excluded(cfg, idx_g, ref, bias, excl, same_row):
+    """Every token left out of the exact comparison must still hold a valid
+    top-K of the oracle's keys: within 1e-5 where the normalised rows agree,
+    within 1e-3 where they differ by an ulp (the keys then differ by ~1e-5)."""
+    if not excl.any():
+        return
+    keys = O.selection_keys(ref["scores"][excl], bias).astype(np.float64)
+    for j, t in enumerate(np.nonzero(excl)[0]):
+        tol = MARGIN_EXCLUDE if same_row[t] else LOOSE_MARGIN
+        assert valid_topk_choice(idx_g[t], keys[j], cfg.K, tol=tol), \
+            f"token {t}: chosen {sorted(idx_g[t].tolist())} is not a top-{cfg.K} within {tol}"
+
+
+def _check_prenorm_layer(cfg, run, ref, same_row, bias, tol_check, rerun):
+    """Routing of the pre-normed layer against the oracle, then tol_check(ref')
+    on every token, where ref' is ref with the excluded tokens' rows recomputed
+    by rerun(rows, idx) on the GPU's (validated) choice."""
     idx_g, gates_g = run.idx.cpu().numpy(), run.gates.cpu().numpy()
     margin = ref["margin"]
     strict = (margin >= MARGIN_EXCLUDE) & same_row
@@ -153,7 +172,8 @@ def _check_prenorm_layer(cfg, run, ref, same_row, tol_check):
                                np.take_along_axis(ref["gates"], oo, 1)[strict], rtol=0,
                                atol=GATE_ATOL)
     keep = strict | loose
-    tol_check(keep)
+    _validate_excluded(cfg, idx_g, ref, bias, ~keep, same_row)
+    tol_check(with_gpu_choice(ref, idx_g, keep, rerun))
     return keep
 
 
@@ -166,19 +186,22 @@ def test_forward_prenorm_vs_oracle(name):
     run.forward_prenorm()
     torch.cuda.synchronize()
     assert m.get_status() == 0
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=ar,
-                      n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, norm_w=c["norm_w"],
-                      norm_eps=EPS, act=cfg.act)
+    def layer(**kw):
+        return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=ar,
+                           n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
+                           norm_w=c["norm_w"], norm_eps=EPS, act=cfg.act, **kw)
+
+    ref = layer()
     xn, _ = _norm_gpu(cfg, g)
     same, _, _ = _rows_agree(cfg, xn, c)
     out = to_np(run.out)
-    want = ref["out"] if ar else ref["delta"]
 
-    def tol(keep):
+    def tol(r):
         # with add_residual the oracle's residual is x itself: adding the
         # normalised tokens instead would be off by O(1)
-        assert_close(out[keep], want[keep], cfg.act, f"{name} pre-normed layer")
-    keep = _check_prenorm_layer(cfg, run, ref, same, tol)
+        assert_close(out, r["out"] if ar else r["delta"], cfg.act, f"{name} pre-normed layer")
+    keep = _check_prenorm_layer(cfg, run, ref, same, c["bias"], tol,
+                                lambda rows, ix: layer(tokens=rows, idx=ix))
     assert keep.mean() >= 0.9
     np.testing.assert_array_equal(run.counts.cpu().numpy(),
                                   np.bincount(run.idx.cpu().numpy().reshape(-1), minlength=cfg.E))
@@ -210,22 +233,26 @@ def test_forward_fp8_prenorm_vs_oracle(name):
 
     r0, r1 = run_fp8(0), run_fp8(1)
     assert torch.equal(r0.idx, r1.idx) and torch.equal(r0.gates, r1.gates)
-    ref = O.moe_layer(c, K, cfg.normalize, cfg.score_func, add_residual=1, norm_w=c["norm_w"],
-                      norm_eps=EPS, act=cfg.act)
+    def layer(**kw):
+        return O.moe_layer(c, K, cfg.normalize, cfg.score_func, add_residual=1,
+                           norm_w=c["norm_w"], norm_eps=EPS, act=cfg.act, **kw)
+
+    ref = layer()
     xn, _ = _norm_gpu(cfg, g)
     same, _, _ = _rows_agree(cfg, xn, c)
     got0, got1 = to_np(r0.out), to_np(r1.out)
 
-    def tol(keep):
-        r = rel_frob(got0[keep], ref["delta"][keep])
-        assert r <= 5e-2, f"relative Frobenius of the MoE term {r:.3e}"
+    def tol(r):
+        rf = rel_frob(got0, r["delta"])
+        assert rf <= 5e-2, f"relative Frobenius of the MoE term {rf:.3e}"
         # the residual is x itself (the normalised tokens would be off by
         # O(1)): with and without it the outputs differ by x, up to the two
         # bf16 roundings
-        res = got1[keep] - got0[keep] - to_np(g["x"])[keep]
-        bound = 2.0 ** -8 * (np.abs(got1[keep]) + np.abs(got0[keep])) + 1e-6
+        res = got1 - got0 - to_np(g["x"])
+        bound = 2.0 ** -8 * (np.abs(got1) + np.abs(got0)) + 1e-6
         assert np.all(np.abs(res) <= bound)
-    _check_prenorm_layer(cfg, r0, ref, same, tol)
+    _check_prenorm_layer(cfg, r0, ref, same, c["bias"], tol,
+                         lambda rows, ix: layer(tokens=rows, idx=ix))
 
 
 def test_forward_prenorm_full_size_sampled():
@@ -245,12 +272,18 @@ def test_forward_prenorm_full_size_sampled():
     rng = np.random.default_rng(4321)
     tok = np.sort(rng.choice(cfg.T, 8, replace=False))
     tok[0], tok[-1] = 0, cfg.T - 1
-    ref = O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=1, tokens=tok,
-                      norm_w=c["norm_w"], norm_eps=EPS, act=cfg.act)
+    def layer(**kw):
+        return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=1,
+                           norm_w=c["norm_w"], norm_eps=EPS, act=cfg.act, **kw)
+
+    ref = layer(tokens=tok)
     xn, _ = _norm_gpu(cfg, g)
     same, _, _ = _rows_agree(cfg, xn, c, tok)
     margin = ref["margin"]
     keep = ((margin >= MARGIN_EXCLUDE) & same) | ((margin >= LOOSE_MARGIN) & ~same)
     np.testing.assert_array_equal(np.sort(idx_g[tok], 1)[keep], np.sort(ref["idx"], 1)[keep])
+    _validate_excluded(cfg, idx_g[tok], ref, c["bias"], ~keep, same)
+    ref = with_gpu_choice(ref, idx_g[tok], keep,
+                          lambda rows, ix: layer(tokens=tok[rows], idx=ix))
     out = to_np(run.out)[tok]
-    assert_close(out[keep], ref["out"][keep], cfg.act, "V3 prefill pre-normed, sampled tokens")
+    assert_close(out, ref["out"], cfg.act, "V3 prefill pre-normed, sampled tokens")

@@ -5,7 +5,8 @@ in a fixed array inside the library instead of a caller workspace.
 
 The file is named to be collected last.  Each case calls the new entry point
 twice in a row through the C ABI and checks both results against moe_experts
-(the workspace entry point) within the layer-output tolerance of the suite.
+(the workspace entry point) within the layer-output tolerance of the suite,
+and, since both run the same deterministic kernels, bit for bit.
 """
 import ctypes
 
@@ -51,6 +52,8 @@ def test_experts_static_matches_workspace_entry_point(name):
         assert m.get_status() == 0
         assert_close(to_np(act), act_ref, cfg.act, f"{name} act, call {call}")
         assert_close(to_np(y), y_ref, cfg.act, f"{name} y, call {call}")
+        # both entry points run the same deterministic kernels: bit for bit
+        assert torch.equal(act, run.act) and torch.equal(y, run.y), f"{name} call {call}"
 
 
 def test_experts_static_rejects_bad_arguments():
