@@ -192,11 +192,21 @@ ForwardLayout forward_layout(const moe_cfg_t& c) {
   return L;
 }
 
-// Pre-normed forward: the forward's workspace, then the normalised tokens.
-size_t prenorm_ws(const moe_cfg_t& c) {
-  return forward_layout(c).total +
-         align_up(static_cast<size_t>(c.T) * c.d * esize(c.act_dtype), 256);
+// Pre-normed forward: the forward's workspace, then the normalised tokens
+// (the shared experts' input), the weighted centroids w * e_i and inv_rms.
+struct PrenormLayout {
+  size_t xs, ew, inv, total;
+};
+int centroid_dtype(const moe_cfg_t& c) { return c.wgt_dtype == MOE_E4M3 ? MOE_BF16 : c.wgt_dtype; }
+PrenormLayout prenorm_layout(const moe_cfg_t& c) {
+  PrenormLayout L{};
+  L.xs = forward_layout(c).total;
+  L.ew = L.xs + align_up(static_cast<size_t>(c.T) * c.d * esize(c.act_dtype), 256);
+  L.inv = L.ew + align_up(static_cast<size_t>(c.E) * c.d * esize(centroid_dtype(c)), 256);
+  L.total = L.inv + align_up(static_cast<size_t>(c.T) * sizeof(float), 256);
+  return L;
 }
+size_t prenorm_ws(const moe_cfg_t& c) { return prenorm_layout(c).total; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -225,10 +235,20 @@ P* at(void* base, size_t off) {
 
 // ---------------------------------------------------------------- step bodies (no checks)
 
+// row_scale [T] (optional): each token's logits are multiplied by it (the
+// layer behind its RMSNorm, routed from the raw tokens; two-kernel router).
 moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
                       const float* bias, int32_t* idx, float* gates, void* ws,
-                      cudaStream_t st, float* scores = nullptr) {
+                      cudaStream_t st, float* scores = nullptr,
+                      const float* row_scale = nullptr) {
   if (c.act_dtype == MOE_BF16) {
+    // E <= 256: one fused kernel, logits reduced on chip
+    FusedRouterPlan fp{};
+    if (!row_scale && fused_router_plan(c.T, c.d, c.E, &fp))
+      return launch_router_fused(fp, x, centroids, bias, c.T, c.d, c.E, c.K, c.score_func,
+                                 c.normalize, c.n_groups, c.topk_groups, idx, gates, scores, 0.f,
+                                 nullptr, device_status_word(), kWaitTimeoutNs, st);
+    // otherwise the split-K router GEMM into fp32 partials, then the top-K kernel
     const RouterPlan p = router_plan(c);
     float* partial = static_cast<float*>(ws);
     GemmMaps maps{};
@@ -258,7 +278,8 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
     moe_status_t s = launch_gemm_tc(GM_ROUTER, maps, a, grid, st);
     if (s != MOE_OK) return s;
     return launch_topk(partial, p.splits, a.out_split_stride, bias, c.T, c.E, c.K, c.score_func,
-                       c.normalize, c.n_groups, c.topk_groups, idx, gates, st, scores);
+                       c.normalize, c.n_groups, c.topk_groups, idx, gates, st, scores,
+                       row_scale);
   }
   float* logits = static_cast<float*>(ws);
   moe_status_t s = launch_logits_f32(static_cast<const float*>(x),
@@ -266,7 +287,7 @@ moe_status_t do_route(const moe_cfg_t& c, const void* x, const void* centroids,
                                      st);
   if (s != MOE_OK) return s;
   return launch_topk(logits, 1, 0, bias, c.T, c.E, c.K, c.score_func, c.normalize, c.n_groups,
-                     c.topk_groups, idx, gates, st, scores);
+                     c.topk_groups, idx, gates, st, scores, row_scale);
 }
 
 // w8 (an FP8 layer's e4m3 weights and block scales) replaces w13..ws2: the
@@ -923,6 +944,112 @@ moe_status_t do_forward_fp8(const moe_cfg_t& c, const void* xin, const void* xre
                         c.d, fr.P, fr.Tp, c.add_residual, st);
 }
 
+// Router of the layer behind its RMSNorm (V3 walk-through, section 4.1):
+// the logit (x * inv_rms * w) . e_i is computed as inv_rms * (x . (w * e_i))
+// from the raw tokens and the weighted centroids ew = w * e (folded here).
+// Fused router (bf16, E <= 256): inv_rms comes from the router kernel and the
+// normalised tokens are formed later by the dispatch (*fused = true).
+// Otherwise the RMSNorm kernel writes xn and inv_rms, and the two-kernel
+// router scales its logits by inv_rms.
+moe_status_t do_route_prenorm(const moe_cfg_t& c, const void* x, const float* norm_w, float eps,
+                              const void* centroids, const float* bias, int32_t* idx,
+                              float* gates, const PrenormLayout& P, void* ws, cudaStream_t st,
+                              bool* fused) {
+  void* ew = at<void>(ws, P.ew);
+  float* inv = at<float>(ws, P.inv);
+  moe_status_t s;
+  if ((s = launch_fold_centroids(centroid_dtype(c), centroids, norm_w, c.E, c.d, ew, st)) !=
+      MOE_OK)
+    return s;
+  FusedRouterPlan fp{};
+  *fused = c.act_dtype == MOE_BF16 && fused_router_plan(c.T, c.d, c.E, &fp);
+  if (*fused)
+    return launch_router_fused(fp, x, ew, bias, c.T, c.d, c.E, c.K, c.score_func, c.normalize,
+                               c.n_groups, c.topk_groups, idx, gates, nullptr, eps, inv,
+                               device_status_word(), kWaitTimeoutNs, st);
+  if ((s = launch_rmsnorm(c.act_dtype, x, norm_w, eps, c.T, c.d, at<void>(ws, P.xs), inv, st)) !=
+      MOE_OK)
+    return s;
+  return do_route(c, x, ew, bias, idx, gates, at<void>(ws, forward_layout(c).route), st, nullptr,
+                  inv);
+}
+
+// The layer behind its RMSNorm, bf16 or fp32 experts: the experts read the
+// normalised tokens (rounded once to the activation type), the residual is x.
+moe_status_t do_forward_prenorm(const moe_cfg_t& c, const void* x, const float* norm_w, float eps,
+                                const void* centroids, const float* bias, const void* w13,
+                                const void* w2, const void* ws13, const void* ws2, int32_t* idx,
+                                float* gates, int32_t* counts, void* out, void* ws,
+                                cudaStream_t st) {
+  const ForwardLayout L = forward_layout(c);
+  const PrenormLayout P = prenorm_layout(c);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  void* xp = at<void>(ws, L.xp);
+  void* xs = at<void>(ws, P.xs);
+  moe_status_t s;
+  bool fused = false;
+  if ((s = do_route_prenorm(c, x, norm_w, eps, centroids, bias, idx, gates, P, ws, st, &fused)) !=
+      MOE_OK)
+    return s;
+  if (fused) {
+    // one read of each token row: normalised, rounded and written to its K
+    // rows and its shared-expert row
+    if ((s = launch_dispatch_index(idx, c.T, c.K, c.E, 1, counts, offsets, perm, pos,
+                                   at<int32_t>(ws, L.dispatch), st)) != MOE_OK)
+      return s;
+    if ((s = launch_scatter_norm(x, at<float>(ws, P.inv), norm_w, c.T, c.K, c.d, pos, xp,
+                                 c.S > 0 ? xs : nullptr, st)) != MOE_OK)
+      return s;
+  } else if ((s = launch_dispatch(xs, static_cast<size_t>(c.d) * esize(c.act_dtype), idx, c.T,
+                                  c.K, c.E, counts, offsets, xp, perm, pos,
+                                  at<int32_t>(ws, L.dispatch), st)) != MOE_OK) {
+    return s;
+  }
+  if ((s = do_experts(c, xp, xs, offsets, w13, w2, ws13, ws2, at<void>(ws, L.act),
+                      at<void>(ws, L.y), at<void>(ws, L.experts), st)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, at<void>(ws, L.y), gates, pos, x, out, c.T, c.K, c.S, c.d,
+                        static_cast<long long>(c.T) * c.K, c.T, c.add_residual, st);
+}
+
+// The FP8 layer behind its RMSNorm: the dispatch quantises the normalised
+// tokens (bf16-rounded, then 1 x 128 e4m3 tiles) in its single read of x.
+moe_status_t do_forward_fp8_prenorm(const moe_cfg_t& c, const void* x, const float* norm_w,
+                                    float eps, const void* centroids, const float* bias,
+                                    const moe_fp8_weights_t* w, int32_t* idx, float* gates,
+                                    int32_t* counts, void* out, void* ws, cudaStream_t st) {
+  const ForwardLayout L = forward_layout(c);
+  const PrenormLayout P = prenorm_layout(c);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  const Fp8Rows fr = fp8_rows(c);
+  moe_status_t s;
+  bool fused = false;
+  if ((s = do_route_prenorm(c, x, norm_w, eps, centroids, bias, idx, gates, P, ws, st, &fused)) !=
+      MOE_OK)
+    return s;
+  if ((s = launch_dispatch_index(idx, c.T, c.K, c.E, 4, counts, offsets, perm, pos,
+                                 at<int32_t>(ws, L.dispatch), st)) != MOE_OK)
+    return s;
+  const int shared_row = c.S > 0 ? static_cast<int>(fr.P) : -1;
+  if (fused)
+    s = launch_scatter_quant_norm(x, at<float>(ws, P.inv), norm_w, c.T, c.K, c.d, pos, shared_row,
+                                  at<void>(ws, L.xp), at<float>(ws, L.xs), fr.rows_in, st);
+  else
+    s = launch_scatter_quant(at<void>(ws, P.xs), c.T, c.K, c.d, pos, shared_row,
+                             at<void>(ws, L.xp), at<float>(ws, L.xs), fr.rows_in, st);
+  if (s != MOE_OK) return s;
+  if ((s = do_experts_fp8(c, at<void>(ws, L.xp), at<float>(ws, L.xs), offsets, counts, *w,
+                          at<void>(ws, L.act), at<float>(ws, L.act_s), at<void>(ws, L.y),
+                          at<void>(ws, L.experts), st)) != MOE_OK)
+    return s;
+  return launch_combine(c.act_dtype, at<void>(ws, L.y), gates, pos, x, out, c.T, c.K, c.S, c.d,
+                        fr.P, fr.Tp, c.add_residual, st);
+}
+
 moe_status_t forward_empty(const moe_cfg_t& c, int32_t* counts, cudaStream_t st) {
   TraceScope tr(st, "forward_empty");
   cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st);
@@ -981,11 +1108,8 @@ moe_status_t moe_forward_prenorm(const moe_cfg_t* cfg, const void* x, const floa
     return s;
   if (c.S > 0 && (s = check_ptrs(c, {ws13, ws2}, {})) != MOE_OK) return s;
   if ((s = check_ws(ws, ws_bytes, prenorm_ws(c))) != MOE_OK) return s;
-  void* xn = at<void>(ws, forward_layout(c).total);
-  if ((s = launch_rmsnorm(c.act_dtype, x, norm_w, eps, c.T, c.d, xn, nullptr, st)) != MOE_OK)
-    return s;
-  return do_forward(c, xn, x, centroids, bias, w13, w2, ws13, ws2, idx, gates, counts, out, ws,
-                    st);
+  return do_forward_prenorm(c, x, norm_w, eps, centroids, bias, w13, w2, ws13, ws2, idx, gates,
+                            counts, out, ws, st);
 }
 
 moe_status_t moe_forward_fp8_prenorm(const moe_cfg_t* cfg, const void* x, const float* norm_w,
@@ -1003,10 +1127,8 @@ moe_status_t moe_forward_fp8_prenorm(const moe_cfg_t* cfg, const void* x, const 
   if ((s = check_ptrs(c, {x, norm_w, centroids, out}, {bias, idx, gates})) != MOE_OK) return s;
   if ((s = check_fp8_weights(c, w)) != MOE_OK) return s;
   if ((s = check_ws(ws, ws_bytes, prenorm_ws(c))) != MOE_OK) return s;
-  void* xn = at<void>(ws, forward_layout(c).total);
-  if ((s = launch_rmsnorm(c.act_dtype, x, norm_w, eps, c.T, c.d, xn, nullptr, st)) != MOE_OK)
-    return s;
-  return do_forward_fp8(c, xn, x, centroids, bias, w, idx, gates, counts, out, ws, st);
+  return do_forward_fp8_prenorm(c, x, norm_w, eps, centroids, bias, w, idx, gates, counts, out,
+                                ws, st);
 }
 
 moe_status_t moe_experts_w8a16(const moe_cfg_t* cfg, const void* xp, const void* x,

@@ -173,14 +173,62 @@ __global__ void __launch_bounds__(256) scatter_kernel(const V* __restrict__ x, i
   }
 }
 
+// 8 bf16 of x scaled by inv and the per-channel weights w0 (4) and w1 (4), in
+// fp32 as (x * inv) * w, rounded once to bf16 (the RMSNorm kernel's rounding).
+__device__ __forceinline__ uint4 norm_bf16x8(const uint4& v, float inv, const float4& w0,
+                                             const float4& w1) {
+  const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+  uint4 o;
+  __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(h[k]);
+    oh[k] = __floats2bfloat162_rn((f.x * inv) * wv[2 * k], (f.y * inv) * wv[2 * k + 1]);
+  }
+  return o;
+}
+
+// Dispatch behind the RMSNorm: each token row is read once, normalised with
+// its inv_rms and the norm weights, and written to its K rows of xp and to its
+// shared-expert row of xs (when xs is not null).
+__global__ void __launch_bounds__(256) scatter_norm_kernel(
+    const uint4* __restrict__ x, const float* __restrict__ inv_rms,
+    const float4* __restrict__ w, int T, int K, int vpr, const int32_t* __restrict__ pos,
+    uint4* __restrict__ xp, uint4* __restrict__ xs, int tok_per_cta) {
+  __shared__ int dst[8][kMaxK];
+  const int t0 = blockIdx.x * tok_per_cta;
+  for (int i = threadIdx.x; i < tok_per_cta * K; i += blockDim.x) {
+    const int tl = i / K, k = i % K;
+    if (t0 + tl < T) dst[tl][k] = __ldg(pos + static_cast<size_t>(t0 + tl) * K + k);
+  }
+  __syncthreads();
+  for (int tl = 0; tl < tok_per_cta; ++tl) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    const float inv = __ldg(inv_rms + t);
+    const uint4* src = x + static_cast<size_t>(t) * vpr;
+    for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+      const uint4 val = norm_bf16x8(__ldg(src + v), inv, __ldg(w + 2 * v), __ldg(w + 2 * v + 1));
+      for (int k = 0; k < K; ++k)
+        if (dst[tl][k] >= 0) xp[static_cast<size_t>(dst[tl][k]) * vpr + v] = val;
+      if (xs) xs[static_cast<size_t>(t) * vpr + v] = val;
+    }
+  }
+}
+
 // FP8 dispatch: each token row is read once (bf16), cut into 1 x 128 tiles
 // (V3 walk-through, section 4.3), each tile scaled by 448 / max|x| and
 // rounded to e4m3, and written to the token's K expert rows and to its
 // shared-expert row.  Scales (max|x| / 448) go K-block-major:
 // xs[kb * ld_s + row].  Sixteen threads hold one tile (8 values each).
+// NORM: the row is first normalised as in scatter_norm_kernel (bf16 values
+// of the normalised row are what gets quantised).
+template <bool NORM>
 __global__ void __launch_bounds__(256) scatter_quant_kernel(
     const uint4* __restrict__ x, int T, int K, int d, const int32_t* __restrict__ pos,
-    int shared_row, uint2* __restrict__ xq, float* __restrict__ xs, long long ld_s) {
+    int shared_row, uint2* __restrict__ xq, float* __restrict__ xs, long long ld_s,
+    const float* __restrict__ inv_rms, const float4* __restrict__ w) {
   const int t = blockIdx.x;
   if (t >= T) return;
   __shared__ int dst[kMaxK + 1];
@@ -193,7 +241,9 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(
     const bool in = v < vpr;                    // a 16-lane group is all in or all out
     float f[8];
     if (in) {
-      const uint4 raw = __ldg(x + static_cast<size_t>(t) * vpr + v);
+      uint4 raw = __ldg(x + static_cast<size_t>(t) * vpr + v);
+      if constexpr (NORM)
+        raw = norm_bf16x8(raw, __ldg(inv_rms + t), __ldg(w + 2 * v), __ldg(w + 2 * v + 1));
       const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -235,8 +285,32 @@ moe_status_t launch_scatter_quant(const void* x, int T, int K, int d, const int3
                                   cudaStream_t stream) {
   if (T <= 0) return MOE_OK;
   TraceScope tr(stream, "dispatch_scatter_fp8");
-  scatter_quant_kernel<<<T, 256, 0, stream>>>(static_cast<const uint4*>(x), T, K, d, pos,
-                                              shared_row, static_cast<uint2*>(xq), xs, ld_s);
+  scatter_quant_kernel<false><<<T, 256, 0, stream>>>(static_cast<const uint4*>(x), T, K, d, pos,
+                                                     shared_row, static_cast<uint2*>(xq), xs,
+                                                     ld_s, nullptr, nullptr);
+  return launch_status();
+}
+
+moe_status_t launch_scatter_quant_norm(const void* x, const float* inv_rms, const float* w, int T,
+                                       int K, int d, const int32_t* pos, int shared_row, void* xq,
+                                       float* xs, long long ld_s, cudaStream_t stream) {
+  if (T <= 0) return MOE_OK;
+  TraceScope tr(stream, "dispatch_scatter_fp8_norm");
+  scatter_quant_kernel<true><<<T, 256, 0, stream>>>(
+      static_cast<const uint4*>(x), T, K, d, pos, shared_row, static_cast<uint2*>(xq), xs, ld_s,
+      inv_rms, reinterpret_cast<const float4*>(w));
+  return launch_status();
+}
+
+moe_status_t launch_scatter_norm(const void* x, const float* inv_rms, const float* w, int T,
+                                 int K, int d, const int32_t* pos, void* xp, void* xs,
+                                 cudaStream_t stream) {
+  if (T <= 0) return MOE_OK;
+  TraceScope tr(stream, "dispatch_scatter_norm");
+  const int tpc = 4;
+  scatter_norm_kernel<<<ceil_div(T, tpc), 256, 0, stream>>>(
+      static_cast<const uint4*>(x), inv_rms, reinterpret_cast<const float4*>(w), T, K, d / 8,
+      pos, static_cast<uint4*>(xp), static_cast<uint4*>(xs), tpc);
   return launch_status();
 }
 

@@ -142,6 +142,30 @@ moe_status_t launch_build_bwd_groups(const int* counts, int T, int E, int S, int
 
 int num_sms();
 
+// Fused router (router_fused.cu): logits, score, biased top-K and gates in one
+// kernel; the K splits of a token block form a thread-block cluster of ck
+// CTAs and reduce through distributed shared memory.  Applies to bf16 tokens
+// with E <= 256 experts (d a multiple of 64).
+struct FusedRouterPlan {
+  int ck;          // CTAs per cluster = K splits
+  int nb;          // tokens per block (multiple of 16, <= 256)
+  int kps;         // K steps (64 wide) per split
+  int nblocks;     // token blocks
+  int nclusters;   // clusters launched (each walks blocks cid, cid + nclusters, ...)
+};
+bool fused_router_applies(int act_dtype, int d, int E);
+// False when the fused router does not apply or no cluster shape fits.
+bool fused_router_plan(int T, int d, int E, FusedRouterPlan* p);
+// inv_rms not null: the layer behind its RMSNorm.  centroids must then be the
+// weighted centroids w * e_i (launch_fold_centroids); the logits are scaled by
+// 1 / sqrt(mean(x^2) + norm_eps) of each raw token row x, written to inv_rms [T].
+moe_status_t launch_router_fused(const FusedRouterPlan& p, const void* x, const void* centroids,
+                                 const float* bias, int T, int d, int E, int K, int score_func,
+                                 int normalize, int n_groups, int topk_groups, int32_t* idx,
+                                 float* gates, float* scores, float norm_eps, float* inv_rms,
+                                 unsigned* status, unsigned long long timeout_ns,
+                                 cudaStream_t stream);
+
 // Token-block size and count for `rows` tokens: blocks of at most max_bs
 // (256 or 128) tokens, balanced, each a multiple of 16.
 __host__ __device__ inline void token_blocks(int rows, int* bs, int* nb, int max_bs = 256) {

@@ -8,11 +8,13 @@ namespace moe {
 
 constexpr int kDispatchChunk = 256;   // tokens per count/rank CTA (8 warps x 32)
 
-// n_groups > 0: node-limited routing over topk_groups of n_groups groups
+// n_groups > 0: node-limited routing over topk_groups of n_groups groups;
+// row_scale [T] (optional) multiplies each token's summed logits
 moe_status_t launch_topk(const float* logits, int splits, long long split_stride,
                          const float* bias, int T, int E, int K, int score_func, int normalize,
                          int n_groups, int topk_groups, int32_t* idx, float* gates,
-                         cudaStream_t stream, float* scores = nullptr);
+                         cudaStream_t stream, float* scores = nullptr,
+                         const float* row_scale = nullptr);
 moe_status_t launch_logits_f32(const float* x, const float* c, int T, int d, int E, float* out,
                                cudaStream_t stream);
 
@@ -42,6 +44,23 @@ moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, co
 // xn = x * w / sqrt(mean(x^2) + eps) per token row; inv_rms [T] optional
 moe_status_t launch_rmsnorm(int act_dtype, const void* x, const float* w, float eps, int T, int d,
                             void* xn, float* inv_rms, cudaStream_t stream);
+
+// ew = w * e per centroid row (weight dtype, rounded once from the exact product)
+moe_status_t launch_fold_centroids(int wgt_dtype, const void* e, const float* w, int E, int d,
+                                   void* ew, cudaStream_t stream);
+
+// Dispatch of the layer behind its RMSNorm (bf16): token t's row normalised on
+// the fly, xn = (x * inv_rms[t]) * w rounded once to bf16, written to its K
+// rows of xp (pos) and, when xs is not null, to row t of xs (shared experts).
+moe_status_t launch_scatter_norm(const void* x, const float* inv_rms, const float* w, int T,
+                                 int K, int d, const int32_t* pos, void* xp, void* xs,
+                                 cudaStream_t stream);
+
+// FP8 dispatch behind the RMSNorm: as launch_scatter_quant on the rows
+// xn = bf16((x * inv_rms[t]) * w), normalised on the fly.
+moe_status_t launch_scatter_quant_norm(const void* x, const float* inv_rms, const float* w, int T,
+                                       int K, int d, const int32_t* pos, int shared_row, void* xq,
+                                       float* xs, long long ld_s, cudaStream_t stream);
 
 // one bounded wait that runs out after limit_ns: the device error word gets
 // the timeout bit (failure-detection self-test)

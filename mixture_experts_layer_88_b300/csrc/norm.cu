@@ -3,12 +3,17 @@
 //   inv_rms_t = 1 / sqrt(mean_j x_tj^2 + eps),   xn_tj = x_tj * inv_rms_t * w_j
 // in fp32, rounded once to the activation type.
 //
+// Also the weighted centroids w * e_i of the router behind the RMSNorm (its
+// logit is (x * inv_rms * w) . e_i = inv_rms * (x . (w * e_i))).
+//
 // HBM-bound: one 128-thread CTA per token row.  The first pass sums the
 // squares (16-byte loads of bf16), the CTA reduces them in a fixed order, and
 // the second pass re-reads the same row (from L1/L2, so DRAM sees it once),
 // scales it and writes it with 16-byte stores.  xn may alias x: every thread
 // reads an element before it writes it, and all reads of the first pass end
 // at the CTA barrier of the reduction.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -82,7 +87,42 @@ __global__ void __launch_bounds__(kNormThreads)
   for (int i = threadIdx.x; i < d; i += kNormThreads) orow[i] = (xr[i] * inv) * __ldg(w + i);
 }
 
+// Weighted centroids of the router behind the RMSNorm: ew[i, j] = w_j * e_ij,
+// from the exact product (a float times a bf16 or float is exact in double)
+// rounded once to the weight type.
+__global__ void fold_bf16_kernel(const __nv_bfloat16* __restrict__ e, const float* __restrict__ w,
+                                 int d, long long n, __nv_bfloat16* __restrict__ ew) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const double v = static_cast<double>(__ldg(w + i % d)) *
+                     static_cast<double>(__bfloat162float(e[i]));
+    ew[i] = __double2bfloat16(v);
+  }
+}
+
+__global__ void fold_f32_kernel(const float* __restrict__ e, const float* __restrict__ w, int d,
+                                long long n, float* __restrict__ ew) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    ew[i] = static_cast<float>(static_cast<double>(__ldg(w + i % d)) * static_cast<double>(e[i]));
+}
+
 }  // namespace
+
+moe_status_t launch_fold_centroids(int wgt_dtype, const void* e, const float* w, int E, int d,
+                                   void* ew, cudaStream_t stream) {
+  if (E <= 0) return MOE_OK;
+  TraceScope tr(stream, "fold_centroids");
+  const long long n = static_cast<long long>(E) * d;
+  const int grid = static_cast<int>(std::min<long long>((n + 255) / 256, 4 * 148));
+  if (wgt_dtype == MOE_BF16)
+    fold_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(e), w, d, n,
+                                               static_cast<__nv_bfloat16*>(ew));
+  else
+    fold_f32_kernel<<<grid, 256, 0, stream>>>(static_cast<const float*>(e), w, d, n,
+                                              static_cast<float*>(ew));
+  return launch_status();
+}
 
 moe_status_t launch_rmsnorm(int act_dtype, const void* x, const float* w, float eps, int T, int d,
                             void* xn, float* inv_rms, cudaStream_t stream) {

@@ -1,0 +1,741 @@
+// Fused router of a DeepSeekMoE layer on the 5th-generation tensor cores.  One
+// kernel computes the affinity logits u_t . e_i ("DeepSeekMoE架构解析", section
+// 2.1, eq. (15)) and, per token, the score, the biased top-K and the gates
+// (eqs. (13)-(16); node-limited groups of section 2.3), and writes only idx
+// and gates (and, for the training forward, every expert's score).  The logits
+// never leave the chip.
+//
+// Behind the layer's RMSNorm (section 4.1) the same kernel reads the raw
+// tokens x: its centroids are the weighted centroids w * e_i (made by
+// launch_fold_centroids), the idle mover warps sum x^2 of every token from the
+// operand tiles while the MMAs run, and the logits are scaled by
+// inv_rms = 1 / sqrt(mean(x^2) + eps), since (x * inv_rms * w) . e_i =
+// inv_rms * (x . (w * e_i)).  inv_rms is written out for the dispatch.
+//
+// Tiling: the experts sit in the MMA's M slot (one accumulator of 128 experts,
+// two for E <= 256), a block of nb <= 256 tokens in its N slot.  The ck CTAs
+// of a thread-block cluster split the hidden dimension of one token block:
+// CTA r accumulates, in TMEM, the partial logits over K steps
+// [r kps, (r+1) kps).  The partials are reduced through distributed shared
+// memory: CTA r owns tokens [r nown, (r+1) nown) of the block (nown = nb / ck,
+// a multiple of 8); every CTA stores its partial of each other CTA's tokens
+// into that CTA's shared memory (16-byte st.shared::cluster, expert-major
+// rows), one cluster barrier later the owner adds the ck partials in rank
+// order (partial 0 + partial 1 + ...), in place, and four lanes per token
+// select the experts from shared memory.
+//
+// Warp roles (320 threads): warp 0 TMA producer (per 64-wide K step the
+// centroid boxes and the block's token rows), warp 1 TMEM owner and MMA
+// issuer, warps 2..9 the movers (two per TMEM lane quadrant: TMEM reads,
+// partial exchange, sums; behind the RMSNorm also the sums of squares); all
+// ten warps select.  The reduction buffers reuse the operand ring, idle by
+// then.  Every mbarrier wait is bounded; a CTA that times out skips its
+// remaining work but still passes every cluster barrier, so its cluster never
+// waits on it, and it lets its own loads land and its MMAs finish before it
+// frees TMEM.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "router_select.cuh"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int FR_BK = 64;                                  // K elements per stage
+constexpr uint32_t FR_ROW = 128;                           // bytes per operand row per stage
+constexpr int FR_STAGES = 3;
+constexpr uint32_t FR_A_BOX = 128 * FR_ROW;                // 16 KB: 128 centroid rows
+constexpr uint32_t FR_STAGE = 2 * FR_A_BOX + 256 * FR_ROW; // 64 KB
+constexpr uint32_t FR_RING = FR_STAGES * FR_STAGE;         // 192 KB
+constexpr uint32_t FR_EPI_MAX = 220 * 1024;              // reduction buffers (alias the ring)
+constexpr int FR_WARPS = 10;
+constexpr int FR_MOVERS = 8;                               // warps 2..9
+constexpr int FR_THREADS = FR_WARPS * 32;
+constexpr uint32_t FR_AREA = FR_EPI_MAX > FR_RING ? FR_EPI_MAX : FR_RING;
+constexpr size_t FR_SMEM = 1024 + FR_AREA + 128;
+constexpr uint32_t FR_TMEM_COLS = 512;
+constexpr int FR_TOKBOXES = 5;                             // token boxes of 16 << i rows
+
+struct FusedMaps {
+  CUtensorMap a;                  // centroids [E, d], boxes of 64 columns x 128 rows
+  CUtensorMap b[FR_TOKBOXES];     // tokens [T, d], boxes of 64 columns x (16 << i) rows
+};
+
+struct FusedArgs {
+  int T, E, K, nacc, epad, d;
+  int k_blocks, kps, ck, nb, nown, nblocks, nclusters;
+  int stride;                     // row stride (floats) of the logits buffer
+  uint32_t ss_off;                // byte offset of the sum-of-squares slots [ck][nown]
+  uint32_t inv_off;               // byte offset of the owned tokens' inv_rms [nown]
+  const float* bias;
+  int score_func, normalize, n_groups, topk_groups;
+  int32_t* idx;
+  float* gates;
+  float* scores;
+  float eps;
+  float* inv_rms;                 // not null: behind the RMSNorm (see header)
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+// Bounded wait by lane 0, result broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long timeout_ns) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0 && !tc::mbar_try_wait(bar, parity))
+    ok = tc::mbar_wait_bounded(bar, parity, abort_flag, tc::globaltimer_ns() + timeout_ns) ? 1
+                                                                                            : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Drain wait after an abort: bounded by the deadline alone.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
+                                           unsigned long long timeout_ns) {
+  if ((threadIdx.x & 31) == 0)
+    tc::mbar_wait_deadline(bar, parity, tc::globaltimer_ns() + timeout_ns);
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- selection
+// Expert keys as unique 64-bit values: the orderable bits of the fp32 key
+// s + b above the complemented expert index, so that a larger value is a
+// larger key, or an equal key of a lower expert.  0 marks an empty slot.
+using u64 = unsigned long long;
+
+__device__ __forceinline__ void cas_desc(u64& a, u64& b) {
+  const u64 hi = a > b ? a : b;
+  const u64 lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// Batcher's odd-even merge sort of 8 values, descending (19 compare-swaps).
+__device__ __forceinline__ void sort8_desc(u64 (&v)[8]) {
+  cas_desc(v[0], v[1]); cas_desc(v[2], v[3]); cas_desc(v[4], v[5]); cas_desc(v[6], v[7]);
+  cas_desc(v[0], v[2]); cas_desc(v[1], v[3]); cas_desc(v[4], v[6]); cas_desc(v[5], v[7]);
+  cas_desc(v[1], v[2]); cas_desc(v[5], v[6]);
+  cas_desc(v[0], v[4]); cas_desc(v[1], v[5]); cas_desc(v[2], v[6]); cas_desc(v[3], v[7]);
+  cas_desc(v[2], v[4]); cas_desc(v[3], v[5]);
+  cas_desc(v[1], v[2]); cas_desc(v[3], v[4]); cas_desc(v[5], v[6]);
+}
+
+// r := the 8 largest of r and c, both sorted descending: the elementwise
+// maximum of r and reversed c is bitonic, and three half-cleaner stages sort it.
+__device__ __forceinline__ void merge_top8(u64 (&r)[8], const u64 (&c)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = r[i] > c[7 - i] ? r[i] : c[7 - i];
+  cas_desc(r[0], r[4]); cas_desc(r[1], r[5]); cas_desc(r[2], r[6]); cas_desc(r[3], r[7]);
+  cas_desc(r[0], r[2]); cas_desc(r[1], r[3]); cas_desc(r[4], r[6]); cas_desc(r[5], r[7]);
+  cas_desc(r[0], r[1]); cas_desc(r[2], r[3]); cas_desc(r[4], r[5]); cas_desc(r[6], r[7]);
+}
+
+__device__ __forceinline__ u64 shfl_xor_u64(u64 v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<u64>(hi) << 32) | lo;
+}
+
+// Selection of one token by the four lanes 4j..4j+3 of a warp (K <= 8, no
+// node-limited groups): lane q of the four takes experts e = 4i + q, whose
+// logits lie in column tl of lg (expert-major rows of lstride floats).  Each
+// lane keeps the sorted 8 largest keys of its experts (chunks of 8: sort,
+// then merge), two shuffle levels merge the four lanes' lists, and the
+// chosen experts' scores are recomputed with the same arithmetic for the
+// gates.  The rules of select_experts: scores by eq. (15) (or Softmax over
+// all E), keys s + b, ties to the lower index, g = s / sum of the chosen s
+// (eq. 13) or s.  ok: this lane's token exists (all four lanes of a token
+// agree); every lane of the warp must call it.
+template <int NACC>
+__device__ __forceinline__ void select_quad(const float* __restrict__ lg, int lstride, int tl,
+                                            bool ok, size_t t, int q,
+                                            const float* __restrict__ bias, int E, int K,
+                                            int score_func, int normalize,
+                                            int32_t* __restrict__ idx, float* __restrict__ gates,
+                                            float* __restrict__ scores) {
+  constexpr int CH = 4 * NACC;                  // chunks of 8 experts per lane
+  const float* col = lg + tl;
+  float m = 0.f, denom = 1.f;
+  if (score_func == MOE_SCORE_SOFTMAX) {
+    m = -INFINITY;
+#pragma unroll 8
+    for (int i = 0; i < 8 * CH; ++i) {
+      const int e = 4 * i + q;
+      if (e < E) m = fmaxf(m, col[e * lstride]);
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    float sum = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < 8 * CH; ++i) {
+      const int e = 4 * i + q;
+      if (e < E) sum += __expf(col[e * lstride] - m);
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    denom = sum;
+  }
+  // fast exponential and reciprocal: a few fp32 ulps, far below the 1e-5 of
+  // the key comparisons and the gates
+  const float rden = 1.0f / denom;
+  auto score = [&](float L) {
+    return score_func == MOE_SCORE_SOFTMAX ? __expf(L - m) * rden
+                                           : __frcp_rn(1.0f + __expf(-L));
+  };
+  u64 r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = 0ull;
+#pragma unroll 1
+  for (int c = 0; c < CH; ++c) {
+    u64 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 4 * (8 * c + i) + q;
+      v[i] = 0ull;
+      if (e < E) {
+        const float s = score(col[e * lstride]);
+        if (scores && ok) scores[t * E + e] = s;
+        v[i] = (static_cast<u64>(orderable(s + __ldg(bias + e))) << 32) |
+               (0xFFFFFFFFu - static_cast<uint32_t>(e));
+      }
+    }
+    sort8_desc(v);
+    merge_top8(r, v);
+  }
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {
+    u64 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = shfl_xor_u64(r[i], off);
+    merge_top8(r, v);
+  }
+  float sk[8];
+  float sum_sel = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    sk[k] = 0.f;
+    if (k < K) {
+      const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(r[k]));
+      sk[k] = score(col[e * lstride]);
+      sum_sel += sk[k];
+    }
+  }
+  if (!ok) return;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (k < K && (k & 3) == q) {
+      const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(r[k]));
+      float g = sk[k];
+      if (normalize) g = sum_sel > 0.f ? sk[k] / sum_sel : 0.f;
+      idx[t * K + k] = e;
+      gates[t * K + k] = g;
+    }
+  }
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(FR_THREADS, 1)
+    router_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + FR_AREA);
+  uint64_t* empty = full + FR_STAGES;
+  uint64_t* tfull = empty + FR_STAGES;
+  uint64_t* drain = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(tc::cluster_ctarank());
+  const int cid = blockIdx.x / a.ck;
+  const bool prenorm = a.inv_rms != nullptr;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < FR_STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      // released by the MMA commit, and behind the RMSNorm also by one arrival
+      // of each mover warp once it has read the stage's token rows
+      tc::mbar_init(empty + s, prenorm ? 1 + FR_MOVERS : 1);
+    }
+    tc::mbar_init(tfull, 1);
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane <= FR_TOKBOXES)
+    tc::tma_prefetch_desc(lane == 0 ? &maps.a : &maps.b[lane - 1]);
+  if (warp == 1) {
+    tc::tmem_alloc<1>(tmem_slot, FR_TMEM_COLS);
+    tc::tmem_relinquish<1>();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const unsigned long long tmo = a.timeout_ns;
+  const int kb0 = rank * a.kps;
+  const int kb1 = min(a.k_blocks, kb0 + a.kps);
+
+  // ring position: producer, MMA issuer and movers walk the same stage sequence
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued = 0, issued_par = 0;   // producer: stages that received loads, and their parity
+  bool mma_issued = false;
+  uint32_t tphase = 0;
+  // reduction buffers (alias the operand ring): receive slots [ck - 1][epad]
+  // rows (the first doubles as the logits buffer: the owner sums in place),
+  // or with ck = 1 the logits buffer [epad] rows; then the sum-of-squares
+  // slots [ck][nown] and the owned tokens' inv_rms [nown]
+  float* lg = reinterpret_cast<float*>(smem);
+  float* ssq = reinterpret_cast<float*>(smem + a.ss_off);
+  float* invs = reinterpret_cast<float*>(smem + a.inv_off);
+  const int quad = warp & 3;                 // TMEM lane quadrant of a mover warp
+  const int half = (warp - 2) >> 2;          // which alternate 8-column chunks it takes
+  const int mv = threadIdx.x - 64;           // mover thread index 0..255: token column
+  const int nch = a.nown >> 3;               // 8-column chunks per owner
+  const size_t slot_floats = static_cast<size_t>(a.epad) * a.stride;
+
+  for (int blk = cid; blk < a.nblocks; blk += a.nclusters) {
+    const int tok0 = blk * a.nb;
+    const int ntok = min(a.nb, a.T - tok0);
+    const int nmma = (ntok + 15) & ~15;
+    float ss = 0.f;                          // movers: sum of x^2 of token column mv
+    if (warp == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      if (!*abort_flag) {
+        const uint32_t bytes = a.nacc * FR_A_BOX + nmma * FR_ROW;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) break;
+          if (lane == 0) {
+            uint8_t* sa = smem + stage * FR_STAGE;
+            tc::mbar_arrive_expect_tx(full + stage, bytes);
+            tc::tma_load_2d(sa, &maps.a, full + stage, kb * FR_BK, 0);
+            if (a.nacc == 2)
+              tc::tma_load_2d(sa + FR_A_BOX, &maps.a, full + stage, kb * FR_BK, 128);
+            int done = 0;
+#pragma unroll
+            for (int bi = FR_TOKBOXES - 1; bi >= 0; --bi) {
+              const int h = 16 << bi;
+              if (nmma & h) {
+                tc::tma_load_2d(sa + 2 * FR_A_BOX + done * FR_ROW, &maps.b[bi], full + stage,
+                                kb * FR_BK, tok0 + done);
+                done += h;
+              }
+            }
+          }
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          __syncwarp();
+          if (++stage == FR_STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (!*abort_flag) {
+        const uint32_t idesc = tc::idesc_bf16_f32(128, nmma);
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+          tc::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = tc::smem_u32(smem + stage * FR_STAGE);
+#pragma unroll
+            for (int kk = 0; kk < FR_BK / 16; ++kk) {
+              const uint64_t db = tc::smem_desc_sw128(sa + 2 * FR_A_BOX + kk * 32);
+              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+              tc::mma_bf16<1>(tmem, tc::smem_desc_sw128(sa + kk * 32), db, idesc, acc);
+              if (a.nacc == 2)
+                tc::mma_bf16<1>(tmem + 256, tc::smem_desc_sw128(sa + FR_A_BOX + kk * 32), db,
+                                idesc, acc);
+            }
+            tc::mma_commit<1>(empty + stage);
+          }
+          mma_issued = true;
+          __syncwarp();
+          if (++stage == FR_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (ok && lane == 0) tc::mma_commit<1>(tfull);
+        __syncwarp();
+      }
+    } else {
+      // ---------------------------------------------------------------- movers
+      if (prenorm && !*abort_flag) {
+        // sum of squares of token row mv over this CTA's K slice, from the
+        // landed operand tiles (128-byte rows, 16-byte pieces swizzled by
+        // row % 8), summed in the row's element order
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!warp_wait(full + stage, phase, abort_flag, tmo)) break;
+          if (mv < nmma) {
+            const uint8_t* rowp = smem + stage * FR_STAGE + 2 * FR_A_BOX + mv * FR_ROW;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((c ^ (mv & 7)) << 4));
+              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(h2[k]);
+                ss = fmaf(f.x, f.x, ss);
+                ss = fmaf(f.y, f.y, ss);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(empty + stage);
+          if (++stage == FR_STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // this CTA's accumulators
+      warp_wait(tfull, tphase, abort_flag, tmo);
+      tc::tc_fence_after();
+    }
+    tphase ^= 1u;
+
+    // B0: this block's MMAs are complete in every CTA of the cluster, so every
+    // operand ring is free for the reduction buffers
+    tc::tc_fence_before();
+    tc::cluster_sync_all();
+    tc::tc_fence_after();
+    const bool live = !*abort_flag;
+    if (warp >= 2 && live) {
+      const int row = quad * 32 + lane;      // expert row of this lane within a half
+      if (a.ck > 1) {
+        // this CTA's partials of every other CTA's tokens, both halves, 8
+        // tokens per pair of 16-byte stores, into that CTA's receive slot
+        for (int i = half; i < (a.ck - 1) * nch; i += 2) {
+          const int oc = i / nch;
+          const int c = oc < rank ? oc : oc + 1;
+          const int jl = (i - oc * nch) * 8;
+          const int slot = rank < c ? rank : rank - 1;
+          const uint32_t tq = tmem + (static_cast<uint32_t>(quad * 32) << 16) + c * a.nown + jl;
+          uint32_t v0[8], v1[8];
+          tc::tmem_ld8(tq, v0);
+          if (a.nacc == 2) tc::tmem_ld8(tq + 256, v1);
+          tc::tmem_wait_ld8(v0);
+          if (a.nacc == 2) tc::tmem_wait_ld8(v1);
+          const uint32_t dst = tc::mapa_shared(
+              tc::smem_u32(lg) +
+                  static_cast<uint32_t>((slot * slot_floats + static_cast<size_t>(row) * a.stride +
+                                         jl) * 4),
+              static_cast<uint32_t>(c));
+          tc::st_shared_cluster_v4(dst, v0[0], v0[1], v0[2], v0[3]);
+          tc::st_shared_cluster_v4(dst + 16, v0[4], v0[5], v0[6], v0[7]);
+          if (a.nacc == 2) {
+            const uint32_t d1 = dst + 128u * static_cast<uint32_t>(a.stride) * 4u;
+            tc::st_shared_cluster_v4(d1, v1[0], v1[1], v1[2], v1[3]);
+            tc::st_shared_cluster_v4(d1 + 16, v1[4], v1[5], v1[6], v1[7]);
+          }
+        }
+      }
+      if (prenorm && mv < a.nb) {
+        // this CTA's sum of squares of token column mv, to the column's owner
+        const int c = mv / a.nown;
+        tc::st_shared_cluster_u32(
+            tc::mapa_shared(tc::smem_u32(ssq) +
+                                static_cast<uint32_t>((rank * a.nown + mv - c * a.nown) * 4),
+                            static_cast<uint32_t>(c)),
+            __float_as_uint(ss));
+      }
+    }
+    // B1: every partial of this CTA's tokens has arrived (release / acquire)
+    tc::cluster_sync_all();
+    if (warp >= 2 && live) {
+      const int row = quad * 32 + lane;
+      if (prenorm) {
+        if (mv < a.nown) {
+          float q = 0.f;
+          for (int src = 0; src < a.ck; ++src) {
+            const float x = ssq[src * a.nown + mv];
+            q = src == 0 ? x : q + x;
+          }
+          const float inv = 1.0f / sqrtf(q / static_cast<float>(a.d) + a.eps);
+          invs[mv] = inv;
+          const int t = tok0 + rank * a.nown + mv;
+          if (t < a.T) a.inv_rms[t] = inv;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(FR_MOVERS * 32) : "memory");
+      }
+      // owner: the ck partials of each owned token added in rank order (in
+      // place over the first receive slot), times inv_rms behind the RMSNorm
+      for (int i = half; i < nch; i += 2) {
+        const int jl = i * 8;
+        const uint32_t tq =
+            tmem + (static_cast<uint32_t>(quad * 32) << 16) + rank * a.nown + jl;
+        uint32_t v0[8], v1[8];
+        tc::tmem_ld8(tq, v0);
+        if (a.nacc == 2) tc::tmem_ld8(tq + 256, v1);
+        tc::tmem_wait_ld8(v0);
+        if (a.nacc == 2) tc::tmem_wait_ld8(v1);
+        float sc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sc[k] = prenorm ? invs[jl + k] : 1.f;
+        for (int h = 0; h < a.nacc; ++h) {
+          const uint32_t* own = h == 0 ? v0 : v1;
+          const size_t r_off = static_cast<size_t>(h * 128 + row) * a.stride + jl;
+          float acc[8];
+          for (int src = 0; src < a.ck; ++src) {
+            float x[8];
+            if (src == rank) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) x[k] = __uint_as_float(own[k]);
+            } else {
+              const float4* p =
+                  reinterpret_cast<const float4*>(lg + (src < rank ? src : src - 1) * slot_floats +
+                                                  r_off);
+              const float4 x0 = p[0], x1 = p[1];
+              x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+              x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = src == 0 ? x[k] : acc[k] + x[k];
+          }
+          if (prenorm) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] *= sc[k];
+          }
+          float4* o = reinterpret_cast<float4*>(lg + r_off);
+          o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+      }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (live) {
+      const int own0 = tok0 + rank * a.nown;
+      if (a.K <= 8 && a.n_groups == 0) {
+        // four lanes per token, eight tokens per warp
+        for (int base = warp * 8; base < a.nown; base += FR_WARPS * 8) {
+          const int tl = base + (lane >> 2);
+          const bool ok = tl < a.nown && own0 + tl < a.T;
+          const int tlr = tl < a.nown ? tl : a.nown - 1;
+          if (a.nacc == 2)
+            select_quad<2>(lg, a.stride, tlr, ok, static_cast<size_t>(own0 + tlr), lane & 3,
+                           a.bias, a.E, a.K, a.score_func, a.normalize, a.idx, a.gates,
+                           a.scores);
+          else
+            select_quad<1>(lg, a.stride, tlr, ok, static_cast<size_t>(own0 + tlr), lane & 3,
+                           a.bias, a.E, a.K, a.score_func, a.normalize, a.idx, a.gates,
+                           a.scores);
+        }
+      } else {
+        // K > 8 or node-limited groups: one warp per token (select_experts)
+        for (int jl = warp; jl < a.nown; jl += FR_WARPS) {
+          const int t = own0 + jl;
+          if (t >= a.T) break;
+          float L[NPL];
+#pragma unroll
+          for (int j = 0; j < NPL; ++j) {
+            const int e = j * 32 + lane;
+            L[j] = e < a.E ? lg[e * a.stride + jl] : -INFINITY;
+          }
+          select_experts<NPL>(L, lane, static_cast<size_t>(t), a.bias, a.E, a.K, a.score_func,
+                              a.normalize, a.n_groups, a.topk_groups, a.idx, a.gates, a.scores);
+        }
+      }
+    }
+    // the ring's generic accesses are complete before the next block's TMA
+    // writes; the next block's B0 orders them against other CTAs' stores
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    tc::tc_fence_after();
+  }
+
+  if (*abort_flag) {
+    if (warp == 0) {
+      for (int s = 0; s < FR_STAGES; ++s)
+        if (issued & (1u << s)) drain_wait(full + s, (issued_par >> s) & 1u, tmo);
+    } else if (warp == 1 && mma_issued) {
+      if (lane == 0) tc::mma_commit<1>(drain);
+      __syncwarp();
+      drain_wait(drain, 0, tmo);
+    }
+  }
+  // the last remote stores were ordered by the last block's B1: no CTA
+  // accesses another's shared memory after it, so each CTA leaves on its own
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc<1>(tmem, FR_TMEM_COLS);
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.status, ERRBIT_TIMEOUT);
+}
+
+// Layout of the reduction buffers (bytes from the start of shared memory).
+// With ck > 1: ck - 1 receive slots of epad expert rows, row stride = 4
+// (mod 32) words, so 16-byte row pieces written and read by one lane per
+// expert meet no bank conflict (the first slot becomes the logits buffer);
+// with ck = 1 only the logits buffer, row stride = 8 (mod 32) words, so the
+// four lanes of a token reading experts 4i + q meet no bank conflict.  Then
+// the sum-of-squares slots [ck][nown] and inv_rms [nown].
+struct FrLayout {
+  int stride;
+  uint32_t ss_off, inv_off, bytes;
+};
+FrLayout fr_layout(int nown, int ck, int epad) {
+  FrLayout L{};
+  const int m = ck > 1 ? 4 : 8;
+  L.stride = nown + (((m - nown % 32) % 32) + 32) % 32;
+  const size_t rows = static_cast<size_t>(ck > 1 ? ck - 1 : 1) * epad;
+  L.ss_off = static_cast<uint32_t>(align_up(rows * L.stride * 4, 16));
+  L.inv_off = static_cast<uint32_t>(align_up(L.ss_off + static_cast<size_t>(ck) * nown * 4, 16));
+  L.bytes = static_cast<uint32_t>(align_up(L.inv_off + static_cast<size_t>(nown) * 4, 16));
+  return L;
+}
+
+template <int NPL>
+cudaLaunchConfig_t fused_config(int ck, int grid, cudaStream_t stream, cudaLaunchAttribute* at) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  lc.blockDim = dim3(FR_THREADS, 1, 1);
+  lc.dynamicSmemBytes = FR_SMEM;
+  lc.stream = stream;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(ck);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return lc;
+}
+
+template <int NPL>
+bool set_smem_attr() {
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && done[dev]) return true;
+  if (cudaFuncSetAttribute(router_fused_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(FR_SMEM)) != cudaSuccess)
+    return false;
+  if (dev < 64) done[dev] = true;
+  return true;
+}
+
+// Clusters of ck CTAs that fit on the device at once (0: none).
+int max_active_clusters(int ck) {
+  static int cache[64][4] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int slot = ck == 1 ? 0 : ck == 2 ? 1 : ck == 4 ? 2 : 3;
+  if (dev < 64 && cache[dev][slot]) return cache[dev][slot];
+  if (!set_smem_attr<8>()) return 0;
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t lc = fused_config<8>(ck, ck, nullptr, at);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, router_fused_kernel<8>, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (dev < 64 && n > 0) cache[dev][slot] = n;
+  return n;
+}
+
+template <int NPL>
+moe_status_t launch_fused(const FusedMaps& maps, const FusedArgs& a, cudaStream_t stream) {
+  if (!set_smem_attr<NPL>()) return MOE_ERR_CUDA;
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t lc = fused_config<NPL>(a.ck, a.nclusters * a.ck, stream, at);
+  if (cudaLaunchKernelEx(&lc, router_fused_kernel<NPL>, maps, a) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launch_status();
+}
+
+}  // namespace
+
+bool fused_router_applies(int act_dtype, int d, int E) {
+  return act_dtype == MOE_BF16 && E >= 1 && E <= 256 && d % 64 == 0 && d > 0;
+}
+
+bool fused_router_plan(int T, int d, int E, FusedRouterPlan* p) {
+  if (T <= 0 || !fused_router_applies(MOE_BF16, d, E)) return false;
+  const int nacc = E > 128 ? 2 : 1;
+  const int epad = 128 * nacc;
+  const int kb = d / 64;
+  bool found = false;
+  FusedRouterPlan best{};
+  int best_waves = 0;
+  for (int ck = 1; ck <= 8; ck *= 2) {
+    const int kps = ceil_div(kb, ck);
+    if ((ck - 1) * kps >= kb) continue;                   // a split would be empty
+    const int maxc = max_active_clusters(ck);
+    if (maxc <= 0) continue;
+    // token blocks: multiples of 16 (MMA N) whose share per CTA is whole
+    // 8-column chunks, at most 256, and whose reduction buffers fit
+    const int step = std::max(16, 8 * ck);
+    int nb = std::min(round_up(ceil_div(T, maxc), step), 256 / step * step);
+    while (nb >= step && fr_layout(nb / ck, ck, epad).bytes > FR_EPI_MAX) nb -= step;
+    if (nb < step) continue;
+    const int nblocks = ceil_div(T, nb);
+    const int nclusters = std::min(maxc, nblocks);
+    const int waves = ceil_div(nblocks, nclusters);
+    // fewest waves, then the widest token blocks (fewer centroid re-reads and
+    // wider MMAs), then the most K splits (smaller share of the centroids per CTA)
+    const bool better = !found || waves < best_waves ||
+                        (waves == best_waves && (nb > best.nb || (nb == best.nb && ck > best.ck)));
+    if (better) {
+      found = true;
+      best_waves = waves;
+      best.ck = ck;
+      best.nb = nb;
+      best.kps = kps;
+      best.nblocks = nblocks;
+      best.nclusters = nclusters;
+    }
+  }
+  if (found) *p = best;
+  return found;
+}
+
+moe_status_t launch_router_fused(const FusedRouterPlan& p, const void* x, const void* centroids,
+                                 const float* bias, int T, int d, int E, int K, int score_func,
+                                 int normalize, int n_groups, int topk_groups, int32_t* idx,
+                                 float* gates, float* scores, float norm_eps, float* inv_rms,
+                                 unsigned* status, unsigned long long timeout_ns,
+                                 cudaStream_t stream) {
+  if (T <= 0) return MOE_OK;
+  FusedMaps maps{};
+  if (!make_tmap_bf16(&maps.a, centroids, E, d, 128)) return MOE_ERR_CUDA;
+  for (int i = 0; i < FR_TOKBOXES; ++i)
+    if (!make_tmap_bf16(&maps.b[i], x, T, d, 16u << i)) return MOE_ERR_CUDA;
+  FusedArgs a{};
+  a.T = T;
+  a.E = E;
+  a.K = K;
+  a.nacc = E > 128 ? 2 : 1;
+  a.epad = 128 * a.nacc;
+  a.k_blocks = d / 64;
+  a.kps = p.kps;
+  a.ck = p.ck;
+  a.nb = p.nb;
+  a.nown = p.nb / p.ck;
+  a.nblocks = p.nblocks;
+  a.nclusters = p.nclusters;
+  const FrLayout L = fr_layout(a.nown, p.ck, a.epad);
+  a.stride = L.stride;
+  a.ss_off = L.ss_off;
+  a.inv_off = L.inv_off;
+  a.d = d;
+  a.eps = norm_eps;
+  a.inv_rms = inv_rms;
+  a.bias = bias;
+  a.score_func = score_func;
+  a.normalize = normalize;
+  a.n_groups = n_groups;
+  a.topk_groups = topk_groups;
+  a.idx = idx;
+  a.gates = gates;
+  a.scores = scores;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  TraceScope tr(stream, "router_fused");
+  if (E <= 32) return launch_fused<1>(maps, a, stream);
+  if (E <= 64) return launch_fused<2>(maps, a, stream);
+  if (E <= 128) return launch_fused<4>(maps, a, stream);
+  return launch_fused<8>(maps, a, stream);
+}
+
+}  // namespace moe

@@ -35,6 +35,15 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t caddr, uint32_t v
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
 }
 
+// 16-byte store to shared memory of a CTA of this cluster (cluster address,
+// 16-byte aligned).
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b,
+                                                     uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
 // Every thread of every CTA in the cluster arrives and waits (hardware barrier).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
@@ -323,6 +332,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
+// Each lane reads 8 consecutive 32-bit columns of its own TMEM lane; valid
+// after tmem_wait_ld8() on the same array.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld8(uint32_t (&r)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+
 // 16 TMEM lanes (from taddr's lane) x 16 columns: thread t receives, for each
 // 8-column half c (registers 4c..4c+3), lane t/4 at columns 2(t%4), 2(t%4)+1
 // and lane t/4 + 8 at the same two columns.  Valid after tmem_wait_ld4().

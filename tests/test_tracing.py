@@ -29,13 +29,33 @@ def test_forward_kernels_traced_once_each():
     torch.cuda.synchronize()
     rec = {name: (n, ms) for name, n, ms in m.trace_read_all()}
     m.trace_enable(False)
-    for name in ("gemm_router", "router_topk", "dispatch_count", "dispatch_scan", "dispatch_rank",
+    # E <= 256 experts: the router is one fused kernel (no logits in memory)
+    for name in ("router_fused", "dispatch_count", "dispatch_scan", "dispatch_rank",
                  "dispatch_scatter", "build_groups",
                  "gemm_gateup_swiglu", "gemm_down", "combine", "update_bias"):
         assert name in rec, f"{name} not traced: {sorted(rec)}"
         n, ms = rec[name]
         assert n == 1 and ms > 0.0
+    assert "gemm_router" not in rec and "router_topk" not in rec
     assert m.trace_read_all() == []           # read clears the record
     layer.forward(g["x"])                     # tracing off: nothing recorded
     torch.cuda.synchronize()
     assert m.trace_read_all() == []
+
+
+@pytest.mark.gpu
+def test_wide_router_traces_split_gemm_and_topk():
+    """More than 256 experts: the split-K router GEMM and the top-K kernel."""
+    cfg = small_cases()["wide_e"]
+    g, _ = gpu_inputs(cfg)
+    layer = m.MoeLayer(m.cfg_from_layer(cfg), g, device="cuda")
+    layer.forward(g["x"])
+    torch.cuda.synchronize()
+    m.trace_enable(True)
+    m.trace_read_all()
+    layer.forward(g["x"])
+    torch.cuda.synchronize()
+    rec = {name: n for name, n, _ in m.trace_read_all()}
+    m.trace_enable(False)
+    assert rec.get("gemm_router") == 1 and rec.get("router_topk") == 1
+    assert "router_fused" not in rec
