@@ -37,8 +37,12 @@ Readings where the pages are silent:
 - If the chosen scores sum to 0 the renormalised gates are 0.
 - The RMSNorm in front of the layer (V3 walk-through, section 4.1, eps 1e-6) is
   the standard one with a per-channel weight, x * w / sqrt(mean(x^2) + eps);
-  its output is held in the activation type like every stored activation, and
-  the residual adds the un-normalised x.
+  the residual adds the un-normalised x.  The experts read the normalised
+  tokens held in the activation type (rounded once, like every stored
+  activation).  The router reads no stored normalised token: its logit is
+  (x * inv_rms * w) . e_i = inv_rms * (x . (w * e_i)), with the weighted
+  centroid w * e_i held in the weight type (rounded once, like every stored
+  weight) and inv_rms = 1 / sqrt(mean(x^2) + eps) applied to the logit.
 - Backward pass (no page writes it out; V3 walk-through, section 2.2, says the
   bias only steers the selection): the gradients of a scalar loss whose
   gradient with respect to the layer output is dout, by the chain rule through
@@ -82,6 +86,18 @@ def rmsnorm(x, w, eps: float = 1e-6):
     xv = _f64(x)
     inv_rms = 1.0 / np.sqrt(np.mean(xv * xv, axis=1) + eps)
     return xv * inv_rms[:, None] * _f64(w)[None, :], inv_rms
+
+
+def prenorm_logits(x, w, centroids, eps: float = 1e-6, wgt: str = "bf16"):
+    """Router logits of the layer behind its RMSNorm (see header): the RMSNorm
+    weight scales the centroids, w * e_i held in the weight type ``wgt``
+    (rounded once), and 1/rms scales the logit:
+      L[t, i] = inv_rms_t * sum_j x_tj (w_j e_ij).
+    Returns (L [T, E] fp64, inv_rms [T] fp64)."""
+    xv = _f64(x)
+    inv_rms = 1.0 / np.sqrt(np.mean(xv * xv, axis=1) + eps)
+    ew = round_act(_f64(w)[None, :] * _f64(centroids), wgt)
+    return inv_rms[:, None] * (xv @ ew.T), inv_rms
 
 
 def round_bf16(v) -> np.ndarray:
@@ -181,7 +197,14 @@ def route(u, centroids, bias, K: int, score_func: int = SIGMOID, normalize: int 
     With n_groups > 0 the top-K runs only over the experts of the topk_groups
     best groups (select_groups); the returned margin is then the smaller of
     the group margin and the expert margin inside the kept groups."""
-    s = expert_scores(affinity_logits(u, centroids), score_func)
+    return route_logits(affinity_logits(u, centroids), bias, K, score_func, normalize,
+                        n_groups, topk_groups)
+
+
+def route_logits(logits, bias, K: int, score_func: int = SIGMOID, normalize: int = 1,
+                 n_groups: int = 0, topk_groups: int = 0):
+    """route() from given affinity logits [T, E] (eqs. (15), (16), (14), (13))."""
+    s = expert_scores(logits, score_func)
     keys = selection_keys(s, bias)
     gmargin = None
     if n_groups > 0:
@@ -256,7 +279,7 @@ def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
 def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
               add_residual: int = 1, tokens=None, n_groups: int = 0,
               topk_groups: int = 0, norm_w=None, norm_eps: float = 1e-6,
-              act: str = "bf16", idx=None) -> dict:
+              act: str = "bf16", idx=None, wgt: str = None) -> dict:
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
@@ -265,9 +288,11 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     used as stored (bf16), unquantised.  Expert weights are read one expert at
     a time, so large layers can be evaluated on a token sample.
 
-    With ``norm_w`` the layer sits behind its RMSNorm: the router and the
-    experts read u = RMSNorm(x) held in the activation type ``act`` (rounded
-    once), and the residual adds x itself (h = x + MoE(RMSNorm(x))).
+    With ``norm_w`` the layer sits behind its RMSNorm: the experts read
+    u = RMSNorm(x) held in the activation type ``act`` (rounded once), the
+    router takes its logits from x by prenorm_logits (weighted centroids in
+    the weight type ``wgt``), and the residual adds x itself
+    (h = x + MoE(RMSNorm(x))).
 
     ``idx`` [n, K], when given, replaces the router's own choice for these
     tokens (another valid top-K where keys tie within rounding); the gates
@@ -282,14 +307,17 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     resid = _f64(x)
     if norm_w is not None:
         u = round_act(rmsnorm(resid, norm_w, norm_eps)[0], act)
+        logits = prenorm_logits(resid, norm_w, inp["centroids"], norm_eps,
+                                wgt if wgt is not None else act)[0]
     else:
         u = resid
+        logits = affinity_logits(u, inp["centroids"])
     n = u.shape[0]
     if idx is None:
-        idx, gates, margin, scores = route(u, inp["centroids"], inp["bias"], K, score_func,
-                                           normalize, n_groups, topk_groups)
+        idx, gates, margin, scores = route_logits(logits, inp["bias"], K, score_func,
+                                                  normalize, n_groups, topk_groups)
     else:
-        scores = expert_scores(affinity_logits(u, inp["centroids"]), score_func)
+        scores = expert_scores(logits, score_func)
         idx = np.asarray(idx, dtype=np.int32).reshape(n, K)
         gates = gate_values(scores, idx, normalize)
         margin = np.full(n, np.nan)

@@ -31,7 +31,10 @@ int main(void) {
   /* xp [T*K, d], act [R, I], y [R, d] in bf16, R = T*K + S*T */
   const size_t R = 8192u * 8u + 8192u;
   if (fwd < 2u * (8192u * 8u * 7168u + R * 2048u + R * 7168u)) return 2;
-  if (moe_workspace_size(&c, MOE_WS_FORWARD_PRENORM) != fwd + 8192u * 7168u * 2u) return 3;
+  /* behind the RMSNorm: + normalised tokens, weighted centroids, inv_rms */
+  if (moe_workspace_size(&c, MOE_WS_FORWARD_PRENORM) !=
+      fwd + 8192u * 7168u * 2u + 256u * 7168u * 2u + 8192u * 4u)
+    return 3;
   c.K = 0;
   if (moe_check_cfg(&c) != MOE_ERR_INVALID_ARG) return 4;
   if (moe_workspace_size(&c, MOE_WS_FORWARD) != 0) return 5;

@@ -114,8 +114,10 @@ def test_argument_errors_return_before_any_launch():
 def test_prenorm_workspace_and_argument_errors():
     c = m.make_cfg(8192, 7168, 256, 8, 1, 2048)
     f = m.workspace_size(c, m.MOE_WS_FORWARD)
-    # the pre-normed forward adds the normalised tokens [T, d] bf16
-    assert m.workspace_size(c, m.MOE_WS_FORWARD_PRENORM) == f + 8192 * 7168 * 2
+    # the pre-normed forward adds the normalised tokens [T, d] bf16 (the shared
+    # experts' input), the weighted centroids [E, d] bf16 and inv_rms [T] fp32
+    assert m.workspace_size(c, m.MOE_WS_FORWARD_PRENORM) == \
+        f + 8192 * 7168 * 2 + 256 * 7168 * 2 + 8192 * 4
     lib = L.lib()
     P = None
     b = _cfg()

@@ -488,6 +488,41 @@ def test_golden_rmsnorm():
         np.testing.assert_allclose(xn[0], _rows(kv[c + "_xn"])[0], rtol=1e-15, atol=0)
 
 
+def test_golden_prenorm_router_logits():
+    """Router logits behind the RMSNorm: the weighted centroids w * e_i held in
+    bf16 (one rounding, nearest even), times inv_rms (V3 walk-through, section
+    4.1 with eq. (15)); the unrounded weighted centroids would miss both."""
+    kv = dict(_read("rmsnorm_router_hand.txt"))
+    x = np.array([_rows(kv["x"])[0]])
+    w = np.array(_rows(kv["w"])[0])
+    C = np.array(_rows(kv["centroids"]))
+    L, inv = O.prenorm_logits(x, w, C, _num(kv["eps"]), "bf16")
+    np.testing.assert_allclose(inv, [_num(kv["inv_rms"])], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(L[0], _rows(kv["logits"])[0], rtol=1e-14, atol=0)
+    exact = inv[:, None] * (x @ (w[None, :] * C).T)
+    assert np.all(np.abs(exact[0] - L[0]) > 1e-3)
+
+
+def test_prenorm_logits_equal_logits_of_normalised_tokens():
+    """(x * inv_rms * w) . e_i = inv_rms * (x . (w * e_i)): with weights that are
+    powers of two the weighted centroids are exact in bf16 and the two forms
+    agree to rounding; with w = 1 they are inv_rms * (x . e_i)."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((20, 64))
+    C = O.round_bf16(rng.standard_normal((12, 64)) * 0.1)
+    w = 2.0 ** rng.integers(-3, 3, 64)
+    L, inv = O.prenorm_logits(x, w, C, 1e-6, "bf16")
+    xn, inv2 = O.rmsnorm(x, w, 1e-6)
+    np.testing.assert_allclose(inv, inv2, rtol=1e-15)
+    np.testing.assert_allclose(L, O.affinity_logits(xn, C), rtol=1e-12, atol=1e-14)
+    L1, inv1 = O.prenorm_logits(x, np.ones(64), C, 1e-6, "bf16")
+    np.testing.assert_allclose(L1, inv1[:, None] * (x @ C.T), rtol=1e-13, atol=1e-15)
+    # f32 weight type: the weighted centroids rounded to float32 instead
+    Lf, _ = O.prenorm_logits(x, w * 1.1, C, 1e-6, "f32")
+    ewf = (1.1 * w[None, :] * C).astype(np.float32).astype(np.float64)
+    np.testing.assert_allclose(Lf, inv[:, None] * (x @ ewf.T), rtol=1e-12, atol=1e-14)
+
+
 def test_rmsnorm_closed_forms():
     rng = np.random.default_rng(5)
     d = 96

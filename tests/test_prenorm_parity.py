@@ -2,18 +2,20 @@
 4.1: an RMSNorm before and after the MoE layer, eps 1e-6) and of the layer
 behind it, h = x + MoE(RMSNorm(x)), through the C ABI.
 
-The kernel computes the norm in fp32 and rounds once to the activation type;
+moe_rmsnorm computes the norm in fp32 and rounds once to the activation type;
 the oracle computes it in fp64 and rounds once.  The two can land on
 neighbouring bf16 values where the exact result lies within fp32 error of a
 rounding boundary (about one element in 10^4), so the norm is compared
 element-wise within one unit in the last place with at most 1e-3 of the
-elements off.  A token whose normalised row differs that way sees routing
-keys that differ by ~1e-5, so the layer's strict routing checks (exact sets,
-gates within 1e-5) cover the tokens whose rows agree; the others must still
-pick the same experts when their K-th vs (K+1)-th margin is above 1e-3.
-Every token left out of those checks must hold a valid top-K of the oracle's
-keys (within 1e-5, or 1e-3 where its normalised row differs), and its output
-is compared with the oracle's layer on that choice.
+elements off.
+
+The layer's router reads no normalised token: its logit is
+inv_rms * (x . (w * e_i)) with the weighted centroids w * e_i held in the
+weight type, on both sides.  The strict routing checks (sets bit-exact,
+gates within 1e-5) therefore apply to every token whose K-th vs (K+1)-th
+margin is >= 1e-5; a token below that margin must hold a valid top-K of the
+oracle's keys and its gates, and its output is compared with the oracle's
+layer on that choice.  The experts read the normalised rows.
 """
 from __future__ import annotations
 
@@ -23,15 +25,14 @@ import torch
 
 from moe_inputs import small_cases, get_config
 from oracle import moe_oracle as O
-from tests._util import (GpuRun, gpu_inputs, assert_close, to_np, GATE_ATOL, MARGIN_EXCLUDE,
-                         rel_frob, valid_topk_choice, with_gpu_choice)
+from tests._util import (GpuRun, gpu_inputs, assert_close, to_np, rel_frob, check_near_ties,
+                         with_gpu_choice)
 
 pytestmark = pytest.mark.gpu
 
 m = pytest.importorskip("mixture_experts_layer_88_b300")
 
 EPS = 1e-6
-LOOSE_MARGIN = 1e-3
 SMALL = ["tiny", "small_bf16", "ragged_bf16", "softmax_norenorm"]
 
 
@@ -123,10 +124,62 @@ class PrenormRun(GpuRun):
                           self.out, ws)
 
 
-@pytest.mark.parametrize("name", SMALL)
-def test_forward_prenorm_is_forward_of_normalised_tokens(name):
-    """moe_forward_prenorm(x) = moe_forward(moe_rmsnorm(x)) bit for bit
-    (MoE term only, add_residual = 0)."""
+def _oracle_prenorm(cfg, c, **kw):
+    return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, n_groups=cfg.n_groups,
+                       topk_groups=cfg.topk_groups, norm_w=c["norm_w"], norm_eps=EPS,
+                       act=cfg.act, wgt="bf16" if cfg.wgt == "e4m3" else cfg.wgt, **kw)
+
+
+def _checked(cfg, c, idx_g, gates_g, add_residual, tokens=None):
+    """The oracle's pre-normed layer (on `tokens`, default all) with routing
+    checked against the GPU's: chosen sets bit-exact where the K-th vs
+    (K+1)-th margin is >= 1e-5, a valid top-K within 1e-5 and its gates
+    elsewhere (those rows recomputed on the GPU's choice).  The router reads
+    the raw tokens and the weighted centroids on both sides, so no token's
+    routing depends on the rounding of its normalised row."""
+    ref = _oracle_prenorm(cfg, c, add_residual=add_residual, tokens=tokens)
+    keep, n_excl = check_near_ties(cfg, idx_g, ref["margin"], ref["scores"], c["bias"], gates_g)
+    if cfg.zipf_s == 0:
+        assert n_excl <= max(2, len(keep) // 50)
+    np.testing.assert_array_equal(np.sort(idx_g, 1)[keep], np.sort(ref["idx"], 1)[keep])
+    tok = np.arange(len(keep)) if tokens is None else np.asarray(tokens)
+    return with_gpu_choice(ref, idx_g, keep, lambda rows, ix: _oracle_prenorm(
+        cfg, c, add_residual=add_residual, tokens=tok[rows], idx=ix))
+
+
+# bf16 small layers take the fused router (logits from the raw tokens and the
+# weighted centroids, 1/rms from its own sums of squares, rows normalised in
+# the dispatch); the fp32 layer ("tiny") and E > 256 ("wide_e") take the
+# RMSNorm kernel and the two-kernel router with its logits scaled by inv_rms
+PRE = SMALL + ["wide_e", "grouped_bf16"]
+
+
+@pytest.mark.parametrize("name", PRE)
+def test_forward_prenorm_vs_oracle(name):
+    cfg = _cfg(name)
+    ar = 1 if name in ("tiny", "small_bf16") else 0
+    g, c = gpu_inputs(cfg)
+    run = PrenormRun(m, cfg, g, add_residual=ar)
+    run.forward_prenorm()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    idx_g = run.idx.cpu().numpy()
+    ref = _checked(cfg, c, idx_g, run.gates.cpu().numpy(), ar)
+    # with add_residual the oracle's residual is x itself: adding the
+    # normalised tokens instead would be off by O(1)
+    assert_close(to_np(run.out), ref["out"] if ar else ref["delta"], cfg.act,
+                 f"{name} pre-normed layer")
+    np.testing.assert_array_equal(run.counts.cpu().numpy(),
+                                  np.bincount(idx_g.reshape(-1), minlength=cfg.E))
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "ragged_bf16", "softmax_norenorm"])
+def test_forward_prenorm_matches_layer_on_normalised_tokens(name):
+    """moe_forward_prenorm(x) and moe_forward(moe_rmsnorm(x)) compute the same
+    layer with the router's one rounding in different places (w * e_i held
+    in bf16 against xn held in bf16: ~2^-9 relative per product, so logits
+    and gates differ by ~1e-3).  They must pick the same experts for nearly
+    every token and, on those tokens, agree within the layer bar."""
     cfg = _cfg(name)
     g, _ = gpu_inputs(cfg)
     a = PrenormRun(m, cfg, g, add_residual=0)
@@ -136,75 +189,32 @@ def test_forward_prenorm_is_forward_of_normalised_tokens(name):
     b.forward()
     torch.cuda.synchronize()
     assert m.get_status() == 0
-    assert torch.equal(a.idx, b.idx) and torch.equal(a.gates, b.gates)
-    assert torch.equal(a.counts, b.counts)
-    assert torch.equal(a.out, b.out)
+    ia, ib = a.idx.cpu().numpy(), b.idx.cpu().numpy()
+    same = np.all(np.sort(ia, 1) == np.sort(ib, 1), axis=1)
+    assert same.mean() >= 0.95, f"routing agrees on {same.mean():.3f} of the tokens"
+    np.testing.assert_allclose(a.gates.cpu().numpy()[same], b.gates.cpu().numpy()[same],
+                               rtol=0, atol=2e-2)
+    assert_close(to_np(a.out)[same], to_np(b.out)[same], cfg.act, f"{name} two forms")
 
 
-def _validate_excluded(cfg, idx_g, ref, bias, excl, same_row):
-    """Every token left out of the exact comparison must still hold a valid
-    top-K of the oracle's keys: within 1e-5 where the normalised rows agree,
-    within 1e-3 where they differ by an ulp (the keys then differ by ~1e-5)."""
-    if not excl.any():
-        return
-    keys = O.selection_keys(ref["scores"][excl], bias).astype(np.float64)
-    for j, t in enumerate(np.nonzero(excl)[0]):
-        tol = MARGIN_EXCLUDE if same_row[t] else LOOSE_MARGIN
-        assert valid_topk_choice(idx_g[t], keys[j], cfg.K, tol=tol), \
-            f"token {t}: chosen {sorted(idx_g[t].tolist())} is not a top-{cfg.K} within {tol}"
-
-
-def _check_prenorm_layer(cfg, run, ref, same_row, bias, tol_check, rerun):
-    """Routing of the pre-normed layer against the oracle, then tol_check(ref')
-    on every token, where ref' is ref with the excluded tokens' rows recomputed
-    by rerun(rows, idx) on the GPU's (validated) choice."""
-    idx_g, gates_g = run.idx.cpu().numpy(), run.gates.cpu().numpy()
-    margin = ref["margin"]
-    strict = (margin >= MARGIN_EXCLUDE) & same_row
-    loose = (margin >= LOOSE_MARGIN) & ~same_row
-    assert int((margin < MARGIN_EXCLUDE).sum()) <= max(2, cfg.T // 50)
-    sg, so = np.sort(idx_g, 1), np.sort(ref["idx"], 1)
-    np.testing.assert_array_equal(sg[strict], so[strict])
-    np.testing.assert_array_equal(sg[loose], so[loose])
-    og = np.argsort(idx_g, 1, kind="stable")
-    oo = np.argsort(ref["idx"], 1, kind="stable")
-    np.testing.assert_allclose(np.take_along_axis(gates_g, og, 1)[strict],
-                               np.take_along_axis(ref["gates"], oo, 1)[strict], rtol=0,
-                               atol=GATE_ATOL)
-    keep = strict | loose
-    _validate_excluded(cfg, idx_g, ref, bias, ~keep, same_row)
-    tol_check(with_gpu_choice(ref, idx_g, keep, rerun))
-    return keep
-
-
-@pytest.mark.parametrize("name", SMALL)
-def test_forward_prenorm_vs_oracle(name):
-    cfg = _cfg(name)
-    ar = 1 if name in ("tiny", "small_bf16") else 0
-    g, c = gpu_inputs(cfg)
-    run = PrenormRun(m, cfg, g, add_residual=ar)
-    run.forward_prenorm()
+def test_prenorm_fused_router_launches_no_norm_pass():
+    """Behind the RMSNorm the bf16 layer's kernels are the weighted-centroid
+    fold, the fused router, the dispatch (which normalises), the experts and
+    the combine: no separate RMSNorm pass and no logits in memory."""
+    cfg = small_cases()["small_bf16"]
+    g, _ = gpu_inputs(cfg)
+    layer = m.MoeLayer(m.cfg_from_layer(cfg), g, device="cuda", norm_w=g["norm_w"],
+                       norm_eps=EPS)
+    layer.forward(g["x"])
     torch.cuda.synchronize()
-    assert m.get_status() == 0
-    def layer(**kw):
-        return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=ar,
-                           n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
-                           norm_w=c["norm_w"], norm_eps=EPS, act=cfg.act, **kw)
-
-    ref = layer()
-    xn, _ = _norm_gpu(cfg, g)
-    same, _, _ = _rows_agree(cfg, xn, c)
-    out = to_np(run.out)
-
-    def tol(r):
-        # with add_residual the oracle's residual is x itself: adding the
-        # normalised tokens instead would be off by O(1)
-        assert_close(out, r["out"] if ar else r["delta"], cfg.act, f"{name} pre-normed layer")
-    keep = _check_prenorm_layer(cfg, run, ref, same, c["bias"], tol,
-                                lambda rows, ix: layer(tokens=rows, idx=ix))
-    assert keep.mean() >= 0.9
-    np.testing.assert_array_equal(run.counts.cpu().numpy(),
-                                  np.bincount(run.idx.cpu().numpy().reshape(-1), minlength=cfg.E))
+    m.trace_enable(True)
+    m.trace_read_all()
+    layer.forward(g["x"])
+    torch.cuda.synchronize()
+    names = {n for n, _, _ in m.trace_read_all()}
+    m.trace_enable(False)
+    assert "rmsnorm" not in names and "gemm_router" not in names and "router_topk" not in names
+    assert {"fold_centroids", "router_fused", "dispatch_scatter_norm"} <= names
 
 
 @pytest.mark.parametrize("name", ["small_fp8", "ragged_fp8"])
@@ -233,26 +243,15 @@ def test_forward_fp8_prenorm_vs_oracle(name):
 
     r0, r1 = run_fp8(0), run_fp8(1)
     assert torch.equal(r0.idx, r1.idx) and torch.equal(r0.gates, r1.gates)
-    def layer(**kw):
-        return O.moe_layer(c, K, cfg.normalize, cfg.score_func, add_residual=1,
-                           norm_w=c["norm_w"], norm_eps=EPS, act=cfg.act, **kw)
-
-    ref = layer()
-    xn, _ = _norm_gpu(cfg, g)
-    same, _, _ = _rows_agree(cfg, xn, c)
+    ref = _checked(cfg, c, r0.idx.cpu().numpy(), r0.gates.cpu().numpy(), 1)
     got0, got1 = to_np(r0.out), to_np(r1.out)
-
-    def tol(r):
-        rf = rel_frob(got0, r["delta"])
-        assert rf <= 5e-2, f"relative Frobenius of the MoE term {rf:.3e}"
-        # the residual is x itself (the normalised tokens would be off by
-        # O(1)): with and without it the outputs differ by x, up to the two
-        # bf16 roundings
-        res = got1 - got0 - to_np(g["x"])
-        bound = 2.0 ** -8 * (np.abs(got1) + np.abs(got0)) + 1e-6
-        assert np.all(np.abs(res) <= bound)
-    _check_prenorm_layer(cfg, r0, ref, same, c["bias"], tol,
-                         lambda rows, ix: layer(tokens=rows, idx=ix))
+    rf = rel_frob(got0, ref["delta"])
+    assert rf <= 5e-2, f"relative Frobenius of the MoE term {rf:.3e}"
+    # the residual is x itself (the normalised tokens would be off by O(1)):
+    # with and without it the outputs differ by x, up to the two bf16 roundings
+    res = got1 - got0 - to_np(g["x"])
+    bound = 2.0 ** -8 * (np.abs(got1) + np.abs(got0)) + 1e-6
+    assert np.all(np.abs(res) <= bound)
 
 
 def test_forward_prenorm_full_size_sampled():
@@ -272,18 +271,6 @@ def test_forward_prenorm_full_size_sampled():
     rng = np.random.default_rng(4321)
     tok = np.sort(rng.choice(cfg.T, 8, replace=False))
     tok[0], tok[-1] = 0, cfg.T - 1
-    def layer(**kw):
-        return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=1,
-                           norm_w=c["norm_w"], norm_eps=EPS, act=cfg.act, **kw)
-
-    ref = layer(tokens=tok)
-    xn, _ = _norm_gpu(cfg, g)
-    same, _, _ = _rows_agree(cfg, xn, c, tok)
-    margin = ref["margin"]
-    keep = ((margin >= MARGIN_EXCLUDE) & same) | ((margin >= LOOSE_MARGIN) & ~same)
-    np.testing.assert_array_equal(np.sort(idx_g[tok], 1)[keep], np.sort(ref["idx"], 1)[keep])
-    _validate_excluded(cfg, idx_g[tok], ref, c["bias"], ~keep, same)
-    ref = with_gpu_choice(ref, idx_g[tok], keep,
-                          lambda rows, ix: layer(tokens=tok[rows], idx=ix))
+    ref = _checked(cfg, c, idx_g[tok], run.gates.cpu().numpy()[tok], 1, tokens=tok)
     out = to_np(run.out)[tok]
     assert_close(out, ref["out"], cfg.act, "V3 prefill pre-normed, sampled tokens")
