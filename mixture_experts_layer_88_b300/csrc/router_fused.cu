@@ -47,16 +47,16 @@ namespace {
 
 constexpr int FR_BK = 64;                                  // K elements per stage
 constexpr uint32_t FR_ROW = 128;                           // bytes per operand row per stage
-constexpr int FR_STAGES = 3;
+constexpr int FR_MAX_STAGES = 6;                           // operand ring: 3..6 stages
 constexpr uint32_t FR_A_BOX = 128 * FR_ROW;                // 16 KB: 128 centroid rows
-constexpr uint32_t FR_STAGE = 2 * FR_A_BOX + 256 * FR_ROW; // 64 KB
-constexpr uint32_t FR_RING = FR_STAGES * FR_STAGE;         // 192 KB
+constexpr uint32_t FR_RING = 220 * 1024;                   // operand ring (stages of A boxes + B rows)
 constexpr uint32_t FR_EPI_MAX = 220 * 1024;              // reduction buffers (alias the ring)
 constexpr int FR_WARPS = 10;
 constexpr int FR_MOVERS = 8;                               // warps 2..9
+constexpr int FR_TB = 6;                                   // tokens a warp selects at once
 constexpr int FR_THREADS = FR_WARPS * 32;
 constexpr uint32_t FR_AREA = FR_EPI_MAX > FR_RING ? FR_EPI_MAX : FR_RING;
-constexpr size_t FR_SMEM = 1024 + FR_AREA + 128;
+constexpr size_t FR_SMEM = 1024 + FR_AREA + 128 + 256 * 4;   // + barriers + bias
 constexpr uint32_t FR_TMEM_COLS = 512;
 constexpr int FR_TOKBOXES = 5;                             // token boxes of 16 << i rows
 
@@ -68,6 +68,8 @@ struct FusedMaps {
 struct FusedArgs {
   int T, E, K, nacc, epad, d;
   int k_blocks, kps, ck, nb, nown, nblocks, nclusters;
+  int nstages;                    // operand ring depth
+  uint32_t stage_bytes, b_off;    // bytes per stage; offset of the token rows in a stage
   int stride;                     // row stride (floats) of the logits buffer
   uint32_t ss_off;                // byte offset of the sum-of-squares slots [ck][nown]
   uint32_t inv_off;               // byte offset of the owned tokens' inv_rms [nown]
@@ -101,137 +103,122 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------- selection
-// Expert keys as unique 64-bit values: the orderable bits of the fp32 key
-// s + b above the complemented expert index, so that a larger value is a
-// larger key, or an equal key of a lower expert.  0 marks an empty slot.
-using u64 = unsigned long long;
-
-__device__ __forceinline__ void cas_desc(u64& a, u64& b) {
-  const u64 hi = a > b ? a : b;
-  const u64 lo = a > b ? b : a;
-  a = hi;
-  b = lo;
+// Approximate exponential and reciprocal (the hardware instructions, about
+// 2 ulp): the scores they give differ from the correctly rounded ones by a few
+// fp32 ulps, far below the 1e-5 margin of the key comparisons and of the gates.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-// Batcher's odd-even merge sort of 8 values, descending (19 compare-swaps).
-__device__ __forceinline__ void sort8_desc(u64 (&v)[8]) {
-  cas_desc(v[0], v[1]); cas_desc(v[2], v[3]); cas_desc(v[4], v[5]); cas_desc(v[6], v[7]);
-  cas_desc(v[0], v[2]); cas_desc(v[1], v[3]); cas_desc(v[4], v[6]); cas_desc(v[5], v[7]);
-  cas_desc(v[1], v[2]); cas_desc(v[5], v[6]);
-  cas_desc(v[0], v[4]); cas_desc(v[1], v[5]); cas_desc(v[2], v[6]); cas_desc(v[3], v[7]);
-  cas_desc(v[2], v[4]); cas_desc(v[3], v[5]);
-  cas_desc(v[1], v[2]); cas_desc(v[3], v[4]); cas_desc(v[5], v[6]);
-}
-
-// r := the 8 largest of r and c, both sorted descending: the elementwise
-// maximum of r and reversed c is bitonic, and three half-cleaner stages sort it.
-__device__ __forceinline__ void merge_top8(u64 (&r)[8], const u64 (&c)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) r[i] = r[i] > c[7 - i] ? r[i] : c[7 - i];
-  cas_desc(r[0], r[4]); cas_desc(r[1], r[5]); cas_desc(r[2], r[6]); cas_desc(r[3], r[7]);
-  cas_desc(r[0], r[2]); cas_desc(r[1], r[3]); cas_desc(r[4], r[6]); cas_desc(r[5], r[7]);
-  cas_desc(r[0], r[1]); cas_desc(r[2], r[3]); cas_desc(r[4], r[5]); cas_desc(r[6], r[7]);
-}
-
-__device__ __forceinline__ u64 shfl_xor_u64(u64 v, int m) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v), m);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), m);
-  return (static_cast<u64>(hi) << 32) | lo;
-}
-
-// Selection of one token by the four lanes 4j..4j+3 of a warp (K <= 8, no
-// node-limited groups): lane q of the four takes experts e = 4i + q, whose
-// logits lie in column tl of lg (expert-major rows of lstride floats).  Each
-// lane keeps the sorted 8 largest keys of its experts (chunks of 8: sort,
-// then merge), two shuffle levels merge the four lanes' lists, and the
-// chosen experts' scores are recomputed with the same arithmetic for the
-// gates.  The rules of select_experts: scores by eq. (15) (or Softmax over
-// all E), keys s + b, ties to the lower index, g = s / sum of the chosen s
-// (eq. 13) or s.  ok: this lane's token exists (all four lanes of a token
-// agree); every lane of the warp must call it.
-template <int NACC>
-__device__ __forceinline__ void select_quad(const float* __restrict__ lg, int lstride, int tl,
-                                            bool ok, size_t t, int q,
-                                            const float* __restrict__ bias, int E, int K,
-                                            int score_func, int normalize,
+// Selection of TB tokens by one warp, interleaved so that the tokens' warp
+// reductions overlap.  col[b]: token b's logits in shared memory, expert e at
+// col[b][e * stride]; ok[b]: the token exists; t[b]: its index.  No
+// node-limited groups, any K <= 32; the rules of select_experts: scores by
+// eq. (15) or Softmax over all E, keys s + b, K rounds taking the largest key,
+// equal keys to the lower index, g = s / sum of the chosen s or s.  Each round
+// takes two single-instruction warp reductions: the maximum of the lanes'
+// best 32-bit orderable keys, then the minimum expert index among the lanes
+// holding that key; only the winning lane rescans its slots (taken slots in a
+// bit mask), and the chosen expert's score is recomputed from its logit with
+// the same arithmetic.  bias_s: the bias in shared memory.
+template <int NPL, int TB>
+__device__ __forceinline__ void select_warp(const float* const (&col)[TB], int stride,
+                                            const bool (&ok)[TB], const size_t (&t)[TB],
+                                            int lane, const float* __restrict__ bias_s, int E,
+                                            int K, int score_func, int normalize,
                                             int32_t* __restrict__ idx, float* __restrict__ gates,
                                             float* __restrict__ scores) {
-  constexpr int CH = 4 * NACC;                  // chunks of 8 experts per lane
-  const float* col = lg + tl;
-  float m = 0.f, denom = 1.f;
-  if (score_func == MOE_SCORE_SOFTMAX) {
-    m = -INFINITY;
-#pragma unroll 8
-    for (int i = 0; i < 8 * CH; ++i) {
-      const int e = 4 * i + q;
-      if (e < E) m = fmaxf(m, col[e * lstride]);
+  constexpr float kLog2e = 1.4426950408889634f;
+  const bool softmax = score_func == MOE_SCORE_SOFTMAX;
+  float m[TB], r[TB];                 // Softmax: maximum logit and 1 / sum
+  uint32_t key[TB][NPL];
+  uint32_t best[TB], taken[TB];
+  int bj[TB];
+#pragma unroll
+  for (int b = 0; b < TB; ++b) {
+    float L[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = j * 32 + lane;
+      L[j] = e < E ? col[b][e * stride] : -INFINITY;
     }
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    float sum = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < 8 * CH; ++i) {
-      const int e = 4 * i + q;
-      if (e < E) sum += __expf(col[e * lstride] - m);
+    m[b] = 0.f;
+    r[b] = 1.f;
+    if (softmax) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) mx = fmaxf(mx, L[j]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) sum += j * 32 + lane < E ? fast_exp2((L[j] - mx) * kLog2e) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      m[b] = mx;
+      r[b] = 1.0f / sum;
     }
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    denom = sum;
+    best[b] = 0u;
+    bj[b] = 0;
+    taken[b] = 0u;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = j * 32 + lane;
+      const float sc = softmax ? fast_exp2((L[j] - m[b]) * kLog2e) * r[b]
+                               : fast_rcp(1.0f + fast_exp2(-L[j] * kLog2e));
+      key[b][j] = e < E ? orderable(sc + bias_s[e]) : 0u;
+      if (scores && ok[b] && e < E) scores[t[b] * E + e] = sc;
+      // this lane's best key and its slot (lower slot = lower expert on equal keys)
+      if (key[b][j] > best[b]) { best[b] = key[b][j]; bj[b] = j; }
+    }
   }
-  // fast exponential and reciprocal: a few fp32 ulps, far below the 1e-5 of
-  // the key comparisons and the gates
-  const float rden = 1.0f / denom;
-  auto score = [&](float L) {
-    return score_func == MOE_SCORE_SOFTMAX ? __expf(L - m) * rden
-                                           : __frcp_rn(1.0f + __expf(-L));
-  };
-  u64 r[8];
+  int my_e[TB];
+  float my_s[TB], sum_sel[TB];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) r[i] = 0ull;
-#pragma unroll 1
-  for (int c = 0; c < CH; ++c) {
-    u64 v[8];
+  for (int b = 0; b < TB; ++b) { my_e[b] = 0; my_s[b] = 0.f; sum_sel[b] = 0.f; }
+  for (int k = 0; k < K; ++k) {
+    uint32_t ew[TB];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = 4 * (8 * c + i) + q;
-      v[i] = 0ull;
-      if (e < E) {
-        const float s = score(col[e * lstride]);
-        if (scores && ok) scores[t * E + e] = s;
-        v[i] = (static_cast<u64>(orderable(s + __ldg(bias + e))) << 32) |
-               (0xFFFFFFFFu - static_cast<uint32_t>(e));
+    for (int b = 0; b < TB; ++b) {
+      const uint32_t mx = __reduce_max_sync(0xffffffffu, best[b]);
+      ew[b] = best[b] == mx ? static_cast<uint32_t>(bj[b] * 32 + lane) : 0xFFFFFFFFu;
+    }
+#pragma unroll
+    for (int b = 0; b < TB; ++b) ew[b] = __reduce_min_sync(0xffffffffu, ew[b]);
+#pragma unroll
+    for (int b = 0; b < TB; ++b) {
+      if (lane == static_cast<int>(ew[b] & 31u)) {
+        taken[b] |= 1u << bj[b];
+        best[b] = 0u;
+        bj[b] = 0;
+#pragma unroll
+        for (int j = 0; j < NPL; ++j)
+          if (!((taken[b] >> j) & 1u) && key[b][j] > best[b]) { best[b] = key[b][j]; bj[b] = j; }
+      }
+      const float Lw = col[b][static_cast<int>(ew[b]) * stride];
+      const float sv = softmax ? fast_exp2((Lw - m[b]) * kLog2e) * r[b]
+                               : fast_rcp(1.0f + fast_exp2(-Lw * kLog2e));
+      sum_sel[b] += sv;
+      if (lane == k) {
+        my_e[b] = static_cast<int>(ew[b]);
+        my_s[b] = sv;
       }
     }
-    sort8_desc(v);
-    merge_top8(r, v);
   }
 #pragma unroll
-  for (int off = 1; off <= 2; off <<= 1) {
-    u64 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = shfl_xor_u64(r[i], off);
-    merge_top8(r, v);
-  }
-  float sk[8];
-  float sum_sel = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    sk[k] = 0.f;
-    if (k < K) {
-      const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(r[k]));
-      sk[k] = score(col[e * lstride]);
-      sum_sel += sk[k];
-    }
-  }
-  if (!ok) return;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    if (k < K && (k & 3) == q) {
-      const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(r[k]));
-      float g = sk[k];
-      if (normalize) g = sum_sel > 0.f ? sk[k] / sum_sel : 0.f;
-      idx[t * K + k] = e;
-      gates[t * K + k] = g;
+  for (int b = 0; b < TB; ++b) {
+    if (ok[b] && lane < K) {
+      float g = my_s[b];
+      if (normalize) g = sum_sel[b] > 0.f ? my_s[b] / sum_sel[b] : 0.f;
+      idx[t[b] * K + lane] = my_e[b];
+      gates[t[b] * K + lane] = g;
     }
   }
 }
@@ -243,11 +230,12 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + FR_AREA);
-  uint64_t* empty = full + FR_STAGES;
-  uint64_t* tfull = empty + FR_STAGES;
+  uint64_t* empty = full + FR_MAX_STAGES;
+  uint64_t* tfull = empty + FR_MAX_STAGES;
   uint64_t* drain = tfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* bias_s = reinterpret_cast<float*>(smem + FR_AREA + 128);   // [E <= 256]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -256,7 +244,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
   const bool prenorm = a.inv_rms != nullptr;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < FR_STAGES; ++s) {
+    for (int s = 0; s < a.nstages; ++s) {
       tc::mbar_init(full + s, 1);
       // released by the MMA commit, and behind the RMSNorm also by one arrival
       // of each mover warp once it has read the stage's token rows
@@ -273,6 +261,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
     tc::tmem_alloc<1>(tmem_slot, FR_TMEM_COLS);
     tc::tmem_relinquish<1>();
   }
+  for (int e = threadIdx.x; e < a.E; e += FR_THREADS) bias_s[e] = __ldg(a.bias + e);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -312,7 +301,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) break;
           if (lane == 0) {
-            uint8_t* sa = smem + stage * FR_STAGE;
+            uint8_t* sa = smem + stage * a.stage_bytes;
             tc::mbar_arrive_expect_tx(full + stage, bytes);
             tc::tma_load_2d(sa, &maps.a, full + stage, kb * FR_BK, 0);
             if (a.nacc == 2)
@@ -322,7 +311,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
             for (int bi = FR_TOKBOXES - 1; bi >= 0; --bi) {
               const int h = 16 << bi;
               if (nmma & h) {
-                tc::tma_load_2d(sa + 2 * FR_A_BOX + done * FR_ROW, &maps.b[bi], full + stage,
+                tc::tma_load_2d(sa + a.b_off + done * FR_ROW, &maps.b[bi], full + stage,
                                 kb * FR_BK, tok0 + done);
                 done += h;
               }
@@ -331,7 +320,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           __syncwarp();
-          if (++stage == FR_STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == a.nstages) { stage = 0; phase ^= 1u; }
         }
       }
     } else if (warp == 1) {
@@ -343,10 +332,10 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
           if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
           tc::tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = tc::smem_u32(smem + stage * FR_STAGE);
+            const uint32_t sa = tc::smem_u32(smem + stage * a.stage_bytes);
 #pragma unroll
             for (int kk = 0; kk < FR_BK / 16; ++kk) {
-              const uint64_t db = tc::smem_desc_sw128(sa + 2 * FR_A_BOX + kk * 32);
+              const uint64_t db = tc::smem_desc_sw128(sa + a.b_off + kk * 32);
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
               tc::mma_bf16<1>(tmem, tc::smem_desc_sw128(sa + kk * 32), db, idesc, acc);
               if (a.nacc == 2)
@@ -357,7 +346,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
           }
           mma_issued = true;
           __syncwarp();
-          if (++stage == FR_STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == a.nstages) { stage = 0; phase ^= 1u; }
         }
         if (ok && lane == 0) tc::mma_commit<1>(tfull);
         __syncwarp();
@@ -371,7 +360,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!warp_wait(full + stage, phase, abort_flag, tmo)) break;
           if (mv < nmma) {
-            const uint8_t* rowp = smem + stage * FR_STAGE + 2 * FR_A_BOX + mv * FR_ROW;
+            const uint8_t* rowp = smem + stage * a.stage_bytes + a.b_off + mv * FR_ROW;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((c ^ (mv & 7)) << 4));
@@ -386,7 +375,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
           }
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(empty + stage);
-          if (++stage == FR_STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == a.nstages) { stage = 0; phase ^= 1u; }
         }
       }
       // this CTA's accumulators
@@ -507,23 +496,24 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
     __syncthreads();
     if (live) {
       const int own0 = tok0 + rank * a.nown;
-      if (a.K <= 8 && a.n_groups == 0) {
-        // four lanes per token, eight tokens per warp
-        for (int base = warp * 8; base < a.nown; base += FR_WARPS * 8) {
-          const int tl = base + (lane >> 2);
-          const bool ok = tl < a.nown && own0 + tl < a.T;
-          const int tlr = tl < a.nown ? tl : a.nown - 1;
-          if (a.nacc == 2)
-            select_quad<2>(lg, a.stride, tlr, ok, static_cast<size_t>(own0 + tlr), lane & 3,
-                           a.bias, a.E, a.K, a.score_func, a.normalize, a.idx, a.gates,
-                           a.scores);
-          else
-            select_quad<1>(lg, a.stride, tlr, ok, static_cast<size_t>(own0 + tlr), lane & 3,
-                           a.bias, a.E, a.K, a.score_func, a.normalize, a.idx, a.gates,
-                           a.scores);
+      if (a.n_groups == 0) {
+        // FR_TB owned tokens per warp at a time
+        for (int jb = warp * FR_TB; jb < a.nown; jb += FR_WARPS * FR_TB) {
+          const float* colp[FR_TB];
+          bool ok[FR_TB];
+          size_t t[FR_TB];
+#pragma unroll
+          for (int b = 0; b < FR_TB; ++b) {
+            const int jl = jb + b < a.nown ? jb + b : a.nown - 1;
+            ok[b] = jb + b < a.nown && own0 + jb + b < a.T;
+            t[b] = static_cast<size_t>(own0 + jl);
+            colp[b] = lg + jl;
+          }
+          select_warp<NPL, FR_TB>(colp, a.stride, ok, t, lane, bias_s, a.E, a.K, a.score_func,
+                                  a.normalize, a.idx, a.gates, a.scores);
         }
       } else {
-        // K > 8 or node-limited groups: one warp per token (select_experts)
+        // node-limited groups: one warp per token (select_experts)
         for (int jl = warp; jl < a.nown; jl += FR_WARPS) {
           const int t = own0 + jl;
           if (t >= a.T) break;
@@ -547,7 +537,7 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
 
   if (*abort_flag) {
     if (warp == 0) {
-      for (int s = 0; s < FR_STAGES; ++s)
+      for (int s = 0; s < a.nstages; ++s)
         if (issued & (1u << s)) drain_wait(full + s, (issued_par >> s) & 1u, tmo);
     } else if (warp == 1 && mma_issued) {
       if (lane == 0) tc::mma_commit<1>(drain);
@@ -650,14 +640,25 @@ bool fused_router_applies(int act_dtype, int d, int E) {
   return act_dtype == MOE_BF16 && E >= 1 && E <= 256 && d % 64 == 0 && d > 0;
 }
 
+// Shape of the launch, by a cost model in SM cycles with rates measured on
+// B300: each CTA's operands (centroid rows and token rows of its K slice)
+// cross from L2 at about 68 B/cycle, the batch's tokens are read from HBM at
+// about 3250 B/cycle for the whole GPU (6.5 TB/s at 2 GHz), the partials move
+// between the CTAs of a cluster at about 9 B/cycle per SM, and a warp selects
+// FR_TB tokens in about 5000 cycles.  Wider token blocks cut the centroid
+// traffic, more K splits cut it further but add exchange: for the V3 prefill
+// layer (T = 8192) this picks clusters of two CTAs and blocks of 112 tokens.
 bool fused_router_plan(int T, int d, int E, FusedRouterPlan* p) {
   if (T <= 0 || !fused_router_applies(MOE_BF16, d, E)) return false;
+  constexpr double kL2BytesPerCycle = 68.0, kHbmBytesPerCycle = 3250.0;
+  constexpr double kDsmemBytesPerCycle = 9.0, kSelectCycles = 5000.0;
   const int nacc = E > 128 ? 2 : 1;
   const int epad = 128 * nacc;
   const int kb = d / 64;
+  const double hbm = static_cast<double>(T) * d * 2 / kHbmBytesPerCycle;
   bool found = false;
   FusedRouterPlan best{};
-  int best_waves = 0;
+  double best_cost = 0.0;
   for (int ck = 1; ck <= 8; ck *= 2) {
     const int kps = ceil_div(kb, ck);
     if ((ck - 1) * kps >= kb) continue;                   // a split would be empty
@@ -672,13 +673,17 @@ bool fused_router_plan(int T, int d, int E, FusedRouterPlan* p) {
     const int nblocks = ceil_div(T, nb);
     const int nclusters = std::min(maxc, nblocks);
     const int waves = ceil_div(nblocks, nclusters);
-    // fewest waves, then the widest token blocks (fewer centroid re-reads and
-    // wider MMAs), then the most K splits (smaller share of the centroids per CTA)
-    const bool better = !found || waves < best_waves ||
-                        (waves == best_waves && (nb > best.nb || (nb == best.nb && ck > best.ck)));
-    if (better) {
+    const int nown = nb / ck;
+    const double kloop = waves * static_cast<double>(kps) * (128.0 * nacc + nb) * 128.0 /
+                         kL2BytesPerCycle;
+    const double exch =
+        waves * static_cast<double>(ck - 1) * nown * epad * 4.0 / kDsmemBytesPerCycle;
+    const double sel = waves * static_cast<double>(ceil_div(nown, FR_WARPS * FR_TB)) *
+                       kSelectCycles;
+    const double cost = std::max(kloop, hbm) + exch + sel;
+    if (!found || cost < best_cost) {
       found = true;
-      best_waves = waves;
+      best_cost = cost;
       best.ck = ck;
       best.nb = nb;
       best.kps = kps;
@@ -714,6 +719,12 @@ moe_status_t launch_router_fused(const FusedRouterPlan& p, const void* x, const 
   a.nown = p.nb / p.ck;
   a.nblocks = p.nblocks;
   a.nclusters = p.nclusters;
+  // operand ring: A boxes (one per 128 experts) then the block's token rows,
+  // 1024-byte aligned for the 128-byte swizzle; as many stages as fit
+  a.b_off = static_cast<uint32_t>(a.nacc) * FR_A_BOX;
+  a.stage_bytes = static_cast<uint32_t>(align_up(a.b_off + static_cast<size_t>(round_up(a.nb, 16)) *
+                                                     FR_ROW, 1024));
+  a.nstages = std::min<int>(FR_MAX_STAGES, static_cast<int>(FR_RING / a.stage_bytes));
   const FrLayout L = fr_layout(a.nown, p.ck, a.epad);
   a.stride = L.stride;
   a.ss_off = L.ss_off;
