@@ -417,7 +417,7 @@ moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,
   int32_t* bs = orow + (G + 1);
   int32_t* bstart = bs + (G + 1);
   const GroupLayout lay{static_cast<int>(fr.P), static_cast<int>(fr.P), static_cast<int>(fr.Tp),
-                        96};   // token blocks of the FP8 GEMMs: at most 96 tokens
+                        192};   // token blocks of the FP8 GEMMs: at most 192 tokens
   moe_status_t s = launch_build_groups(offsets, counts, c.T, c.E, c.S, lay, rows, brow, orow, bs,
                                        bstart, st);
   if (s != MOE_OK) return s;
@@ -426,7 +426,7 @@ moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,
   // gate/up + SwiGLU + e4m3 quantisation of act (1 x 128 along I)
   Fp8GemmMaps m1;
   if (!make_fp8_maps(&m1, w.w13, static_cast<uint64_t>(c.E) * 2 * c.I, sh ? w.ws13 : nullptr,
-                     static_cast<uint64_t>(c.S) * 2 * c.I, xq, fr.rows_in, xs, c.d))
+                     static_cast<uint64_t>(c.S) * 2 * c.I, 64, xq, fr.rows_in, xs, c.d))
     return MOE_ERR_CUDA;
   Fp8GemmArgs a{};
   a.gt = GroupTable{rows, brow, orow, bs, bstart};
@@ -450,13 +450,13 @@ moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,
   // down: A = W2 blocks, B = quantised activations
   Fp8GemmMaps m2;
   if (!make_fp8_maps(&m2, w.w2, static_cast<uint64_t>(c.E) * c.d, sh ? w.ws2 : nullptr,
-                     static_cast<uint64_t>(c.S) * c.d, act, fr.rows_out, act_s, c.I))
+                     static_cast<uint64_t>(c.S) * c.d, 128, act, fr.rows_out, act_s, c.I))
     return MOE_ERR_CUDA;
   Fp8GemmArgs b = a;
   b.gt = GroupTable{rows, orow, orow, bs, bstart};
   b.m_blocks = ceil_div(c.d, 256);
   b.a_rows_per_group = c.d;
-  b.a1_off = 128;
+  b.a1_off = 0;
   b.k_blocks = c.I / 128;
   b.w_scale[0] = w.w2_scale;
   b.w_scale[1] = sh ? w.ws2_scale : w.w2_scale;
