@@ -139,6 +139,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok != 0;
 }
 
+// Bounded wait of a single thread (roles whose loop runs on one thread).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag,
+                                            unsigned long long timeout_ns) {
+  if (CLUSTER ? tc::mbar_try_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity))
+    return true;
+  return tc::mbar_wait_bounded<CLUSTER>(bar, parity, abort_flag,
+                                        tc::globaltimer_ns() + timeout_ns);
+}
+
 // Drain wait after an abort: lane 0 waits up to timeout_ns whatever the abort
 // flag says, so the loads and MMAs this CTA issued complete before TMEM is
 // freed and the CTA exits.
@@ -299,6 +310,29 @@ struct TileQueue {
     ++i;
     return true;
   }
+  // single-thread forms of publish() and next() for roles that run on one thread
+  __device__ __forceinline__ bool publish1(int t, int& tile) {
+    const int s = i % EX_QUEUE;
+    const uint32_t ph = static_cast<uint32_t>(i / EX_QUEUE) & 1u;
+    if (!thread_wait<true>(qempty + s, ph ^ 1u, abort_flag, tmo)) return false;
+    tq[s] = t;
+    tc::st_shared_cluster_u32(tc::mapa_shared(tc::smem_u32(const_cast<int*>(tq) + s), 1),
+                              static_cast<uint32_t>(t));
+    tc::mbar_arrive(qfull + s);
+    tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(qfull + s), 1));
+    tile = t;
+    ++i;
+    return true;
+  }
+  __device__ __forceinline__ bool next1(int& tile) {
+    const int s = i % EX_QUEUE;
+    const uint32_t ph = static_cast<uint32_t>(i / EX_QUEUE) & 1u;
+    if (!thread_wait<true>(qfull + s, ph, abort_flag, tmo)) return false;
+    tile = tq[s];
+    tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(qempty + s), 0));
+    ++i;
+    return true;
+  }
   // any other role: read the next published tile and release the slot
   __device__ __forceinline__ bool next(int& tile) {
     const int s = i % EX_QUEUE;
@@ -392,12 +426,15 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
   TileQueue queue{qfull, qempty, tq, rank, abort_flag, tmo, args.tile_counter};
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // One thread runs the loop: no warp-collective step sits between its
+    // barrier tests and its TMA instructions.
+    if (lane == 0) {
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, issued_par = 0;   // per stage: a load is in flight / its parity
     bool ok = true;
     int tile = 0;
-    ok = rank == 0 ? queue.publish(queue.take(), tile) : queue.next(tile);
+    ok = rank == 0 ? queue.publish1(queue.take(), tile) : queue.next1(tile);
     while (ok && tile < ntiles) {
       const int claimed = rank == 0 ? queue.take() : 0;   // the tile after this one
       Tile t;
@@ -416,8 +453,8 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
       // the raw weight boxes count on this CTA's own raw_full barrier)
       const uint32_t bytes = (W8 ? 0u : 2 * EX_A_BOX_BYTES) + half * ROW_BYTES;
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
-        if (lane == 0) {
+        if (!thread_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        {
           // Only the even CTA arrives, expecting the bytes of both CTAs; the
           // odd CTA's loads just count their bytes on the even CTA's barrier.
           // (The odd CTA reuses stage s only after the MMAs that consumed it
@@ -454,45 +491,47 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
         }
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-        __syncwarp();
         if (++stage == NST) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      ok = rank == 0 ? queue.publish(claimed, tile) : queue.next(tile);
+      ok = rank == 0 ? queue.publish1(claimed, tile) : queue.next1(tile);
     }
     if (!ok) {
       // abort: let every load counted on this CTA's barriers land before exit
+      const unsigned long long dl = tc::globaltimer_ns() + tmo;
       for (int s = 0; s < NST; ++s) {
         if (!(issued & (1u << s))) continue;
-        if (rank == 0) drain_wait(full + s, (issued_par >> s) & 1u, tmo);
-        if (W8) drain_wait(raw_full + s, (issued_par >> s) & 1u, tmo);
+        if (rank == 0) tc::mbar_wait_deadline(full + s, (issued_par >> s) & 1u, dl);
+        if (W8) tc::mbar_wait_deadline(raw_full + s, (issued_par >> s) & 1u, dl);
       }
     }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (rank == 0) {
+    if (rank == 0 && lane == 0) {   // one thread runs the loop
       int stage = 0, aslot = 0;
       uint32_t phase = 0, tphase = 0, aphase = 0;
       bool ok = true, issued_any = false;
       for (;;) {
         int tile;
-        if (!queue.next(tile)) { ok = false; break; }
+        if (!queue.next1(tile)) { ok = false; break; }
         if (tile >= ntiles) break;
         Tile t;
         decode_group_tile(args, tile, t);
-        if (!warp_wait<true>(tempty, tphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+        if (!thread_wait<true>(tempty, tphase ^ 1u, abort_flag, tmo)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t idesc = tc::idesc_bf16_f32_mn(256, t.nmma, MODE == GM_DGRAD, false);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+          if (!thread_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
           // W8: the dequantised weights of both CTAs (written by threads,
           // published with release at cluster scope)
-          if (W8 && !warp_wait<true>(a_full + aslot, aphase, abort_flag, tmo)) {
+          if (W8 && !thread_wait<true>(a_full + aslot, aphase, abort_flag, tmo)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          if (lane == 0) {
+          {
             const uint32_t sa = tc::smem_u32(smem + stage * STB);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -524,21 +563,19 @@ __global__ void __launch_bounds__(ex_threads(W8), 1)
             if (W8) tc::mma_commit<2>(a_empty + aslot);
           }
           issued_any = true;
-          __syncwarp();
           if (++stage == NST) { stage = 0; phase ^= 1u; }
           if (W8 && ++aslot == W8_A_SLOTS) { aslot = 0; aphase ^= 1u; }
         }
         if (!ok) break;
-        if (lane == 0) tc::mma_commit<2>(tfull);  // accumulators complete, both CTAs
-        __syncwarp();
+        tc::mma_commit<2>(tfull);  // accumulators complete, both CTAs
         tphase ^= 1u;
       }
       if (!ok && issued_any) {
-        if (lane == 0) tc::mma_commit<2>(drain, 0x1);
-        __syncwarp();
-        drain_wait(drain, 0, tmo);
+        tc::mma_commit<2>(drain, 0x1);
+        tc::mbar_wait_deadline(drain, 0, tc::globaltimer_ns() + tmo);
       }
     }
+    __syncwarp();
   } else if (W8 && warp >= 2 + EX_EPI_WARPS) {
     // ------------------------------------------------------------ dequantisation (W8)
     // Group grp takes the K steps ks with ks % 2 == grp (A slot grp).  Thread
