@@ -293,24 +293,8 @@ struct TileQueue {
   __device__ __forceinline__ int take() const {
     return (threadIdx.x & 31) == 0 ? atomicAdd(counter, 1) : 0;
   }
-  // even CTA, producer warp: publish a claimed tile to both CTAs; every lane
-  // gets it back
-  __device__ __forceinline__ bool publish(int t, int& tile) {
-    const int s = i % EX_QUEUE;
-    const uint32_t ph = static_cast<uint32_t>(i / EX_QUEUE) & 1u;
-    if (!warp_wait<true>(qempty + s, ph ^ 1u, abort_flag, tmo)) return false;
-    if ((threadIdx.x & 31) == 0) {
-      tq[s] = t;
-      tc::st_shared_cluster_u32(tc::mapa_shared(tc::smem_u32(const_cast<int*>(tq) + s), 1),
-                                static_cast<uint32_t>(t));
-      tc::mbar_arrive(qfull + s);
-      tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(qfull + s), 1));
-    }
-    tile = __shfl_sync(0xffffffffu, t, 0);
-    ++i;
-    return true;
-  }
-  // single-thread forms of publish() and next() for roles that run on one thread
+  // even CTA, producer thread: publish a claimed tile to both CTAs.  Other
+  // single-thread roles: read the next published tile and release the slot.
   __device__ __forceinline__ bool publish1(int t, int& tile) {
     const int s = i % EX_QUEUE;
     const uint32_t ph = static_cast<uint32_t>(i / EX_QUEUE) & 1u;
@@ -872,16 +856,18 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // A loads (ai) and B loads (bi) each run through their ring of slots; a
-    // slot is refilled after the MMAs committed its "empty" barrier.
+    // slot is refilled after the MMAs committed its "empty" barrier.  One
+    // thread runs the loop.
+    if (lane == 0) {
     uint32_t ai = 0, bi = 0;
     uint32_t a_iss = 0, a_par = 0, b_iss = 0, b_par = 0;   // per slot: load in flight, parity
     bool ok = true;
     int tile = 0;
-    ok = rank == 0 ? queue.publish(queue.take(), tile) : queue.next(tile);
+    ok = rank == 0 ? queue.publish1(queue.take(), tile) : queue.next1(tile);
     auto load_a = [&](const WTile& t, int kb) -> bool {
       const uint32_t s = ai % WG_A_SLOTS, ph = (ai / WG_A_SLOTS) & 1u;
-      if (!warp_wait(a_empty + s, ph ^ 1u, abort_flag, tmo)) return false;
-      if (lane == 0) {
+      if (!thread_wait(a_empty + s, ph ^ 1u, abort_flag, tmo)) return false;
+      {
         const uint32_t fb = tc::mapa_shared(tc::smem_u32(a_full + s), 0);
         if (rank == 0) tc::mbar_arrive_expect_tx(a_full + s, 2 * WG_SLOT_BYTES);
         uint8_t* sa = smem + s * WG_SLOT_BYTES;
@@ -892,14 +878,13 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
       }
       a_iss |= 1u << s;
       a_par = (a_par & ~(1u << s)) | (ph << s);
-      __syncwarp();
       ++ai;
       return true;
     };
     auto load_b = [&](const WTile& t, int nb, int kb) -> bool {
       const uint32_t s = bi % WG_B_STAGES, ph = (bi / WG_B_STAGES) & 1u;
-      if (!warp_wait(b_empty + s, ph ^ 1u, abort_flag, tmo)) return false;
-      if (lane == 0) {
+      if (!thread_wait(b_empty + s, ph ^ 1u, abort_flag, tmo)) return false;
+      {
         const uint32_t fb = tc::mapa_shared(tc::smem_u32(b_full + s), 0);
         if (rank == 0) tc::mbar_arrive_expect_tx(b_full + s, 2 * WG_SLOT_BYTES);
         uint8_t* sb = smem + WG_B_OFF + s * WG_SLOT_BYTES;
@@ -911,7 +896,6 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
       }
       b_iss |= 1u << s;
       b_par = (b_par & ~(1u << s)) | (ph << s);
-      __syncwarp();
       ++bi;
       return true;
     };
@@ -928,24 +912,27 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
           if (ok) ok = load_b(t, nb, kb);
         }
       if (!ok) break;
-      ok = rank == 0 ? queue.publish(claimed, tile) : queue.next(tile);
+      ok = rank == 0 ? queue.publish1(claimed, tile) : queue.next1(tile);
     }
     if (!ok && rank == 0) {
       // abort: let every load counted on this CTA's barriers land before exit
+      const unsigned long long dl = tc::globaltimer_ns() + tmo;
       for (int s = 0; s < WG_A_SLOTS; ++s)
-        if (a_iss & (1u << s)) drain_wait(a_full + s, (a_par >> s) & 1u, tmo);
+        if (a_iss & (1u << s)) tc::mbar_wait_deadline(a_full + s, (a_par >> s) & 1u, dl);
       for (int s = 0; s < WG_B_STAGES; ++s)
-        if (b_iss & (1u << s)) drain_wait(b_full + s, (b_par >> s) & 1u, tmo);
+        if (b_iss & (1u << s)) tc::mbar_wait_deadline(b_full + s, (b_par >> s) & 1u, dl);
     }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (rank == 0) {
+    if (rank == 0 && lane == 0) {   // one thread runs the loop
       uint32_t ai = 0, bi = 0, acc_n = 0;
       bool ok = true, issued_any = false;
       const uint32_t idesc = tc::idesc_bf16_f32_mn(256, 256, true, true);
       for (;;) {
         int tile;
-        if (!queue.next(tile)) { ok = false; break; }
+        if (!queue.next1(tile)) { ok = false; break; }
         if (tile >= ntiles) break;
         WTile t;
         decode_wgrad_tile(args, tile, t);
@@ -956,20 +943,20 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         if (res) ai += nk;
         for (int nb = t.nb0; ok && nb <= t.nb1; ++nb) {
           const uint32_t slot = acc_n & 1u, use = acc_n >> 1;
-          if (!warp_wait<true>(tempty + slot, (use & 1u) ^ 1u, abort_flag, tmo)) { ok = false; break; }
+          if (!thread_wait<true>(tempty + slot, (use & 1u) ^ 1u, abort_flag, tmo)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t dcol = tmem_base + slot * 256;
           for (int kb = 0; kb < nk; ++kb) {
             const uint32_t aj = res ? a0 + kb : ai++;
             const uint32_t as = aj % WG_A_SLOTS, bs = bi % WG_B_STAGES;
-            if (!warp_wait(a_full + as, (aj / WG_A_SLOTS) & 1u, abort_flag, tmo) ||
-                !warp_wait(b_full + bs, (bi / WG_B_STAGES) & 1u, abort_flag, tmo)) {
+            if (!thread_wait(a_full + as, (aj / WG_A_SLOTS) & 1u, abort_flag, tmo) ||
+                !thread_wait(b_full + bs, (bi / WG_B_STAGES) & 1u, abort_flag, tmo)) {
               ok = false;
               break;
             }
             ++bi;
             tc::tc_fence_after();
-            if (lane == 0) {
+            {
               const uint32_t sa = tc::smem_u32(smem + as * WG_SLOT_BYTES);
               const uint32_t sb = tc::smem_u32(smem + WG_B_OFF + bs * WG_SLOT_BYTES);
               const int left = t.kn - kb * BK;
@@ -984,27 +971,23 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
               if (!res) tc::mma_commit<2>(a_empty + as);
             }
             issued_any = true;
-            __syncwarp();
           }
           if (!ok) break;
-          if (lane == 0) tc::mma_commit<2>(tfull + slot);
-          __syncwarp();
+          tc::mma_commit<2>(tfull + slot);
           ++acc_n;
         }
         if (!ok) break;
         if (res) {
           // the unit's MMAs are issued: its A slots free once they complete
-          if (lane == 0)
-            for (int kb = 0; kb < nk; ++kb) tc::mma_commit<2>(a_empty + (a0 + kb) % WG_A_SLOTS);
-          __syncwarp();
+          for (int kb = 0; kb < nk; ++kb) tc::mma_commit<2>(a_empty + (a0 + kb) % WG_A_SLOTS);
         }
       }
       if (!ok && issued_any) {
-        if (lane == 0) tc::mma_commit<2>(drain, 0x1);
-        __syncwarp();
-        drain_wait(drain, 0, tmo);
+        tc::mma_commit<2>(drain, 0x1);
+        tc::mbar_wait_deadline(drain, 0, tc::globaltimer_ns() + tmo);
       }
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     // warp w: TMEM lanes 32 (w % 4).. (dW rows), columns 128 h .. of each
