@@ -94,6 +94,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Bounded wait of a single thread (the producer and MMA loops run on one thread).
+__device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag,
+                                            unsigned long long timeout_ns) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  return tc::mbar_wait_bounded(bar, parity, abort_flag, tc::globaltimer_ns() + timeout_ns);
+}
+
 // Drain wait after an abort: bounded by the deadline alone.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
                                            unsigned long long timeout_ns) {
@@ -296,11 +304,12 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
     float ss = 0.f;                          // movers: sum of x^2 of token column mv
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA producer
-      if (!*abort_flag) {
+      // (one thread: no warp-collective step between its waits and its loads)
+      if (lane == 0 && !*abort_flag) {
         const uint32_t bytes = a.nacc * FR_A_BOX + nmma * FR_ROW;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!warp_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) break;
-          if (lane == 0) {
+          if (!thread_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) break;
+          {
             uint8_t* sa = smem + stage * a.stage_bytes;
             tc::mbar_arrive_expect_tx(full + stage, bytes);
             tc::tma_load_2d(sa, &maps.a, full + stage, kb * FR_BK, 0);
@@ -319,19 +328,19 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
           }
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-          __syncwarp();
           if (++stage == a.nstages) { stage = 0; phase ^= 1u; }
         }
       }
+      __syncwarp();
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
-      if (!*abort_flag) {
+      if (lane == 0 && !*abort_flag) {   // one thread
         const uint32_t idesc = tc::idesc_bf16_f32(128, nmma);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!warp_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+          if (!thread_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
           tc::tc_fence_after();
-          if (lane == 0) {
+          {
             const uint32_t sa = tc::smem_u32(smem + stage * a.stage_bytes);
 #pragma unroll
             for (int kk = 0; kk < FR_BK / 16; ++kk) {
@@ -345,12 +354,11 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
             tc::mma_commit<1>(empty + stage);
           }
           mma_issued = true;
-          __syncwarp();
           if (++stage == a.nstages) { stage = 0; phase ^= 1u; }
         }
-        if (ok && lane == 0) tc::mma_commit<1>(tfull);
-        __syncwarp();
+        if (ok) tc::mma_commit<1>(tfull);
       }
+      __syncwarp();
     } else {
       // ---------------------------------------------------------------- movers
       if (prenorm && !*abort_flag) {
@@ -535,7 +543,12 @@ __global__ void __launch_bounds__(FR_THREADS, 1)
     tc::tc_fence_after();
   }
 
-  if (*abort_flag) {
+  // the producer's and MMA issuer's loop state lives in lane 0: share it
+  // with the warp, and take one view of the abort flag per warp
+  issued = __shfl_sync(0xffffffffu, issued, 0);
+  issued_par = __shfl_sync(0xffffffffu, issued_par, 0);
+  mma_issued = __shfl_sync(0xffffffffu, mma_issued ? 1 : 0, 0) != 0;
+  if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
     if (warp == 0) {
       for (int s = 0; s < a.nstages; ++s)
         if (issued & (1u << s)) drain_wait(full + s, (issued_par >> s) & 1u, tmo);
