@@ -100,6 +100,44 @@ __global__ void fold_bf16_kernel(const __nv_bfloat16* __restrict__ e, const floa
   }
 }
 
+// bf16 of the exact product w * e, rounded once, in fp32 arithmetic: p = w * e
+// rounded to fp32 and its error err = w * e - p (exact through an FMA, the
+// TwoProduct error-free transformation).  Rounding p to bf16 gives the correctly
+// rounded product except when p sits exactly halfway between two bf16 values
+// and err is not zero; then the exact product lies on err's side of the
+// midpoint and is rounded that way.  (Products here are far from fp32's
+// subnormal range, where err could itself round.)
+__device__ __forceinline__ __nv_bfloat16 product_bf16(float w, float e) {
+  const float p = w * e;
+  const float err = fmaf(w, e, -p);
+  const uint32_t u = __float_as_uint(p);
+  if ((u & 0xffffu) == 0x8000u && err != 0.f) {
+    const bool away = (err > 0.f) == (p > 0.f);   // the exact magnitude is larger
+    const uint32_t r = away ? (u + 0x8000u) >> 16 : u >> 16;
+    return __ushort_as_bfloat16(static_cast<unsigned short>(r));
+  }
+  return __float2bfloat16_rn(p);
+}
+
+// The same fold as fold_bf16_kernel, eight elements per thread with 16-byte
+// loads and stores (d a multiple of 8), the product rounded by product_bf16.
+__global__ void fold_bf16_x8_kernel(const uint4* __restrict__ e, const float4* __restrict__ w,
+                                    int vpr, int nvec, uint4* __restrict__ ew) {
+  for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += gridDim.x * blockDim.x) {
+    const int c = v % vpr;                       // 8-element column block of the row
+    const uint4 q = __ldg(e + v);
+    const float4 w0 = __ldg(w + 2 * c), w1 = __ldg(w + 2 * c + 1);
+    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&q);
+    uint4 o;
+    __nv_bfloat16* oh = reinterpret_cast<__nv_bfloat16*>(&o);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      oh[k] = product_bf16(wv[k], __bfloat162float(h[k]));
+    ew[v] = o;
+  }
+}
+
 __global__ void fold_f32_kernel(const float* __restrict__ e, const float* __restrict__ w, int d,
                                 long long n, float* __restrict__ ew) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
@@ -115,12 +153,23 @@ moe_status_t launch_fold_centroids(int wgt_dtype, const void* e, const float* w,
   TraceScope tr(stream, "fold_centroids");
   const long long n = static_cast<long long>(E) * d;
   const int grid = static_cast<int>(std::min<long long>((n + 255) / 256, 4 * 148));
-  if (wgt_dtype == MOE_BF16)
+  const bool aligned = d % 8 == 0 && n / 8 < (1LL << 31) &&
+                       reinterpret_cast<uintptr_t>(e) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(w) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(ew) % 16 == 0;
+  if (wgt_dtype == MOE_BF16 && aligned) {
+    const int nvec = static_cast<int>(n / 8);
+    const int g8 = std::min((nvec + 255) / 256, 8 * 148);
+    fold_bf16_x8_kernel<<<g8, 256, 0, stream>>>(static_cast<const uint4*>(e),
+                                                reinterpret_cast<const float4*>(w), d / 8, nvec,
+                                                static_cast<uint4*>(ew));
+  } else if (wgt_dtype == MOE_BF16) {
     fold_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(e), w, d, n,
                                                static_cast<__nv_bfloat16*>(ew));
-  else
+  } else {
     fold_f32_kernel<<<grid, 256, 0, stream>>>(static_cast<const float*>(e), w, d, n,
                                               static_cast<float*>(ew));
+  }
   return launch_status();
 }
 
