@@ -65,6 +65,49 @@ __global__ void __launch_bounds__(128) combine_bf16_kernel(
   }
 }
 
+// The same for K <= KMAX: every routed row's index and gate is read first and
+// every row load is issued before the first sum, so a thread has up to
+// K + S + 1 loads in flight instead of one; the sums run in the same order.
+template <int KMAX>
+__global__ void __launch_bounds__(128) combine_bf16_unrolled_kernel(
+    const uint4* __restrict__ y, const float* __restrict__ gates, const int32_t* __restrict__ pos,
+    const uint4* __restrict__ x, uint4* __restrict__ out, int T, int K, int S, int vpr,
+    long long shared0, long long shared_stride, int add_residual) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= vpr) return;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    int r[KMAX];
+    float g[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      r[k] = k < K ? __ldg(pos + static_cast<size_t>(t) * K + k) : -1;
+      g[k] = k < K ? __ldg(gates + static_cast<size_t>(t) * K + k) : 0.f;
+    }
+    uint4 yv[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (r[k] >= 0) yv[k] = __ldg(y + static_cast<size_t>(r[k]) * vpr + v);   // r < 0: rejected
+    uint4 sv = make_uint4(0, 0, 0, 0), xv = make_uint4(0, 0, 0, 0);
+    if (S > 0) sv = __ldg(y + static_cast<size_t>(shared0 + t) * vpr + v);
+    if (add_residual) xv = __ldg(x + static_cast<size_t>(t) * vpr + v);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (r[k] >= 0) bf16x8_fma(acc, yv[k], g[k]);
+    if (S > 0) bf16x8_add(acc, sv);
+    for (int s = 1; s < S; ++s)
+      bf16x8_add(acc, __ldg(y + static_cast<size_t>(shared0 + s * shared_stride + t) * vpr + v));
+    if (add_residual) bf16x8_add(acc, xv);
+    uint4 o;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    out[static_cast<size_t>(t) * vpr + v] = o;
+  }
+}
+
 __global__ void __launch_bounds__(128) combine_f32_kernel(
     const float* __restrict__ y, const float* __restrict__ gates, const int32_t* __restrict__ pos,
     const float* __restrict__ x, float* __restrict__ out, int T, int K, int S, int d,
@@ -135,9 +178,14 @@ moe_status_t launch_combine(int act_dtype, const void* y, const float* gates, co
   if (act_dtype == MOE_BF16) {
     const int vpr = d / 8;
     dim3 grid(ceil_div(vpr, 128), T < 65535 ? T : 65535);
-    combine_bf16_kernel<<<grid, 128, 0, stream>>>(
-        static_cast<const uint4*>(y), gates, pos, static_cast<const uint4*>(x),
-        static_cast<uint4*>(out), T, K, S, vpr, shared0, shared_stride, add_residual);
+    if (K <= 8)
+      combine_bf16_unrolled_kernel<8><<<grid, 128, 0, stream>>>(
+          static_cast<const uint4*>(y), gates, pos, static_cast<const uint4*>(x),
+          static_cast<uint4*>(out), T, K, S, vpr, shared0, shared_stride, add_residual);
+    else
+      combine_bf16_kernel<<<grid, 128, 0, stream>>>(
+          static_cast<const uint4*>(y), gates, pos, static_cast<const uint4*>(x),
+          static_cast<uint4*>(out), T, K, S, vpr, shared0, shared_stride, add_residual);
   } else {
     dim3 grid(ceil_div(d, 128), T < 65535 ? T : 65535);
     combine_f32_kernel<<<grid, 128, 0, stream>>>(static_cast<const float*>(y), gates, pos,

@@ -165,10 +165,25 @@ __global__ void __launch_bounds__(256) scatter_kernel(const V* __restrict__ x, i
     const int t = t0 + tl;
     if (t >= T) break;
     const V* src = x + static_cast<size_t>(t) * vpr;
-    for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
-      const V val = __ldg(src + v);
+    // up to four of the row's vectors in flight per thread before the stores
+    constexpr int kIn = 4;
+    V val[kIn];
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int v = threadIdx.x + j * blockDim.x;
+      if (v < vpr) val[j] = __ldg(src + v);
+    }
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int v = threadIdx.x + j * blockDim.x;
+      if (v < vpr)
+        for (int k = 0; k < K; ++k)
+          if (dst[tl][k] >= 0) xp[static_cast<size_t>(dst[tl][k]) * vpr + v] = val[j];
+    }
+    for (int v = threadIdx.x + kIn * blockDim.x; v < vpr; v += blockDim.x) {
+      const V vv = __ldg(src + v);
       for (int k = 0; k < K; ++k)
-        if (dst[tl][k] >= 0) xp[static_cast<size_t>(dst[tl][k]) * vpr + v] = val;
+        if (dst[tl][k] >= 0) xp[static_cast<size_t>(dst[tl][k]) * vpr + v] = vv;
     }
   }
 }
