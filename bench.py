@@ -759,7 +759,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="v3_prefill")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=8,
+    ap.add_argument("--cpu-tokens", type=int, default=24,
                     help="tokens of the oracle CPU-baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=1,
                     help="tokens per step of the reference (oracle) arm")
