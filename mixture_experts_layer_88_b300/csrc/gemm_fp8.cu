@@ -10,14 +10,14 @@
 //   P_kb[w, t] = sum_{k in block kb} qA[w, k] * qB[t, k]     (e4m3 x e4m3, fp32)
 // P_kb comes from the tensor cores into a fresh TMEM buffer; the promotion
 // warps read it, scale it and add it into fp32 running sums held in
-// registers.  Four TMEM buffers rotate, so the MMAs run up to three K blocks
-// ahead of the promotion.
+// registers.  Two TMEM buffers alternate, so the MMAs of block kb + 1 run
+// while block kb is promoted.
 //
 // Layout is swap-AB as in the bf16 kernel (weights in the MMA's M slot, tokens
 // in N), and a tile runs on a CTA pair (a cluster of two CTAs): one MMA of
 // M = 256 weight rows spans both CTAs, each CTA holding 128 rows of A and of
 // the partial sums and half of the tile's token rows.  One tile = group g,
-// weight-row block mb, one token block of N <= 128 tokens:
+// weight-row block mb, one token block of N <= 192 tokens:
 //   GATEUP: the pair covers intermediate columns c = 128 mb .. c + 127; CTA r
 //           holds gate rows c + 64 r .. +63 of W13_g in TMEM lanes 0..63 and
 //           the matching up rows (+I) in lanes 64..127, so SwiGLU pairs lane l
@@ -28,22 +28,24 @@
 //   DOWN:   the pair covers rows m = 256 mb .. of W2_g; CTA r holds rows
 //           m + 128 r .. +127; the tile ends with y in bf16
 // Per 128-wide K block the even CTA issues four MMAs (K = 32 each, M = 256,
-// N = tokens) into partial buffer b = block % 4 (TMEM columns 128 b ..).  Per
-// CTA that is 24 KB of operands for 4.2 MFLOP at N = 128, and 128 x 128 fp32
-// running sums: 64 per thread of the eight promotion warps.
+// N = tokens) into partial buffer b = block % 2 (TMEM columns 192 b ..).  Per
+// CTA that is 28 KB of operands for 6.3 MFLOP at N = 192, and 128 x 192 fp32
+// running sums: 64 per thread of the twelve promotion warps (a CTA of 14 warps
+// lets a thread hold 128 registers).
 //
 // Activation scales sit K-block-major ([K/128][rows], fp32), so the scales of
 // a tile's tokens for block kb are one contiguous run that TMA brings in.
 // Group rows start on multiples of 4 (16 bytes of scales).
 //
-// Warp roles (320 threads per CTA, one CTA per SM):
-//   warp 0      TMA producer: per K block this CTA's 128 weight rows (GATEUP:
-//               two 64-row boxes) and its half of the token rows (bytes
-//               counted on the even CTA's "full" barrier), and the scales of
-//               all the tile's tokens into an 8-slot ring of this CTA
-//   warp 1      TMEM owner; in the even CTA also the MMA issuer
-//   warps 2..9  promotion + epilogue: warp w reads TMEM lanes 32 (w % 4)..
-//               and token columns [64 h, 64 h + 64), h = (w - 2) / 4
+// Warp roles (448 threads per CTA, one CTA per SM):
+//   warp 0       TMA producer (one thread): per K block this CTA's 128 weight
+//                rows (GATEUP: two 64-row boxes) and its half of the token
+//                rows (bytes counted on the even CTA's "full" barrier), and
+//                the scales of all the tile's tokens into an 8-slot ring of
+//                this CTA
+//   warp 1       TMEM owner; in the even CTA also the MMA issuer (one thread)
+//   warps 2..13  promotion + epilogue: warp w reads TMEM lanes 32 (w % 4)..
+//                and token columns [64 h, 64 h + 64), h = (w - 2) / 4
 // Every barrier wait is bounded (abort flag, device error word), as in the
 // bf16 kernel.
 #include <cudaTypedefs.h>
