@@ -881,8 +881,9 @@ def main():
                    "parallelism": (f"data parallel x{ws}, load counts all-reduced for the "
                                    f"bias update" if ws > 1 else "one replica"),
                    "launch": "CUDA graph replay" if args.graph else "eager stream launches",
-                   "l2": "inputs larger than L2: 22.6 GB of expert weights streamed per step"
-                         if cfg.name.startswith("v3") else "inputs larger than L2"},
+                   "l2": (f"inputs larger than L2: "
+                          f"{(cfg.E + cfg.S) * 3 * cfg.I * cfg.d * {'e4m3': 1, 'bf16': 2}.get(cfg.wgt, 4) / 1e9:.1f} GB "
+                          f"of expert weights streamed per step")},
         "grouped_gemm": {"tflops": round(gemm_tflops, 1) if gemm_tflops else None,
                          "frac_of_peak": round(gemm_tflops / gemm_peak, 4)
                          if gemm_tflops else None,
