@@ -56,14 +56,15 @@ class ClockSampler:
     its own samples.  Falls back to an nvidia-smi query loop (whole-run
     samples) when NVML cannot be loaded."""
 
-    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown",
-               0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap",
-               0x80: "hw_power_brake_slowdown"}
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
 
     def __init__(self, device: torch.device, period_s: float = 0.005):
         self.device = device
         self.period = period_s
-        self.samples = []          # (monotonic time, sm MHz, reasons bitmask)
+        self.samples = []          # (monotonic time, sm MHz, reasons bitmask, power W)
         self.windows = []
         self.sm_max = None
         self._stop = None
@@ -118,10 +119,13 @@ class ClockSampler:
         def loop():
             clk = ctypes.c_uint()
             rs = ctypes.c_ulonglong()
+            mw = ctypes.c_uint()
             while not self._stop.is_set():
                 if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and
                         reasons_fn(h, ctypes.byref(rs)) == 0):
-                    self.samples.append((time.monotonic(), float(clk.value), int(rs.value)))
+                    pw = (mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0
+                          else None)
+                    self.samples.append((time.monotonic(), float(clk.value), int(rs.value), pw))
                 self._stop.wait(self.period)
 
         self._thread = threading.Thread(target=loop, daemon=True)
@@ -178,10 +182,22 @@ class ClockSampler:
                     "samples": 0}
         wins = self.windows if windows is None else windows
         inside = [x for x in self.samples if any(a <= x[0] <= b for a, b in wins)]
-        reasons = sorted({n for _, _, rs in inside for bit, n in self.REASONS.items()
-                          if rs & bit})
+        known = 0
+        for bit in self.REASONS:
+            known |= bit
+        share = {}
+        for x in inside:
+            names = [n for bit, n in self.REASONS.items() if x[2] & bit]
+            if x[2] & ~known:
+                names.append(hex(x[2] & ~known))
+            for n in names:
+                share[n] = share.get(n, 0) + 1
+        power = [x[3] for x in inside if x[3] is not None]
         return {"sm_mhz": statistics.median(x[1] for x in inside) if inside else None,
-                "sm_max_mhz": self.sm_max, "reasons": reasons, "samples": len(inside),
+                "sm_max_mhz": self.sm_max, "reasons": sorted(share),
+                "reason_share": {n: round(c / len(inside), 3) for n, c in sorted(share.items())},
+                "power_w": round(statistics.median(power), 1) if power else None,
+                "samples": len(inside),
                 "source": f"NVML every {self.period * 1e3:.0f} ms inside the timed region"}
 
     def _smi_summary(self):
