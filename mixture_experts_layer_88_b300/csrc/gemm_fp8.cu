@@ -10,14 +10,14 @@
 //   P_kb[w, t] = sum_{k in block kb} qA[w, k] * qB[t, k]     (e4m3 x e4m3, fp32)
 // P_kb comes from the tensor cores into a fresh TMEM buffer; the promotion
 // warps read it, scale it and add it into fp32 running sums held in
-// registers.  Two TMEM buffers alternate, so the MMAs of block kb + 1 run
-// while block kb is promoted.
+// registers.  Three TMEM buffers rotate, so the MMAs of blocks kb + 1 and
+// kb + 2 run while block kb is promoted.
 //
 // Layout is swap-AB as in the bf16 kernel (weights in the MMA's M slot, tokens
 // in N), and a tile runs on a CTA pair (a cluster of two CTAs): one MMA of
 // M = 256 weight rows spans both CTAs, each CTA holding 128 rows of A and of
 // the partial sums and half of the tile's token rows.  One tile = group g,
-// weight-row block mb, one token block of N <= 192 tokens:
+// weight-row block mb, one token block of N <= 160 tokens:
 //   GATEUP: the pair covers intermediate columns c = 128 mb .. c + 127; CTA r
 //           holds gate rows c + 64 r .. +63 of W13_g in TMEM lanes 0..63 and
 //           the matching up rows (+I) in lanes 64..127, so SwiGLU pairs lane l
@@ -28,10 +28,10 @@
 //   DOWN:   the pair covers rows m = 256 mb .. of W2_g; CTA r holds rows
 //           m + 128 r .. +127; the tile ends with y in bf16
 // Per 128-wide K block the even CTA issues four MMAs (K = 32 each, M = 256,
-// N = tokens) into partial buffer b = block % 2 (TMEM columns 192 b ..).  Per
-// CTA that is 28 KB of operands for 6.3 MFLOP at N = 192, and 128 x 192 fp32
-// running sums: 64 per thread of the twelve promotion warps (a CTA of 14 warps
-// lets a thread hold 128 registers).
+// N = tokens) into partial buffer b = block % 3 (TMEM columns 160 b ..).  Per
+// CTA that is 26 KB of operands for 5.2 MFLOP at N = 160, and 128 x 160 fp32
+// running sums: up to 64 per thread of the twelve promotion warps (a CTA of
+// 14 warps lets a thread hold 128 registers).
 //
 // Activation scales sit K-block-major ([K/128][rows], fp32), so the scales of
 // a tile's tokens for block kb are one contiguous run that TMA brings in.
@@ -45,7 +45,7 @@
 //                this CTA
 //   warp 1       TMEM owner; in the even CTA also the MMA issuer (one thread)
 //   warps 2..13  promotion + epilogue: warp w reads TMEM lanes 32 (w % 4)..
-//                and token columns [64 h, 64 h + 64), h = (w - 2) / 4
+//                and token columns [64 h, min(64 h + 64, 160)), h = (w - 2) / 4
 // Every barrier wait is bounded (abort flag, device error word), as in the
 // bf16 kernel.
 #include <cudaTypedefs.h>
@@ -63,15 +63,15 @@ namespace {
 
 constexpr int KB = 128;                       // K elements (= bytes) per stage
 constexpr uint32_t ROW = 128;                 // bytes per operand row per stage
-constexpr int STAGES = 5;
-constexpr int MAX_N = 192;                    // tokens per tile
+constexpr int STAGES = 6;
+constexpr int MAX_N = 160;                    // tokens per tile
 constexpr uint32_t A_BYTES = 128 * ROW;       // 16 KB: this CTA's weight rows
-constexpr uint32_t STAGE_BYTES = A_BYTES + (MAX_N / 2) * ROW;   // 28 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + (MAX_N / 2) * ROW;   // 26 KB
 constexpr int EPI_WARPS = 12;
 constexpr int CW = 64;                        // token columns per promotion warp
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int PBUFS = 2;                      // partial buffers of MAX_N columns
+constexpr int PBUFS = 3;                      // partial buffers of MAX_N columns
 constexpr int SC_SLOTS = 8;
 // shared memory after the stages: the gate/up exchange, the token-scale ring,
 // per-warp premultiplied scales, the act amax exchange, barriers
@@ -82,7 +82,11 @@ constexpr uint32_t AM_OFF = PS_OFF + EPI_WARPS * CW * 4;
 constexpr uint32_t BAR_OFF = AM_OFF + 2 * 2 * 2 * MAX_N * 4;       // [2 par][2 rank][2 q][MAX_N]
 constexpr size_t SMEM_BYTES = BAR_OFF + 512 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "fp8 GEMM shared memory");
-static_assert(MAX_N == (EPI_WARPS / 4) * CW && PBUFS * MAX_N <= TMEM_COLS, "TMEM partial buffers");
+// the last column group of warps is narrow (32 columns) when MAX_N is not a
+// multiple of CW
+static_assert((EPI_WARPS / 4) * CW >= MAX_N && (EPI_WARPS / 4 - 1) * CW + 32 <= MAX_N &&
+                  MAX_N % 32 == 0 && PBUFS * MAX_N <= TMEM_COLS, "TMEM partial buffers");
+static_assert(STAGE_BYTES % 1024 == 0, "128B-swizzled stages start on 1 KB");
 constexpr int HALF_WARPS = EPI_WARPS / 2;    // GATEUP: up (or gate) warps
 
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
@@ -429,6 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;                        // TMEM lane quarter of this warp
     const int h = ew >> 2;                         // token columns [CW h, CW h + CW)
     const int c0 = h * CW;
+    const bool wide = c0 + CW <= MAX_N;            // else columns c0 .. c0 + 31 only
     const bool up = kGU && q >= 2;                 // GATEUP: lanes 64..127 hold up rows
     float* my_ps = psc + ew * CW;
     const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -470,13 +475,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (active) {
           const float* sx = sc_ring + slot * MAX_N + c0;
           my_ps[lane] = sw * sx[lane];
-          my_ps[32 + lane] = sw * sx[32 + lane];
+          if (wide) my_ps[32 + lane] = sw * sx[32 + lane];
           __syncwarp();
           // two TMEM round trips of 32 columns (the running sums take 64
           // registers, the loaded partials 32)
           const uint32_t tb = tl + pb * MAX_N + c0;
 #pragma unroll
           for (int j = 0; j < CW / 32; ++j) {
+            if (j > 0 && !wide) break;
             uint32_t p[32];
             tc::tmem_ld32(tb + 32 * j, p);
             tc::tmem_wait_ld32(p);
@@ -508,7 +514,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (tcount > 0 && !all_wait(xfree, tpar ^ 1u, abort_flag, tmo)) { ok = false; break; }
           if (active) {
 #pragma unroll
-            for (int i = 0; i < CW; ++i) xch[(c0 + i) * 64 + xr] = acc[i];
+            for (int i = 0; i < CW; ++i)
+              if (i < 32 || wide) xch[(c0 + i) * 64 + xr] = acc[i];
           }
           tc::mbar_arrive(xup);
           continue;
@@ -516,7 +523,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!all_wait(xup, tpar, abort_flag, tmo)) { ok = false; break; }
         if (active) {
 #pragma unroll
-          for (int i = 0; i < CW; ++i) acc[i] = silu_mul(acc[i], xch[(c0 + i) * 64 + xr]);
+          for (int i = 0; i < CW; ++i)
+            if (i < 32 || wide) acc[i] = silu_mul(acc[i], xch[(c0 + i) * 64 + xr]);
         }
         tc::mbar_arrive(xfree);
         // per-token max of |act| over this warp's 32 columns, to both CTAs
@@ -525,6 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           float* am = amx + ((par * 2 + static_cast<int>(rank)) * 2 + (q & 1)) * MAX_N + c0;
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {       // tokens c0 + 32 hh + lane
+            if (hh > 0 && !wide) break;
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = fabsf(acc[32 * hh + i]);
@@ -547,6 +556,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int i = 32 * u + lane;
+            if (u > 0 && !wide) { m[u] = 0.f; my_ps[i] = 0.f; break; }
             m[u] = fmaxf(fmaxf(am0[i], am0[MAX_N + i]), fmaxf(am0[2 * MAX_N + i], am0[3 * MAX_N + i]));
             my_ps[i] = m[u] > 0.f ? 448.0f / m[u] : 0.f;
           }
