@@ -417,7 +417,7 @@ moe_status_t do_experts_fp8(const moe_cfg_t& c, const void* xq, const float* xs,
   int32_t* bs = orow + (G + 1);
   int32_t* bstart = bs + (G + 1);
   const GroupLayout lay{static_cast<int>(fr.P), static_cast<int>(fr.P), static_cast<int>(fr.Tp),
-                        160};   // token blocks of the FP8 GEMMs: at most 160 tokens
+                        kFp8TileTokens};
   moe_status_t s = launch_build_groups(offsets, counts, c.T, c.E, c.S, lay, rows, brow, orow, bs,
                                        bstart, st);
   if (s != MOE_OK) return s;

@@ -64,7 +64,7 @@ namespace {
 constexpr int KB = 128;                       // K elements (= bytes) per stage
 constexpr uint32_t ROW = 128;                 // bytes per operand row per stage
 constexpr int STAGES = 6;
-constexpr int MAX_N = 160;                    // tokens per tile
+constexpr int MAX_N = kFp8TileTokens;         // tokens per tile
 constexpr uint32_t A_BYTES = 128 * ROW;       // 16 KB: this CTA's weight rows
 constexpr uint32_t STAGE_BYTES = A_BYTES + (MAX_N / 2) * ROW;   // 26 KB
 constexpr int EPI_WARPS = 12;
@@ -474,8 +474,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!warp_wait(sfull + slot, sph, abort_flag, tmo)) { ok = false; break; }
         if (active) {
           const float* sx = sc_ring + slot * MAX_N + c0;
-          my_ps[lane] = sw * sx[lane];
-          if (wide) my_ps[32 + lane] = sw * sx[32 + lane];
+#pragma unroll
+          for (int j = 0; j < CW / 32; ++j)
+            if (j == 0 || wide) my_ps[32 * j + lane] = sw * sx[32 * j + lane];
           __syncwarp();
           // two TMEM round trips of 32 columns (the running sums take 64
           // registers, the loaded partials 32)
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (active) {
           float* am = amx + ((par * 2 + static_cast<int>(rank)) * 2 + (q & 1)) * MAX_N + c0;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {       // tokens c0 + 32 hh + lane
+          for (int hh = 0; hh < CW / 32; ++hh) {   // tokens c0 + 32 hh + lane
             if (hh > 0 && !wide) break;
             float v[32];
 #pragma unroll
@@ -552,9 +553,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (active && valid) {
           // 1 / scale of tokens c0 + lane, c0 + 32 + lane (max over both CTAs' 64 columns)
           const float* am0 = amx + par * 4 * MAX_N + c0;
-          float m[2];
+          float m[CW / 32];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
+          for (int u = 0; u < CW / 32; ++u) {
             const int i = 32 * u + lane;
             if (u > 0 && !wide) { m[u] = 0.f; my_ps[i] = 0.f; break; }
             m[u] = fmaxf(fmaxf(am0[i], am0[MAX_N + i]), fmaxf(am0[2 * MAX_N + i], am0[3 * MAX_N + i]));
@@ -573,7 +574,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           // scale of each token for K block mb of the down GEMM: even CTA, q = 0
           if (rank == 0 && q == 0) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < CW / 32; ++u)
               if (32 * u + lane < nval)
                 args.out_scale[static_cast<size_t>(t.mb) * args.out_scale_ld + orow0 + 32 * u + lane] =
                     m[u] / 448.0f;

@@ -7,6 +7,10 @@
 
 namespace moe {
 
+// Largest token block of one FP8 tile: the group table is built with blocks of
+// at most this many tokens.
+constexpr int kFp8TileTokens = 160;
+
 struct Fp8GemmMaps {
   CUtensorMap a[2];               // e4m3 weights: routed (0) / shared (1), boxes of 64 (GATEUP) or 128 rows
   CUtensorMap b[2][kTokBoxes];    // e4m3 token rows, boxes of 8 << i rows (both entries alike)
