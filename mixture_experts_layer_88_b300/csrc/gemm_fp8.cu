@@ -163,12 +163,29 @@ __device__ __forceinline__ bool test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-#ifndef FP8_WAIT_SLEEP_NS
-#define FP8_WAIT_SLEEP_NS 0
-#endif
+// Bounded wait of one thread (the TMA producer or the MMA issuer): try_wait,
+// which may suspend the thread until the phase completes; the abort flag and
+// the wall clock are checked every 16 polls.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long timeout_ns) {
+  if (test_wait<CLUSTER>(bar, parity)) return true;
+  const unsigned long long deadline = tc::globaltimer_ns() + timeout_ns;
+  uint32_t polls = 0;
+  while (!(CLUSTER ? tc::mbar_try_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity))) {
+    if ((++polls & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (tc::globaltimer_ns() > deadline) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
 
-// Bounded wait of one thread: polls with test_wait (sleeping FP8_WAIT_SLEEP_NS
-// between polls) and checks the abort flag and the wall clock every 64 polls.
+// Bounded wait of one lane of a promotion warp: polls with test_wait and
+// checks the abort flag and the wall clock every 64 polls.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag,
@@ -177,7 +194,6 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
   const unsigned long long deadline = tc::globaltimer_ns() + timeout_ns;
   uint32_t polls = 0;
   while (!test_wait<CLUSTER>(bar, parity)) {
-    if (FP8_WAIT_SLEEP_NS > 0) __nanosleep(FP8_WAIT_SLEEP_NS);
     if ((++polls & 63u) == 0) {
       if (*abort_flag) return false;
       if (tc::globaltimer_ns() > deadline) {
@@ -351,8 +367,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t phase = (kc / STAGES) & 1u;
           const int slot = kc % SC_SLOTS;
           const uint32_t sph = (kc / SC_SLOTS) & 1u;
-          if (!wait_bounded(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
-          if (!wait_bounded(sempty + slot, sph ^ 1u, abort_flag, tmo)) { ok = false; break; }
+          if (!role_wait(empty + stage, phase ^ 1u, abort_flag, tmo)) { ok = false; break; }
+          if (!role_wait(sempty + slot, sph ^ 1u, abort_flag, tmo)) { ok = false; break; }
           // Only the even CTA arrives, expecting both CTAs' bytes; the odd
           // CTA's loads count on it (a stage is reused only after the MMAs
           // that read it completed, so the bytes land in their own phase).
@@ -405,8 +421,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t phase = (kc / STAGES) & 1u;
           const int pb = kc % PBUFS;
           const uint32_t puse = (kc / PBUFS) & 1u;
-          if (!wait_bounded<true>(pempty + pb, puse ^ 1u, abort_flag, tmo)) { ok = false; break; }
-          if (!wait_bounded(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
+          if (!role_wait<true>(pempty + pb, puse ^ 1u, abort_flag, tmo)) { ok = false; break; }
+          if (!role_wait(full + stage, phase, abort_flag, tmo)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t d = tmem_base + pb * MAX_N;
