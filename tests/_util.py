@@ -114,6 +114,20 @@ def with_gpu_choice(ref, idx_g, keep, rerun):
     return out
 
 
+def idx_with_counts(counts, K, seed=0):
+    """A routing [T, K] (T = sum(counts) / K) in which expert e is chosen by
+    exactly counts[e] tokens, each token's K experts distinct (every count
+    must stay below T), tokens in a seeded random order."""
+    counts = np.asarray(counts)
+    T = int(counts.sum()) // K
+    assert T * K == counts.sum() and counts.max() < T
+    ids = np.repeat(np.arange(len(counts)), counts)
+    idx = ids.reshape(K, T).T          # expert ids T apart: distinct per token
+    assert all(len(set(r)) == K for r in idx.tolist())
+    rng = np.random.default_rng(seed)
+    return np.ascontiguousarray(idx[rng.permutation(T)]).astype(np.int32)
+
+
 def rel_frob(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)

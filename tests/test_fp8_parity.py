@@ -15,7 +15,7 @@ import torch
 
 from moe_inputs import small_cases, get_config, make_inputs, make_tokens
 from oracle import moe_oracle as O
-from tests._util import check_near_ties, gpu_inputs, rel_frob, with_gpu_choice
+from tests._util import check_near_ties, gpu_inputs, idx_with_counts, rel_frob, with_gpu_choice
 
 pytestmark = pytest.mark.gpu
 
@@ -253,6 +253,28 @@ def test_fp8_bias_update_steps_skewed():
         if hot is None:
             hot = int(np.argmax(counts))
     assert bias_o[hot] < 0
+
+
+def test_fp8_token_block_boundaries():
+    """Experts whose row counts sit on either side of the FP8 tiles' token
+    block (160 rows) and of the 16-row MMA step, on a routing fixed by the
+    test (K = 2) with the oracle's gates for it: dispatch -> experts ->
+    combine against the oracle's layer."""
+    counts = np.array([2, 16, 17, 159, 160, 161, 320, 321])
+    idx = idx_with_counts(counts, 2, seed=5)
+    cfg = small_cases()["ragged_fp8"].with_(name="fp8_blocks", T=len(idx), E=len(counts), K=2)
+    g, c = gpu_inputs(cfg)
+    ref = _oracle(cfg, c, idx=idx)
+    run = Fp8Run(cfg, g)
+    run.dispatch(torch.as_tensor(idx, device="cuda"))
+    run.gates.copy_(torch.as_tensor(ref["gates"], dtype=torch.float32))
+    run.experts()
+    run.combine()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    np.testing.assert_array_equal(run.counts.cpu().numpy(), counts)
+    got = run.out.double().cpu().numpy()
+    assert rel_frob(got, ref["delta"]) <= FP8_TOL
 
 
 FP8_EDGE = {

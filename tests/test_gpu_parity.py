@@ -16,6 +16,7 @@ import torch
 from moe_inputs import small_cases, get_config, make_inputs
 from oracle import moe_oracle as O
 from tests._util import (GpuRun, gpu_inputs, assert_close, to_np, GATE_ATOL, MARGIN_EXCLUDE,
+                         idx_with_counts,
                          rel_frob, check_near_ties, with_gpu_choice)
 
 pytestmark = pytest.mark.gpu
@@ -192,6 +193,36 @@ def test_expert_outputs_rowwise(name):
     for s in range(cfg.S):
         want[TK + s * cfg.T: TK + (s + 1) * cfg.T] = O.swiglu_ffn(u, c["ws13"][s], c["ws2"][s])
     assert_close(y, want, cfg.act, f"{name} expert rows")
+
+
+# ---------------------------------------------------------------- token-block boundaries
+
+# expert row counts on either side of the 16-row MMA step and of the token
+# blocks: 256 rows for batches above 512 tokens, 64 below
+BLOCK_COUNTS = {
+    "blocks_256": [2, 16, 17, 255, 256, 257, 512, 513],
+    "blocks_64": [2, 16, 17, 63, 64, 65, 128, 129],
+}
+
+
+@pytest.mark.parametrize("case", list(BLOCK_COUNTS))
+def test_expert_token_block_boundaries(case):
+    """Experts and combine on a routing fixed by the test (K = 2, every
+    expert's row count chosen) with the oracle's gates for it."""
+    counts = np.array(BLOCK_COUNTS[case])
+    idx = idx_with_counts(counts, 2, seed=5)
+    cfg = small_cases()["ragged_bf16"].with_(name=case, T=len(idx), E=len(counts), K=2)
+    assert (cfg.T > 512) == (case == "blocks_256")
+    g, c = gpu_inputs(cfg)
+    run = GpuRun(m, cfg, g, add_residual=0)
+    ref = _layer(cfg, c, add_residual=0, idx=idx)
+    run.dispatch(torch.as_tensor(idx, device="cuda"))
+    run.experts()
+    run.combine(gates=torch.as_tensor(ref["gates"], dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    np.testing.assert_array_equal(to_np(run.counts), counts)
+    assert_close(to_np(run.out), ref["delta"], cfg.act, f"{case} delta")
 
 
 # ---------------------------------------------------------------- whole layer
