@@ -20,7 +20,8 @@ import torch
 
 from moe_inputs import get_config, make_dout, make_inputs, small_cases
 from oracle import moe_oracle as O
-from tests._util import check_near_ties, gpu_inputs, rel_frob, to_np, with_gpu_choice
+from tests._util import (check_near_ties, gpu_inputs, idx_with_counts, rel_frob, to_np,
+                         with_gpu_choice)
 
 pytestmark = pytest.mark.gpu
 
@@ -244,6 +245,33 @@ def test_backward_hot_expert_long_k():
     run, dout = _run(cfg, g)
     assert int(run.state["counts"][5].item()) == cfg.T
     _check_against_oracle(cfg, run, c, dout, "hot expert")
+
+
+def test_backward_token_block_boundaries():
+    """Experts chosen by 1, 63, 64, 65, 383, 384, 385 and 449 tokens: either
+    side of the 64-token K step of the weight gradients and of the 384 tokens
+    of A they keep in shared memory.  The router is steered through its
+    inputs: token t carries +8 on feature e for each of its two experts e and
+    centroid e is 1 on feature e and 0 on the other first E features, so the
+    chosen logits sit about 8 above the rest (whose random part has a
+    standard deviation of about 0.6)."""
+    counts = np.array([1, 63, 64, 65, 383, 384, 385, 449])
+    idx = idx_with_counts(counts, 2, seed=3)
+    cfg = small_cases()["ragged_bf16"].with_(name="bwd_blocks", T=len(idx), E=len(counts), K=2)
+    E = cfg.E
+    _, c = gpu_inputs(cfg)
+    x = c["x"].clone()
+    x[:, :E] = 0
+    x[torch.arange(cfg.T).repeat_interleave(2), torch.as_tensor(idx.reshape(-1)).long()] = 8.0
+    cen = c["centroids"].clone()
+    cen[:, :E] = 0
+    cen[torch.arange(E), torch.arange(E)] = 1.0
+    c = dict(c, x=x, centroids=cen)
+    g = {k: v.cuda() for k, v in c.items()}
+    run, dout = _run(cfg, g)
+    np.testing.assert_array_equal(np.sort(run.state["idx"].cpu().numpy(), 1), np.sort(idx, 1))
+    np.testing.assert_array_equal(run.state["counts"].cpu().numpy(), counts)
+    _check_against_oracle(cfg, run, c, dout, "block boundaries")
 
 
 def test_backward_empty_batch_zeroes_gradients():
