@@ -761,6 +761,36 @@ def fp8_record(m, device, peaks, clk, steps, warmup, balance_steps):
     return rec
 
 
+def dsmoe16b_record(m, device, peaks, clk, steps, warmup):
+    """The 16B-shape layer (T = 32768, d = 2048, 64 routed experts top-6 with
+    Softmax scores and no renormalisation, 2 shared experts, I = 1408): ms per
+    step, tokens/s and the bf16 expert GEMMs' TFLOP/s against the measured
+    bf16 peaks."""
+    cfg = get_config("dsmoe16b")
+    inp = make_inputs(cfg, device)
+    layer = m.MoeLayer(m.cfg_from_layer(cfg), inp, device=device)
+    x = inp["x"]
+    out = torch.empty_like(x)
+    n0 = len(clk.windows)
+    ms, traces, st = time_layer(m, layer, x, out, steps, warmup, clk)
+    names = ("gemm_gateup_swiglu", "gemm_down")
+    gemm_ms = sum(t[2] for t in traces if t[0] in names) / steps
+    tf = cfg.gemm_flops() / (gemm_ms / 1e3) / 1e12
+    rec = {"workload": cfg.name, "T": cfg.T, "steps": steps, "warmup": warmup,
+           "ms_per_step": round(ms, 4), "tokens_per_s": round(cfg.T / (ms / 1e3), 1),
+           "grouped_gemm": {"tflops": round(tf, 1), "peak_tflops": peaks["bf16_tflops"],
+                            "frac": round(tf / peaks["bf16_tflops"], 4),
+                            "peak_kind": f"bf16 burst, {peaks['source']}",
+                            "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                            "ms_per_step": round(gemm_ms, 4), "kernels": list(names)},
+           "kernels": kernel_roofline(cfg, traces, peaks),
+           "gpu_launches": sum(t[1] for t in traces), "device_status": st,
+           "clocks": clk.summary(clk.windows[n0:])}
+    del layer, inp
+    torch.cuda.empty_cache()
+    return rec
+
+
 def _workload(cfg, args) -> str:
     w = cfg.name + ("+rmsnorm" if args.prenorm else "")
     if cfg.wgt == "e4m3":
@@ -792,7 +822,7 @@ def main():
     ap.add_argument("--train", action="store_true",
                     help="training step: forward with saved state + backward + bias update")
     ap.add_argument("--no-subconfigs", action="store_true",
-                    help="skip the decode and FP8 sub-records of the default V3 prefill run")
+                    help="skip the decode, FP8 and 16B-shape sub-records of the default V3 prefill run")
     ap.add_argument("--sub-steps", type=int, default=20,
                     help="timed steps of each sub-record")
     ap.add_argument("--override", default="",
@@ -961,6 +991,8 @@ def main():
         torch.cuda.empty_cache()
         line["subconfigs"]["v3_skewed_fp8"] = fp8_record(m, device, peaks, clk, args.sub_steps,
                                                          args.warmup, args.balance_steps)
+        line["subconfigs"]["dsmoe16b"] = dsmoe16b_record(m, device, peaks, clk, args.sub_steps,
+                                                         args.warmup)
     clk.__exit__(None, None, None)
     print(json.dumps(line), flush=True)
     if dist is not None:
