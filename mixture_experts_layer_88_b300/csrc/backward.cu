@@ -96,20 +96,22 @@ __device__ __forceinline__ float sigmoidf(float z) { return 1.0f / (1.0f + expf(
 // ---------------------------------------------------------------- training forward
 
 // act = SiLU(gate) * up from the stored pre-activations h = [gate | up].
+// Rows are taken block by block (no per-element division); SiLU(g) * u uses
+// the fast exponential and division, as the inference epilogue does.
 __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const uint4* __restrict__ h,
                                                          uint4* __restrict__ act, long long rows,
                                                          int vI) {
-  const long long n = rows * vI;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = i / vI;
-    const int v = static_cast<int>(i - r * vI);
-    float g[8], u[8], a[8];
-    unpack8(__ldg(h + r * 2 * vI + v), g);
-    unpack8(__ldg(h + r * 2 * vI + vI + v), u);
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint4* hr = h + r * 2 * vI;
+    uint4* ar = act + r * vI;
+    for (int v = threadIdx.x; v < vI; v += blockDim.x) {
+      float g[8], u[8], a[8];
+      unpack8(__ldg(hr + v), g);
+      unpack8(__ldg(hr + vI + v), u);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) a[j] = g[j] * sigmoidf(g[j]) * u[j];
-    act[r * vI + v] = pack8(a);
+      for (int j = 0; j < 8; ++j) a[j] = __fdividef(g[j] * u[j], 1.0f + __expf(-g[j]));
+      ar[v] = pack8(a);
+    }
   }
 }
 
@@ -455,8 +457,7 @@ moe_status_t launch_swiglu_fwd(const void* h, void* act, long long rows, int I,
                                cudaStream_t stream) {
   if (rows <= 0) return MOE_OK;
   TraceScope tr(stream, "swiglu_fwd");
-  const long long n = rows * (I / 8);
-  const int grid = static_cast<int>(n < 148LL * 16 * 256 ? (n + 255) / 256 : 148LL * 16);
+  const int grid = static_cast<int>(rows < 148LL * 8 ? rows : 148LL * 8);
   swiglu_fwd_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(h),
                                               static_cast<uint4*>(act), rows, I / 8);
   return launch_status();
