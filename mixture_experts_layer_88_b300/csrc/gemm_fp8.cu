@@ -485,8 +485,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t sph = (kc / SC_SLOTS) & 1u;
         if (!warp_wait(pfull + pb, puse, abort_flag, tmo)) { ok = false; break; }
         tc::tc_fence_after();
-        // all 64 columns in one TMEM round trip; the buffer is released as
-        // soon as the loads complete, before the arithmetic
         if (!warp_wait(sfull + slot, sph, abort_flag, tmo)) { ok = false; break; }
         if (active) {
           const float* sx = sc_ring + slot * MAX_N + c0;
