@@ -18,7 +18,8 @@ import torch
 
 from moe_inputs import small_cases, get_config, make_inputs
 from oracle import moe_oracle as O
-from tests._util import check_near_ties, gpu_inputs, assert_close, to_np, with_gpu_choice
+from tests._util import (check_near_ties, gpu_inputs, assert_close, idx_with_counts, to_np,
+                         with_gpu_choice)
 
 pytestmark = pytest.mark.gpu
 
@@ -233,3 +234,26 @@ def test_w8a16_v3_skewed_full_size_sampled():
                        run.gates.cpu().numpy()[tok], tokens=tok)
     got = to_np(run.out[torch.as_tensor(tok, device="cuda")])
     assert_close(got, ref["delta"], "bf16", "C3 W8A16 sampled tokens")
+
+
+def test_w8a16_token_block_boundaries():
+    """Experts whose row counts sit on either side of the W8A16 tiles' token
+    block (192 rows) and of the 16-row MMA step, on a routing fixed by the
+    test (K = 2) with the oracle's gates for it: dispatch -> experts -> combine
+    against the oracle's layer."""
+    counts = np.array([2, 16, 17, 191, 192, 193, 384, 385])
+    idx = idx_with_counts(counts, 2, seed=5)
+    cfg = small_cases()["ragged_fp8"].with_(name="w8_blocks", T=len(idx), E=len(counts), K=2)
+    g, c = gpu_inputs(cfg)
+    ref = _oracle(cfg, c, idx=idx)
+    run = W8Run(cfg, g)
+    m.dispatch(run.c16, g["x"], torch.as_tensor(idx, device="cuda"), run.counts, run.offsets,
+               run.xp, run.perm, run.pos, run.ws[m.MOE_WS_DISPATCH])
+    m.experts_w8a16(run.cfg, run.xp, g["x"], run.offsets, run.w, run.act, run.y,
+                    run.ws[m.MOE_WS_EXPERTS])
+    gates = torch.as_tensor(ref["gates"], dtype=torch.float32, device="cuda")
+    m.combine(run.c16, run.y, gates, run.pos, g["x"], run.out)
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    np.testing.assert_array_equal(run.counts.cpu().numpy(), counts)
+    assert_close(to_np(run.out), ref["delta"], cfg.act, "w8a16 block boundaries")
