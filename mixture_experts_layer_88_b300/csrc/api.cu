@@ -505,7 +505,7 @@ BackwardLayout backward_layout(const moe_cfg_t& c) {
   L.dl = take(sm ? static_cast<size_t>(c.T) * c.E * sizeof(float) : 0);
   L.dxr = take(sm ? static_cast<size_t>(c.T) * c.d * sizeof(float) : 0);
   L.part = take((sm ? static_cast<size_t>(ceil_div(c.T, 256)) * c.E
-                    : static_cast<size_t>(L.max_blocks)) *
+                    : static_cast<size_t>(L.max_blocks) * kDcentSub) *
                 c.d * sizeof(float));
   const size_t R = static_cast<size_t>(L.rows_max);
   L.dy = take(R * c.d * 2);

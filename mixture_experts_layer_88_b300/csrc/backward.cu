@@ -357,8 +357,12 @@ __global__ void __launch_bounds__(128) dx_kernel(
 
 // ---------------------------------------------------------------- centroid gradients
 
-// Sigmoid: partial[b] = sum over the rows r of token block b (the input-
-// gradient GEMMs' routed blocks, <= 256 rows of one expert) of dlrow[r] xp[r].
+// Sigmoid: partial[q] = sum over the rows r of chunk q of dlrow[r] xp[r], where
+// chunk q = b * kDcentSub + s holds rows [64 s, 64 s + 64) of token block b
+// (the input-gradient GEMMs' routed blocks, <= 256 rows of one expert; the
+// last chunk takes any rows past 64 kDcentSub).  Chunks without rows write
+// zeros.
+constexpr int kDcentChunkRows = 64;
 __global__ void __launch_bounds__(128) dcent_sparse_partial_kernel(
     const float* __restrict__ dlrow, const uint4* __restrict__ xp,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
@@ -366,32 +370,36 @@ __global__ void __launch_bounds__(128) dcent_sparse_partial_kernel(
     float* __restrict__ part) {
   const int v = blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= vpr) return;
-  for (int b = blockIdx.y; b < __ldg(bstart + E); b += gridDim.y) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(bstart + mid) <= b) lo = mid; else hi = mid - 1;
-  }
-  const int lb = b - __ldg(bstart + lo);
-  const int sz = __ldg(bs + lo);
-  const int r0 = __ldg(offsets + lo) + lb * sz;
-  const int n = min(sz, __ldg(counts + lo) - lb * sz);
-  float acc[8], f[8];
+  const int nq = __ldg(bstart + E) * kDcentSub;
+  for (int q = blockIdx.y; q < nq; q += gridDim.y) {
+    const int b = q / kDcentSub, s = q - b * kDcentSub;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(bstart + mid) <= b) lo = mid; else hi = mid - 1;
+    }
+    const int lb = b - __ldg(bstart + lo);
+    const int sz = __ldg(bs + lo);
+    const int nrows = min(sz, __ldg(counts + lo) - lb * sz);   // rows of block b
+    const int s0 = s * kDcentChunkRows;
+    const int n = s == kDcentSub - 1 ? nrows - s0 : min(kDcentChunkRows, nrows - s0);
+    const int r0 = __ldg(offsets + lo) + lb * sz + s0;
+    float acc[8], f[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-  for (int i = 0; i < n; ++i) {
-    const float w = __ldg(dlrow + r0 + i);
-    unpack8(__ldg(xp + static_cast<size_t>(r0 + i) * vpr + v), f);
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int i = 0; i < n; ++i) {
+      const float w = __ldg(dlrow + r0 + i);
+      unpack8(__ldg(xp + static_cast<size_t>(r0 + i) * vpr + v), f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
-  }
-  float4* o = reinterpret_cast<float4*>(part + static_cast<size_t>(b) * vpr * 8) + 2 * v;
-  o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
+    }
+    float4* o = reinterpret_cast<float4*>(part + static_cast<size_t>(q) * vpr * 8) + 2 * v;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
-// dC[e] = sum of the partials of expert e's blocks, in block order.
+// dC[e] = sum of the partials of expert e's chunks, in block and chunk order.
 __global__ void __launch_bounds__(128) dcent_sparse_reduce_kernel(const float* __restrict__ part,
                                                                   const int32_t* __restrict__ bstart,
                                                                   int d, float* __restrict__ dc) {
@@ -399,8 +407,8 @@ __global__ void __launch_bounds__(128) dcent_sparse_reduce_kernel(const float* _
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= d) return;
   float acc = 0.f;
-  for (int b = __ldg(bstart + e); b < __ldg(bstart + e + 1); ++b)
-    acc += __ldg(part + static_cast<size_t>(b) * d + c);
+  for (int q = __ldg(bstart + e) * kDcentSub; q < __ldg(bstart + e + 1) * kDcentSub; ++q)
+    acc += __ldg(part + static_cast<size_t>(q) * d + c);
   dc[static_cast<size_t>(e) * d + c] = acc;
 }
 
@@ -523,7 +531,7 @@ moe_status_t launch_dcent_sparse(const float* dlrow, const void* xp, const int32
                                  float* part, float* dc, cudaStream_t stream) {
   {
     TraceScope tr(stream, "dcent_partial");
-    const dim3 grid(ceil_div(d / 8, 128), grid_y(max_blocks));
+    const dim3 grid(ceil_div(d / 8, 128), grid_y(max_blocks * kDcentSub));
     dcent_sparse_partial_kernel<<<grid, 128, 0, stream>>>(dlrow, static_cast<const uint4*>(xp),
                                                           counts, offsets, bs, bstart, E, d / 8,
                                                           part);

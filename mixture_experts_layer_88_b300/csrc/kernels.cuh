@@ -108,7 +108,10 @@ moe_status_t launch_dx(const void* dxp, const int32_t* pos, const int32_t* idx,
                        const void* cent, const float* dxr, const void* dout, void* dx, int T,
                        int K, int E, int S, int d, int add_residual, cudaStream_t stream);
 // dC [E,d] fp32 = sum over expert e's rows of dlrow * xp (blocks of the
-// input-gradient group table: bs, bstart), via part [max_blocks, d]
+// input-gradient group table: bs, bstart), via part [max_blocks * kDcentSub, d]:
+// each token block is summed in kDcentSub row chunks (many small items fill the
+// GPU in several waves), and the chunks are added in block and chunk order
+constexpr int kDcentSub = 4;
 moe_status_t launch_dcent_sparse(const float* dlrow, const void* xp, const int32_t* counts,
                                  const int32_t* offsets, const int32_t* bs,
                                  const int32_t* bstart, int E, int d, int max_blocks,
