@@ -9,7 +9,7 @@ meet only in the seeded inputs of ``moe_inputs``.
 Plain, slow and written to be checked by eye against the pages:
 everything is float64 numpy, one step per equation, no blocking or fusion.
 Library primitives used as steps: matrix product (``@``), ``np.exp``,
-``np.lexsort``, ``np.bincount``, ``np.cumsum``.
+``np.lexsort``, ``np.bincount``, ``np.cumsum``, ``np.frexp``, ``np.round``.
 
 Sources (DeepSeekMoE pages):
 - "DeepSeekMoE架构解析" (V3 walk-through), section 2.1, eqs. (13)-(15): Sigmoid
@@ -266,6 +266,42 @@ def _expert_weight(inp: dict, key: str, e: int):
     return w
 
 
+def round_e4m3(v) -> np.ndarray:
+    """Nearest e4m3 value, ties to even, saturating at +-448.  The format (the
+    FP8 type of the V3 walk-through, section 4.3): 1 sign bit, 4 exponent
+    bits with bias 7, 3 mantissa bits, largest finite value 448, no
+    infinities.  A binade [2^e, 2^(e+1)) holds 8 values 2^(e-3) apart for
+    e = -6 .. 8; below 2^-6 the subnormals are 2^-9 apart.  fp64 in, fp64 out
+    (every e4m3 value is exact in fp64)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                       # a = m 2^ex, 0.5 <= m < 1
+    e = np.clip(ex - 1, -6, 8)                # binade of a (subnormals share e = -6)
+    step = np.ldexp(1.0, e - 3)
+    q = np.round(a / step) * step             # np.round: halves go to the even step
+    q = np.minimum(q, 448.0)
+    return np.copysign(q, v)
+
+
+def quantize_tiles_e4m3(v, tile: int = 128) -> np.ndarray:
+    """Online FP8 quantisation of activations (V3 walk-through, section 4.3):
+    every 1 x 128 tile along the last axis gets the fp32 scale
+    s = max|v| / 448 and its values the e4m3 codes q = e4m3(v * (448 / max|v|)),
+    so the tile's largest value lands on 448.  The page fixes no precision for
+    forming the code; it is taken in float32 (max|v|, 448 / max|v| and the
+    product each rounded once), as the CUDA kernels form it.  Returns q * s in
+    fp64 (an all-zero tile stays zero)."""
+    v32 = np.asarray(v, dtype=np.float64).astype(np.float32)
+    n, m = v32.shape
+    t = v32.reshape(n, m // tile, tile)
+    amax = np.abs(t).max(axis=2, keepdims=True)
+    safe = np.where(amax > 0, amax, np.float32(1))
+    inv = np.where(amax > 0, np.float32(448) / safe, np.float32(0)).astype(np.float32)
+    q = round_e4m3((t * inv).astype(np.float32))
+    scale = (amax / np.float32(448)).astype(np.float32)
+    return (q * scale.astype(np.float64)).reshape(n, m)
+
+
 def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
     """One expert: W2 (SiLU(Wg u) * (Wu u)); w13 [2I, d] = [Wg; Wu], w2 [d, I].
     u [n, d] fp64 -> [n, d] fp64."""
@@ -276,10 +312,25 @@ def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
     return a @ _f64(w2).T
 
 
+def swiglu_ffn_fp8(u: np.ndarray, w13, w2) -> np.ndarray:
+    """One expert of an FP8 layer as the V3 walk-through, section 4.3, runs it:
+    the expert's input rows and its SwiGLU output are quantised in 1 x 128
+    tiles (``quantize_tiles_e4m3``) before the GEMM that reads them; the
+    weights are the dequantised 128 x 128 blocks.  Products are summed in
+    fp64: the promotion to fp32 every 128 elements changes only the rounding
+    order."""
+    w13 = _f64(w13)
+    I = w13.shape[0] // 2
+    h = quantize_tiles_e4m3(u) @ w13.T
+    a = silu(h[:, :I]) * h[:, I:]
+    return quantize_tiles_e4m3(a) @ _f64(w2).T
+
+
 def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
               add_residual: int = 1, tokens=None, n_groups: int = 0,
               topk_groups: int = 0, norm_w=None, norm_eps: float = 1e-6,
-              act: str = "bf16", idx=None, wgt: str = None) -> dict:
+              act: str = "bf16", idx=None, wgt: str = None,
+              act_quant: bool = False) -> dict:
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
@@ -297,6 +348,10 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     ``idx`` [n, K], when given, replaces the router's own choice for these
     tokens (another valid top-K where keys tie within rounding); the gates
     are then those of eq. (13)/(14) for that choice and the margin is NaN.
+
+    ``act_quant`` (FP8 layers): every expert also quantises its input rows and
+    its SwiGLU output to e4m3 in 1 x 128 tiles (``swiglu_ffn_fp8``), as the
+    page's FP8 scheme does; without it the activations stay as stored.
 
     Returns out (fp64), delta = out - residual, idx, gates, margin, and the
     scores s [n, E] of every expert."""
@@ -324,13 +379,14 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     d = u.shape[1]
     delta = np.zeros((n, d))
     S = inp["ws13"].shape[0]
+    ffn = swiglu_ffn_fp8 if act_quant else swiglu_ffn
     for s in range(S):
-        delta += swiglu_ffn(u, _expert_weight(inp, "ws13", s), _expert_weight(inp, "ws2", s))
+        delta += ffn(u, _expert_weight(inp, "ws13", s), _expert_weight(inp, "ws2", s))
     routed = np.zeros((n, K, d))
     for e in np.unique(idx):
         rows, slots = np.nonzero(idx == e)
-        routed[rows, slots] = swiglu_ffn(u[rows], _expert_weight(inp, "w13", int(e)),
-                                         _expert_weight(inp, "w2", int(e)))
+        routed[rows, slots] = ffn(u[rows], _expert_weight(inp, "w13", int(e)),
+                                  _expert_weight(inp, "w2", int(e)))
     for k in range(K):
         delta += gates[:, k:k + 1] * routed[:, k]
     out = delta + resid if add_residual else delta.copy()

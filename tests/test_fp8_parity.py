@@ -75,12 +75,13 @@ class Fp8Run:
                       self.counts, self.out if out is None else out, self.ws[m.MOE_WS_FORWARD])
 
 
-def _oracle(cfg, c, tokens=None, idx=None):
+def _oracle(cfg, c, tokens=None, idx=None, act_quant=False):
     return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=0, tokens=tokens,
-                       n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, idx=idx)
+                       n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, idx=idx,
+                       act_quant=act_quant)
 
 
-def _checked_ref(cfg, c, ref, idx_g, gates_g, tokens=None):
+def _checked_ref(cfg, c, ref, idx_g, gates_g, tokens=None, act_quant=False):
     """Routing of the oracle's tokens (ref's rows) against the GPU's: chosen
     sets bit-exact where the K-th vs (K+1)-th margin is >= 1e-5, a valid top-K
     within 1e-5 (and its gates) elsewhere; returns ref with the near-tie rows
@@ -94,7 +95,8 @@ def _checked_ref(cfg, c, ref, idx_g, gates_g, tokens=None):
     np.testing.assert_array_equal(np.sort(idx_g, 1)[keep], np.sort(ref["idx"], 1)[keep])
     tok = np.arange(len(keep)) if tokens is None else np.asarray(tokens)
     return with_gpu_choice(ref, idx_g, keep,
-                           lambda rows, ix: _oracle(cfg, c, tokens=tok[rows], idx=ix))
+                           lambda rows, ix: _oracle(cfg, c, tokens=tok[rows], idx=ix,
+                                                    act_quant=act_quant))
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -134,6 +136,8 @@ def test_fp8_dispatch_rows_and_quantisation(name):
     np.testing.assert_allclose(xs[:, rows].T, tile_max / 448.0, rtol=1e-6, atol=0)
     tol = np.abs(ref) * 2.0 ** -4 + np.repeat(tile_max / 448.0, 128, axis=1) * 2.0 ** -10
     assert np.all(np.abs(deq - ref) <= tol * (1 + 1e-5) + 1e-30)
+    # the codes and scales themselves: the oracle's tile quantisation, bit for bit
+    np.testing.assert_array_equal(deq, O.quantize_tiles_e4m3(ref))
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -151,6 +155,28 @@ def test_fp8_layer_parity(name):
     got = run.out.double().cpu().numpy()
     r = rel_frob(got, ref["delta"])
     assert r <= FP8_TOL, f"relative Frobenius {r:.3e}"
+
+
+# The oracle that also quantises the activations (1 x 128 e4m3 tiles of the
+# expert inputs and of the SwiGLU output, as the kernels do) leaves only the
+# rounding of fp32 sums, of y to bf16, and rare e4m3 codes that fp32 partial
+# sums put on the other side of a rounding boundary: the bf16 bar applies.
+FP8Q_TOL = 1e-2
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_fp8_layer_parity_quantised_activations(name):
+    cfg = small_cases()[name]
+    g, c = gpu_inputs(cfg)
+    run = Fp8Run(cfg, g)
+    run.forward()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    ref = _checked_ref(cfg, c, _oracle(cfg, c, act_quant=True), run.idx.cpu().numpy(),
+                       run.gates.cpu().numpy(), act_quant=True)
+    got = run.out.double().cpu().numpy()
+    r = rel_frob(got, ref["delta"])
+    assert r <= FP8Q_TOL, f"relative Frobenius {r:.3e}"
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -224,6 +250,10 @@ def test_fp8_v3_skewed_full_size_sampled():
                        run.gates.cpu().numpy()[tok], tokens=tok)
     got = run.out[torch.as_tensor(tok, device="cuda")].double().cpu().numpy()
     assert rel_frob(got, ref["delta"]) <= FP8_TOL
+    # against the oracle that quantises the activations as the kernels do
+    refq = _checked_ref(cfg, host, _oracle(cfg, host, tokens=tok, act_quant=True), idx[tok],
+                        run.gates.cpu().numpy()[tok], tokens=tok, act_quant=True)
+    assert rel_frob(got, refq["delta"]) <= FP8Q_TOL
 
 
 def test_fp8_bias_update_steps_skewed():

@@ -365,6 +365,119 @@ def test_golden_fp8_block_scales():
     assert np.all(w[mask] == 0.0)
 
 
+# ---------------------------------------------------------------- FP8 activation quantisation
+
+def _read_e4m3_fixture():
+    rounds, tiles = [], []
+    with open(os.path.join(GOLDEN, "e4m3_round_hand.txt")) as f:
+        for ln in f:
+            ln = ln.strip()
+            if not ln or ln.startswith("#"):
+                continue
+            key, rest = ln.split(":", 1)
+            parts = rest.split()
+            if key == "round":
+                rounds.append((float(parts[0]), float(parts[1])))
+            elif key == "tile":
+                vals = [float(v) for v in parts[1].split(",")]
+                codes = [float(v) for v in parts[2].split(",")]
+                if "/" in parts[3]:
+                    num, den = parts[3].split("/")
+                    scale = np.float32(float(num)) / np.float32(float(den))
+                else:
+                    scale = np.float32(float(parts[3]))
+                tiles.append((parts[0], vals, codes, float(scale)))
+    return rounds, tiles
+
+
+def test_golden_e4m3_rounding():
+    """round_e4m3 gives the hand-worked values: ties to the even mantissa,
+    subnormals, the binade carry and saturation at 448."""
+    rounds, _ = _read_e4m3_fixture()
+    got = O.round_e4m3(np.array([x for x, _ in rounds]))
+    want = np.array([y for _, y in rounds])
+    assert np.array_equal(got, want), np.stack([got, want], 1)[got != want]
+
+
+def test_round_e4m3_matches_torch_cast():
+    """round_e4m3 against torch's float32 -> float8_e4m3fn conversion (round to
+    nearest even) on every finite e4m3 value, every midpoint between two of
+    them, the float32 neighbours of both, and random values over 18 binades;
+    all within +-448 (the torch cast does not saturate above)."""
+    codes = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    vals = codes[torch.isfinite(codes)].double().unique().numpy()
+    pos = vals[vals >= 0]
+    pts = np.concatenate([pos, (pos[:-1] + pos[1:]) / 2]).astype(np.float32)
+    pts = np.concatenate([pts, np.nextafter(pts, np.float32(np.inf)),
+                          np.nextafter(pts, np.float32(-np.inf))])
+    rng = np.random.default_rng(0)
+    rnd = (rng.standard_normal(100000) * np.exp(rng.uniform(-12, 6, 100000))).astype(np.float32)
+    v = np.concatenate([pts, -pts, rnd])
+    v = v[np.abs(v) <= 448]
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).double().numpy()
+    got = O.round_e4m3(v.astype(np.float64))
+    assert np.array_equal(got, want), v[got != want][:8]
+
+
+def test_golden_e4m3_tiles():
+    """quantize_tiles_e4m3 on the hand-worked tiles: codes times the fp32 scale."""
+    _, tiles = _read_e4m3_fixture()
+    for name, vals, codes, scale in tiles:
+        v = np.zeros((1, 128), dtype=np.float32)
+        v[0, :len(vals)] = vals
+        got = O.quantize_tiles_e4m3(v.astype(np.float64))
+        want = np.zeros(128)
+        want[:len(codes)] = np.array(codes) * scale
+        assert np.array_equal(got[0], want), (name, got[0, :len(codes)], want[:len(codes)])
+
+
+def test_quantize_tiles_e4m3_properties():
+    """Each 1 x 128 tile independently: its largest magnitude maps to the code
+    448 and comes back within fp32 rounding; every value comes back within half
+    an e4m3 step; scaling a tile by 2^k scales its result by exactly 2^k; an
+    all-zero tile stays zero."""
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal((16, 384)) * np.exp(rng.uniform(-3, 3, (16, 3))).repeat(128, 1))
+    v = v.astype(np.float32).astype(np.float64)
+    q = O.quantize_tiles_e4m3(v)
+    t, qt = v.reshape(16, 3, 128), q.reshape(16, 3, 128)
+    amax = np.abs(t).max(axis=2)
+    imax = np.abs(t).argmax(axis=2)
+    back = np.take_along_axis(qt, imax[..., None], 2)[..., 0]
+    assert np.all(np.abs(np.abs(back) - amax) <= 2.0 ** -20 * amax)
+    s = amax[..., None] / 448.0
+    assert np.all(np.abs(qt - t) <= 2.0 ** -4 * np.abs(t) + 2.0 ** -10 * s * (1 + 1e-6))
+    for k in (-8, -3, 1, 7):
+        assert np.array_equal(O.quantize_tiles_e4m3(v * 2.0 ** k), q * 2.0 ** k), k
+    z = v.copy()
+    z[:, 128:256] = 0.0
+    qz = O.quantize_tiles_e4m3(z)
+    assert not np.any(qz[:, 128:256])
+    assert np.array_equal(qz[:, :128], q[:, :128]) and np.array_equal(qz[:, 256:], q[:, 256:])
+
+
+def test_swiglu_ffn_fp8_quantises_input_and_swiglu_output():
+    """swiglu_ffn_fp8 differs from the unquantised expert by what the two
+    e4m3 roundings explain (between 2^-12 and 2^-3 of the output's norm), and
+    from each variant that leaves one of the two activations unquantised by
+    more than rounding noise: neither quantisation step is missing."""
+    rng = np.random.default_rng(9)
+    d, I, n = 256, 256, 12
+    u = rng.standard_normal((n, d)).astype(np.float32).astype(np.float64)
+    w13 = rng.standard_normal((2 * I, d)) * 0.05
+    w2 = rng.standard_normal((d, I)) * 0.05
+    y = O.swiglu_ffn_fp8(u, w13, w2)
+    ref = O.swiglu_ffn(u, w13, w2)
+    rel = np.linalg.norm(y - ref) / np.linalg.norm(ref)
+    assert 2.0 ** -12 < rel < 2.0 ** -3, rel
+    h = O.quantize_tiles_e4m3(u) @ w13.T
+    only_in = (O.silu(h[:, :I]) * h[:, I:]) @ w2.T
+    h0 = u @ w13.T
+    only_out = O.quantize_tiles_e4m3(O.silu(h0[:, :I]) * h0[:, I:]) @ w2.T
+    for other in (only_in, only_out):
+        assert np.linalg.norm(y - other) > 1e-6 * np.linalg.norm(ref)
+
+
 def test_fp8_layer_equals_layer_on_dequantised_weights():
     """An FP8 layer is the same layer on the weights q * scale (the activations
     enter unquantised): the oracle's FP8 path agrees bit for bit with its
