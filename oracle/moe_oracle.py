@@ -302,14 +302,20 @@ def quantize_tiles_e4m3(v, tile: int = 128) -> np.ndarray:
     return (q * scale.astype(np.float64)).reshape(n, m)
 
 
-def swiglu_ffn(u: np.ndarray, w13, w2) -> np.ndarray:
+def swiglu_ffn(u: np.ndarray, w13, w2, stored: str = None) -> np.ndarray:
     """One expert: W2 (SiLU(Wg u) * (Wu u)); w13 [2I, d] = [Wg; Wu], w2 [d, I].
-    u [n, d] fp64 -> [n, d] fp64."""
+    u [n, d] fp64 -> [n, d] fp64.  With ``stored`` ('bf16' or 'f32') the
+    SwiGLU output and the expert output are rounded once to that type, as a
+    layer that stores them does (reading: act and y are stored in the
+    activation type)."""
     w13 = _f64(w13)
     I = w13.shape[0] // 2
     h = u @ w13.T
     a = silu(h[:, :I]) * h[:, I:]
-    return a @ _f64(w2).T
+    if stored is not None:
+        a = round_act(a, stored)
+    y = a @ _f64(w2).T
+    return y if stored is None else round_act(y, stored)
 
 
 def swiglu_ffn_fp8(u: np.ndarray, w13, w2) -> np.ndarray:
@@ -330,7 +336,7 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
               add_residual: int = 1, tokens=None, n_groups: int = 0,
               topk_groups: int = 0, norm_w=None, norm_eps: float = 1e-6,
               act: str = "bf16", idx=None, wgt: str = None,
-              act_quant: bool = False) -> dict:
+              act_quant: bool = False, stored_rounding: bool = False) -> dict:
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
@@ -352,6 +358,11 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     ``act_quant`` (FP8 layers): every expert also quantises its input rows and
     its SwiGLU output to e4m3 in 1 x 128 tiles (``swiglu_ffn_fp8``), as the
     page's FP8 scheme does; without it the activations stay as stored.
+
+    ``stored_rounding`` (bf16 and fp32 weights): every expert's SwiGLU output
+    and output rows are rounded once to the activation type ``act``, and so is
+    the layer output, the points where a layer that stores them in that type
+    rounds (the sums stay fp64).
 
     Returns out (fp64), delta = out - residual, idx, gates, margin, and the
     scores s [n, E] of every expert."""
@@ -379,7 +390,13 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     d = u.shape[1]
     delta = np.zeros((n, d))
     S = inp["ws13"].shape[0]
-    ffn = swiglu_ffn_fp8 if act_quant else swiglu_ffn
+    if act_quant:
+        ffn = swiglu_ffn_fp8
+    elif stored_rounding:
+        def ffn(x_, w13_, w2_):
+            return swiglu_ffn(x_, w13_, w2_, stored=act)
+    else:
+        ffn = swiglu_ffn
     for s in range(S):
         delta += ffn(u, _expert_weight(inp, "ws13", s), _expert_weight(inp, "ws2", s))
     routed = np.zeros((n, K, d))
@@ -390,6 +407,9 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     for k in range(K):
         delta += gates[:, k:k + 1] * routed[:, k]
     out = delta + resid if add_residual else delta.copy()
+    if stored_rounding:
+        out = round_act(out, act)
+        delta = out - resid if add_residual else out.copy()
     return {"out": out, "delta": delta, "idx": idx, "gates": gates, "margin": margin,
             "scores": scores}
 

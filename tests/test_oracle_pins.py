@@ -365,6 +365,35 @@ def test_golden_fp8_block_scales():
     assert np.all(w[mask] == 0.0)
 
 
+# ---------------------------------------------------------------- stored rounding
+
+def test_stored_rounding_points():
+    """moe_layer(stored_rounding=True) rounds each expert's SwiGLU output and
+    output rows, and the layer output, to the activation type: the outputs are
+    bf16 values, within a few bf16 steps of the unrounded layer, and distinct
+    from an expert that skips the rounding of its SwiGLU output."""
+    cfg = small_cases()["ragged_bf16"]
+    inp = make_inputs(cfg, "cpu")
+    exact = O.moe_layer(inp, cfg.K, add_residual=0)
+    rnd = O.moe_layer(inp, cfg.K, add_residual=0, act="bf16", stored_rounding=True)
+    assert np.array_equal(O.round_bf16(rnd["delta"]), rnd["delta"])
+    rel = np.linalg.norm(rnd["delta"] - exact["delta"]) / np.linalg.norm(exact["delta"])
+    assert 2.0 ** -14 < rel < 2.0 ** -6, rel
+    u = O._f64(inp["x"])
+    w13, w2 = inp["w13"][0], inp["w2"][0]
+    y = O.swiglu_ffn(u, w13, w2, stored="bf16")
+    assert np.array_equal(O.round_bf16(y), y)
+    I = cfg.I
+    h = u @ O._f64(w13).T
+    y_no_act_rounding = O.round_bf16((O.silu(h[:, :I]) * h[:, I:]) @ O._f64(w2).T)
+    assert np.any(y != y_no_act_rounding)
+    # fp32 layers round to fp32
+    tiny = small_cases()["tiny_f32_ragged"]
+    t_in = make_inputs(tiny, "cpu")
+    t_out = O.moe_layer(t_in, tiny.K, add_residual=0, act="f32", stored_rounding=True)["delta"]
+    assert np.array_equal(t_out.astype(np.float32).astype(np.float64), t_out)
+
+
 # ---------------------------------------------------------------- FP8 activation quantisation
 
 def _read_e4m3_fixture():
