@@ -130,21 +130,21 @@ def _oracle_prenorm(cfg, c, **kw):
                        act=cfg.act, wgt="bf16" if cfg.wgt == "e4m3" else cfg.wgt, **kw)
 
 
-def _checked(cfg, c, idx_g, gates_g, add_residual, tokens=None):
+def _checked(cfg, c, idx_g, gates_g, add_residual, tokens=None, **kw):
     """The oracle's pre-normed layer (on `tokens`, default all) with routing
     checked against the GPU's: chosen sets bit-exact where the K-th vs
     (K+1)-th margin is >= 1e-5, a valid top-K within 1e-5 and its gates
     elsewhere (those rows recomputed on the GPU's choice).  The router reads
     the raw tokens and the weighted centroids on both sides, so no token's
     routing depends on the rounding of its normalised row."""
-    ref = _oracle_prenorm(cfg, c, add_residual=add_residual, tokens=tokens)
+    ref = _oracle_prenorm(cfg, c, add_residual=add_residual, tokens=tokens, **kw)
     keep, n_excl = check_near_ties(cfg, idx_g, ref["margin"], ref["scores"], c["bias"], gates_g)
     if cfg.zipf_s == 0:
         assert n_excl <= max(2, len(keep) // 50)
     np.testing.assert_array_equal(np.sort(idx_g, 1)[keep], np.sort(ref["idx"], 1)[keep])
     tok = np.arange(len(keep)) if tokens is None else np.asarray(tokens)
     return with_gpu_choice(ref, idx_g, keep, lambda rows, ix: _oracle_prenorm(
-        cfg, c, add_residual=add_residual, tokens=tok[rows], idx=ix))
+        cfg, c, add_residual=add_residual, tokens=tok[rows], idx=ix, **kw))
 
 
 # bf16 small layers take the fused router (logits from the raw tokens and the
@@ -171,6 +171,12 @@ def test_forward_prenorm_vs_oracle(name):
                  f"{name} pre-normed layer")
     np.testing.assert_array_equal(run.counts.cpu().numpy(),
                                   np.bincount(idx_g.reshape(-1), minlength=cfg.E))
+    # against the oracle that also rounds act, y and the output where the
+    # kernels store them (its normalised rows are rounded to the activation
+    # type in either form)
+    refr = _checked(cfg, c, idx_g, run.gates.cpu().numpy(), ar, stored_rounding=True)
+    r = rel_frob(to_np(run.out), refr["out"] if ar else refr["delta"])
+    assert r <= {"bf16": 1e-3, "f32": 1e-5}[cfg.act], f"{name}: stored rounding {r:.3e}"
 
 
 @pytest.mark.parametrize("name", ["small_bf16", "ragged_bf16", "softmax_norenorm"])
@@ -247,6 +253,10 @@ def test_forward_fp8_prenorm_vs_oracle(name):
     got0, got1 = to_np(r0.out), to_np(r1.out)
     rf = rel_frob(got0, ref["delta"])
     assert rf <= 5e-2, f"relative Frobenius of the MoE term {rf:.3e}"
+    # against the oracle that quantises the activations as the kernels do
+    refq = _checked(cfg, c, r0.idx.cpu().numpy(), r0.gates.cpu().numpy(), 1, act_quant=True)
+    rq = rel_frob(got0, refq["delta"])
+    assert rq <= 1e-2, f"relative Frobenius against the quantising oracle {rq:.3e}"
     # the residual is x itself (the normalised tokens would be off by O(1)):
     # with and without it the outputs differ by x, up to the two bf16 roundings
     res = got1 - got0 - to_np(g["x"])
