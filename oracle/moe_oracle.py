@@ -258,11 +258,15 @@ def dequantize_blocks(q, scale, block: int = 128) -> np.ndarray:
     return qv * np.repeat(np.repeat(sc, block, axis=0), block, axis=1)
 
 
-def _expert_weight(inp: dict, key: str, e: int):
-    """Weight ``key`` of expert e, dequantised when the layer stores FP8 blocks."""
+def _expert_weight(inp: dict, key: str, e: int, dequant_round: str = None):
+    """Weight ``key`` of expert e, dequantised when the layer stores FP8 blocks;
+    with ``dequant_round`` ('bf16') each dequantised weight q * scale is then
+    rounded once to that type, as a layer that multiplies in it holds it."""
     w = inp[key][e]
     if key + "_scale" in inp:
-        return dequantize_blocks(w, inp[key + "_scale"][e])
+        w = dequantize_blocks(w, inp[key + "_scale"][e])
+        if dequant_round is not None:
+            w = round_act(w, dequant_round)
     return w
 
 
@@ -336,7 +340,8 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
               add_residual: int = 1, tokens=None, n_groups: int = 0,
               topk_groups: int = 0, norm_w=None, norm_eps: float = 1e-6,
               act: str = "bf16", idx=None, wgt: str = None,
-              act_quant: bool = False, stored_rounding: bool = False) -> dict:
+              act_quant: bool = False, stored_rounding: bool = False,
+              dequant_round: str = None) -> dict:
     """Forward of one DeepSeekMoE layer for all tokens, or for the listed token
     ids.  out_t = [u_t] + sum_s FFN_s(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t).
 
@@ -363,6 +368,10 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
     and output rows are rounded once to the activation type ``act``, and so is
     the layer output, the points where a layer that stores them in that type
     rounds (the sums stay fp64).
+
+    ``dequant_round`` (FP8 layers): each dequantised weight is rounded once to
+    that type ('bf16'), the weights a layer that dequantises to bf16 and
+    multiplies on bf16 tensor cores uses.
 
     Returns out (fp64), delta = out - residual, idx, gates, margin, and the
     scores s [n, E] of every expert."""
@@ -397,13 +406,15 @@ def moe_layer(inp: dict, K: int, normalize: int = 1, score_func: int = SIGMOID,
             return swiglu_ffn(x_, w13_, w2_, stored=act)
     else:
         ffn = swiglu_ffn
+    def weight(key, e):
+        return _expert_weight(inp, key, e, dequant_round)
+
     for s in range(S):
-        delta += ffn(u, _expert_weight(inp, "ws13", s), _expert_weight(inp, "ws2", s))
+        delta += ffn(u, weight("ws13", s), weight("ws2", s))
     routed = np.zeros((n, K, d))
     for e in np.unique(idx):
         rows, slots = np.nonzero(idx == e)
-        routed[rows, slots] = ffn(u[rows], _expert_weight(inp, "w13", int(e)),
-                                  _expert_weight(inp, "w2", int(e)))
+        routed[rows, slots] = ffn(u[rows], weight("w13", int(e)), weight("w2", int(e)))
     for k in range(K):
         delta += gates[:, k:k + 1] * routed[:, k]
     out = delta + resid if add_residual else delta.copy()

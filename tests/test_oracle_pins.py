@@ -394,6 +394,22 @@ def test_stored_rounding_points():
     assert np.array_equal(t_out.astype(np.float32).astype(np.float64), t_out)
 
 
+def test_dequant_round_weights():
+    """dequant_round='bf16' turns each dequantised FP8 weight q * scale into the
+    nearest bf16 value (the dequantisation itself is pinned by the FP8
+    fixture); the layer moves by the size of that rounding."""
+    cfg = small_cases()["ragged_fp8"]
+    inp = make_inputs(cfg, "cpu")
+    w = O._expert_weight(inp, "w13", 3)
+    wr = O._expert_weight(inp, "w13", 3, dequant_round="bf16")
+    assert np.array_equal(O.round_bf16(w), wr) and not np.array_equal(w, wr)
+    assert np.all(np.abs(wr - w) <= 2.0 ** -9 * np.abs(w))
+    a = O.moe_layer(inp, cfg.K, add_residual=0)["delta"]
+    b = O.moe_layer(inp, cfg.K, add_residual=0, dequant_round="bf16")["delta"]
+    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 2.0 ** -14 < rel < 2.0 ** -7, rel
+
+
 # ---------------------------------------------------------------- FP8 activation quantisation
 
 def _read_e4m3_fixture():

@@ -18,8 +18,8 @@ import torch
 
 from moe_inputs import small_cases, get_config, make_inputs
 from oracle import moe_oracle as O
-from tests._util import (check_near_ties, gpu_inputs, assert_close, idx_with_counts, to_np,
-                         with_gpu_choice)
+from tests._util import (check_near_ties, gpu_inputs, assert_close, idx_with_counts, rel_frob,
+                         to_np, with_gpu_choice)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,13 +71,13 @@ class W8Run:
         m.combine(self.c16, self.y, self.gates, self.pos, g["x"], self.out)
 
 
-def _oracle(cfg, c, tokens=None, add_residual=0, idx=None):
+def _oracle(cfg, c, tokens=None, add_residual=0, idx=None, **kw):
     return O.moe_layer(c, cfg.K, cfg.normalize, cfg.score_func, add_residual=add_residual,
                        tokens=tokens, n_groups=cfg.n_groups, topk_groups=cfg.topk_groups,
-                       idx=idx)
+                       idx=idx, **kw)
 
 
-def _checked_ref(cfg, c, ref, idx_g, gates_g, tokens=None, add_residual=0):
+def _checked_ref(cfg, c, ref, idx_g, gates_g, tokens=None, add_residual=0, **kw):
     """Chosen sets bit-exact where the oracle's K-th vs (K+1)-th margin is
     >= 1e-5, a valid top-K within 1e-5 (and its gates) elsewhere; returns ref
     with the near-tie rows recomputed on the GPU's choice."""
@@ -89,7 +89,7 @@ def _checked_ref(cfg, c, ref, idx_g, gates_g, tokens=None, add_residual=0):
     np.testing.assert_array_equal(np.sort(idx_g, 1)[keep], np.sort(ref["idx"], 1)[keep])
     tok = np.arange(len(keep)) if tokens is None else np.asarray(tokens)
     return with_gpu_choice(ref, idx_g, keep, lambda rows, ix: _oracle(
-        cfg, c, tokens=tok[rows], add_residual=add_residual, idx=ix))
+        cfg, c, tokens=tok[rows], add_residual=add_residual, idx=ix, **kw))
 
 
 def _check(cfg, run, c, what):
@@ -109,6 +109,28 @@ def test_w8a16_layer_parity(name):
     torch.cuda.synchronize()
     assert m.get_status() == 0
     _check(cfg, run, c, f"{name} W8A16 layer")
+
+
+# The oracle that rounds each dequantised weight to bf16 (as the kernels hold
+# it) and rounds act, y and the output where the kernels store them leaves
+# only the fp32 rounding of the sums and the values it moves across a
+# rounding boundary.
+ROUNDED = dict(dequant_round="bf16", stored_rounding=True, act="bf16")
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_w8a16_layer_parity_rounded_oracle(name):
+    cfg = small_cases()[name]
+    g, c = gpu_inputs(cfg)
+    run = W8Run(cfg, g)
+    run.forward()
+    torch.cuda.synchronize()
+    assert m.get_status() == 0
+    idx = run.idx.cpu().numpy()
+    ref = _checked_ref(cfg, c, _oracle(cfg, c, **ROUNDED), idx, run.gates.cpu().numpy(),
+                       **ROUNDED)
+    r = rel_frob(to_np(run.out), ref["delta"])
+    assert r <= 1e-3, f"{name}: relative Frobenius {r:.3e}"
 
 
 @pytest.mark.parametrize("name", SMALL)
