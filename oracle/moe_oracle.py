@@ -434,26 +434,32 @@ def _torch_index(tokens, ref):
 # Backward pass: gradients of L with dL/d(out) = dout, chosen experts fixed
 # ----------------------------------------------------------------------------
 
-def swiglu_ffn_backward(u: np.ndarray, w13, w2, dy: np.ndarray):
+def _keep(v):
+    return v
+
+
+def swiglu_ffn_backward(u: np.ndarray, w13, w2, dy: np.ndarray, rnd=_keep):
     """Gradients of one expert y = W2 a, a = SiLU(g) * v, [g; v] = W13 u, for
     rows u [n, d] and output gradients dy [n, d]:
       da = dy W2,  dW2 = dy^T a,
       dg = da * v * SiLU'(g) with SiLU'(g) = sig(g) (1 + g (1 - sig(g))),
       dv = da * SiLU(g),  dh = [dg, dv],  dW13 = dh^T u,  du = dh W13.
-    Returns du [n, d], dw13 [2I, d], dw2 [d, I], all fp64."""
+    ``rnd`` is applied where a layer that stores them rounds: h, a, da, dh
+    and du (identity by default).  Returns du [n, d], dw13 [2I, d],
+    dw2 [d, I], all fp64."""
     w13 = _f64(w13)
     w2 = _f64(w2)
     I = w13.shape[0] // 2
-    h = u @ w13.T
+    h = rnd(u @ w13.T)
     g, v = h[:, :I], h[:, I:]
     sig = 1.0 / (1.0 + np.exp(-g))
-    a = g * sig * v
-    da = dy @ w2
+    a = rnd(g * sig * v)
+    da = rnd(dy @ w2)
     dw2 = dy.T @ a
     dg = da * v * sig * (1.0 + g * (1.0 - sig))
     dv = da * g * sig
-    dh = np.concatenate([dg, dv], axis=1)
-    return dh @ w13, dh.T @ u, dw2
+    dh = rnd(np.concatenate([dg, dv], axis=1))
+    return rnd(dh @ w13), dh.T @ u, dw2
 
 
 def router_backward(u: np.ndarray, centroids, s: np.ndarray, idx: np.ndarray,
@@ -490,7 +496,8 @@ def router_backward(u: np.ndarray, centroids, s: np.ndarray, idx: np.ndarray,
 
 def moe_layer_backward(inp: dict, K: int, dout, normalize: int = 1,
                        score_func: int = SIGMOID, add_residual: int = 1,
-                       n_groups: int = 0, topk_groups: int = 0, idx=None) -> dict:
+                       n_groups: int = 0, topk_groups: int = 0, idx=None,
+                       stored_rounding: bool = False) -> dict:
     """Backward of ``moe_layer`` (no RMSNorm in front) for all T tokens:
     dout [T, d] is dL/d(out).  The routed term g_k FFN_k(u) gives
       dgates[t, k] = dout_t . FFN_k(u_t),  dFFN_k = g_k dout_t,
@@ -501,9 +508,16 @@ def moe_layer_backward(inp: dict, K: int, dout, normalize: int = 1,
     gates, margin; every array fp64.  Weight gradients of experts that no
     token chose are zero.  ``idx`` [T, K], when given, replaces the router's
     own choice (another valid choice where keys tie); the gates are then
-    those of eq. (13)/(14) for that choice and the margin is NaN."""
+    those of eq. (13)/(14) for that choice and the margin is NaN.
+
+    ``stored_rounding``: values a bf16 training layer stores are rounded once
+    to bf16 where it stores them: the training forward's h = [gate | up], act
+    and y; the row gradients g * dout, da, [dgate, dup] and du; and the
+    outputs dx and the weight gradients.  Sums stay fp64; dgates, dlogit and
+    the centroid gradients are not rounded."""
     u = _f64(inp["x"])
     go = _f64(dout)
+    rnd = round_bf16 if stored_rounding else _keep
     T, d = u.shape
     if idx is None:
         idx, gates, margin, s = route(u, inp["centroids"], inp["bias"], K, score_func,
@@ -525,23 +539,29 @@ def moe_layer_backward(inp: dict, K: int, dout, normalize: int = 1,
     dgates = np.zeros((T, K))
     for sx in range(S):
         du, dw13_s, dw2_s = swiglu_ffn_backward(u, _expert_weight(inp, "ws13", sx),
-                                                _expert_weight(inp, "ws2", sx), go)
+                                                _expert_weight(inp, "ws2", sx), go, rnd)
         dx += du
-        dws13[sx] = dw13_s
-        dws2[sx] = dw2_s
+        dws13[sx] = rnd(dw13_s)
+        dws2[sx] = rnd(dw2_s)
     for e in np.unique(idx):
         rows, slots = np.nonzero(idx == e)
         ue = u[rows]
         w13e = _expert_weight(inp, "w13", int(e))
         w2e = _expert_weight(inp, "w2", int(e))
-        ye = swiglu_ffn(ue, w13e, w2e)
+        if stored_rounding:
+            # the training forward's y: from the stored h, act stored, y stored
+            he = rnd(ue @ _f64(w13e).T)
+            ye = rnd(rnd(silu(he[:, :I]) * he[:, I:]) @ _f64(w2e).T)
+        else:
+            ye = swiglu_ffn(ue, w13e, w2e)
         dgates[rows, slots] = np.sum(go[rows] * ye, axis=1)
-        dye = gates[rows, slots][:, None] * go[rows]
-        du, dw13[e], dw2[e] = swiglu_ffn_backward(ue, w13e, w2e, dye)
+        dye = rnd(gates[rows, slots][:, None] * go[rows])
+        du, dw13_e, dw2_e = swiglu_ffn_backward(ue, w13e, w2e, dye, rnd)
+        dw13[e], dw2[e] = rnd(dw13_e), rnd(dw2_e)
         np.add.at(dx, rows, du)
     du_r, dcent, dlogit = router_backward(u, inp["centroids"], s, idx, gates, dgates,
                                           normalize, score_func)
-    dx += du_r
+    dx = rnd(dx + du_r)
     return {"dx": dx, "dcentroids": dcent, "dw13": dw13, "dw2": dw2, "dws13": dws13,
             "dws2": dws2, "dgates": dgates, "dlogit": dlogit, "idx": idx, "gates": gates,
             "margin": margin}

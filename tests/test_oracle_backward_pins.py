@@ -138,3 +138,22 @@ def test_given_choice_reproduces_router_choice():
     b = O.moe_layer_backward(inp, 3, dout, 1, O.SIGMOID, 1, idx=a["idx"])
     for k in ("dx", "dcentroids", "dw13", "dw2", "dws13", "dws2", "dgates"):
         np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_stored_rounding_backward():
+    """stored_rounding=True rounds the stored values to bf16: dx and the
+    weight gradients come out as bf16 values within a few bf16 steps of the
+    unrounded gradients; dgates use the rounded y of the training forward,
+    and the centroid gradients stay unrounded fp64."""
+    inp = _layer(T=16, d=128, E=8, I=64, S=1, seed=21)
+    for k in ("x", "centroids", "w13", "w2", "ws13", "ws2"):
+        inp[k] = O.round_bf16(inp[k] * 0.2)
+    dout = O.round_bf16(np.random.default_rng(4).normal(0, 1.0, inp["x"].shape))
+    a = O.moe_layer_backward(inp, 2, dout, 1, O.SIGMOID, 1)
+    b = O.moe_layer_backward(inp, 2, dout, 1, O.SIGMOID, 1, idx=a["idx"], stored_rounding=True)
+    for k in ("dx", "dw13", "dw2", "dws13", "dws2"):
+        assert np.array_equal(O.round_bf16(b[k]), b[k]), k
+        rel = np.linalg.norm(b[k] - a[k]) / np.linalg.norm(a[k])
+        assert 2.0 ** -16 < rel < 2.0 ** -6, (k, rel)
+    assert not np.array_equal(a["dgates"], b["dgates"])
+    assert not np.array_equal(O.round_bf16(b["dcentroids"]), b["dcentroids"])
