@@ -416,7 +416,7 @@ def run_reference(args, cfg, dist, rank, ws, device):
     value = tok / secs
     line = {"impl": "reference", "metric": TRAIN_METRIC if args.train else METRIC,
             "value": round(value, 4), "unit": UNIT,
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(secs / len(rates) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": _workload(cfg, args) + ("+train" if args.train else ""),
@@ -426,7 +426,8 @@ def run_reference(args, cfg, dist, rank, ws, device):
                              "kind": "oracle",
                              "sample": f"{per_step} random tokens of the {cfg.name} batch per "
                                        f"step through the fp64 oracle" +
-                                       (", forward and backward" if args.train else "")},
+                                       (", forward and backward" if args.train else "") +
+                                       (f"; rank 0 of {ws} alone" if ws > 1 else "")},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
