@@ -219,3 +219,12 @@ def test_header_compiles_as_c99_and_links(tmp_path):
     res = subprocess.run([exe], capture_output=True, text=True)
     assert res.returncode == 0, f"check {res.returncode} failed: {res.stdout}{res.stderr}"
     assert "abi ok" in res.stdout
+
+
+def test_missing_library_fails_loudly():
+    """No CPU fallback: without libmoe.so the loader raises instead of
+    returning anything that could run the layer elsewhere."""
+    from mixture_experts_layer_88_b300 import _lib
+    with pytest.raises(ImportError, match="libmoe.so not built"):
+        _lib.load_library(os.path.join(os.path.dirname(_lib.LIB_PATH), "no_such_dir",
+                                       "libmoe.so"))
