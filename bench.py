@@ -689,7 +689,7 @@ def time_layer(m, layer, x, out, steps, warmup, clk, dist=None, device=None, gra
     return ms / steps, traces, st
 
 
-def decode_record(m, cfg_prefill, inp, device, peaks, clk, steps, warmup):
+def decode_record(m, cfg_prefill, inp, device, peaks, clk, steps, warmup, graph=False):
     """The V3 decode batch (T = 128) on the same layer weights as the prefill
     run: weight streaming.  ms per step, tokens/s and the touched expert
     weights (every expert at least one token chose, plus the shared experts,
@@ -705,11 +705,12 @@ def decode_record(m, cfg_prefill, inp, device, peaks, clk, steps, warmup):
     x = make_tokens(cfg, device)
     out = torch.empty_like(x)
     n0 = len(clk.windows)
-    ms, traces, st = time_layer(m, layer, x, out, steps, warmup, clk)
+    ms, traces, st = time_layer(m, layer, x, out, steps, warmup, clk, graph=graph)
     touched = int((layer.counts > 0).sum().item()) + cfg.S
     wbytes = touched * 3.0 * cfg.I * cfg.d * 2 + cfg.E * cfg.d * 2
     gemm_ms = sum(t[2] for t in traces if t[0] in ("gemm_gateup_swiglu", "gemm_down")) / steps
     return {"workload": cfg.name, "T": cfg.T, "steps": steps, "warmup": warmup,
+            "launch": _launch(graph),
             "ms_per_step": round(ms, 4), "tokens_per_s": round(cfg.T / (ms / 1e3), 1),
             "touched_experts": touched, "weight_bytes_per_step": int(wbytes),
             "weight_stream": {"achieved_gbs": round(wbytes / (gemm_ms / 1e3) / 1e9, 1),
@@ -724,7 +725,7 @@ def decode_record(m, cfg_prefill, inp, device, peaks, clk, steps, warmup):
             "clocks": clk.summary(clk.windows[n0:])}
 
 
-def fp8_record(m, device, peaks, clk, steps, warmup, balance_steps):
+def fp8_record(m, device, peaks, clk, steps, warmup, balance_steps, graph=False):
     """The Zipf-skewed V3 layer (T = 16384) with e4m3 128x128 block-scaled
     expert weights: ms per step, tokens/s, the e4m3 expert GEMMs' TFLOP/s
     against the fp8 peak (2 x the measured bf16 burst peak), and the max /
@@ -736,7 +737,7 @@ def fp8_record(m, device, peaks, clk, steps, warmup, balance_steps):
     x = inp["x"]
     out = torch.empty_like(x)
     n0 = len(clk.windows)
-    ms, traces, st = time_layer(m, layer, x, out, steps, warmup, clk)
+    ms, traces, st = time_layer(m, layer, x, out, steps, warmup, clk, graph=graph)
     names = ("gemm_fp8_gateup_swiglu", "gemm_fp8_down")
     gemm_ms = sum(t[2] for t in traces if t[0] in names) / steps
     tf = cfg.gemm_flops() / (gemm_ms / 1e3) / 1e12
@@ -747,6 +748,7 @@ def fp8_record(m, device, peaks, clk, steps, warmup, balance_steps):
         layer.forward(make_tokens(cfg, device, step=step + 1), out)
         loads.append(round(float(layer.update_bias()[0].item()), 3))
     rec = {"workload": cfg.name + "+e4m3", "T": cfg.T, "steps": steps, "warmup": warmup,
+           "launch": _launch(graph),
            "ms_per_step": round(ms, 4), "tokens_per_s": round(cfg.T / (ms / 1e3), 1),
            "grouped_gemm": {"tflops": round(tf, 1), "peak_tflops": fp8_peak,
                             "frac": round(tf / fp8_peak, 4),
@@ -762,7 +764,7 @@ def fp8_record(m, device, peaks, clk, steps, warmup, balance_steps):
     return rec
 
 
-def dsmoe16b_record(m, device, peaks, clk, steps, warmup):
+def dsmoe16b_record(m, device, peaks, clk, steps, warmup, graph=False):
     """The 16B-shape layer (T = 32768, d = 2048, 64 routed experts top-6 with
     Softmax scores and no renormalisation, 2 shared experts, I = 1408): ms per
     step, tokens/s and the bf16 expert GEMMs' TFLOP/s against the measured
@@ -773,11 +775,12 @@ def dsmoe16b_record(m, device, peaks, clk, steps, warmup):
     x = inp["x"]
     out = torch.empty_like(x)
     n0 = len(clk.windows)
-    ms, traces, st = time_layer(m, layer, x, out, steps, warmup, clk)
+    ms, traces, st = time_layer(m, layer, x, out, steps, warmup, clk, graph=graph)
     names = ("gemm_gateup_swiglu", "gemm_down")
     gemm_ms = sum(t[2] for t in traces if t[0] in names) / steps
     tf = cfg.gemm_flops() / (gemm_ms / 1e3) / 1e12
     rec = {"workload": cfg.name, "T": cfg.T, "steps": steps, "warmup": warmup,
+           "launch": _launch(graph),
            "ms_per_step": round(ms, 4), "tokens_per_s": round(cfg.T / (ms / 1e3), 1),
            "grouped_gemm": {"tflops": round(tf, 1), "peak_tflops": peaks["bf16_tflops"],
                             "frac": round(tf / peaks["bf16_tflops"], 4),
@@ -790,6 +793,10 @@ def dsmoe16b_record(m, device, peaks, clk, steps, warmup):
     del layer, inp
     torch.cuda.empty_cache()
     return rec
+
+
+def _launch(graph: bool) -> str:
+    return "CUDA graph replay" if graph else "eager stream launches"
 
 
 def _workload(cfg, args) -> str:
@@ -817,7 +824,9 @@ def main():
                     help="FP8 layers: e4m3 x e4m3 with fp32 promotion every 128 K (e4m3) or "
                          "e4m3 weights dequantised to bf16 on the fly (w8a16)")
     ap.add_argument("--graph", action="store_true",
-                    help="replay the step from a CUDA graph captured after the warm-up")
+                    help="replay the step from a CUDA graph captured after the warm-up (the "
+                         "per-kernel figures then come from traced eager steps after the "
+                         "timed region, so the default times eager launches)")
     ap.add_argument("--prenorm", action="store_true",
                     help="the layer behind its RMSNorm: h = x + MoE(RMSNorm(x))")
     ap.add_argument("--train", action="store_true",
@@ -832,6 +841,8 @@ def main():
     args.warmup = max(3, args.warmup)
 
     dist, rank, ws, local = _dist()
+    if ws > 1:
+        args.graph = False    # the count all-reduce is not captured into a graph
     device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     if device.type == "cuda":
         torch.cuda.set_device(device)
@@ -927,7 +938,7 @@ def main():
                    "K": cfg.K, "S": cfg.S, "I": cfg.I, "renormalize": bool(cfg.normalize),
                    "parallelism": (f"data parallel x{ws}, load counts all-reduced for the "
                                    f"bias update" if ws > 1 else "one replica"),
-                   "launch": "CUDA graph replay" if args.graph else "eager stream launches",
+                   "launch": _launch(args.graph),
                    "l2": (f"inputs larger than L2: "
                           f"{(cfg.E + cfg.S) * 3 * cfg.I * cfg.d * {'e4m3': 1, 'bf16': 2}.get(cfg.wgt, 4) / 1e9:.1f} GB "
                           f"of expert weights streamed per step")},
@@ -970,11 +981,12 @@ def main():
         line["balance"] = {"steps": args.balance_steps, "gamma": cfg.gamma,
                            "max_over_mean_load": loads}
     sub = (ws == 1 and not args.no_subconfigs and not args.override and not args.prenorm
-           and not args.graph and args.config == "v3_prefill")
+           and args.config == "v3_prefill")
     if sub:
         # the other V3 configurations, each with its own timed region and clocks
         line["subconfigs"] = {"v3_decode": decode_record(m, cfg, inp, device, peaks, clk,
-                                                         args.sub_steps, args.warmup)}
+                                                         args.sub_steps, args.warmup,
+                                                         args.graph)}
     if not args.no_cpu_baseline:
         rate, secs, cores = cpu_oracle_tokens_per_s(cfg, inp, args.cpu_tokens,
                                                     prenorm=args.prenorm)
@@ -991,9 +1003,10 @@ def main():
         del layer, pipe, inp, x, out
         torch.cuda.empty_cache()
         line["subconfigs"]["v3_skewed_fp8"] = fp8_record(m, device, peaks, clk, args.sub_steps,
-                                                         args.warmup, args.balance_steps)
+                                                         args.warmup, args.balance_steps,
+                                                         args.graph)
         line["subconfigs"]["dsmoe16b"] = dsmoe16b_record(m, device, peaks, clk, args.sub_steps,
-                                                         args.warmup)
+                                                         args.warmup, args.graph)
     clk.__exit__(None, None, None)
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -13,12 +13,16 @@ pytestmark = pytest.mark.gpu
 m = pytest.importorskip("mixture_experts_layer_88_b300")
 
 
-@pytest.mark.parametrize("name", ["small_bf16", "small_fp8"])
-def test_layer_step_replayed_from_cuda_graph(name):
+@pytest.mark.parametrize("name,prenorm", [("small_bf16", False), ("small_fp8", False),
+                                          ("softmax_norenorm", False), ("small_bf16", True)])
+def test_layer_step_replayed_from_cuda_graph(name, prenorm):
     cfg = small_cases()[name]
     g, _ = gpu_inputs(cfg)
-    eager = m.MoeLayer(m.cfg_from_layer(cfg), dict(g, bias=g["bias"].clone()), device="cuda")
-    graphed = m.MoeLayer(m.cfg_from_layer(cfg), dict(g, bias=g["bias"].clone()), device="cuda")
+    kw = dict(norm_w=g["norm_w"]) if prenorm else {}
+    eager = m.MoeLayer(m.cfg_from_layer(cfg), dict(g, bias=g["bias"].clone()), device="cuda",
+                       **kw)
+    graphed = m.MoeLayer(m.cfg_from_layer(cfg), dict(g, bias=g["bias"].clone()), device="cuda",
+                         **kw)
     x = g["x"]
     out_e, out_g = torch.empty_like(x), torch.empty_like(x)
     eager.step(x, out_e)              # first calls: kernel attributes, occupancy, buffers
