@@ -449,7 +449,9 @@ const char* moe_status_string(moe_status_t st);
  * Kernel timing (tracing).  While enabled, every kernel the calls above
  * launch is bracketed by CUDA events on its own stream, and its name, launch
  * count and summed device time are kept per calling thread.  Events come from
- * a pool created on first use; no device memory is allocated.
+ * a pool created on first use; no device memory is allocated.  Calls made
+ * while their stream is being captured into a CUDA graph record their events
+ * as event-record nodes of the graph: read them after the graph has run.
  */
 typedef struct {
   char name[48];

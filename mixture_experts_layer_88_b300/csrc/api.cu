@@ -51,15 +51,24 @@ struct TraceState {
 thread_local TraceState g_trace;
 }  // namespace
 
+// While the stream is being captured into a CUDA graph the events become
+// event-record nodes of the graph, recorded each time the graph runs.
+void trace_record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
 void trace_begin(cudaStream_t s, const char* name) {
   if (!g_trace.on) return;
   TraceRec r{name, g_trace.get(), g_trace.get()};
-  cudaEventRecord(r.ev0, s);
+  trace_record(r.ev0, s);
   g_trace.recs.push_back(r);
 }
 void trace_end(cudaStream_t s) {
   if (!g_trace.on || g_trace.recs.empty()) return;
-  cudaEventRecord(g_trace.recs.back().ev1, s);
+  trace_record(g_trace.recs.back().ev1, s);
 }
 
 // ---------------------------------------------------------------- plans

@@ -59,3 +59,31 @@ def test_wide_router_traces_split_gemm_and_topk():
     m.trace_enable(False)
     assert rec.get("gemm_router") == 1 and rec.get("router_topk") == 1
     assert "router_fused" not in rec
+
+
+@pytest.mark.gpu
+def test_trace_events_captured_into_a_graph():
+    """Steps captured into a CUDA graph with tracing on record their events as
+    graph nodes: after a replay the trace holds every launch of the captured
+    steps with its device time, as eager steps would."""
+    cfg = small_cases()["small_bf16"]
+    g, _ = gpu_inputs(cfg)
+    layer = m.MoeLayer(m.cfg_from_layer(cfg), g, device="cuda")
+    out = torch.empty_like(g["x"])
+    layer.step(g["x"], out)
+    torch.cuda.synchronize()
+    m.trace_enable(True)
+    m.trace_read_all()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(3):
+            layer.step(g["x"], out)
+    graph.replay()
+    torch.cuda.synchronize()
+    rec = {name: (n, ms) for name, n, ms in m.trace_read_all()}
+    m.trace_enable(False)
+    assert m.get_status() == 0
+    for name in ("router_fused", "dispatch_scatter", "gemm_gateup_swiglu", "gemm_down",
+                 "combine", "update_bias"):
+        n, ms = rec[name]
+        assert n == 3 and ms > 0.0, (name, n, ms)
