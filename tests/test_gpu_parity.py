@@ -390,6 +390,11 @@ def test_edge_cases(name):
                              ref["margin"], ref["scores"], c["bias"])
     ref = _ties_on_gpu_choice(cfg, c, ref, idx_g, keep, add_residual=0)
     assert_close(to_np(run.out), ref["delta"], cfg.act, name)
+    refr = _layer(cfg, c, add_residual=0, act=cfg.act, stored_rounding=True)
+    refr = _ties_on_gpu_choice(cfg, c, refr, idx_g, keep, add_residual=0, act=cfg.act,
+                               stored_rounding=True)
+    r = rel_frob(to_np(run.out), refr["delta"])
+    assert r <= STORED_TOL[cfg.act], f"{name}: stored rounding {r:.3e}"
 
 
 def test_hot_expert_spans_several_token_blocks():
