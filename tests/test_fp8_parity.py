@@ -210,9 +210,12 @@ def test_fp8_hot_expert_many_token_blocks():
     torch.cuda.synchronize()
     assert m.get_status() == 0
     assert int(run.counts[3].item()) == cfg.T
-    ref = _checked_ref(cfg, c, _oracle(cfg, c), run.idx.cpu().numpy(), run.gates.cpu().numpy())
+    idx, gates = run.idx.cpu().numpy(), run.gates.cpu().numpy()
+    ref = _checked_ref(cfg, c, _oracle(cfg, c), idx, gates)
     got = run.out.double().cpu().numpy()
     assert rel_frob(got, ref["delta"]) <= FP8_TOL
+    refq = _checked_ref(cfg, c, _oracle(cfg, c, act_quant=True), idx, gates, act_quant=True)
+    assert rel_frob(got, refq["delta"]) <= FP8Q_TOL
 
 
 def test_fp8_v3_skewed_full_size_sampled():
@@ -305,6 +308,8 @@ def test_fp8_token_block_boundaries():
     np.testing.assert_array_equal(run.counts.cpu().numpy(), counts)
     got = run.out.double().cpu().numpy()
     assert rel_frob(got, ref["delta"]) <= FP8_TOL
+    refq = _oracle(cfg, c, idx=idx, act_quant=True)      # same routing, same gates
+    assert rel_frob(got, refq["delta"]) <= FP8Q_TOL
 
 
 FP8_EDGE = {
@@ -327,6 +332,9 @@ def test_fp8_edge_cases(name):
     run.forward()
     torch.cuda.synchronize()
     assert m.get_status() == 0
-    ref = _checked_ref(cfg, c, _oracle(cfg, c), run.idx.cpu().numpy(), run.gates.cpu().numpy())
+    idx, gates = run.idx.cpu().numpy(), run.gates.cpu().numpy()
+    ref = _checked_ref(cfg, c, _oracle(cfg, c), idx, gates)
     got = run.out.double().cpu().numpy()
     assert rel_frob(got, ref["delta"]) <= FP8_TOL
+    refq = _checked_ref(cfg, c, _oracle(cfg, c, act_quant=True), idx, gates, act_quant=True)
+    assert rel_frob(got, refq["delta"]) <= FP8Q_TOL
