@@ -223,6 +223,8 @@ def test_expert_token_block_boundaries(case):
     assert run.status() == 0
     np.testing.assert_array_equal(to_np(run.counts), counts)
     assert_close(to_np(run.out), ref["delta"], cfg.act, f"{case} delta")
+    refr = _layer(cfg, c, add_residual=0, idx=idx, act=cfg.act, stored_rounding=True)
+    assert rel_frob(to_np(run.out), refr["delta"]) <= STORED_TOL[cfg.act]
 
 
 # ---------------------------------------------------------------- whole layer
@@ -416,6 +418,10 @@ def test_hot_expert_spans_several_token_blocks():
                              ref["margin"], ref["scores"], c["bias"])
     ref = _ties_on_gpu_choice(cfg, c, ref, idx_g, keep, add_residual=0)
     assert_close(to_np(run.out), ref["delta"], cfg.act, "hot expert")
+    refr = _layer(cfg, c, add_residual=0, act=cfg.act, stored_rounding=True)
+    refr = _ties_on_gpu_choice(cfg, c, refr, idx_g, keep, add_residual=0, act=cfg.act,
+                               stored_rounding=True)
+    assert rel_frob(to_np(run.out), refr["delta"]) <= STORED_TOL[cfg.act]
 
 
 def test_bad_expert_ids_are_flagged_and_skipped():

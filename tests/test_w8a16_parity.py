@@ -92,12 +92,26 @@ def _checked_ref(cfg, c, ref, idx_g, gates_g, tokens=None, add_residual=0, **kw)
         cfg, c, tokens=tok[rows], add_residual=add_residual, idx=ix, **kw))
 
 
+# The oracle that rounds each dequantised weight to bf16 (as the kernels hold
+# it) and rounds act, y and the output where the kernels store them leaves
+# only the fp32 rounding of the sums and the values it moves across a
+# rounding boundary.
+ROUNDED = dict(dequant_round="bf16", stored_rounding=True, act="bf16")
+
+
 def _check(cfg, run, c, what):
+    """The bf16 bar against the oracle on the exact dequantised weights, and
+    1e-3 against the oracle that rounds them and the stored values as the
+    kernels do."""
     idx = run.idx.cpu().numpy()
     ref = _checked_ref(cfg, c, _oracle(cfg, c), idx, run.gates.cpu().numpy())
     np.testing.assert_array_equal(run.counts.cpu().numpy(),
                                   np.bincount(idx.reshape(-1), minlength=cfg.E))
     assert_close(to_np(run.out), ref["delta"], "bf16", what)
+    refr = _checked_ref(cfg, c, _oracle(cfg, c, **ROUNDED), idx, run.gates.cpu().numpy(),
+                        **ROUNDED)
+    r = rel_frob(to_np(run.out), refr["delta"])
+    assert r <= 1e-3, f"{what}: rounded oracle {r:.3e}"
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -109,13 +123,6 @@ def test_w8a16_layer_parity(name):
     torch.cuda.synchronize()
     assert m.get_status() == 0
     _check(cfg, run, c, f"{name} W8A16 layer")
-
-
-# The oracle that rounds each dequantised weight to bf16 (as the kernels hold
-# it) and rounds act, y and the output where the kernels store them leaves
-# only the fp32 rounding of the sums and the values it moves across a
-# rounding boundary.
-ROUNDED = dict(dequant_round="bf16", stored_rounding=True, act="bf16")
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -279,3 +286,5 @@ def test_w8a16_token_block_boundaries():
     assert m.get_status() == 0
     np.testing.assert_array_equal(run.counts.cpu().numpy(), counts)
     assert_close(to_np(run.out), ref["delta"], cfg.act, "w8a16 block boundaries")
+    refr = _oracle(cfg, c, idx=idx, **ROUNDED)
+    assert rel_frob(to_np(run.out), refr["delta"]) <= 1e-3
